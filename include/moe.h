@@ -1,0 +1,243 @@
+/*
+ * moe.h — C ABI of the routed Mixture-of-Experts expert layer for one GB300
+ * (sm_103a): router softmax / top-k, atomic-free permute into a padded
+ * expert-grouped layout, grouped SwiGLU expert GEMMs, score-weighted
+ * gather-sum combine, and the backward of all of them.
+ *
+ * Sources (the web pages this layer is built from):
+ *   [HALO]  Halo "Performance" — §Levers that help (grouped GEMM, atomic-free
+ *           expert permute, fused GLU), §Levers that do not help here
+ *           (small-M experts are bound by weight bandwidth).
+ *   [PLLM]  PocketLLM "Qwen4-Exp Heterogeneous TP4 Performance" — §Runtime
+ *           architecture (512 routed experts, top-10 routing).
+ *   [PRL]   prime-rl PR #3885 (DeepSeek-V4.1 Flash perf work) — §Changes:
+ *           "Single-pass DeepEP local layout" (one gather into the padded
+ *           expert-grouped layout, one fp32 score-weighted gather-sum back,
+ *           gathers in backward), "FP8 routed experts" (grouped forward,
+ *           dgrad and wgrad GEMMs), "FP8 Mega MoE" (K-grouped wgrad),
+ *           "dispatch.type = mega_moe" (gradients for x, the top-k weights
+ *           and the expert weights), the 32-bit offset overflow fix (element
+ *           offsets here are 64-bit), "Spread balanced routing".
+ *
+ * Conventions shared by every entry point:
+ *   - moe_bf16 is the raw 16-bit pattern of a bfloat16.
+ *   - Every pointer is a DEVICE pointer unless stated otherwise; every buffer
+ *     is owned by the caller. No entry point allocates, frees or
+ *     synchronises device memory (moe_status and the timer read are the only
+ *     calls that synchronise). All work is enqueued on `stream` in order.
+ *   - Matrices are row-major and densely packed.
+ *   - T tokens of width d; E experts of ffn width f; top-k routing; pair
+ *     p = t*k + j is token t's j-th choice; P = T*k.
+ *   - The padded layout: expert e owns rows [offsets[e], offsets[e+1]) of
+ *     every "row buffer" ([R_cap, ...]); its n_e real rows come first in
+ *     ascending pair id, then zero padding up to a multiple of `align`.
+ *     R_cap >= T*k + E*(align-1) bounds the padded size for any routing, so
+ *     the host never needs the counts.
+ *   - Return codes below; MOE_ERR_ARG etc. are detected on the host before
+ *     anything is enqueued. MOE_ERR_DEVICE_* are raised by kernels into a
+ *     per-device status word and reported by moe_status().
+ */
+#ifndef MOE_GB300_H
+#define MOE_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef uint16_t moe_bf16;
+typedef struct CUstream_st* moe_stream_t; /* the same handle as cudaStream_t */
+
+#define MOE_OK                 0
+#define MOE_ERR_ARG            1 /* null required pointer, size <= 0, k > E, bad align, ... */
+#define MOE_ERR_UNSUPPORTED    2 /* shape the kernels do not take (d or f not a multiple of 8, E > 1024) */
+#define MOE_ERR_CAPACITY       3 /* R_cap < T*k + E*(align-1) */
+#define MOE_ERR_CUDA           4 /* a CUDA runtime / driver call failed */
+#define MOE_ERR_DEVICE_INDEX   5 /* device: an expert id outside [0, E) in a caller-supplied index */
+#define MOE_ERR_DEVICE_TIMEOUT 6 /* device: a bounded wait inside a kernel gave up */
+
+/* ------------------------------------------------------------------------
+ * moe_route — router logits, top-k selection and renormalised weights.
+ * [PLLM §Runtime architecture] top-k routing over many experts; the
+ * softmax / top-k / renormalise formula is the plainest reading (the pages do
+ * not write it out): l_t = x_t . W_r (+ b) in fp32; S_t = the k largest
+ * logits by descending value, equal logits -> lower expert index first;
+ * w_t,j = exp(l_S_j - l_S_0) / sum_j' exp(l_S_j' - l_S_0) (a softmax over
+ * all E experts restricted to S_t and renormalised is the same number).
+ *
+ *  x          [T, d] bf16            w_router [d, E] fp32     bias [E] fp32 or NULL
+ *  forced_idx [T, k] int32 or NULL:  when given, S_t is taken from it instead
+ *             of the top-k (slot order as given; weights are still the
+ *             renormalised softmax over it). [PRL "Spread balanced routing"]
+ *             An id outside [0, E) raises MOE_ERR_DEVICE_INDEX (the slot's
+ *             weight is written as 0).
+ *  logits     [T, E] fp32 out        topk_idx [T, k] int32 out    topk_w [T, k] fp32 out
+ * Limits: 1 <= k <= min(E, 32); E <= 1024.
+ * ------------------------------------------------------------------------ */
+int moe_route(const moe_bf16* x, const float* w_router, const float* bias,
+              const int32_t* forced_idx, int64_t T, int d, int E, int k,
+              float* logits, int32_t* topk_idx, float* topk_w, moe_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * moe_permute — the padded expert-grouped layout and the gather into it.
+ * [PRL "Single-pass DeepEP local layout"] one gather of token copies into a
+ * padded expert-grouped layout; [HALO §Levers that help] atomic-free expert
+ * permute: a per-block histogram (warp match, no atomics), a fixed-order
+ * exclusive scan over (block, expert), stable ranks — deterministic.
+ *
+ *  topk_idx [T, k] int32 in (ids outside [0, E) raise MOE_ERR_DEVICE_INDEX;
+ *           such pairs are dropped from the layout, their dst_row is -1)
+ *  x        [T, d] bf16 in
+ *  counts   [E] int32 out: n_e
+ *  offsets  [E+1] int64 out: offsets[e] = sum_{e'<e} ceil(n_e'/align)*align
+ *  dst_row  [T*k] int32 out: row of pair p
+ *  src_pair [R_cap] int32 out: pair held by row r, -1 for padding and for
+ *           rows past offsets[E]
+ *  xp       [R_cap, d] bf16 out: xp[r] = x[src_pair[r] / k]; padding rows
+ *           inside groups are 0; rows >= offsets[E] are not written
+ *  align    power of two in [16, 256] (the grouped GEMMs consume rows in
+ *           steps of 16, one bf16 MMA K-step, so every group must be a
+ *           multiple of 16 rows)
+ *  ws       workspace of moe_workspace_size(MOE_WS_PERMUTE, ...) bytes
+ * ------------------------------------------------------------------------ */
+int moe_permute(const int32_t* topk_idx, int64_t T, int k, int E, int align,
+                const moe_bf16* x, int d, int64_t R_cap,
+                int32_t* counts, int64_t* offsets, int32_t* dst_row, int32_t* src_pair,
+                moe_bf16* xp, void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * moe_expert_fwd — grouped gate/up GEMM with fused SwiGLU, grouped down GEMM.
+ * [HALO §Levers that help] one grouped expert matmul instead of a loop, fused
+ * GLU; [PRL "Kept expert activations"] G and U are kept for backward.
+ * Per expert e on its rows:  G = Xp.W_gate[e], U = Xp.W_up[e] (fp32
+ * accumulation in tensor memory), A = silu(G)*U from the fp32 accumulators,
+ * Yp = A.W_down[e] (times row_w[r] in fp32 when row_w is given).
+ *
+ *  xp [R_cap, d] bf16, offsets [E+1] int64 (from moe_permute)
+ *  w_gate, w_up [E, d, f] bf16;  w_down [E, f, d] bf16
+ *  row_w [R_cap] fp32 or NULL (NULL: Yp is the unscaled expert output, the
+ *        layout the combine and moe_expert_bwd expect)
+ *  g, u, a [R_cap, f] bf16 out;  yp [R_cap, d] bf16 out
+ * Rows of every group, padding included, are written; padding rows come out
+ * 0 because their xp rows are 0. Rows >= offsets[E] are not written.
+ * Limits: d, f multiples of 8 (16-byte rows for TMA); E <= 1024.
+ * ------------------------------------------------------------------------ */
+int moe_expert_fwd(const moe_bf16* xp, const int64_t* offsets, const float* row_w,
+                   int E, int d, int f, int64_t R_cap,
+                   const moe_bf16* w_gate, const moe_bf16* w_up, const moe_bf16* w_down,
+                   moe_bf16* g, moe_bf16* u, moe_bf16* a, moe_bf16* yp,
+                   moe_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * moe_combine — fp32 score-weighted gather-sum back to token order.
+ * [PRL "Single-pass DeepEP local layout"] out[t] = sum_{j<k} w[t,j] *
+ * rows[dst_row[t*k+j]], accumulated in fp32 in slot order, rounded once to
+ * bf16. With topk_w == NULL the weights are 1: that is the permute's
+ * transpose (dx_t = sum_j dXp[dst_row]) used in backward.
+ *  rows [R_cap, d] bf16 in;  dst_row [T*k] int32;  topk_w [T, k] fp32 or NULL
+ *  out  [T, d] bf16 out
+ * ------------------------------------------------------------------------ */
+int moe_combine(const moe_bf16* rows, const int32_t* dst_row, const float* topk_w,
+                int64_t T, int k, int d, moe_bf16* out, moe_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * moe_expert_bwd — backward of the combine and of the experts.
+ * [PRL "Single-pass DeepEP local layout"] gathers in backward;
+ * [PRL "FP8 routed experts"] grouped dgrad and wgrad; [PRL "FP8 Mega MoE"]
+ * K-grouped wgrad; [PRL "dispatch.type = mega_moe"] gradient of the top-k
+ * weights. Steps:
+ *   combine transpose:  dyp[r] = w(p) * dy[t(p)] (0 on padding rows),
+ *                       d_topk_w[p] = <dy[t(p)], yp[r]>   (fp32, yp unscaled)
+ *   down dgrad:         dA = dyp . W_down[e]^T, and in the same epilogue
+ *                       dg = dA * U * silu'(G), du = dA * silu(G)
+ *   gate/up dgrad:      dxp = dg . W_gate[e]^T + du . W_up[e]^T  (one K = 2f sum)
+ *   K-grouped wgrad:    dW_down[e] = A_e^T . dyp_e, dW_gate[e] = Xp_e^T . dg_e,
+ *                       dW_up[e] = Xp_e^T . du_e   (an empty expert gets zeros)
+ *  dy [T, d] bf16; src_pair [R_cap], dst_row [T*k] int32; topk_w [T, k] fp32;
+ *  offsets [E+1]; xp, g, u, a, yp as written by moe_permute / moe_expert_fwd
+ *  (row_w == NULL); weights as in moe_expert_fwd.
+ *  Outputs: dyp [R_cap, d], dg, du [R_cap, f], dxp [R_cap, d] bf16 (row
+ *  buffers, caller-owned, may be reused after the call); d_topk_w [T, k]
+ *  fp32 (pairs dropped from the layout get no value); dw_gate, dw_up
+ *  [E, d, f], dw_down [E, f, d] bf16 (overwritten).
+ * ------------------------------------------------------------------------ */
+int moe_expert_bwd(const moe_bf16* dy, const int32_t* src_pair, const int32_t* dst_row,
+                   const float* topk_w, const int64_t* offsets,
+                   int64_t T, int k, int E, int d, int f, int64_t R_cap,
+                   const moe_bf16* xp, const moe_bf16* g, const moe_bf16* u,
+                   const moe_bf16* a, const moe_bf16* yp,
+                   const moe_bf16* w_gate, const moe_bf16* w_up, const moe_bf16* w_down,
+                   moe_bf16* dyp, moe_bf16* dg, moe_bf16* du, moe_bf16* dxp,
+                   float* d_topk_w, moe_bf16* dw_gate, moe_bf16* dw_up, moe_bf16* dw_down,
+                   moe_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * moe_route_bwd — backward of the router.
+ * [PRL "dispatch.type = mega_moe"] gradients for x through the top-k weights.
+ * dl_t,S_j = w_j (dw_j - sum_j' w_j' dw_j') on the selected experts (0
+ * elsewhere; the selection is piecewise constant); then
+ *   dx[t] += sum_j dl_t,j W_r[:, S_j]        (read-modify-write of bf16 dx,
+ *                                             sum in fp32)
+ *   dW_r[:, e] = sum over e's rows of dl * xp[row]   (fp32, fixed order)
+ *   dbias[e]   = sum over e's rows of dl             (fp32, fixed order)
+ *  d_topk_w, topk_w [T, k] fp32; topk_idx [T, k] int32; w_router [d, E] fp32;
+ *  offsets, src_pair, xp from moe_permute (with the same `align`).
+ *  dx_inout [T, d] bf16 (added to); dw_router [d, E] fp32 out; dbias [E]
+ *  fp32 out or NULL.
+ *  ws: moe_workspace_size(MOE_WS_ROUTE_BWD, ...) bytes, 256-byte aligned.
+ * ------------------------------------------------------------------------ */
+int moe_route_bwd(const float* d_topk_w, const float* topk_w, const int32_t* topk_idx,
+                  const float* w_router, const int64_t* offsets, const int32_t* src_pair,
+                  const moe_bf16* xp, int64_t T, int d, int E, int k, int align,
+                  moe_bf16* dx_inout, float* dw_router, float* dbias,
+                  void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Workspace sizes (bytes) for the calls that take `ws`. Any 256-byte-aligned
+ * device buffer of at least this size works; its contents need no
+ * initialisation and are scratch after the call.
+ * ------------------------------------------------------------------------ */
+#define MOE_WS_PERMUTE   1
+#define MOE_WS_ROUTE_BWD 2
+size_t moe_workspace_size(int which, int64_t T, int d, int E, int k, int align);
+
+/* Smallest valid R_cap: T*k + E*(align-1). */
+int64_t moe_row_capacity(int64_t T, int k, int E, int align);
+
+/* Synchronises `stream`, then reads and clears this device's status word.
+ * Returns MOE_OK or the first MOE_ERR_DEVICE_* a kernel raised since the
+ * last call (a CUDA error is reported as MOE_ERR_CUDA). */
+int moe_status(moe_stream_t stream);
+
+/* Human-readable name of a return code (static string). */
+const char* moe_status_str(int code);
+
+/* ------------------------------------------------------------------------
+ * Kernel timer (measurement only). moe_timer_start(kernel, n) makes the
+ * library record a CUDA event pair around each of the next n launches of
+ * `kernel` (one of MOE_KERNEL_*; a group id covers every launch of that
+ * step); moe_timer_read waits for them and returns the summed device time in
+ * ms and the number of launches timed. One timer at a time per process.
+ * Events are created in start and destroyed in read.
+ * ------------------------------------------------------------------------ */
+#define MOE_KERNEL_ROUTER_LOGITS 1
+#define MOE_KERNEL_TOPK          2
+#define MOE_KERNEL_PERMUTE       3
+#define MOE_KERNEL_GATEUP_FWD    4
+#define MOE_KERNEL_DOWN_FWD      5
+#define MOE_KERNEL_COMBINE       6
+#define MOE_KERNEL_COMBINE_BWD   7
+#define MOE_KERNEL_DOWN_DGRAD    8
+#define MOE_KERNEL_GATEUP_DGRAD  9
+#define MOE_KERNEL_WGRAD_DOWN    10
+#define MOE_KERNEL_WGRAD_GATEUP  11
+#define MOE_KERNEL_ROUTE_BWD     12
+int moe_timer_start(int kernel, int max_launches);
+int moe_timer_read(float* total_ms, int* launches);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_GB300_H */

@@ -1,0 +1,289 @@
+// api.cu — the C ABI declared in include/moe.h: argument checks, the
+// per-device status word, workspace sizes, the kernel timer, and the order
+// in which each entry point launches its kernels.
+#include <mutex>
+#include <vector>
+
+#include "common.cuh"
+#include "internal.h"
+
+// Per-device status word: kernels raise MOE_ERR_DEVICE_* into it.
+__device__ int g_moe_status;
+
+namespace moe {
+
+static constexpr int kMaxDevices = 64;
+
+int* device_status_ptr() {
+  static int* ptrs[kMaxDevices] = {};
+  static std::mutex mu;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!ptrs[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_moe_status) != cudaSuccess) return nullptr;
+    ptrs[dev] = static_cast<int*>(p);
+  }
+  return ptrs[dev];
+}
+
+int num_sms() {
+  static int sms[kMaxDevices] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 1;
+  if (!sms[dev]) {
+    int n = 0;
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    sms[dev] = n > 0 ? n : 1;
+  }
+  return sms[dev];
+}
+
+// ------------------------------------------------------------ kernel timer --
+struct Timer {
+  std::mutex mu;
+  int kernel = 0;
+  int cap = 0;
+  int count = 0;
+  std::vector<cudaEvent_t> start, stop;
+};
+static Timer g_timer;
+
+void timer_before(int kernel, cudaStream_t s) {
+  if (g_timer.kernel != kernel) return;
+  std::lock_guard<std::mutex> lock(g_timer.mu);
+  if (g_timer.kernel == kernel && g_timer.count < g_timer.cap)
+    cudaEventRecord(g_timer.start[g_timer.count], s);
+}
+void timer_after(int kernel, cudaStream_t s) {
+  if (g_timer.kernel != kernel) return;
+  std::lock_guard<std::mutex> lock(g_timer.mu);
+  if (g_timer.kernel == kernel && g_timer.count < g_timer.cap)
+    cudaEventRecord(g_timer.stop[g_timer.count++], s);
+}
+
+}  // namespace moe
+
+using namespace moe;
+
+static bool is_pow2(int v) { return v > 0 && (v & (v - 1)) == 0; }
+static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+static int cuda_code(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+extern "C" {
+
+int64_t moe_row_capacity(int64_t T, int k, int E, int align) {
+  return T * k + (int64_t)E * (align - 1);
+}
+
+size_t moe_workspace_size(int which, int64_t T, int d, int E, int k, int align) {
+  if (T < 0 || d <= 0 || E <= 0 || k <= 0) return 0;
+  switch (which) {
+    case MOE_WS_PERMUTE: return permute_ws_bytes(T, k, E);
+    case MOE_WS_ROUTE_BWD: return (align > 0) ? route_bwd_ws_bytes(T, d, E, k, align) : 0;
+    default: return 0;
+  }
+}
+
+const char* moe_status_str(int code) {
+  switch (code) {
+    case MOE_OK: return "MOE_OK";
+    case MOE_ERR_ARG: return "MOE_ERR_ARG: invalid argument";
+    case MOE_ERR_UNSUPPORTED: return "MOE_ERR_UNSUPPORTED: shape not supported by the kernels";
+    case MOE_ERR_CAPACITY: return "MOE_ERR_CAPACITY: R_cap below T*k + E*(align-1)";
+    case MOE_ERR_CUDA: return "MOE_ERR_CUDA: a CUDA call failed";
+    case MOE_ERR_DEVICE_INDEX: return "MOE_ERR_DEVICE_INDEX: expert id outside [0, E)";
+    case MOE_ERR_DEVICE_TIMEOUT: return "MOE_ERR_DEVICE_TIMEOUT: a bounded wait in a kernel gave up";
+    default: return "unknown moe status code";
+  }
+}
+
+int moe_status(moe_stream_t stream) {
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(s) != cudaSuccess) return MOE_ERR_CUDA;
+  int* st = device_status_ptr();
+  if (!st) return MOE_ERR_CUDA;
+  int v = 0;
+  if (cudaMemcpy(&v, st, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return MOE_ERR_CUDA;
+  if (v != 0) {
+    const int zero = 0;
+    if (cudaMemcpy(st, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess)
+      return MOE_ERR_CUDA;
+  }
+  return v;
+}
+
+int moe_timer_start(int kernel, int max_launches) {
+  if (kernel < MOE_KERNEL_ROUTER_LOGITS || kernel > MOE_KERNEL_ROUTE_BWD || max_launches <= 0)
+    return MOE_ERR_ARG;
+  std::lock_guard<std::mutex> lock(g_timer.mu);
+  if (g_timer.kernel != 0) return MOE_ERR_ARG;
+  g_timer.start.assign(max_launches, nullptr);
+  g_timer.stop.assign(max_launches, nullptr);
+  for (int i = 0; i < max_launches; ++i) {
+    if (cudaEventCreate(&g_timer.start[i]) != cudaSuccess ||
+        cudaEventCreate(&g_timer.stop[i]) != cudaSuccess)
+      return MOE_ERR_CUDA;
+  }
+  g_timer.cap = max_launches;
+  g_timer.count = 0;
+  g_timer.kernel = kernel;
+  return MOE_OK;
+}
+
+int moe_timer_read(float* total_ms, int* launches) {
+  if (!total_ms || !launches) return MOE_ERR_ARG;
+  std::lock_guard<std::mutex> lock(g_timer.mu);
+  if (g_timer.kernel == 0) return MOE_ERR_ARG;
+  int rc = MOE_OK;
+  float sum = 0.f;
+  for (int i = 0; i < g_timer.count; ++i) {
+    float ms = 0.f;
+    if (cudaEventSynchronize(g_timer.stop[i]) != cudaSuccess ||
+        cudaEventElapsedTime(&ms, g_timer.start[i], g_timer.stop[i]) != cudaSuccess)
+      rc = MOE_ERR_CUDA;
+    sum += ms;
+  }
+  *total_ms = sum;
+  *launches = g_timer.count;
+  for (int i = 0; i < g_timer.cap; ++i) {
+    if (g_timer.start[i]) cudaEventDestroy(g_timer.start[i]);
+    if (g_timer.stop[i]) cudaEventDestroy(g_timer.stop[i]);
+  }
+  g_timer.start.clear();
+  g_timer.stop.clear();
+  g_timer.kernel = 0;
+  g_timer.cap = g_timer.count = 0;
+  return rc;
+}
+
+int moe_route(const moe_bf16* x, const float* w_router, const float* bias,
+              const int32_t* forced_idx, int64_t T, int d, int E, int k, float* logits,
+              int32_t* topk_idx, float* topk_w, moe_stream_t stream) {
+  if (!x || !w_router || !logits || !topk_idx || !topk_w) return MOE_ERR_ARG;
+  if (T < 0 || d <= 0 || E <= 0 || k <= 0 || k > E) return MOE_ERR_ARG;
+  if (k > kMaxTopK || E > kMaxExperts || d % 8 != 0) return MOE_ERR_UNSUPPORTED;
+  if (!aligned16(x)) return MOE_ERR_ARG;
+  if (T == 0) return MOE_OK;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  int* st = device_status_ptr();
+  if (!st) return MOE_ERR_CUDA;
+  cudaError_t e = launch_router_logits(x, w_router, bias, T, d, E, logits, s);
+  if (e == cudaSuccess) e = launch_topk(logits, forced_idx, T, E, k, topk_idx, topk_w, st, s);
+  return cuda_code(e);
+}
+
+int moe_permute(const int32_t* topk_idx, int64_t T, int k, int E, int align, const moe_bf16* x,
+                int d, int64_t R_cap, int32_t* counts, int64_t* offsets, int32_t* dst_row,
+                int32_t* src_pair, moe_bf16* xp, void* ws, size_t ws_bytes,
+                moe_stream_t stream) {
+  if (!topk_idx || !x || !counts || !offsets || !dst_row || !src_pair || !xp) return MOE_ERR_ARG;
+  if (T < 0 || k <= 0 || E <= 0 || d <= 0 || k > E) return MOE_ERR_ARG;
+  if (!is_pow2(align) || align < 16 || align > 256) return MOE_ERR_ARG;
+  if (E > kMaxExperts || d % 8 != 0) return MOE_ERR_UNSUPPORTED;
+  if (R_cap < moe_row_capacity(T, k, E, align)) return MOE_ERR_CAPACITY;
+  if (R_cap >= ((int64_t)1 << 31) || T * k >= ((int64_t)1 << 31)) return MOE_ERR_UNSUPPORTED;
+  if (!aligned16(x) || !aligned16(xp)) return MOE_ERR_ARG;
+  const size_t need = permute_ws_bytes(T, k, E);
+  if (need > 0 && (!ws || ws_bytes < need)) return MOE_ERR_ARG;
+  int* st = device_status_ptr();
+  if (!st) return MOE_ERR_CUDA;
+  return cuda_code(launch_permute(topk_idx, T, k, E, align, x, d, R_cap, counts, offsets,
+                                  dst_row, src_pair, xp, ws, st,
+                                  reinterpret_cast<cudaStream_t>(stream)));
+}
+
+static int check_expert_dims(int E, int d, int f, int64_t R_cap) {
+  if (E <= 0 || d <= 0 || f <= 0 || R_cap <= 0) return MOE_ERR_ARG;
+  if (E > kMaxExperts || d % 8 != 0 || f % 8 != 0) return MOE_ERR_UNSUPPORTED;
+  if (R_cap >= ((int64_t)1 << 31)) return MOE_ERR_UNSUPPORTED;
+  return MOE_OK;
+}
+
+int moe_expert_fwd(const moe_bf16* xp, const int64_t* offsets, const float* row_w, int E, int d,
+                   int f, int64_t R_cap, const moe_bf16* w_gate, const moe_bf16* w_up,
+                   const moe_bf16* w_down, moe_bf16* g, moe_bf16* u, moe_bf16* a, moe_bf16* yp,
+                   moe_stream_t stream) {
+  if (!xp || !offsets || !w_gate || !w_up || !w_down || !g || !u || !a || !yp) return MOE_ERR_ARG;
+  int rc = check_expert_dims(E, d, f, R_cap);
+  if (rc) return rc;
+  for (const void* p : {(const void*)xp, (const void*)w_gate, (const void*)w_up,
+                        (const void*)w_down, (const void*)g, (const void*)u, (const void*)a,
+                        (const void*)yp})
+    if (!aligned16(p)) return MOE_ERR_ARG;
+  int* st = device_status_ptr();
+  if (!st) return MOE_ERR_CUDA;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  GroupedDims gd{offsets, E, d, f, R_cap};
+  cudaError_t e = launch_gateup_fwd(gd, xp, w_gate, w_up, g, u, a, st, s);
+  if (e == cudaSuccess) e = launch_down_fwd(gd, a, w_down, row_w, yp, st, s);
+  return cuda_code(e);
+}
+
+int moe_combine(const moe_bf16* rows, const int32_t* dst_row, const float* topk_w, int64_t T,
+                int k, int d, moe_bf16* out, moe_stream_t stream) {
+  if (!rows || !dst_row || !out) return MOE_ERR_ARG;
+  if (T < 0 || k <= 0 || d <= 0) return MOE_ERR_ARG;
+  if (k > kMaxTopK || d % 8 != 0) return MOE_ERR_UNSUPPORTED;
+  if (!aligned16(rows) || !aligned16(out)) return MOE_ERR_ARG;
+  if (T == 0) return MOE_OK;
+  return cuda_code(
+      launch_combine(rows, dst_row, topk_w, T, k, d, out, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int moe_expert_bwd(const moe_bf16* dy, const int32_t* src_pair, const int32_t* dst_row,
+                   const float* topk_w, const int64_t* offsets, int64_t T, int k, int E, int d,
+                   int f, int64_t R_cap, const moe_bf16* xp, const moe_bf16* g,
+                   const moe_bf16* u, const moe_bf16* a, const moe_bf16* yp,
+                   const moe_bf16* w_gate, const moe_bf16* w_up, const moe_bf16* w_down,
+                   moe_bf16* dyp, moe_bf16* dg, moe_bf16* du, moe_bf16* dxp, float* d_topk_w,
+                   moe_bf16* dw_gate, moe_bf16* dw_up, moe_bf16* dw_down, moe_stream_t stream) {
+  if (!dy || !src_pair || !dst_row || !topk_w || !offsets || !xp || !g || !u || !a || !yp ||
+      !w_gate || !w_up || !w_down || !dyp || !dg || !du || !dxp || !d_topk_w || !dw_gate ||
+      !dw_up || !dw_down)
+    return MOE_ERR_ARG;
+  if (T < 0 || k <= 0 || k > E) return MOE_ERR_ARG;
+  int rc = check_expert_dims(E, d, f, R_cap);
+  if (rc) return rc;
+  if (R_cap < T * k) return MOE_ERR_CAPACITY;
+  for (const void* p : {(const void*)dy, (const void*)xp, (const void*)g, (const void*)u,
+                        (const void*)a, (const void*)yp, (const void*)w_gate, (const void*)w_up,
+                        (const void*)w_down, (const void*)dyp, (const void*)dg, (const void*)du,
+                        (const void*)dxp, (const void*)dw_gate, (const void*)dw_up,
+                        (const void*)dw_down})
+    if (!aligned16(p)) return MOE_ERR_ARG;
+  int* st = device_status_ptr();
+  if (!st) return MOE_ERR_CUDA;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  GroupedDims gd{offsets, E, d, f, R_cap};
+  cudaError_t e = launch_combine_bwd(dy, yp, src_pair, topk_w, offsets, T, k, E, d, R_cap, dyp,
+                                     d_topk_w, s);
+  if (e == cudaSuccess) e = launch_down_dgrad(gd, dyp, w_down, g, u, dg, du, st, s);
+  if (e == cudaSuccess) e = launch_gateup_dgrad(gd, dg, du, w_gate, w_up, dxp, st, s);
+  if (e == cudaSuccess) e = launch_wgrad_down(gd, a, dyp, dw_down, st, s);
+  if (e == cudaSuccess) e = launch_wgrad_gateup(gd, xp, dg, du, dw_gate, dw_up, st, s);
+  return cuda_code(e);
+}
+
+int moe_route_bwd(const float* d_topk_w, const float* topk_w, const int32_t* topk_idx,
+                  const float* w_router, const int64_t* offsets, const int32_t* src_pair,
+                  const moe_bf16* xp, int64_t T, int d, int E, int k, int align,
+                  moe_bf16* dx_inout, float* dw_router, float* dbias, void* ws, size_t ws_bytes,
+                  moe_stream_t stream) {
+  if (!d_topk_w || !topk_w || !topk_idx || !w_router || !offsets || !src_pair || !xp ||
+      !dx_inout || !dw_router)
+    return MOE_ERR_ARG;
+  if (T < 0 || d <= 0 || E <= 0 || k <= 0 || k > E) return MOE_ERR_ARG;
+  if (!is_pow2(align) || align < 16 || align > 256) return MOE_ERR_ARG;
+  if (k > kMaxTopK || E > kMaxExperts || d % 8 != 0) return MOE_ERR_UNSUPPORTED;
+  if (moe_row_capacity(T, k, E, align) >= ((int64_t)1 << 31)) return MOE_ERR_UNSUPPORTED;
+  if (!aligned16(xp) || !aligned16(dx_inout)) return MOE_ERR_ARG;
+  const size_t need = route_bwd_ws_bytes(T, d, E, k, align);
+  if (!ws || ws_bytes < need || (reinterpret_cast<uintptr_t>(ws) & 255u)) return MOE_ERR_ARG;
+  return cuda_code(launch_route_bwd(d_topk_w, topk_w, topk_idx, w_router, offsets, src_pair, xp,
+                                    T, d, E, k, align, dx_inout, dw_router, dbias, ws,
+                                    reinterpret_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"

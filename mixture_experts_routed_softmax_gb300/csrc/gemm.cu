@@ -1,0 +1,646 @@
+// gemm.cu — grouped expert GEMMs on the 5th-generation tensor cores.
+//
+// Halo "Performance", §Levers that help: one grouped expert matmul instead of
+// a per-expert loop, with the GLU fused. prime-rl PR #3885 (DeepSeek-V4.1
+// Flash perf work), §Changes: grouped forward, dgrad and wgrad GEMMs ("FP8
+// routed experts"), the weight gradient as a K-grouped GEMM and the bf16
+// gate/up output kept for backward ("FP8 Mega MoE"), tasks ordered
+// expert-major so each expert's weights are read about once.
+//
+// One persistent, warp-specialised kernel template serves all six GEMMs:
+//   warp 0     TMA producer: tiles of A and B into a 4-stage shared-memory ring
+//   warp 1     MMA issuer: tcgen05.mma 128 x N x 16 (bf16 in, fp32 in tensor
+//              memory), two accumulator buffers so the epilogue of one tile
+//              overlaps the main loop of the next
+//   warp 2     tensor-memory allocator
+//   warps 4-7  epilogue: tcgen05.ld of the accumulator (one row per thread),
+//              the fused element-wise step, bf16 stores with row/col masks
+// Kinds:
+//   GateUpFwd    [G | U] = Xp . [W_gate[e] | W_up[e]]  (two accumulators),
+//                epilogue A = silu(G) * U, stores G, U, A       (M-grouped)
+//   DownFwd      Yp = A . W_down[e]  (optionally * row_w)       (M-grouped)
+//   DownDgrad    dA = dYp . W_down[e]^T, epilogue dG = dA*U*silu'(G),
+//                dU = dA*silu(G)                                (M-grouped)
+//   GateUpDgrad  dXp = dG . W_gate[e]^T + dU . W_up[e]^T (two K segments)
+//   WgradDown    dW_down[e] = A_e^T . dYp_e                     (K-grouped)
+//   WgradGateUp  dW_gate[e] = Xp_e^T . dG_e, dW_up[e] = Xp_e^T . dU_e
+// "M-grouped": expert e's output rows are its rows [offsets[e], offsets[e+1])
+// of the padded layout, cut into 128-row tiles (a tile may run past the group
+// end; those rows are computed and not stored). "K-grouped": the reduction
+// runs over expert e's rows, in 64-row steps; the last step issues only the
+// 16-row MMA slices inside the group (groups are multiples of 16 rows), and
+// an expert with no rows gets a zero tile.
+#include "common.cuh"
+#include "internal.h"
+
+#include <mutex>
+
+namespace moe {
+
+enum class Kind { GateUpFwd, DownFwd, DownDgrad, GateUpDgrad, WgradDown, WgradGateUp };
+
+template <Kind K>
+struct Tr {
+  static constexpr bool dual = (K == Kind::GateUpFwd || K == Kind::WgradGateUp);
+  static constexpr bool two_seg = (K == Kind::GateUpDgrad);
+  static constexpr bool kgrouped = (K == Kind::WgradDown || K == Kind::WgradGateUp);
+  static constexpr bool a_mn = kgrouped;                                   // A is M-contiguous
+  static constexpr bool b_mn = (K == Kind::GateUpFwd || K == Kind::DownFwd || kgrouped);
+  static constexpr int BN = dual ? 128 : 256;                              // per accumulator
+  static constexpr int kernel_id =
+      K == Kind::GateUpFwd ? MOE_KERNEL_GATEUP_FWD
+      : K == Kind::DownFwd ? MOE_KERNEL_DOWN_FWD
+      : K == Kind::DownDgrad ? MOE_KERNEL_DOWN_DGRAD
+      : K == Kind::GateUpDgrad ? MOE_KERNEL_GATEUP_DGRAD
+      : K == Kind::WgradDown ? MOE_KERNEL_WGRAD_DOWN
+                             : MOE_KERNEL_WGRAD_GATEUP;
+};
+
+constexpr int BM = 128;            // tile rows (TMEM lanes)
+constexpr int BK = 64;             // k per stage: one 128-byte swizzle atom of bf16
+constexpr int kStages = 4;
+constexpr int kABytes = BM * BK * 2;                      // 16 KiB
+constexpr int kStageBytes = 3 * kABytes;                  // 48 KiB: A + 32 KiB of B
+constexpr int kTmemCols = 512;                            // 2 accumulator buffers x 256 columns
+constexpr int kThreads = 256;
+constexpr int kSmemBytes = kStages * kStageBytes + 1024 /*bars*/ + 4 * (kMaxExperts + 1) + 1024;
+
+struct GemmArgs {
+  const int64_t* offsets;
+  int E;
+  int M, N;        // K-grouped: per-expert output is M x N. M-grouped: N output columns
+  int nk_seg;      // M-grouped: k-steps per K segment
+  int64_t R_cap;
+  moe_bf16* out0;
+  moe_bf16* out1;
+  moe_bf16* out2;
+  const moe_bf16* in0;
+  const moe_bf16* in1;
+  const float* row_w;
+  int* status;
+};
+
+struct TileInfo {
+  int e;
+  int64_t m0;       // first output row (M-grouped: row of the layout; K-grouped: row of dW[e])
+  int n0;
+  int nk;           // k-steps
+  int64_t row_end;  // M-grouped: end of the expert's group; K-grouped: group length (rows)
+  int64_t kbeg;     // K-grouped: first row of the group
+};
+
+template <Kind K>
+__device__ __forceinline__ void decode_tile(int tile, const GemmArgs& a, const int* tstart,
+                                            int nN, TileInfo& ti) {
+  using T = Tr<K>;
+  const int nt = tile % nN;
+  const int mt = tile / nN;
+  ti.n0 = nt * T::BN;
+  if constexpr (T::kgrouped) {
+    const int nM = (a.M + BM - 1) / BM;
+    ti.e = mt / nM;
+    ti.m0 = (int64_t)(mt % nM) * BM;
+    ti.kbeg = a.offsets[ti.e];
+    ti.row_end = a.offsets[ti.e + 1] - ti.kbeg;
+    ti.nk = (int)((ti.row_end + BK - 1) / BK);
+  } else {
+    int lo = 0, hi = a.E;  // largest e with tstart[e] <= mt
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (tstart[mid] <= mt) lo = mid; else hi = mid;
+    }
+    ti.e = lo;
+    ti.m0 = a.offsets[lo] + (int64_t)(mt - tstart[lo]) * BM;
+    ti.row_end = a.offsets[lo + 1];
+    ti.kbeg = 0;
+    ti.nk = a.nk_seg * (T::two_seg ? 2 : 1);
+  }
+}
+
+// bounded wait used on the way out: ignores the abort flag, still time-limited
+__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, int* status) {
+  volatile int never = 0;
+  mbar_wait_bounded(bar, parity, &never, status);
+}
+
+template <Kind K>
+__global__ void __launch_bounds__(kThreads, 1)
+    grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA0,
+                        const __grid_constant__ CUtensorMap mapA1,
+                        const __grid_constant__ CUtensorMap mapB0,
+                        const __grid_constant__ CUtensorMap mapB1, const GemmArgs args) {
+  using T = Tr<K>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~(uintptr_t)1023);
+  const uint32_t s_base = smem_u32(smem);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kStages * kStageBytes);
+  // bars: full[kStages], empty[kStages], tfull[2], tempty[2], drain
+  const uint32_t bar0 = smem_u32(bars);
+  auto full_bar = [&](int s) { return bar0 + 8u * s; };
+  auto empty_bar = [&](int s) { return bar0 + 8u * (kStages + s); };
+  auto tfull_bar = [&](int b) { return bar0 + 8u * (2 * kStages + b); };
+  auto tempty_bar = [&](int b) { return bar0 + 8u * (2 * kStages + 2 + b); };
+  const uint32_t drain_bar = bar0 + 8u * (2 * kStages + 4);
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bars + 2 * kStages + 5);
+  volatile int* s_abort = reinterpret_cast<volatile int*>(s_tmem + 1);
+  int* tstart = reinterpret_cast<int*>(smem + kStages * kStageBytes + 1024);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(tfull_bar(b), 1);
+      mbar_init(tempty_bar(b), 4);
+    }
+    mbar_init(drain_bar, 1);
+    *s_abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&mapA0);
+    tma_prefetch_desc(&mapB0);
+    if (T::two_seg) tma_prefetch_desc(&mapA1);
+    if (T::dual || T::two_seg) tma_prefetch_desc(&mapB1);
+  }
+  if (warp == 2) {
+    tmem_alloc(smem_u32(s_tmem), kTmemCols);
+    tmem_relinquish();
+  }
+  // M-grouped tile table: tstart[e] = sum_{e'<e} ceil(L_e' / BM)
+  if constexpr (!T::kgrouped) {
+    for (int e = threadIdx.x; e < args.E; e += kThreads) {
+      const int64_t L = args.offsets[e + 1] - args.offsets[e];
+      tstart[e + 1] = (int)((L + BM - 1) / BM);
+    }
+    __syncthreads();
+    if (warp == 3) {
+      int run = 0;
+      for (int b = 0; b < args.E; b += 32) {
+        const int e = b + lane;
+        int v = (e < args.E) ? tstart[e + 1] : 0;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+          const int o = __shfl_up_sync(0xFFFFFFFFu, v, off);
+          if (lane >= off) v += o;
+        }
+        if (e < args.E) tstart[e + 1] = run + v;
+        run += __shfl_sync(0xFFFFFFFFu, v, 31);
+      }
+      if (lane == 0) tstart[0] = 0;
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *s_tmem;
+
+  const int nN = (args.N + T::BN - 1) / T::BN;
+  int total;
+  if constexpr (T::kgrouped) {
+    total = args.E * ((args.M + BM - 1) / BM) * nN;
+  } else {
+    total = tstart[args.E] * nN;
+  }
+  constexpr uint32_t kIdesc = idesc_bf16(BM, T::BN, T::a_mn ? 1 : 0, T::b_mn ? 1 : 0);
+  constexpr uint32_t kBBytes = (uint32_t)T::BN * BK * 2;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ------------------------------------------------------ producer --
+      int stage = 0;
+      uint32_t phase = 0;
+      int fills = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+        TileInfo ti;
+        decode_tile<K>(tile, args, tstart, nN, ti);
+        for (int ks = 0; ks < ti.nk; ++ks) {
+          if (!mbar_wait_bounded(empty_bar(stage), phase ^ 1u, s_abort, args.status)) {
+            ok = false;
+            break;
+          }
+          const uint32_t fb = full_bar(stage);
+          const uint32_t sA = s_base + stage * kStageBytes;
+          const uint32_t sB0 = sA + kABytes;
+          const uint32_t sB1 = sB0 + kBBytes;
+          mbar_arrive_expect_tx(fb, kStageBytes);
+          if constexpr (T::kgrouped) {
+            const int row0 = (int)(ti.kbeg + (int64_t)ks * BK);
+#pragma unroll
+            for (int i = 0; i < BM / 64; ++i)
+              tma_load_2d(sA + i * (BK * 128), &mapA0, fb, (int)ti.m0 + 64 * i, row0);
+#pragma unroll
+            for (int j = 0; j < T::BN / 64; ++j) {
+              tma_load_2d(sB0 + j * (BK * 128), &mapB0, fb, ti.n0 + 64 * j, row0);
+              if constexpr (T::dual)
+                tma_load_2d(sB1 + j * (BK * 128), &mapB1, fb, ti.n0 + 64 * j, row0);
+            }
+          } else {
+            const int seg = (T::two_seg && ks >= args.nk_seg) ? 1 : 0;
+            const int kk = (ks - seg * args.nk_seg) * BK;
+            const void* mA = seg ? (const void*)&mapA1 : (const void*)&mapA0;
+            const void* mB = seg ? (const void*)&mapB1 : (const void*)&mapB0;
+            tma_load_2d(sA, mA, fb, kk, (int)ti.m0);
+            if constexpr (T::b_mn) {
+#pragma unroll
+              for (int j = 0; j < T::BN / 64; ++j) {
+                tma_load_3d(sB0 + j * (BK * 128), &mapB0, fb, ti.n0 + 64 * j, kk, ti.e);
+                if constexpr (T::dual)
+                  tma_load_3d(sB1 + j * (BK * 128), &mapB1, fb, ti.n0 + 64 * j, kk, ti.e);
+              }
+            } else {
+              tma_load_3d(sB0, mB, fb, kk, ti.n0, ti.e);
+            }
+          }
+          ++fills;
+          if (++stage == kStages) { stage = 0; phase ^= 1u; }
+        }
+      }
+      if (*s_abort) {
+        // let the copies already issued land before the CTA's shared memory goes away
+        const int outstanding = fills < kStages ? fills : kStages;
+        int st = stage;
+        uint32_t ph = phase;
+        for (int i = 0; i < outstanding; ++i) {
+          if (--st < 0) { st = kStages - 1; ph ^= 1u; }
+          drain_wait(full_bar(st), ph, args.status);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ---------------------------------------------------------- MMA --
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+        TileInfo ti;
+        decode_tile<K>(tile, args, tstart, nN, ti);
+        if (ti.nk == 0) continue;
+        if (!mbar_wait_bounded(tempty_bar(acc), acc_phase ^ 1u, s_abort, args.status)) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + (uint32_t)acc * 256u;
+        for (int ks = 0; ks < ti.nk; ++ks) {
+          if (!mbar_wait_bounded(full_bar(stage), phase, s_abort, args.status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sA = s_base + stage * kStageBytes;
+          const uint32_t sB0 = sA + kABytes;
+          const uint32_t sB1 = sB0 + kBBytes;
+          int nsub = BK / 16;
+          if constexpr (T::kgrouped) {
+            const int64_t left = ti.row_end - (int64_t)ks * BK;
+            if (left < BK) nsub = (int)(left / 16);
+          }
+          for (int kk = 0; kk < nsub; ++kk) {
+            const uint64_t ad = T::a_mn ? sdesc_sw128(sA + kk * 2048, BK * 128, 1024)
+                                        : sdesc_sw128(sA + kk * 32, 16, 1024);
+            const uint64_t bd0 = T::b_mn ? sdesc_sw128(sB0 + kk * 2048, BK * 128, 1024)
+                                         : sdesc_sw128(sB0 + kk * 32, 16, 1024);
+            const uint32_t accum = (ks > 0 || kk > 0) ? 1u : 0u;
+            umma_bf16(d_tmem, ad, bd0, kIdesc, accum);
+            if constexpr (T::dual) {
+              const uint64_t bd1 = sdesc_sw128(sB1 + kk * 2048, BK * 128, 1024);
+              umma_bf16(d_tmem + 128u, ad, bd1, kIdesc, accum);
+            }
+          }
+          umma_commit(empty_bar(stage));
+          if (++stage == kStages) { stage = 0; phase ^= 1u; }
+        }
+        if (!ok) break;
+        umma_commit(tfull_bar(acc));
+        if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+      }
+      // every MMA issued by this thread has finished before tensor memory is freed
+      umma_commit(drain_bar);
+      drain_wait(drain_bar, 0, args.status);
+    }
+  } else if (warp >= 4) {
+    // ------------------------------------------------------------ epilogue --
+    const int wq = warp - 4;                   // TMEM lane quarter of this warp
+    const int rloc = wq * 32 + lane;           // accumulator row of this thread
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
+      TileInfo ti;
+      decode_tile<K>(tile, args, tstart, nN, ti);
+      const int64_t row = ti.m0 + rloc;
+      if constexpr (T::kgrouped) {
+        const bool row_ok = row < args.M;
+        const int64_t estride = (int64_t)args.M * args.N;
+        if (ti.nk == 0) {
+          if (row_ok) {
+            const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+            for (int c = 0; c < T::BN; c += 8) {
+              const int col = ti.n0 + c;
+              if (col >= args.N) break;
+              const int64_t o = ti.e * estride + row * args.N + col;
+              *reinterpret_cast<uint4*>(args.out0 + o) = z;
+              if constexpr (T::dual) *reinterpret_cast<uint4*>(args.out1 + o) = z;
+            }
+          }
+          continue;
+        }
+      }
+      if (!mbar_wait_bounded(tfull_bar(acc), acc_phase, s_abort, args.status)) break;
+      tc_fence_after();
+      const uint32_t t_row = tmem_base + ((uint32_t)(wq * 32) << 16) + (uint32_t)acc * 256u;
+
+      if constexpr (K == Kind::GateUpFwd) {
+        const bool row_ok = row < ti.row_end;
+#pragma unroll 1
+        for (int c = 0; c < T::BN; c += 32) {
+          uint32_t g[32], u[32];
+          tmem_ld32(t_row + c, g);
+          tmem_ld32(t_row + 128 + c, u);
+          tmem_ld_wait();
+          if (row_ok) {
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+              const int col = ti.n0 + c + 8 * v;
+              if (col < args.N) {
+                float gf[8], uf[8], af[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                  gf[i] = __uint_as_float(g[8 * v + i]);
+                  uf[i] = __uint_as_float(u[8 * v + i]);
+                  af[i] = gf[i] / (1.0f + __expf(-gf[i])) * uf[i];
+                }
+                const int64_t o = row * args.N + col;
+                *reinterpret_cast<uint4*>(args.out0 + o) = pack8(gf);
+                *reinterpret_cast<uint4*>(args.out1 + o) = pack8(uf);
+                *reinterpret_cast<uint4*>(args.out2 + o) = pack8(af);
+              }
+            }
+          }
+        }
+      } else if constexpr (K == Kind::WgradGateUp) {
+        const bool row_ok = row < args.M;
+        const int64_t base = ti.e * (int64_t)args.M * args.N + row * args.N;
+#pragma unroll 1
+        for (int c = 0; c < T::BN; c += 32) {
+          uint32_t g[32], u[32];
+          tmem_ld32(t_row + c, g);
+          tmem_ld32(t_row + 128 + c, u);
+          tmem_ld_wait();
+          if (row_ok) {
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+              const int col = ti.n0 + c + 8 * v;
+              if (col < args.N) {
+                float gf[8], uf[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                  gf[i] = __uint_as_float(g[8 * v + i]);
+                  uf[i] = __uint_as_float(u[8 * v + i]);
+                }
+                *reinterpret_cast<uint4*>(args.out0 + base + col) = pack8(gf);
+                *reinterpret_cast<uint4*>(args.out1 + base + col) = pack8(uf);
+              }
+            }
+          }
+        }
+      } else {
+        // single accumulator, 256 columns
+        bool row_ok;
+        int64_t base;
+        if constexpr (K == Kind::WgradDown) {
+          row_ok = row < args.M;
+          base = ti.e * (int64_t)args.M * args.N + row * args.N;
+        } else {
+          row_ok = row < ti.row_end;
+          base = row * args.N;
+        }
+        float scale = 1.0f;
+        if constexpr (K == Kind::DownFwd) {
+          if (args.row_w && row_ok) scale = args.row_w[row];
+        }
+#pragma unroll 1
+        for (int c = 0; c < T::BN; c += 32) {
+          uint32_t r[32];
+          tmem_ld32(t_row + c, r);
+          tmem_ld_wait();
+          if (!row_ok) continue;
+#pragma unroll
+          for (int v = 0; v < 4; ++v) {
+            const int col = ti.n0 + c + 8 * v;
+            if (col >= args.N) continue;
+            float f[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) f[i] = __uint_as_float(r[8 * v + i]);
+            if constexpr (K == Kind::DownDgrad) {
+              float gf[8], uf[8], dg[8], du[8];
+              unpack8(*reinterpret_cast<const uint4*>(args.in0 + base + col), gf);
+              unpack8(*reinterpret_cast<const uint4*>(args.in1 + base + col), uf);
+#pragma unroll
+              for (int i = 0; i < 8; ++i) {
+                const float sg = 1.0f / (1.0f + __expf(-gf[i]));
+                dg[i] = f[i] * uf[i] * (sg * (1.0f + gf[i] * (1.0f - sg)));
+                du[i] = f[i] * gf[i] * sg;
+              }
+              *reinterpret_cast<uint4*>(args.out0 + base + col) = pack8(dg);
+              *reinterpret_cast<uint4*>(args.out1 + base + col) = pack8(du);
+            } else {
+              if constexpr (K == Kind::DownFwd) {
+#pragma unroll
+                for (int i = 0; i < 8; ++i) f[i] *= scale;
+              }
+              *reinterpret_cast<uint4*>(args.out0 + base + col) = pack8(f);
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(tempty_bar(acc));
+      if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 2) tmem_dealloc(tmem_base, kTmemCols);
+}
+
+// ------------------------------------------------------------------ host --
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// 2-D bf16 map over a row-major [outer, inner] matrix, box [box_outer, 64], 128-byte swizzle
+static bool map2d(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer,
+                  uint32_t box_outer) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {inner * 2};
+  cuuint32_t box[2] = {64, box_outer};
+  cuuint32_t es[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box,
+            es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// 3-D bf16 map over [E, d1, d0] (d0 innermost), box [1, box1, 64]
+static bool map3d(CUtensorMap* m, const void* ptr, uint64_t d0, uint64_t d1, uint64_t E,
+                  uint32_t box1) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {d0, d1, E};
+  cuuint64_t strides[2] = {d0 * 2, d0 * d1 * 2};
+  cuuint32_t box[3] = {64, box1, 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box,
+            es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <Kind K>
+static cudaError_t launch_kind(const CUtensorMap& a0, const CUtensorMap& a1,
+                               const CUtensorMap& b0, const CUtensorMap& b1, const GemmArgs& args,
+                               int64_t tiles_upper, cudaStream_t s) {
+  static std::once_flag once;
+  static cudaError_t attr_err = cudaSuccess;
+  std::call_once(once, [] {
+    attr_err = cudaFuncSetAttribute(grouped_gemm_kernel<K>,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  });
+  if (attr_err != cudaSuccess) return attr_err;
+  int64_t grid = num_sms();
+  if (tiles_upper < grid) grid = tiles_upper;
+  if (grid < 1) grid = 1;
+  timer_before(Tr<K>::kernel_id, s);
+  grouped_gemm_kernel<K><<<(unsigned)grid, kThreads, kSmemBytes, s>>>(a0, a1, b0, b1, args);
+  timer_after(Tr<K>::kernel_id, s);
+  return cudaGetLastError();
+}
+
+static GemmArgs base_args(const GroupedDims& g, int* status) {
+  GemmArgs a{};
+  a.offsets = g.offsets;
+  a.E = g.E;
+  a.R_cap = g.R_cap;
+  a.status = status;
+  return a;
+}
+
+static int64_t mgrouped_tiles_upper(const GroupedDims& g, int N, int BN) {
+  return ((g.R_cap + BM - 1) / BM + g.E) * ((N + BN - 1) / BN);
+}
+
+cudaError_t launch_gateup_fwd(const GroupedDims& g, const moe_bf16* xp, const moe_bf16* w_gate,
+                              const moe_bf16* w_up, moe_bf16* G, moe_bf16* U, moe_bf16* A,
+                              int* status, cudaStream_t s) {
+  CUtensorMap a0, b0, b1;
+  if (!map2d(&a0, xp, g.d, g.R_cap, BM) || !map3d(&b0, w_gate, g.f, g.d, g.E, BK) ||
+      !map3d(&b1, w_up, g.f, g.d, g.E, BK))
+    return cudaErrorInvalidValue;
+  GemmArgs a = base_args(g, status);
+  a.N = g.f;
+  a.nk_seg = (g.d + BK - 1) / BK;
+  a.out0 = G; a.out1 = U; a.out2 = A;
+  return launch_kind<Kind::GateUpFwd>(a0, a0, b0, b1, a, mgrouped_tiles_upper(g, g.f, 128), s);
+}
+
+cudaError_t launch_down_fwd(const GroupedDims& g, const moe_bf16* A, const moe_bf16* w_down,
+                            const float* row_w, moe_bf16* yp, int* status, cudaStream_t s) {
+  CUtensorMap a0, b0;
+  if (!map2d(&a0, A, g.f, g.R_cap, BM) || !map3d(&b0, w_down, g.d, g.f, g.E, BK))
+    return cudaErrorInvalidValue;
+  GemmArgs a = base_args(g, status);
+  a.N = g.d;
+  a.nk_seg = (g.f + BK - 1) / BK;
+  a.out0 = yp;
+  a.row_w = row_w;
+  return launch_kind<Kind::DownFwd>(a0, a0, b0, b0, a, mgrouped_tiles_upper(g, g.d, 256), s);
+}
+
+cudaError_t launch_down_dgrad(const GroupedDims& g, const moe_bf16* dyp, const moe_bf16* w_down,
+                              const moe_bf16* G, const moe_bf16* U, moe_bf16* dG, moe_bf16* dU,
+                              int* status, cudaStream_t s) {
+  CUtensorMap a0, b0;
+  // dA[r, c] = sum_j dyp[r, j] W_down[e][c, j]: B is W_down[e] read as [N = f rows, K = d]
+  if (!map2d(&a0, dyp, g.d, g.R_cap, BM) || !map3d(&b0, w_down, g.d, g.f, g.E, 256))
+    return cudaErrorInvalidValue;
+  GemmArgs a = base_args(g, status);
+  a.N = g.f;
+  a.nk_seg = (g.d + BK - 1) / BK;
+  a.in0 = G; a.in1 = U;
+  a.out0 = dG; a.out1 = dU;
+  return launch_kind<Kind::DownDgrad>(a0, a0, b0, b0, a, mgrouped_tiles_upper(g, g.f, 256), s);
+}
+
+cudaError_t launch_gateup_dgrad(const GroupedDims& g, const moe_bf16* dG, const moe_bf16* dU,
+                                const moe_bf16* w_gate, const moe_bf16* w_up, moe_bf16* dxp,
+                                int* status, cudaStream_t s) {
+  CUtensorMap a0, a1, b0, b1;
+  // dXp[r, i] = sum_c dG[r, c] W_gate[e][i, c] + dU[r, c] W_up[e][i, c]:
+  // B is W_gate[e] / W_up[e] read as [N = d rows, K = f]
+  if (!map2d(&a0, dG, g.f, g.R_cap, BM) || !map2d(&a1, dU, g.f, g.R_cap, BM) ||
+      !map3d(&b0, w_gate, g.f, g.d, g.E, 256) || !map3d(&b1, w_up, g.f, g.d, g.E, 256))
+    return cudaErrorInvalidValue;
+  GemmArgs a = base_args(g, status);
+  a.N = g.d;
+  a.nk_seg = (g.f + BK - 1) / BK;
+  a.out0 = dxp;
+  return launch_kind<Kind::GateUpDgrad>(a0, a1, b0, b1, a, mgrouped_tiles_upper(g, g.d, 256), s);
+}
+
+cudaError_t launch_wgrad_down(const GroupedDims& g, const moe_bf16* A, const moe_bf16* dyp,
+                              moe_bf16* dw_down, int* status, cudaStream_t s) {
+  CUtensorMap a0, b0;
+  // dW_down[e] (f x d) = A_e^T . dYp_e: A read as [K = rows, M = f], B as [K = rows, N = d]
+  if (!map2d(&a0, A, g.f, g.R_cap, BK) || !map2d(&b0, dyp, g.d, g.R_cap, BK))
+    return cudaErrorInvalidValue;
+  GemmArgs a = base_args(g, status);
+  a.M = g.f;
+  a.N = g.d;
+  a.out0 = dw_down;
+  const int64_t tiles = (int64_t)g.E * ((g.f + BM - 1) / BM) * ((g.d + 255) / 256);
+  return launch_kind<Kind::WgradDown>(a0, a0, b0, b0, a, tiles, s);
+}
+
+cudaError_t launch_wgrad_gateup(const GroupedDims& g, const moe_bf16* xp, const moe_bf16* dG,
+                                const moe_bf16* dU, moe_bf16* dw_gate, moe_bf16* dw_up,
+                                int* status, cudaStream_t s) {
+  CUtensorMap a0, b0, b1;
+  // dW_gate[e] (d x f) = Xp_e^T . dG_e: A read as [K = rows, M = d], B as [K = rows, N = f]
+  if (!map2d(&a0, xp, g.d, g.R_cap, BK) || !map2d(&b0, dG, g.f, g.R_cap, BK) ||
+      !map2d(&b1, dU, g.f, g.R_cap, BK))
+    return cudaErrorInvalidValue;
+  GemmArgs a = base_args(g, status);
+  a.M = g.d;
+  a.N = g.f;
+  a.out0 = dw_gate;
+  a.out1 = dw_up;
+  const int64_t tiles = (int64_t)g.E * ((g.d + BM - 1) / BM) * ((g.f + 127) / 128);
+  return launch_kind<Kind::WgradGateUp>(a0, a0, b0, b1, a, tiles, s);
+}
+
+}  // namespace moe

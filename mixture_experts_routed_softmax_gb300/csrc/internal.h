@@ -1,0 +1,70 @@
+// internal.h — host-side launchers of the kernels, called by the C ABI in
+// api.cu after it has checked the arguments. Each launcher enqueues work on
+// `s` and returns the cudaError_t of its launches.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/moe.h"
+
+namespace moe {
+
+// Kernel timer hooks (api.cu): no-ops unless moe_timer_start armed `kernel`.
+void timer_before(int kernel, cudaStream_t s);
+void timer_after(int kernel, cudaStream_t s);
+// The per-device status word kernels raise errors into.
+int* device_status_ptr();
+int num_sms();
+
+// route.cu
+cudaError_t launch_router_logits(const moe_bf16* x, const float* w_router, const float* bias,
+                                 int64_t T, int d, int E, float* logits, cudaStream_t s);
+cudaError_t launch_topk(const float* logits, const int32_t* forced_idx, int64_t T, int E, int k,
+                        int32_t* topk_idx, float* topk_w, int* status, cudaStream_t s);
+size_t route_bwd_ws_bytes(int64_t T, int d, int E, int k, int align);
+cudaError_t launch_route_bwd(const float* d_topk_w, const float* topk_w, const int32_t* topk_idx,
+                             const float* w_router, const int64_t* offsets,
+                             const int32_t* src_pair, const moe_bf16* xp, int64_t T, int d, int E,
+                             int k, int align, moe_bf16* dx_inout, float* dw_router, float* dbias,
+                             void* ws, cudaStream_t s);
+
+// permute.cu
+size_t permute_ws_bytes(int64_t T, int k, int E);
+cudaError_t launch_permute(const int32_t* topk_idx, int64_t T, int k, int E, int align,
+                           const moe_bf16* x, int d, int64_t R_cap, int32_t* counts,
+                           int64_t* offsets, int32_t* dst_row, int32_t* src_pair, moe_bf16* xp,
+                           void* ws, int* status, cudaStream_t s);
+
+// combine.cu
+cudaError_t launch_combine(const moe_bf16* rows, const int32_t* dst_row, const float* topk_w,
+                           int64_t T, int k, int d, moe_bf16* out, cudaStream_t s);
+cudaError_t launch_combine_bwd(const moe_bf16* dy, const moe_bf16* yp, const int32_t* src_pair,
+                               const float* topk_w, const int64_t* offsets, int64_t T, int k,
+                               int E, int d, int64_t R_cap, moe_bf16* dyp, float* d_topk_w,
+                               cudaStream_t s);
+
+// gemm.cu (tcgen05 grouped GEMMs)
+struct GroupedDims {
+  const int64_t* offsets;
+  int E, d, f;
+  int64_t R_cap;
+};
+cudaError_t launch_gateup_fwd(const GroupedDims& g, const moe_bf16* xp, const moe_bf16* w_gate,
+                              const moe_bf16* w_up, moe_bf16* G, moe_bf16* U, moe_bf16* A,
+                              int* status, cudaStream_t s);
+cudaError_t launch_down_fwd(const GroupedDims& g, const moe_bf16* A, const moe_bf16* w_down,
+                            const float* row_w, moe_bf16* yp, int* status, cudaStream_t s);
+cudaError_t launch_down_dgrad(const GroupedDims& g, const moe_bf16* dyp, const moe_bf16* w_down,
+                              const moe_bf16* G, const moe_bf16* U, moe_bf16* dG, moe_bf16* dU,
+                              int* status, cudaStream_t s);
+cudaError_t launch_gateup_dgrad(const GroupedDims& g, const moe_bf16* dG, const moe_bf16* dU,
+                                const moe_bf16* w_gate, const moe_bf16* w_up, moe_bf16* dxp,
+                                int* status, cudaStream_t s);
+cudaError_t launch_wgrad_down(const GroupedDims& g, const moe_bf16* A, const moe_bf16* dyp,
+                              moe_bf16* dw_down, int* status, cudaStream_t s);
+cudaError_t launch_wgrad_gateup(const GroupedDims& g, const moe_bf16* xp, const moe_bf16* dG,
+                                const moe_bf16* dU, moe_bf16* dw_gate, moe_bf16* dw_up,
+                                int* status, cudaStream_t s);
+
+}  // namespace moe

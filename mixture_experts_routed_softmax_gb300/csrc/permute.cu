@@ -1,0 +1,221 @@
+// permute.cu — the padded expert-grouped layout, built without atomics, and
+// the single gather of token copies into it.
+//
+// Halo "Performance", §Levers that help: the atomic-free expert permute.
+// prime-rl PR #3885 (DeepSeek-V4.1 Flash perf work), §Changes, "Single-pass
+// DeepEP local layout": one gather into the padded expert-grouped layout
+// instead of several full copies of the routed activations.
+//
+// Four kernels, all deterministic:
+//   hist    per block of 4096 pairs: per-warp expert histograms built with
+//           warp match (__match_any_sync) — the leader lane of each expert
+//           group adds the group's size, so no two lanes ever write the same
+//           counter; warp-local ranks are kept per pair.
+//   scan    one CTA: exclusive scan over blocks for each expert (n_e and each
+//           block's base), the padded sizes ceil(n_e/align)*align and their
+//           exclusive scan over experts (the 64-bit offsets).
+//   scatter dst_row[p] = offsets[e] + block base + rank; src_pair[dst] = p.
+//   gather  xp[r] = x[src_pair[r] / k] for real rows, zeros for padding rows.
+// Pair p's rank inside its expert is therefore its rank in ascending p.
+#include "common.cuh"
+#include "internal.h"
+
+namespace moe {
+
+constexpr int kHistWarps = 16;
+constexpr int kHistSteps = 8;
+constexpr int kHistChunk = kHistWarps * 32 * kHistSteps;   // pairs per block
+
+static inline size_t al256(size_t b) { return (b + 255) & ~(size_t)255; }
+
+static inline int64_t hist_blocks(int64_t P) { return (P + kHistChunk - 1) / kHistChunk; }
+
+size_t permute_ws_bytes(int64_t T, int k, int E) {
+  const int64_t P = T * k;
+  return al256((size_t)hist_blocks(P) * E * 4) + al256((size_t)P * 4);
+}
+
+__device__ __forceinline__ int valid_expert(const int32_t* idx, int64_t p, int64_t P, int E,
+                                            int* status) {
+  if (p >= P) return -1;
+  const int e = idx[p];
+  if (e < 0 || e >= E) {
+    raise_status(status, MOE_ERR_DEVICE_INDEX);
+    return -1;
+  }
+  return e;
+}
+
+__global__ void __launch_bounds__(kHistWarps * 32) permute_hist_kernel(
+    const int32_t* __restrict__ idx, int64_t P, int E, int32_t* __restrict__ blk_count,
+    int32_t* __restrict__ rank_in_blk, int* status) {
+  extern __shared__ int32_t hist[];   // [kHistWarps][E]
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  for (int i = threadIdx.x; i < kHistWarps * E; i += blockDim.x) hist[i] = 0;
+  __syncthreads();
+  const int64_t base = (int64_t)blockIdx.x * kHistChunk + (int64_t)w * 32 * kHistSteps;
+  int32_t* wh = hist + w * E;
+  const uint32_t lt_mask = (1u << lane) - 1u;
+#pragma unroll
+  for (int step = 0; step < kHistSteps; ++step) {
+    const int64_t p = base + step * 32 + lane;
+    const int e = valid_expert(idx, p, P, E, status);
+    const uint32_t same = __match_any_sync(0xFFFFFFFFu, e);
+    const int before = __popc(same & lt_mask);
+    const int cur = (e >= 0) ? wh[e] : 0;
+    __syncwarp();
+    if (e >= 0 && before == 0) wh[e] = cur + __popc(same);
+    __syncwarp();
+    if (p < P) rank_in_blk[p] = (e >= 0) ? cur + before : -1;
+  }
+  __syncthreads();
+  // each expert: exclusive scan over the warps, block total to global
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    int run = 0;
+#pragma unroll
+    for (int ww = 0; ww < kHistWarps; ++ww) {
+      const int c = hist[ww * E + e];
+      hist[ww * E + e] = run;
+      run += c;
+    }
+    blk_count[(int64_t)blockIdx.x * E + e] = run;
+  }
+  __syncthreads();
+  // warp-local rank -> rank inside the block
+#pragma unroll
+  for (int step = 0; step < kHistSteps; ++step) {
+    const int64_t p = base + step * 32 + lane;
+    if (p >= P) continue;
+    const int e = idx[p];
+    if (e < 0 || e >= E) continue;
+    rank_in_blk[p] += wh[e];
+  }
+}
+
+// One CTA of 1024 threads; thread e owns expert e.
+__global__ void __launch_bounds__(1024) permute_scan_kernel(int32_t* __restrict__ blk_count,
+                                                            int64_t nblk, int E, int align,
+                                                            int32_t* __restrict__ counts,
+                                                            int64_t* __restrict__ offsets) {
+  __shared__ int64_t warp_tot[32];
+  const int e = threadIdx.x;
+  const int lane = e & 31, w = e >> 5;
+  int64_t n = 0;
+  if (e < E) {
+    for (int64_t b = 0; b < nblk; ++b) {
+      const int32_t c = blk_count[b * E + e];
+      blk_count[b * E + e] = (int32_t)n;
+      n += c;
+    }
+  }
+  const int64_t padded = (e < E) ? ((n + align - 1) / align) * align : 0;
+  // block-wide exclusive scan of `padded`
+  int64_t incl = padded;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int64_t o = __shfl_up_sync(0xFFFFFFFFu, incl, off);
+    if (lane >= off) incl += o;
+  }
+  if (lane == 31) warp_tot[w] = incl;
+  __syncthreads();
+  if (w == 0) {
+    int64_t v = warp_tot[lane];
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int64_t o = __shfl_up_sync(0xFFFFFFFFu, v, off);
+      if (lane >= off) v += o;
+    }
+    warp_tot[lane] = v;   // inclusive over warps
+  }
+  __syncthreads();
+  const int64_t excl = incl - padded + (w > 0 ? warp_tot[w - 1] : 0);
+  if (e < E) {
+    counts[e] = (int32_t)n;
+    offsets[e] = excl;
+    for (int64_t b = 0; b < nblk; ++b) blk_count[b * E + e] += (int32_t)excl;
+  }
+  if (e == E - 1) offsets[E] = excl + padded;
+}
+
+__global__ void permute_scatter_kernel(const int32_t* __restrict__ idx, int64_t P, int E,
+                                       const int32_t* __restrict__ blk_base,
+                                       const int32_t* __restrict__ rank_in_blk,
+                                       int32_t* __restrict__ dst_row,
+                                       int32_t* __restrict__ src_pair) {
+  const int64_t p = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (p >= P) return;
+  const int e = idx[p];
+  if (e < 0 || e >= E) {
+    dst_row[p] = -1;
+    return;
+  }
+  const int32_t dst = blk_base[(p / kHistChunk) * E + e] + rank_in_blk[p];
+  dst_row[p] = dst;
+  src_pair[dst] = (int32_t)p;
+}
+
+__device__ __forceinline__ int expert_of_row_p(const int64_t* offsets, int E, int64_t r) {
+  int lo = 0, hi = E;
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (offsets[mid] <= r) lo = mid; else hi = mid;
+  }
+  return lo;
+}
+
+// one warp per row
+__global__ void __launch_bounds__(256) permute_gather_kernel(
+    const moe_bf16* __restrict__ x, int d, int k, const int64_t* __restrict__ offsets,
+    const int32_t* __restrict__ counts, int E, int64_t R_cap, int32_t* __restrict__ src_pair,
+    moe_bf16* __restrict__ xp) {
+  const int lane = threadIdx.x & 31;
+  const int64_t r = (int64_t)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
+  if (r >= R_cap) return;
+  const int64_t R_pad = offsets[E];
+  if (r >= R_pad) {
+    if (lane == 0) src_pair[r] = -1;
+    return;
+  }
+  const int e = expert_of_row_p(offsets, E, r);
+  const bool real = (r - offsets[e]) < (int64_t)counts[e];
+  uint4* dst = reinterpret_cast<uint4*>(xp + r * d);
+  const int nv = d / 8;
+  if (real) {
+    const int64_t t = src_pair[r] / k;
+    const uint4* src = reinterpret_cast<const uint4*>(x + t * d);
+    for (int v = lane; v < nv; v += 32) dst[v] = src[v];
+  } else {
+    if (lane == 0) src_pair[r] = -1;
+    for (int v = lane; v < nv; v += 32) dst[v] = make_uint4(0u, 0u, 0u, 0u);
+  }
+}
+
+cudaError_t launch_permute(const int32_t* topk_idx, int64_t T, int k, int E, int align,
+                           const moe_bf16* x, int d, int64_t R_cap, int32_t* counts,
+                           int64_t* offsets, int32_t* dst_row, int32_t* src_pair, moe_bf16* xp,
+                           void* ws, int* status, cudaStream_t s) {
+  const int64_t P = T * k;
+  const int64_t nblk = hist_blocks(P);
+  int32_t* blk_count = static_cast<int32_t*>(ws);
+  int32_t* rank_in_blk =
+      reinterpret_cast<int32_t*>(static_cast<char*>(ws) + al256((size_t)nblk * E * 4));
+  const size_t hist_smem = (size_t)kHistWarps * E * 4;
+  cudaError_t err = cudaFuncSetAttribute(permute_hist_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)hist_smem);
+  if (err != cudaSuccess) return err;
+  timer_before(MOE_KERNEL_PERMUTE, s);
+  if (P > 0)
+    permute_hist_kernel<<<(unsigned)nblk, kHistWarps * 32, hist_smem, s>>>(
+        topk_idx, P, E, blk_count, rank_in_blk, status);
+  permute_scan_kernel<<<1, 1024, 0, s>>>(blk_count, nblk, E, align, counts, offsets);
+  if (P > 0)
+    permute_scatter_kernel<<<(unsigned)((P + 255) / 256), 256, 0, s>>>(
+        topk_idx, P, E, blk_count, rank_in_blk, dst_row, src_pair);
+  permute_gather_kernel<<<(unsigned)((R_cap + 7) / 8), 256, 0, s>>>(x, d, k, offsets, counts, E,
+                                                                    R_cap, src_pair, xp);
+  timer_after(MOE_KERNEL_PERMUTE, s);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

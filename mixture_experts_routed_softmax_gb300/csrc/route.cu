@@ -1,0 +1,374 @@
+// route.cu — router: logits, top-k with renormalised softmax weights, and the
+// router backward.
+//
+// Routing over many experts with top-k selection is the setting of PocketLLM
+// "Qwen4-Exp Heterogeneous TP4 Performance", §Runtime architecture (512
+// routed experts, top-10), where the router is its own per-layer phase
+// (§Remaining prefill attribution). The formula (softmax over the experts,
+// keep the k largest, renormalise over them) is the plainest reading: the
+// full softmax denominator cancels, so selecting on the logits and taking
+// the softmax over the selected ones gives the same weights without ties
+// created by rounding of exp.
+#include "common.cuh"
+#include "internal.h"
+
+namespace moe {
+
+// ---------------------------------------------------------------------------
+// logits[T, E] = x[T, d] (bf16) . W_r[d, E] (fp32) + b, fp32 accumulation in
+// k order. A 64x64 output tile per CTA, 16-deep k slices staged in shared
+// memory, a 4x4 register micro-tile per thread.
+// ---------------------------------------------------------------------------
+constexpr int kRBM = 64, kRBN = 64, kRBK = 16;
+
+__global__ void __launch_bounds__(256) router_logits_kernel(const moe_bf16* __restrict__ x,
+                                                            const float* __restrict__ wr,
+                                                            const float* __restrict__ bias,
+                                                            int64_t T, int d, int E,
+                                                            float* __restrict__ logits) {
+  __shared__ float xs[kRBK][kRBM + 4];
+  __shared__ float ws[kRBK][kRBN + 4];
+  const int tid = threadIdx.x;
+  const int tx = tid % 16, ty = tid / 16;
+  const int64_t m0 = (int64_t)blockIdx.y * kRBM;
+  const int n0 = blockIdx.x * kRBN;
+  float acc[4][4] = {};
+  // loader coordinates: x tile 64 rows x 16 k (4 bf16 per thread); w tile 16 k x 64 cols
+  const int xr = tid / 4, xk = (tid % 4) * 4;
+  const int wk = tid / 16, wc = (tid % 16) * 4;
+  for (int k0 = 0; k0 < d; k0 += kRBK) {
+    {
+      const int64_t row = m0 + xr;
+      const int kk = k0 + xk;
+      float v[4] = {0.f, 0.f, 0.f, 0.f};
+      if (row < T && kk < d) {  // d is a multiple of 8, so the 4-group is whole
+        const uint2 raw = *reinterpret_cast<const uint2*>(x + row * d + kk);
+        v[0] = bf16_lo(raw.x); v[1] = bf16_hi(raw.x); v[2] = bf16_lo(raw.y); v[3] = bf16_hi(raw.y);
+      }
+#pragma unroll
+      for (int i = 0; i < 4; ++i) xs[xk + i][xr] = v[i];
+    }
+    {
+      const int kk = k0 + wk;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int c = n0 + wc + i;
+        ws[wk][wc + i] = (kk < d && c < E) ? wr[(int64_t)kk * E + c] : 0.f;
+      }
+    }
+    __syncthreads();
+#pragma unroll
+    for (int kk = 0; kk < kRBK; ++kk) {
+      float a[4], b[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) a[i] = xs[kk][ty * 4 + i];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) b[j] = ws[kk][tx * 4 + j];
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+    }
+    __syncthreads();
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int64_t row = m0 + ty * 4 + i;
+    if (row >= T) continue;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int c = n0 + tx * 4 + j;
+      if (c < E) logits[row * E + c] = acc[i][j] + (bias ? bias[c] : 0.f);
+    }
+  }
+}
+
+cudaError_t launch_router_logits(const moe_bf16* x, const float* w_router, const float* bias,
+                                 int64_t T, int d, int E, float* logits, cudaStream_t s) {
+  dim3 grid((E + kRBN - 1) / kRBN, (unsigned)((T + kRBM - 1) / kRBM));
+  timer_before(MOE_KERNEL_ROUTER_LOGITS, s);
+  router_logits_kernel<<<grid, 256, 0, s>>>(x, w_router, bias, T, d, E, logits);
+  timer_after(MOE_KERNEL_ROUTER_LOGITS, s);
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// Top-k and weights: one warp per token. Each lane keeps the logits of
+// experts lane, lane+32, ... in registers; k rounds of a warp arg-max pick the
+// slots in descending order (equal values: lower index first). Slot j's lane
+// then computes exp(l_j - l_0) and the warp sums them.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ bool ranks_above(float va, int ia, float vb, int ib) {
+  return va > vb || (va == vb && ia < ib);
+}
+
+__global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ logits,
+                                                   const int32_t* __restrict__ forced, int64_t T,
+                                                   int E, int k, int32_t* __restrict__ topk_idx,
+                                                   float* __restrict__ topk_w, int* status) {
+  const int lane = threadIdx.x & 31;
+  const int64_t t = (int64_t)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
+  if (t >= T) return;
+  const float* lrow = logits + t * E;
+  float my_v = -INFINITY;  // slot `lane`'s logit (lanes < k)
+  int my_i = 0;
+  bool valid = true;
+  if (forced) {
+    if (lane < k) {
+      my_i = forced[t * k + lane];
+      valid = (my_i >= 0 && my_i < E);
+      if (valid) my_v = lrow[my_i];
+      else raise_status(status, MOE_ERR_DEVICE_INDEX);
+    }
+  } else {
+    float v[kMaxExperts / 32];
+#pragma unroll
+    for (int i = 0; i < kMaxExperts / 32; ++i) {
+      const int e = lane + 32 * i;
+      v[i] = (e < E) ? lrow[e] : -INFINITY;
+    }
+    uint32_t taken = 0;
+    for (int j = 0; j < k; ++j) {
+      float bv = -INFINITY;
+      int bi = 0x7FFFFFFF;
+#pragma unroll
+      for (int i = 0; i < kMaxExperts / 32; ++i) {
+        const int e = lane + 32 * i;
+        if (e < E && !((taken >> i) & 1u) && ranks_above(v[i], e, bv, bi)) {
+          bv = v[i];
+          bi = e;
+        }
+      }
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) {
+        const float ov = __shfl_xor_sync(0xFFFFFFFFu, bv, off);
+        const int oi = __shfl_xor_sync(0xFFFFFFFFu, bi, off);
+        if (ranks_above(ov, oi, bv, bi)) { bv = ov; bi = oi; }
+      }
+      if (bi != 0x7FFFFFFF && (bi & 31) == lane) taken |= 1u << (bi >> 5);
+      if (lane == j) { my_v = bv; my_i = (bi == 0x7FFFFFFF) ? 0 : bi; }
+    }
+  }
+  // renormalised softmax over the k slots
+  float m = (lane < k && valid) ? my_v : -INFINITY;
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, off));
+  float ex = (lane < k && valid) ? expf(my_v - m) : 0.f;
+  float sum = ex;
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xFFFFFFFFu, sum, off);
+  if (lane < k) {
+    topk_idx[t * k + lane] = my_i;
+    topk_w[t * k + lane] = sum > 0.f ? ex / sum : 0.f;
+  }
+}
+
+cudaError_t launch_topk(const float* logits, const int32_t* forced_idx, int64_t T, int E, int k,
+                        int32_t* topk_idx, float* topk_w, int* status, cudaStream_t s) {
+  const int warps = 8;
+  dim3 grid((unsigned)((T + warps - 1) / warps));
+  timer_before(MOE_KERNEL_TOPK, s);
+  topk_kernel<<<grid, warps * 32, 0, s>>>(logits, forced_idx, T, E, k, topk_idx, topk_w, status);
+  timer_after(MOE_KERNEL_TOPK, s);
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// Router backward.
+//   dl_t,j = w_j (dw_j - sum_j' w_j' dw_j')  on the selected slots
+//   dx[t] += sum_j dl_t,j W_r[:, e_j]
+//   dW_r[:, e] = sum over e's rows of dl * xp[row];  db[e] = sum of dl
+// The last two are fixed-order two-phase sums: phase 1 sums each (128-row
+// block) n (expert group) segment of the padded layout into a partial row,
+// phase 2 adds each expert's partial rows in row order. No atomics.
+// ---------------------------------------------------------------------------
+constexpr int kRbRows = 128;   // rows of the padded layout per phase-1 CTA
+constexpr int kRbCols = 256;   // columns of d per CTA (128 threads x 2)
+
+static inline int seg_unit(int align) { return align < kRbRows ? align : kRbRows; }
+
+static inline size_t al256(size_t b) { return (b + 255) & ~(size_t)255; }
+
+size_t route_bwd_ws_bytes(int64_t T, int d, int E, int k, int align) {
+  const int64_t R_cap = T * k + (int64_t)E * (align - 1);
+  const int64_t slots = (R_cap + seg_unit(align) - 1) / seg_unit(align);
+  return al256((size_t)E * d * 4) + al256((size_t)T * k * 4) + al256((size_t)slots * d * 4) +
+         al256((size_t)slots * 4);
+}
+
+__global__ void transpose_f32_kernel(const float* __restrict__ in, int rows, int cols,
+                                     float* __restrict__ out) {
+  __shared__ float tile[32][33];
+  const int c = blockIdx.x * 32 + threadIdx.x;
+  for (int i = threadIdx.y; i < 32; i += 8) {
+    const int r = blockIdx.y * 32 + i;
+    tile[i][threadIdx.x] = (r < rows && c < cols) ? in[(int64_t)r * cols + c] : 0.f;
+  }
+  __syncthreads();
+  const int r2 = blockIdx.y * 32 + threadIdx.x;
+  for (int i = threadIdx.y; i < 32; i += 8) {
+    const int c2 = blockIdx.x * 32 + i;
+    if (c2 < cols && r2 < rows) out[(int64_t)c2 * rows + r2] = tile[threadIdx.x][i];
+  }
+}
+
+// one warp per token: dl for its k slots, and dx[t] += dl . W_r^T
+__global__ void __launch_bounds__(256) route_bwd_token_kernel(
+    const float* __restrict__ d_topk_w, const float* __restrict__ topk_w,
+    const int32_t* __restrict__ topk_idx, const float* __restrict__ wrT, int64_t T, int d, int E,
+    int k, float* __restrict__ dl_pair, moe_bf16* __restrict__ dx) {
+  const int lane = threadIdx.x & 31;
+  const int64_t t = (int64_t)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
+  if (t >= T) return;
+  float w = 0.f, dw = 0.f;
+  int e = -1;
+  if (lane < k) {
+    w = topk_w[t * k + lane];
+    dw = d_topk_w[t * k + lane];
+    e = topk_idx[t * k + lane];
+    if (e < 0 || e >= E) { e = -1; w = 0.f; dw = 0.f; }
+  }
+  float inner = w * dw;
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) inner += __shfl_xor_sync(0xFFFFFFFFu, inner, off);
+  const float dl = w * (dw - inner);
+  if (lane < k) dl_pair[t * k + lane] = dl;
+  moe_bf16* dxr = dx + t * d;
+  for (int c = lane * 8; c < d; c += 256) {
+    float acc[8];
+    unpack8(*reinterpret_cast<const uint4*>(dxr + c), acc);
+    float add[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    for (int j = 0; j < k; ++j) {
+      const float dlj = __shfl_sync(0xFFFFFFFFu, dl, j);
+      const int ej = __shfl_sync(0xFFFFFFFFu, e, j);
+      if (ej < 0) continue;
+      const float4 a = *reinterpret_cast<const float4*>(wrT + (int64_t)ej * d + c);
+      const float4 b = *reinterpret_cast<const float4*>(wrT + (int64_t)ej * d + c + 4);
+      add[0] = fmaf(dlj, a.x, add[0]); add[1] = fmaf(dlj, a.y, add[1]);
+      add[2] = fmaf(dlj, a.z, add[2]); add[3] = fmaf(dlj, a.w, add[3]);
+      add[4] = fmaf(dlj, b.x, add[4]); add[5] = fmaf(dlj, b.y, add[5]);
+      add[6] = fmaf(dlj, b.z, add[6]); add[7] = fmaf(dlj, b.w, add[7]);
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc[i] += add[i];
+    *reinterpret_cast<uint4*>(dxr + c) = pack8(acc);
+  }
+}
+
+__device__ __forceinline__ int expert_of_row(const int64_t* offsets, int E, int64_t r) {
+  // largest e with offsets[e] <= r (offsets non-decreasing, offsets[0] = 0)
+  int lo = 0, hi = E;  // answer in [lo, hi)
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (offsets[mid] <= r) lo = mid; else hi = mid;
+  }
+  return lo;
+}
+
+// phase 1: CTA (b, cb) sums rows [b*128, b*128+128) for columns [cb*256, +256),
+// one partial row per expert segment it meets; slot = segment start / unit.
+__global__ void __launch_bounds__(128) route_bwd_partial_kernel(
+    const int64_t* __restrict__ offsets, const int32_t* __restrict__ src_pair,
+    const moe_bf16* __restrict__ xp, const float* __restrict__ dl_pair, int E, int d, int unit,
+    float* __restrict__ part, float* __restrict__ part_db) {
+  __shared__ float s_dl[kRbRows];     // dl of each row's pair, 0 for padding rows
+  __shared__ int s_real[kRbRows];
+  const int64_t r_begin = (int64_t)blockIdx.x * kRbRows;
+  const int64_t R_pad = offsets[E];
+  if (r_begin >= R_pad) return;
+  const int64_t r_end = min(r_begin + kRbRows, R_pad);
+  {
+    const int64_t q = r_begin + threadIdx.x;
+    const int pr = (q < r_end) ? src_pair[q] : -1;
+    s_real[threadIdx.x] = pr >= 0;
+    s_dl[threadIdx.x] = pr >= 0 ? dl_pair[pr] : 0.f;
+  }
+  __syncthreads();
+  const int c = blockIdx.y * kRbCols + threadIdx.x * 2;
+  int64_t r = r_begin;
+  while (r < r_end) {
+    const int e = expert_of_row(offsets, E, r);
+    const int64_t seg_end = min(r_end, offsets[e + 1]);
+    const int64_t slot = r / unit;
+    float a0 = 0.f, a1 = 0.f, adb = 0.f;
+#pragma unroll 4
+    for (int64_t q = r; q < seg_end; ++q) {
+      const int i = (int)(q - r_begin);
+      if (!s_real[i]) continue;
+      const float dl = s_dl[i];
+      adb += dl;
+      if (c < d) {
+        const uint32_t v = *reinterpret_cast<const uint32_t*>(xp + q * d + c);
+        a0 = fmaf(dl, bf16_lo(v), a0);
+        a1 = fmaf(dl, bf16_hi(v), a1);
+      }
+    }
+    if (c < d) {
+      part[slot * d + c] = a0;
+      part[slot * d + c + 1] = a1;
+    }
+    if (blockIdx.y == 0 && threadIdx.x == 0) part_db[slot] = adb;
+    r = seg_end;
+  }
+}
+
+// phase 2: per expert, add its partial rows in row order.
+__global__ void __launch_bounds__(128) route_bwd_reduce_kernel(
+    const int64_t* __restrict__ offsets, const float* __restrict__ part,
+    const float* __restrict__ part_db, int E, int d, int unit, float* __restrict__ dw_router,
+    float* __restrict__ dbias) {
+  const int e = blockIdx.x;
+  const int c = blockIdx.y * kRbCols + threadIdx.x * 2;
+  const int64_t g0 = offsets[e], g1 = offsets[e + 1];
+  float a0 = 0.f, a1 = 0.f, adb = 0.f;
+  int64_t r = g0;
+  while (r < g1) {
+    const int64_t slot = r / unit;
+    if (c < d) {
+      a0 += part[slot * d + c];
+      a1 += part[slot * d + c + 1];
+    }
+    adb += part_db[slot];
+    r = min(g1, (r / kRbRows + 1) * kRbRows);  // next 128-row block boundary
+  }
+  if (c < d) {
+    dw_router[(int64_t)c * E + e] = a0;
+    dw_router[(int64_t)(c + 1) * E + e] = a1;
+  }
+  if (dbias && blockIdx.y == 0 && threadIdx.x == 0) dbias[e] = adb;
+}
+
+cudaError_t launch_route_bwd(const float* d_topk_w, const float* topk_w, const int32_t* topk_idx,
+                             const float* w_router, const int64_t* offsets,
+                             const int32_t* src_pair, const moe_bf16* xp, int64_t T, int d, int E,
+                             int k, int align, moe_bf16* dx_inout, float* dw_router, float* dbias,
+                             void* ws, cudaStream_t s) {
+  const int64_t R_cap = T * k + (int64_t)E * (align - 1);
+  const int unit = seg_unit(align);
+  char* p = static_cast<char*>(ws);
+  float* wrT = reinterpret_cast<float*>(p);
+  p += al256((size_t)E * d * 4);
+  float* dl_pair = reinterpret_cast<float*>(p);
+  p += al256((size_t)T * k * 4);
+  const int64_t slots = (R_cap + unit - 1) / unit;
+  float* part = reinterpret_cast<float*>(p);
+  p += al256((size_t)slots * d * 4);
+  float* part_db = reinterpret_cast<float*>(p);
+
+  timer_before(MOE_KERNEL_ROUTE_BWD, s);
+  transpose_f32_kernel<<<dim3((E + 31) / 32, (d + 31) / 32), dim3(32, 8), 0, s>>>(w_router, d, E,
+                                                                                  wrT);
+  if (T > 0)
+    route_bwd_token_kernel<<<(unsigned)((T + 7) / 8), 256, 0, s>>>(d_topk_w, topk_w, topk_idx,
+                                                                   wrT, T, d, E, k, dl_pair,
+                                                                   dx_inout);
+  const int cblocks = (d + kRbCols - 1) / kRbCols;
+  route_bwd_partial_kernel<<<dim3((unsigned)((R_cap + kRbRows - 1) / kRbRows), cblocks), 128, 0,
+                             s>>>(offsets, src_pair, xp, dl_pair, E, d, unit, part, part_db);
+  route_bwd_reduce_kernel<<<dim3(E, cblocks), 128, 0, s>>>(offsets, part, part_db, E, d, unit,
+                                                           dw_router, dbias);
+  timer_after(MOE_KERNEL_ROUTE_BWD, s);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,185 @@
+"""The routed MoE expert layer on one GPU, driven through the C ABI.
+
+PyTorch supplies device memory and the stream; every step of the layer runs
+in the library's kernels. Forward: moe_route -> moe_permute -> moe_expert_fwd
+-> moe_combine. Backward: moe_expert_bwd -> moe_combine (unweighted, the
+permute's transpose) -> moe_route_bwd.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass
+from typing import Optional
+
+import torch
+
+from . import _lib
+
+BF16 = torch.bfloat16
+
+
+def _p(t: Optional[torch.Tensor]):
+    return None if t is None else t.data_ptr()
+
+
+def _stream(stream: Optional[torch.cuda.Stream]) -> int:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+@dataclass
+class Buffers:
+    """Every device buffer one forward + backward of T tokens needs."""
+    T: int
+    R_cap: int
+    logits: torch.Tensor
+    topk_idx: torch.Tensor
+    topk_w: torch.Tensor
+    counts: torch.Tensor
+    offsets: torch.Tensor
+    dst_row: torch.Tensor
+    src_pair: torch.Tensor
+    xp: torch.Tensor
+    g: torch.Tensor
+    u: torch.Tensor
+    a: torch.Tensor
+    yp: torch.Tensor
+    y: torch.Tensor
+    ws_permute: torch.Tensor
+    # backward
+    dyp: Optional[torch.Tensor] = None
+    dg: Optional[torch.Tensor] = None
+    du: Optional[torch.Tensor] = None
+    dxp: Optional[torch.Tensor] = None
+    d_topk_w: Optional[torch.Tensor] = None
+    dx: Optional[torch.Tensor] = None
+    dw_gate: Optional[torch.Tensor] = None
+    dw_up: Optional[torch.Tensor] = None
+    dw_down: Optional[torch.Tensor] = None
+    dw_router: Optional[torch.Tensor] = None
+    dbias: Optional[torch.Tensor] = None
+    ws_route_bwd: Optional[torch.Tensor] = None
+
+
+class MoELayer:
+    """Weights of one layer (device tensors) and the calls that run it.
+
+    w_router [d, E] fp32, bias [E] fp32 or None, w_gate / w_up [E, d, f] bf16,
+    w_down [E, f, d] bf16; top-k routing; ``align`` pads each expert's rows.
+    """
+
+    def __init__(self, w_router, bias, w_gate, w_up, w_down, k: int, align: int = 128):
+        self.lib = _lib.load()
+        self.w_router = w_router.contiguous()
+        self.bias = None if bias is None else bias.contiguous()
+        self.w_gate = w_gate.contiguous()
+        self.w_up = w_up.contiguous()
+        self.w_down = w_down.contiguous()
+        self.E, self.d, self.f = w_gate.shape
+        self.k = k
+        self.align = align
+        dev = w_gate.device
+        if dev.type != "cuda":
+            raise RuntimeError("MoELayer runs on a CUDA device only")
+        self.device = dev
+
+    @classmethod
+    def from_inputs(cls, inp: dict, k: int, align: int = 128, device="cuda"):
+        mv = lambda t: None if t is None else t.to(device)  # noqa: E731
+        return cls(mv(inp["w_router"]), mv(inp.get("bias")), mv(inp["w_gate"]),
+                   mv(inp["w_up"]), mv(inp["w_down"]), k, align)
+
+    def row_capacity(self, T: int) -> int:
+        return int(self.lib.moe_row_capacity(T, self.k, self.E, self.align))
+
+    def buffers(self, T: int, backward: bool = True) -> Buffers:
+        E, d, f, k = self.E, self.d, self.f, self.k
+        R = self.row_capacity(T)
+        kw = dict(device=self.device)
+        ws_p = int(self.lib.moe_workspace_size(_lib.MOE_WS_PERMUTE, T, d, E, k, self.align))
+        b = Buffers(
+            T=T, R_cap=R,
+            logits=torch.empty(T, E, dtype=torch.float32, **kw),
+            topk_idx=torch.empty(T, k, dtype=torch.int32, **kw),
+            topk_w=torch.empty(T, k, dtype=torch.float32, **kw),
+            counts=torch.empty(E, dtype=torch.int32, **kw),
+            offsets=torch.empty(E + 1, dtype=torch.int64, **kw),
+            dst_row=torch.empty(T * k, dtype=torch.int32, **kw),
+            src_pair=torch.empty(R, dtype=torch.int32, **kw),
+            xp=torch.empty(R, d, dtype=BF16, **kw),
+            g=torch.empty(R, f, dtype=BF16, **kw),
+            u=torch.empty(R, f, dtype=BF16, **kw),
+            a=torch.empty(R, f, dtype=BF16, **kw),
+            yp=torch.empty(R, d, dtype=BF16, **kw),
+            y=torch.empty(T, d, dtype=BF16, **kw),
+            ws_permute=torch.empty(max(ws_p, 256), dtype=torch.uint8, **kw),
+        )
+        if backward:
+            ws_r = int(self.lib.moe_workspace_size(_lib.MOE_WS_ROUTE_BWD, T, d, E, k, self.align))
+            b.dyp = torch.empty(R, d, dtype=BF16, **kw)
+            b.dg = torch.empty(R, f, dtype=BF16, **kw)
+            b.du = torch.empty(R, f, dtype=BF16, **kw)
+            b.dxp = torch.empty(R, d, dtype=BF16, **kw)
+            b.d_topk_w = torch.empty(T, k, dtype=torch.float32, **kw)
+            b.dx = torch.empty(T, d, dtype=BF16, **kw)
+            b.dw_gate = torch.empty(E, d, f, dtype=BF16, **kw)
+            b.dw_up = torch.empty(E, d, f, dtype=BF16, **kw)
+            b.dw_down = torch.empty(E, f, d, dtype=BF16, **kw)
+            b.dw_router = torch.empty(d, E, dtype=torch.float32, **kw)
+            b.dbias = torch.empty(E, dtype=torch.float32, **kw)
+            b.ws_route_bwd = torch.empty(max(ws_r, 256), dtype=torch.uint8, **kw)
+        return b
+
+    # ------------------------------------------------------------- calls --
+    def route(self, x, b: Buffers, forced_idx=None, stream=None):
+        _lib.call("moe_route", _p(x), _p(self.w_router), _p(self.bias), _p(forced_idx),
+                  b.T, self.d, self.E, self.k, _p(b.logits), _p(b.topk_idx), _p(b.topk_w),
+                  _stream(stream))
+
+    def permute(self, x, b: Buffers, topk_idx=None, stream=None):
+        idx = b.topk_idx if topk_idx is None else topk_idx
+        _lib.call("moe_permute", _p(idx), b.T, self.k, self.E, self.align, _p(x), self.d,
+                  b.R_cap, _p(b.counts), _p(b.offsets), _p(b.dst_row), _p(b.src_pair),
+                  _p(b.xp), _p(b.ws_permute), b.ws_permute.numel(), _stream(stream))
+
+    def expert_fwd(self, b: Buffers, row_w=None, stream=None):
+        _lib.call("moe_expert_fwd", _p(b.xp), _p(b.offsets), _p(row_w), self.E, self.d, self.f,
+                  b.R_cap, _p(self.w_gate), _p(self.w_up), _p(self.w_down), _p(b.g), _p(b.u),
+                  _p(b.a), _p(b.yp), _stream(stream))
+
+    def combine(self, rows, b: Buffers, out, weights=True, stream=None):
+        _lib.call("moe_combine", _p(rows), _p(b.dst_row), _p(b.topk_w) if weights else None,
+                  b.T, self.k, self.d, _p(out), _stream(stream))
+
+    def expert_bwd(self, dy, b: Buffers, stream=None):
+        _lib.call("moe_expert_bwd", _p(dy), _p(b.src_pair), _p(b.dst_row), _p(b.topk_w),
+                  _p(b.offsets), b.T, self.k, self.E, self.d, self.f, b.R_cap,
+                  _p(b.xp), _p(b.g), _p(b.u), _p(b.a), _p(b.yp),
+                  _p(self.w_gate), _p(self.w_up), _p(self.w_down),
+                  _p(b.dyp), _p(b.dg), _p(b.du), _p(b.dxp), _p(b.d_topk_w),
+                  _p(b.dw_gate), _p(b.dw_up), _p(b.dw_down), _stream(stream))
+
+    def route_bwd(self, b: Buffers, stream=None):
+        _lib.call("moe_route_bwd", _p(b.d_topk_w), _p(b.topk_w), _p(b.topk_idx),
+                  _p(self.w_router), _p(b.offsets), _p(b.src_pair), _p(b.xp), b.T, self.d,
+                  self.E, self.k, self.align, _p(b.dx), _p(b.dw_router), _p(b.dbias),
+                  _p(b.ws_route_bwd), b.ws_route_bwd.numel(), _stream(stream))
+
+    # ------------------------------------------------------ whole layer --
+    def forward(self, x, b: Buffers, forced_idx=None, stream=None):
+        """y = layer(x) into b.y; every intermediate stays in ``b``."""
+        self.route(x, b, forced_idx, stream)
+        self.permute(x, b, None, stream)
+        self.expert_fwd(b, None, stream)
+        self.combine(b.yp, b, b.y, True, stream)
+        return b.y
+
+    def backward(self, dy, b: Buffers, stream=None):
+        """Gradients of sum(y * dy) into b.dx, b.dw_*, b.dbias, b.d_topk_w."""
+        self.expert_bwd(dy, b, stream)
+        self.combine(b.dxp, b, b.dx, False, stream)
+        self.route_bwd(b, stream)
+        return b.dx
+
+    def status(self, stream=None) -> int:
+        """Synchronise and read (and clear) the device status word."""
+        return int(self.lib.moe_status(_stream(stream)))

@@ -1,0 +1,81 @@
+"""The C ABI library loads and exports every entry point include/moe.h
+declares; host-side argument checks reject bad calls before any CUDA work
+(these calls never reach the device, so they run without a GPU)."""
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "moe.h")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_]*\s*\**\s+(moe_[a-z0-9_]+)\s*\(",
+                       text, flags=re.M)
+    return sorted(set(names))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from mixture_experts_routed_softmax_gb300.build import build
+    from mixture_experts_routed_softmax_gb300 import _lib
+    build()
+    return _lib.load()
+
+
+def test_header_declares_the_layer_calls():
+    names = declared_functions()
+    for n in ("moe_route", "moe_permute", "moe_expert_fwd", "moe_expert_bwd", "moe_combine",
+              "moe_route_bwd", "moe_workspace_size", "moe_status", "moe_status_str"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    from mixture_experts_routed_softmax_gb300 import _lib
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+        assert name in _lib.SIGNATURES, f"{name} has no binding"
+
+
+def test_capacity_and_workspace_sizes(lib):
+    assert lib.moe_row_capacity(16384, 4, 32, 128) == 16384 * 4 + 32 * 127
+    assert lib.moe_workspace_size(1, 8192, 2560, 512, 10, 128) > 0
+    assert lib.moe_workspace_size(2, 8192, 2560, 512, 10, 128) > 0
+    assert lib.moe_workspace_size(99, 8192, 2560, 512, 10, 128) == 0
+    assert lib.moe_status_str(0) == b"MOE_OK"
+
+
+def test_host_argument_checks(lib):
+    from mixture_experts_routed_softmax_gb300 import _lib as L
+    P = 0x1000  # a non-null, 16-byte aligned stand-in; these calls return before touching it
+    # null required pointers
+    assert lib.moe_route(None, P, None, None, 4, 8, 4, 2, P, P, P, None) == L.MOE_ERR_ARG
+    # k > E
+    assert lib.moe_route(P, P, None, None, 4, 8, 4, 5, P, P, P, None) == L.MOE_ERR_ARG
+    # d not a multiple of 8
+    assert lib.moe_route(P, P, None, None, 4, 12, 4, 2, P, P, P, None) == L.MOE_ERR_UNSUPPORTED
+    # E above the limit
+    assert lib.moe_route(P, P, None, None, 4, 8, 2048, 2, P, P, P, None) == L.MOE_ERR_UNSUPPORTED
+    ws = lib.moe_workspace_size(1, 4, 8, 4, 2, 16)
+    cap = lib.moe_row_capacity(4, 2, 4, 16)
+    # align not a power of two / out of range
+    for align in (0, 24, 8, 512):
+        assert lib.moe_permute(P, 4, 2, 4, align, P, 8, cap, P, P, P, P, P, P, ws, None) == L.MOE_ERR_ARG
+    # capacity too small
+    assert lib.moe_permute(P, 4, 2, 4, 16, P, 8, cap - 1, P, P, P, P, P, P, ws, None) == L.MOE_ERR_CAPACITY
+    # workspace too small
+    assert lib.moe_permute(P, 4, 2, 4, 16, P, 8, cap, P, P, P, P, P, P, ws - 1, None) == L.MOE_ERR_ARG
+    # misaligned activation pointer
+    assert lib.moe_permute(P, 4, 2, 4, 16, P + 2, 8, cap, P, P, P, P, P, P, ws, None) == L.MOE_ERR_ARG
+    # expert GEMMs: f not a multiple of 8
+    assert lib.moe_expert_fwd(P, P, None, 4, 8, 12, cap, P, P, P, P, P, P, P, None) == L.MOE_ERR_UNSUPPORTED
+    assert lib.moe_expert_fwd(P, None, None, 4, 8, 16, cap, P, P, P, P, P, P, P, None) == L.MOE_ERR_ARG
+    # combine: k above the slot limit
+    assert lib.moe_combine(P, P, None, 4, 33, 8, P, None) == L.MOE_ERR_UNSUPPORTED
+    # route backward: workspace missing
+    assert lib.moe_route_bwd(P, P, P, P, P, P, P, 4, 8, 4, 2, 16, P, P, None, None, 0, None) == L.MOE_ERR_ARG
+    # timer: bad kernel id
+    assert lib.moe_timer_start(0, 4) == L.MOE_ERR_ARG

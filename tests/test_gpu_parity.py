@@ -1,0 +1,118 @@
+"""Parity of the CUDA path (through the C ABI) with the float64 oracle.
+
+Complete comparisons at sizes the oracle finishes in seconds: several tiles
+in every GEMM dimension, ragged tails (d and f not multiples of the tile
+widths), skewed loads with empty experts, k = 1 and k = E, one token, one
+expert, every padding multiple. Integers bit-exact, values within
+2e-2 x RMS (the bar for bf16 outputs with fp32 accumulation).
+"""
+import numpy as np
+import pytest
+import torch
+
+import workloads
+from harness import compare_full, gpu_forward_backward, to_np
+
+pytestmark = pytest.mark.gpu
+
+
+def _layer(inp, k, align):
+    from mixture_experts_routed_softmax_gb300.layer import MoELayer
+    return MoELayer.from_inputs(inp, k, align)
+
+
+def _case(name, T, d, f, E, k, align, zipf=None, tau=None):
+    wl = workloads.Workload(name, T=T, d=d, f=f, E=E, k=k, zipf_s=zipf, align=align)
+    inp = workloads.generate(wl, tau=tau)
+    return wl, inp
+
+
+CASES = {
+    # name: (T, d, f, E, k, align, zipf_s, tau)
+    "tiny": (256, 128, 256, 8, 2, 128, None, None),
+    "ragged_a16": (300, 200, 136, 6, 2, 16, None, None),
+    "multi_tile": (520, 392, 520, 8, 3, 128, None, None),
+    "skewed_empty": (700, 264, 384, 16, 4, 32, 1.2, 1.5),
+    "one_expert_k1": (333, 128, 256, 1, 1, 64, None, None),
+    "k_equals_E": (64, 64, 64, 4, 4, 16, None, None),
+    "one_token": (1, 128, 128, 8, 2, 16, None, None),
+    "seven_tokens": (7, 96, 160, 8, 3, 256, None, None),
+    "wide_E": (256, 128, 64, 160, 6, 16, 1.1, 0.8),
+}
+
+
+@pytest.mark.parametrize("name", sorted(CASES))
+def test_layer_parity(name):
+    T, d, f, E, k, align, zipf, tau = CASES[name]
+    wl, inp = _case(name, T, d, f, E, k, align, zipf, tau)
+    layer = _layer(inp, k, align)
+    out, _ = compare_full(layer, inp, k, align)
+    print(name, {k_: (round(v, 5) if isinstance(v, float) else v) for k_, v in out.items()})
+
+
+def test_all_tokens_to_one_expert():
+    T, d, f, E, k, align = 200, 128, 192, 8, 1, 16
+    wl, inp = _case("one_hot", T, d, f, E, k, align)
+    layer = _layer(inp, k, align)
+    forced = torch.full((T, k), 3, dtype=torch.int32)
+    b, _, _ = gpu_forward_backward(layer, inp, forced)
+    counts = to_np(b.counts)
+    assert counts[3] == T and counts.sum() == T
+    for e in range(E):
+        if e != 3:
+            assert torch.count_nonzero(b.dw_gate[e]).item() == 0
+            assert torch.count_nonzero(b.dw_down[e]).item() == 0
+    # k = 1: every weight is exactly 1
+    assert torch.all(b.topk_w == 1.0)
+
+
+def test_two_runs_bitwise_equal():
+    T, d, f, E, k, align = 512, 256, 384, 16, 4, 32
+    wl, inp = _case("det", T, d, f, E, k, align, 1.1, 1.0)
+    layer = _layer(inp, k, align)
+    b1, _, _ = gpu_forward_backward(layer, inp)
+    b2, _, _ = gpu_forward_backward(layer, inp)
+    for name in ("logits", "topk_idx", "topk_w", "offsets", "dst_row", "src_pair", "y", "dx",
+                 "dw_gate", "dw_up", "dw_down", "dw_router", "dbias", "d_topk_w"):
+        assert torch.equal(getattr(b1, name), getattr(b2, name)), name
+    R = int(b1.offsets[-1])
+    for name in ("xp", "g", "u", "a", "yp", "dyp", "dg", "du", "dxp"):
+        assert torch.equal(getattr(b1, name)[:R], getattr(b2, name)[:R]), name
+
+
+def test_epilogue_row_scaling_matches_unscaled_times_weight():
+    """moe_expert_fwd with row_w scales each output row in the fp32 epilogue."""
+    T, d, f, E, k, align = 256, 128, 256, 8, 2, 16
+    wl, inp = _case("roww", T, d, f, E, k, align)
+    layer = _layer(inp, k, align)
+    b, _, _ = gpu_forward_backward(layer, inp, backward=False)
+    R = b.R_cap
+    rng = np.random.default_rng(0)
+    row_w = torch.tensor(rng.random(R), dtype=torch.float32, device="cuda")
+    unscaled = b.yp.clone()
+    layer.expert_fwd(b, row_w=row_w)
+    torch.cuda.synchronize()
+    Rp = int(b.offsets[-1])
+    ref = unscaled[:Rp].float() * row_w[:Rp, None]
+    got = b.yp[:Rp].float()
+    # the epilogue scales the fp32 accumulator before the one bf16 rounding
+    assert torch.max(torch.abs(got - ref)).item() <= 2 ** -7 * torch.max(torch.abs(ref)).item()
+
+
+def test_bad_forced_index_raises_device_status():
+    from mixture_experts_routed_softmax_gb300 import _lib
+    T, d, f, E, k, align = 64, 64, 64, 4, 2, 16
+    wl, inp = _case("badidx", T, d, f, E, k, align)
+    layer = _layer(inp, k, align)
+    b = layer.buffers(T, backward=False)
+    forced = torch.zeros(T, k, dtype=torch.int32, device="cuda")
+    forced[:, 1] = 1
+    forced[5, 1] = E + 3          # out of range: reported, never dereferenced
+    layer.route(inp["x"].cuda(), b, forced_idx=forced)
+    assert layer.status() == _lib.MOE_ERR_DEVICE_INDEX
+    assert float(b.topk_w[5, 1]) == 0.0
+    layer.permute(inp["x"].cuda(), b, topk_idx=forced)   # the bad pair is dropped from the layout
+    assert layer.status() == _lib.MOE_ERR_DEVICE_INDEX
+    assert int(b.dst_row[5 * k + 1]) == -1
+    assert int(b.counts.sum()) == T * k - 1
+    assert layer.status() == 0           # the status word was cleared by the read
