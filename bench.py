@@ -1,0 +1,433 @@
+#!/usr/bin/env python
+"""Throughput of the routed MoE expert layer (forward + backward) on GB300.
+
+Default workload: the GPT-OSS-20B-shaped layer (T = 16384 tokens = 4 x 4096,
+d = f = 2880, E = 32 experts, top-4), seeded synthetic inputs, bf16.
+
+One step = the whole layer: moe_route -> moe_permute -> moe_expert_fwd ->
+moe_combine -> moe_expert_bwd -> moe_combine (dx) -> moe_route_bwd, inputs
+resident in HBM. W untimed warm-up steps, then K steps timed with CUDA events
+between a barrier + synchronize on both sides; the slowest rank's time counts.
+Prints one JSON line (rank 0).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--config NAME] [--no-cpu-baseline]
+
+--impl reference times the float64 CPU oracle (the deliberately slow,
+obviously correct definition) on a bounded sample of the same workload on
+the host cores; under torchrun only rank 0 runs it.
+
+Several GPUs: one process per GPU under torchrun, each an independent replica
+of the layer (the layer needs no exchange between GPUs on this path);
+value = tokens of all ranks / the slowest rank's time, "scaling": "weak".
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "routed tokens/s per MoE layer fwd+bwd, bf16, 1 GB300; % of roofline"
+UNIT = "tokens/s"
+DEFAULT_CONFIG = "gptoss20b"
+STEP_KERNELS = ["router_logits", "topk", "permute", "gateup_fwd", "down_fwd", "combine",
+                "combine_bwd", "down_dgrad", "gateup_dgrad", "wgrad_down", "wgrad_gateup",
+                "route_bwd"]
+FWD_KERNELS = STEP_KERNELS[:6]
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", default=DEFAULT_CONFIG)
+    ap.add_argument("--align", type=int, default=None)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-tokens", type=int, default=8192,
+                    help="tokens in the oracle's bounded sample (cpu_baseline)")
+    ap.add_argument("--ref-tokens", type=int, default=1,
+                    help="tokens per step of the reference (oracle) arm")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args(argv)
+
+
+# ----------------------------------------------------------------- peaks --
+
+def load_peaks() -> dict:
+    """Measured denominators (MEASURED_PEAKS.json), else the stated fallback."""
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as fh:
+            p = json.load(fh)
+        return {"hbm_gbs": float(p["hbm_gbs"]), "bf16_tflops": float(p["bf16_tflops"]),
+                "bf16_tflops_sustained": float(p.get("bf16_tflops_sustained", p["bf16_tflops"])),
+                "source": "measured"}
+    except Exception:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+                "source": "fallback"}
+
+
+# -------------------------------------------------------------- clocks --
+
+CLOCK_QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons while running."""
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(prefix="clocks_", suffix=".csv")
+            os.close(fd)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={CLOCK_QUERY}",
+                 "--format=csv,noheader", "-lms", "200"], stdout=self.fh,
+                stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        return self
+
+    def stop(self) -> dict | None:
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.fh.close()
+        rows = []
+        with open(self.path) as fh:
+            for line in fh:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        return parse_clock_rows(rows)
+
+
+def parse_clock_rows(rows) -> dict | None:
+    def mhz(s):
+        m = re.match(r"([0-9.]+)", s)
+        return float(m.group(1)) if m else None
+
+    sm = [mhz(r[1]) for r in rows if mhz(r[1]) is not None]
+    mx = [mhz(r[2]) for r in rows if mhz(r[2]) is not None]
+    if not sm:
+        return None
+    names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+    reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+    return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx) if mx else None,
+            "samples": len(sm), "reasons": reasons}
+
+
+# ---------------------------------------------------------- distributed --
+
+def dist_env():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def max_over_ranks(value: float, device=None) -> float:
+    """Max of a float over all ranks (identity when not distributed)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()):
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier():
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        dist.barrier()
+
+
+# ------------------------------------------------------------- oracle --
+
+def blas_threads() -> int:
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads") for i in threadpool_info() if i.get("user_api") == "blas"]
+        if n and n[0]:
+            return int(n[0])
+    except Exception:
+        pass
+    return len(os.sched_getaffinity(0))
+
+
+def oracle_sample(inp: dict, wl, tokens: int) -> float:
+    """Seconds the float64 oracle takes for forward + backward of the first
+    `tokens` tokens of the workload (all experts' weights as in the layer)."""
+    from oracle import moe_oracle as mo
+    t0 = time.perf_counter()
+    x = inp["x"][:tokens]
+    fw = mo.forward(x, inp["w_router"], inp.get("bias"), inp["w_gate"], inp["w_up"],
+                    inp["w_down"], wl.k)
+    if wl.backward:
+        mo.backward(x, inp["w_router"], inp.get("bias"), inp["w_gate"], inp["w_up"],
+                    inp["w_down"], wl.k, inp["dy"][:tokens], fwd=fw)
+    return time.perf_counter() - t0
+
+
+# ------------------------------------------------------------- traffic --
+
+def csrc_digest() -> str:
+    h = hashlib.sha256()
+    base = os.path.join(ROOT, "mixture_experts_routed_softmax_gb300", "csrc")
+    for f in sorted(os.listdir(base)):
+        with open(os.path.join(base, f), "rb") as fh:
+            h.update(f.encode() + b"\0" + fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel: str, config: str):
+    """DRAM bytes per launch from a committed ncu summary of the same kernel
+    source (profiles/<kernel>_<config>.md), else None."""
+    path = os.path.join(ROOT, "profiles", f"{kernel}_{config}.md")
+    if not os.path.exists(path):
+        return None
+    text = open(path).read()
+    m = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    s = re.search(r"csrc_sha256_16:\s*([0-9a-f]+)", text)
+    if not m or not s or s.group(1) != csrc_digest():
+        return None
+    return float(m.group(1))
+
+
+# ---------------------------------------------------------------- ours --
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+    import workloads
+    from mixture_experts_routed_softmax_gb300 import _lib, accounting
+    from mixture_experts_routed_softmax_gb300.layer import MoELayer
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    wl = workloads.CONFIGS[args.config]
+    if args.align:
+        wl = wl.with_(align=args.align)
+    inp = workloads.generate(wl, with_dy=wl.backward)
+    layer = MoELayer.from_inputs(inp, wl.k, wl.align, device=dev)
+    b = layer.buffers(wl.T, backward=wl.backward)
+    x = inp["x"].to(dev)
+    dy = inp["dy"].to(dev) if wl.backward else None
+    lib = _lib.load()
+
+    def step():
+        layer.forward(x, b)
+        if wl.backward:
+            layer.backward(dy, b)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    status = layer.status()
+    if status != 0:
+        raise RuntimeError(f"device status {status}: {_lib.status_str(status)}")
+
+    kernels = STEP_KERNELS if wl.backward else FWD_KERNELS
+    # one profiled step per kernel group (outside the timed region)
+    per_kernel = {}
+    for name in kernels:
+        _lib.call("moe_timer_start", _lib.KERNELS[name], 4)
+        step()
+        ms, n = _lib.ctypes.c_float(), _lib.ctypes.c_int()
+        _lib.call("moe_timer_read", _lib.ctypes.byref(ms), _lib.ctypes.byref(n))
+        per_kernel[name] = ms.value / max(n.value, 1)
+    # "combine" fires twice per step (y and dx); the timer averaged both
+    dominant = max(per_kernel, key=per_kernel.get)
+
+    # ------------------------------------------------------ timed region --
+    stream = torch.cuda.current_stream()
+    _lib.call("moe_timer_start", _lib.KERNELS[dominant], args.steps * 2)
+    sampler = ClockSampler(local_rank).start()
+    launches0 = int(lib.moe_kernel_launches())
+    barrier()
+    torch.cuda.synchronize()
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for _ in range(args.steps):
+        step()
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    elapsed_ms = ev0.elapsed_time(ev1)
+    launches = int(lib.moe_kernel_launches()) - launches0
+    clocks = sampler.stop()
+    ms, n = _lib.ctypes.c_float(), _lib.ctypes.c_int()
+    _lib.call("moe_timer_read", _lib.ctypes.byref(ms), _lib.ctypes.byref(n))
+    dom_ms = ms.value / max(n.value, 1)
+    status = layer.status()
+    if status != 0:
+        raise RuntimeError(f"device status {status}: {_lib.status_str(status)}")
+    max_ms = max_over_ranks(elapsed_ms, dev)
+
+    # --------------------------------------------------------- end to end --
+    e2e = None
+    if not args.no_e2e:
+        x_h = inp["x"].pin_memory()
+        dy_h = inp["dy"].pin_memory() if wl.backward else None
+        y_h = torch.empty_like(inp["x"]).pin_memory()
+        dx_h = torch.empty_like(inp["x"]).pin_memory() if wl.backward else None
+        bi = x_h.numel() * 2 + (dy_h.numel() * 2 if wl.backward else 0)
+        bo = y_h.numel() * 2 + (dx_h.numel() * 2 if wl.backward else 0)
+        barrier()
+        torch.cuda.synchronize()
+        ev0.record(stream)
+        for _ in range(args.steps):
+            x.copy_(x_h, non_blocking=True)
+            if wl.backward:
+                dy.copy_(dy_h, non_blocking=True)
+            step()
+            y_h.copy_(b.y, non_blocking=True)
+            if wl.backward:
+                dx_h.copy_(b.dx, non_blocking=True)
+        ev1.record(stream)
+        torch.cuda.synchronize()
+        barrier()
+        e2e_ms = max_over_ranks(ev0.elapsed_time(ev1), dev)
+        e2e = {"value": world * wl.T * args.steps / (e2e_ms / 1e3), "unit": UNIT,
+               "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo}
+
+    # ----------------------------------------------------------- roofline --
+    counts = b.counts.cpu()
+    shape = accounting.Shape(T=wl.T, d=wl.d, f=wl.f, E=wl.E, k=wl.k,
+                             E_active=int((counts > 0).sum()))
+    costs = accounting.kernel_costs(shape, wl.backward)
+    peaks = load_peaks()
+    key = "combine" if dominant == "combine" else dominant
+    fl, by = costs[key]
+    t_tensor = fl / (peaks["bf16_tflops_sustained"] * 1e12)
+    t_hbm = by / (peaks["hbm_gbs"] * 1e9)
+    if t_tensor >= t_hbm:
+        achieved = fl / (dom_ms * 1e-3) / 1e12
+        roof = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops_sustained"],
+                "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops_sustained"]}
+        roof["peak_kind"] = f"bf16 sustained, {peaks['source']}"
+    else:
+        achieved = by / (dom_ms * 1e-3) / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": achieved / peaks["hbm_gbs"]}
+        roof["peak_kind"] = f"hbm copy, {peaks['source']}"
+    roof["kernel"] = dominant
+    roof["ms_per_launch"] = dom_ms
+    roof["algorithmic_flops_per_launch"] = fl
+    roof["algorithmic_bytes_per_launch"] = by
+    roof["traffic"] = recorded_traffic(dominant, args.config)
+
+    ms_per_step = max_ms / args.steps
+    F, B = accounting.totals(shape, wl.backward)
+    t_roof = accounting.roofline_seconds(F, B, peaks["bf16_tflops"], peaks["hbm_gbs"])
+    value = world * wl.T * args.steps / (max_ms / 1e3)
+
+    out = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": max(args.warmup, 3), "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": f"{wl.name}: {wl.note}", "T": wl.T, "d": wl.d, "f": wl.f,
+                   "E": wl.E, "k": wl.k, "align": wl.align, "backward": wl.backward,
+                   "tau": inp.get("tau"), "seed": wl.seed,
+                   "l2": "inputs larger than L2 (no flush): one step moves several GB",
+                   "parallelism": f"replicas x{world}"},
+        "roofline": roof,
+        "layer_roofline": {"flops": F, "bytes": B, "t_roof_ms": t_roof * 1e3,
+                           "frac": t_roof * 1e3 / ms_per_step,
+                           "peaks": f"bf16 {peaks['bf16_tflops']} TFLOP/s burst, "
+                                    f"HBM {peaks['hbm_gbs']} GB/s, {peaks['source']}",
+                           "tflops_achieved": F / (ms_per_step * 1e-3) / 1e12,
+                           "E_active": shape.E_active},
+        "pairs_per_s": value * wl.k,
+        "kernels_ms": {k_: round(v, 4) for k_, v in per_kernel.items()},
+        "gpu_launches": launches,
+        "clocks": clocks,
+        "e2e": e2e,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        tokens = min(args.cpu_tokens, wl.T)
+        secs = oracle_sample(inp, wl, tokens)
+        out["cpu_baseline"] = {"value": tokens / secs, "unit": UNIT, "cores": blas_threads(),
+                               "kind": "oracle",
+                               "sample": f"first {tokens} of {wl.T} tokens, all {wl.E} experts, "
+                                         f"{'fwd+bwd' if wl.backward else 'fwd'}, float64 numpy",
+                               "seconds": secs}
+    return out
+
+
+# ----------------------------------------------------------- reference --
+
+def run_reference(args):
+    import workloads
+    wl = workloads.CONFIGS[args.config]
+    inp = workloads.generate(wl, with_dy=wl.backward)
+    tokens = min(args.ref_tokens, wl.T)
+    for _ in range(args.warmup):
+        oracle_sample(inp, wl, tokens)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle_sample(inp, wl, tokens)
+    secs = time.perf_counter() - t0
+    value = tokens * args.steps / secs
+    sample = (f"first {tokens} of {wl.T} tokens per step, all {wl.E} experts, "
+              f"{'fwd+bwd' if wl.backward else 'fwd'}, float64 numpy")
+    return {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 0,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": secs * 1e3 / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": f"{wl.name}: {wl.note}", "T": wl.T, "d": wl.d, "f": wl.f,
+                   "E": wl.E, "k": wl.k, "align": wl.align, "backward": wl.backward},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": blas_threads(),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    rank, world, local_rank = dist_env()
+    if args.impl == "reference":
+        if rank != 0:
+            return 0
+        print(json.dumps(run_reference(args)), flush=True)
+        return 0
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    out = run_ours(args, rank, world, local_rank)
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

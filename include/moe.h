@@ -237,6 +237,10 @@ const char* moe_status_str(int code);
 int moe_timer_start(int kernel, int max_launches);
 int moe_timer_read(float* total_ms, int* launches);
 
+/* Number of kernels this library has enqueued in this process so far (all
+ * devices, all streams). Measurement only. */
+uint64_t moe_kernel_launches(void);
+
 #ifdef __cplusplus
 }
 #endif

@@ -31,6 +31,7 @@ SIGNATURES = {
     "moe_status_str": (ctypes.c_char_p, [_I]),
     "moe_timer_start": (_I, [_I, _I]),
     "moe_timer_read": (_I, [ctypes.POINTER(ctypes.c_float), ctypes.POINTER(ctypes.c_int)]),
+    "moe_kernel_launches": (ctypes.c_uint64, []),
 }
 
 MOE_OK = 0

@@ -1,6 +1,7 @@
 // api.cu — the C ABI declared in include/moe.h: argument checks, the
 // per-device status word, workspace sizes, the kernel timer, and the order
 // in which each entry point launches its kernels.
+#include <atomic>
 #include <mutex>
 #include <vector>
 
@@ -40,6 +41,9 @@ int num_sms() {
   return sms[dev];
 }
 
+static std::atomic<unsigned long long> g_launches{0};
+void note_launches(int n) { g_launches.fetch_add((unsigned long long)n, std::memory_order_relaxed); }
+
 // ------------------------------------------------------------ kernel timer --
 struct Timer {
   std::mutex mu;
@@ -72,6 +76,8 @@ static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 
 static int cuda_code(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
 
 extern "C" {
+
+uint64_t moe_kernel_launches(void) { return g_launches.load(std::memory_order_relaxed); }
 
 int64_t moe_row_capacity(int64_t T, int k, int E, int align) {
   return T * k + (int64_t)E * (align - 1);

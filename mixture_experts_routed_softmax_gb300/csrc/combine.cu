@@ -28,18 +28,20 @@ __global__ void __launch_bounds__(256) combine_kernel(const moe_bf16* __restrict
   }
   const int nv = d / 8;
   uint4* dst = reinterpret_cast<uint4*>(out + t * d);
-  for (int v = lane; v < nv; v += 32) {
+  // every lane runs the same number of iterations: the shuffles need the whole warp
+  for (int v0 = 0; v0 < nv; v0 += 32) {
+    const int v = v0 + lane;
     float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
     for (int j = 0; j < k; ++j) {
       const int32_t r = __shfl_sync(0xFFFFFFFFu, my_r, j);
       const float wj = __shfl_sync(0xFFFFFFFFu, my_w, j);
-      if (r < 0) continue;
+      if (r < 0 || v >= nv) continue;
       float f[8];
       unpack8(reinterpret_cast<const uint4*>(rows + (int64_t)r * d)[v], f);
 #pragma unroll
       for (int i = 0; i < 8; ++i) acc[i] = fmaf(wj, f[i], acc[i]);
     }
-    dst[v] = pack8(acc);
+    if (v < nv) dst[v] = pack8(acc);
   }
 }
 
@@ -47,6 +49,7 @@ cudaError_t launch_combine(const moe_bf16* rows, const int32_t* dst_row, const f
                            int64_t T, int k, int d, moe_bf16* out, cudaStream_t s) {
   timer_before(MOE_KERNEL_COMBINE, s);
   combine_kernel<<<(unsigned)((T + 7) / 8), 256, 0, s>>>(rows, dst_row, topk_w, T, k, d, out);
+  note_launches(1);
   timer_after(MOE_KERNEL_COMBINE, s);
   return cudaGetLastError();
 }
@@ -100,6 +103,7 @@ cudaError_t launch_combine_bwd(const moe_bf16* dy, const moe_bf16* yp, const int
   combine_bwd_kernel<<<(unsigned)((R_cap + 7) / 8), 256, 0, s>>>(dy, yp, src_pair, topk_w,
                                                                  offsets, k, E, d, R_cap, dyp,
                                                                  d_topk_w);
+  note_launches(1);
   timer_after(MOE_KERNEL_COMBINE_BWD, s);
   return cudaGetLastError();
 }

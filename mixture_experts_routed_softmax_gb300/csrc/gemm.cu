@@ -537,6 +537,7 @@ static cudaError_t launch_kind(const CUtensorMap& a0, const CUtensorMap& a1,
   if (grid < 1) grid = 1;
   timer_before(Tr<K>::kernel_id, s);
   grouped_gemm_kernel<K><<<(unsigned)grid, kThreads, kSmemBytes, s>>>(a0, a1, b0, b1, args);
+  note_launches(1);
   timer_after(Tr<K>::kernel_id, s);
   return cudaGetLastError();
 }

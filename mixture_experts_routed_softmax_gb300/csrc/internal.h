@@ -13,6 +13,8 @@ namespace moe {
 // Kernel timer hooks (api.cu): no-ops unless moe_timer_start armed `kernel`.
 void timer_before(int kernel, cudaStream_t s);
 void timer_after(int kernel, cudaStream_t s);
+// Launch counter behind moe_kernel_launches().
+void note_launches(int n);
 // The per-device status word kernels raise errors into.
 int* device_status_ptr();
 int num_sms();

@@ -214,6 +214,7 @@ cudaError_t launch_permute(const int32_t* topk_idx, int64_t T, int k, int E, int
         topk_idx, P, E, blk_count, rank_in_blk, dst_row, src_pair);
   permute_gather_kernel<<<(unsigned)((R_cap + 7) / 8), 256, 0, s>>>(x, d, k, offsets, counts, E,
                                                                     R_cap, src_pair, xp);
+  note_launches(P > 0 ? 4 : 2);
   timer_after(MOE_KERNEL_PERMUTE, s);
   return cudaGetLastError();
 }

@@ -88,6 +88,7 @@ cudaError_t launch_router_logits(const moe_bf16* x, const float* w_router, const
   dim3 grid((E + kRBN - 1) / kRBN, (unsigned)((T + kRBM - 1) / kRBM));
   timer_before(MOE_KERNEL_ROUTER_LOGITS, s);
   router_logits_kernel<<<grid, 256, 0, s>>>(x, w_router, bias, T, d, E, logits);
+  note_launches(1);
   timer_after(MOE_KERNEL_ROUTER_LOGITS, s);
   return cudaGetLastError();
 }
@@ -169,6 +170,7 @@ cudaError_t launch_topk(const float* logits, const int32_t* forced_idx, int64_t 
   dim3 grid((unsigned)((T + warps - 1) / warps));
   timer_before(MOE_KERNEL_TOPK, s);
   topk_kernel<<<grid, warps * 32, 0, s>>>(logits, forced_idx, T, E, k, topk_idx, topk_w, status);
+  note_launches(1);
   timer_after(MOE_KERNEL_TOPK, s);
   return cudaGetLastError();
 }
@@ -234,14 +236,17 @@ __global__ void __launch_bounds__(256) route_bwd_token_kernel(
   const float dl = w * (dw - inner);
   if (lane < k) dl_pair[t * k + lane] = dl;
   moe_bf16* dxr = dx + t * d;
-  for (int c = lane * 8; c < d; c += 256) {
-    float acc[8];
-    unpack8(*reinterpret_cast<const uint4*>(dxr + c), acc);
+  // every lane runs the same number of iterations: the shuffles need the whole warp
+  for (int c0 = 0; c0 < d; c0 += 256) {
+    const int c = c0 + lane * 8;
+    const bool in = c < d;
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    if (in) unpack8(*reinterpret_cast<const uint4*>(dxr + c), acc);
     float add[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
     for (int j = 0; j < k; ++j) {
       const float dlj = __shfl_sync(0xFFFFFFFFu, dl, j);
       const int ej = __shfl_sync(0xFFFFFFFFu, e, j);
-      if (ej < 0) continue;
+      if (ej < 0 || !in) continue;
       const float4 a = *reinterpret_cast<const float4*>(wrT + (int64_t)ej * d + c);
       const float4 b = *reinterpret_cast<const float4*>(wrT + (int64_t)ej * d + c + 4);
       add[0] = fmaf(dlj, a.x, add[0]); add[1] = fmaf(dlj, a.y, add[1]);
@@ -251,7 +256,7 @@ __global__ void __launch_bounds__(256) route_bwd_token_kernel(
     }
 #pragma unroll
     for (int i = 0; i < 8; ++i) acc[i] += add[i];
-    *reinterpret_cast<uint4*>(dxr + c) = pack8(acc);
+    if (in) *reinterpret_cast<uint4*>(dxr + c) = pack8(acc);
   }
 }
 
@@ -367,6 +372,7 @@ cudaError_t launch_route_bwd(const float* d_topk_w, const float* topk_w, const i
                              s>>>(offsets, src_pair, xp, dl_pair, E, d, unit, part, part_db);
   route_bwd_reduce_kernel<<<dim3(E, cblocks), 128, 0, s>>>(offsets, part, part_db, E, d, unit,
                                                            dw_router, dbias);
+  note_launches(T > 0 ? 4 : 3);
   timer_after(MOE_KERNEL_ROUTE_BWD, s);
   return cudaGetLastError();
 }

@@ -1,0 +1,73 @@
+"""Kernel-level numerics: the CUDA path against a PyTorch fp32 emulation of
+the same steps with the same bf16 rounding points (tests/emulation.py).
+
+Far tighter than the oracle parity: the two differ only by fp32 summation
+order and the bf16 roundings it flips, so every element must be within
+max(2^-6 |ref| + 1e-2 RMS(ref), u M) — an ulp-level flip of a bf16 value
+upstream, propagated; M is the first-order error magnitude of the oracle
+parity harness, u = 2^-8 (a quarter of the parity bound): near a zero of
+silu' a flip of G moves dG by more than its own ulp — and the RMS-relative
+difference within 2e-3.
+"""
+import numpy as np
+import pytest
+import torch
+
+import workloads
+from emulation import emulate
+from harness import U_BF16, gpu_forward_backward, magnitudes, to_np
+from oracle import moe_oracle as mo
+
+pytestmark = pytest.mark.gpu
+
+CASES = {
+    "tiny": (256, 128, 256, 8, 2, 128, None, None),
+    "ragged_a16": (300, 200, 136, 6, 2, 16, None, None),
+    "multi_tile": (520, 392, 520, 8, 3, 128, None, None),
+    "skewed_empty": (700, 264, 384, 16, 4, 32, 1.2, 1.5),
+    "qwen_like": (1024, 2048, 768, 128, 8, 16, 1.1, 0.2),
+}
+
+
+def _close(name, got, ref, mag):
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    diff = np.abs(got - ref)
+    norm = np.sqrt(np.sum(ref * ref))
+    rms = norm / np.sqrt(ref.size)
+    rel = np.sqrt(np.sum(diff * diff)) / max(norm, 1e-300)
+    bound = np.maximum(2.0 ** -6 * np.abs(ref) + 1e-2 * rms, U_BF16 * np.asarray(mag))
+    worst = float(np.max(diff / (bound + 1e-30)))
+    assert rel <= 2e-3 and worst <= 1.0, f"{name}: rms-rel {rel:.2e}, worst ratio {worst:.2f}"
+    return rel
+
+
+@pytest.mark.parametrize("name", sorted(CASES))
+def test_kernels_match_fp32_emulation(name):
+    from mixture_experts_routed_softmax_gb300.layer import MoELayer
+    T, d, f, E, k, align, zipf, tau = CASES[name]
+    wl = workloads.Workload(name, T=T, d=d, f=f, E=E, k=k, zipf_s=zipf, align=align)
+    inp = workloads.generate(wl, tau=tau)
+    x64 = mo.as_f64(inp["x"])
+    lg = mo.router_logits(x64, mo.as_f64(inp["w_router"]),
+                          None if inp["bias"] is None else mo.as_f64(inp["bias"]))
+    idx = mo.select_topk(lg, k)
+    fw = mo.forward(inp["x"], inp["w_router"], inp["bias"], inp["w_gate"], inp["w_up"],
+                    inp["w_down"], k, idx=idx)
+    bw = mo.backward(inp["x"], inp["w_router"], inp["bias"], inp["w_gate"], inp["w_up"],
+                     inp["w_down"], k, inp["dy"], fwd=fw)
+    mag = magnitudes(inp, fw, bw, k)
+    layer = MoELayer.from_inputs(inp, k, align)
+    b, _, _ = gpu_forward_backward(layer, inp, idx)
+    em = emulate(inp, idx, k)
+    dst = to_np(b.dst_row).astype(np.int64)
+    R = int(b.offsets[-1])
+    rel = {}
+    for key, buf in (("G", b.g), ("U", b.u), ("A", b.a), ("Yu", b.yp), ("dYu", b.dyp),
+                     ("dG", b.dg), ("dU", b.du), ("dXp", b.dxp)):
+        rel[key] = _close(key, to_np(buf[:R])[dst], em[key].cpu().numpy(), mag[key])
+    for key, buf in (("y", b.y), ("dx", b.dx), ("dw_gate", b.dw_gate), ("dw_up", b.dw_up),
+                     ("dw_down", b.dw_down), ("d_topk_w", b.d_topk_w),
+                     ("dw_router", b.dw_router), ("dbias", b.dbias)):
+        rel[key] = _close(key, to_np(buf), em[key].cpu().numpy(), mag[key])
+    print(name, {k_: f"{v:.1e}" for k_, v in rel.items()})

@@ -90,6 +90,10 @@ CONFIGS = {
     "fine512": Workload("fine512", T=8192, d=2560, f=640, E=512, k=10, zipf_s=1.2,
                         note="fine-grained 512-expert top-10 layer, Zipf(1.2) router bias"),
 }
+# a smaller case of the GPT-OSS-20B-shaped layer (one sequence of 4096 tokens)
+# for ncu captures, whose replays save and restore device memory
+CONFIGS["gptoss20b_T4096"] = Workload("gptoss20b_T4096", T=4096, d=2880, f=2880, E=32, k=4,
+                                      note="GPT-OSS-20B-shaped layer, one 4096-token sequence")
 for _T in (128, 512, 1024, 2048):
     CONFIGS[f"smallm_T{_T}"] = Workload(
         f"smallm_T{_T}", T=_T, d=2048, f=768, E=128, k=8, backward=False,
