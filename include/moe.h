@@ -108,6 +108,36 @@ int moe_permute(const int32_t* topk_idx, int64_t T, int k, int E, int align,
                 moe_bf16* xp, void* ws, size_t ws_bytes, moe_stream_t stream);
 
 /* ------------------------------------------------------------------------
+ * moe_permute_noalloc — moe_permute without a workspace argument.
+ * (No counterpart on the source pages: this is a calling convention of this
+ * library, not part of the method.)
+ * For callers that cannot allocate device memory: a host application that
+ * owns all device memory through its own fixed pool and forbids other
+ * allocations, or a latency-critical path where cudaMalloc's implicit
+ * device synchronisation and its possible failure under memory pressure are
+ * not acceptable. The kernels' scratch lives in a 2 MiB array built into the
+ * library (every GPU that loads the library keeps it until process exit), so
+ * this call allocates nothing; the caller still passes every input and
+ * output, with the meaning, layout and limits of moe_permute.
+ *  - The scratch needed is 4*ceil(T*k/4096)*E + 4*T*k bytes (each part
+ *    rounded up to 256); problems needing more than 2 MiB return
+ *    MOE_ERR_UNSUPPORTED before anything is enqueued (T*k up to about 500k
+ *    pairs at E = 64; use moe_permute with a workspace beyond that).
+ *  - The first call on each device looks up the array's device address with
+ *    cudaGetSymbolAddress (a host-side call with that device current); make
+ *    that first call before any stream capture begins.
+ *  - All calls share the one array, and it keeps the last call's contents:
+ *    calls whose work overlaps on the GPU (different streams, or different
+ *    host threads on one device) race on it and must be serialised by the
+ *    caller. The kernels overwrite every scratch word before reading it, so
+ *    nothing needs clearing between calls.
+ * ------------------------------------------------------------------------ */
+int moe_permute_noalloc(const int32_t* topk_idx, int64_t T, int k, int E, int align,
+                        const moe_bf16* x, int d, int64_t R_cap,
+                        int32_t* counts, int64_t* offsets, int32_t* dst_row, int32_t* src_pair,
+                        moe_bf16* xp, moe_stream_t stream);
+
+/* ------------------------------------------------------------------------
  * moe_expert_fwd — grouped gate/up GEMM with fused SwiGLU, grouped down GEMM.
  * [HALO §Levers that help] one grouped expert matmul instead of a loop, fused
  * GLU; [PRL "Kept expert activations"] G and U are kept for backward.
