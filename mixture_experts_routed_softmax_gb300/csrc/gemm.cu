@@ -207,7 +207,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     total = tstart[args.E] * nN;
   }
-  constexpr uint32_t kIdesc = idesc_bf16(BM, T::BN, T::a_mn ? 1 : 0, T::b_mn ? 1 : 0);
+  // dual kinds: the two B tiles sit side by side in shared memory ([B0 | B1],
+  // 64-column chunks at a fixed stride), so one N = 256 MMA fills both
+  // accumulators (columns 0-127 and 128-255) and the A tile is read once
+  constexpr uint32_t kIdesc =
+      idesc_bf16(BM, T::dual ? 2 * T::BN : T::BN, T::a_mn ? 1 : 0, T::b_mn ? 1 : 0);
   constexpr uint32_t kBBytes = (uint32_t)T::BN * BK * 2;
 
   if (warp == 0) {
@@ -296,7 +300,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_after();
           const uint32_t sA = s_base + stage * kStageBytes;
           const uint32_t sB0 = sA + kABytes;
-          const uint32_t sB1 = sB0 + kBBytes;
           int nsub = BK / 16;
           if constexpr (T::kgrouped) {
             const int64_t left = ti.row_end - (int64_t)ks * BK;
@@ -309,10 +312,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                                          : sdesc_sw128(sB0 + kk * 32, 16, 1024);
             const uint32_t accum = (ks > 0 || kk > 0) ? 1u : 0u;
             umma_bf16(d_tmem, ad, bd0, kIdesc, accum);
-            if constexpr (T::dual) {
-              const uint64_t bd1 = sdesc_sw128(sB1 + kk * 2048, BK * 128, 1024);
-              umma_bf16(d_tmem + 128u, ad, bd1, kIdesc, accum);
-            }
           }
           umma_commit(empty_bar(stage));
           if (++stage == kStages) { stage = 0; phase ^= 1u; }
@@ -410,8 +409,58 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
         }
+      } else if constexpr (K == Kind::DownDgrad) {
+        // dG = dA * U * silu'(G), dU = dA * silu(G); the saved G, U of chunk c+1
+        // are loaded while chunk c is computed
+        const bool row_ok = row < ti.row_end;
+        const int64_t base = row * args.N;
+        uint4 gc[4], uc[4], gn[4], un[4];
+        auto load_gu = [&](int c, uint4* g, uint4* u) {
+#pragma unroll
+          for (int v = 0; v < 4; ++v) {
+            const int col = ti.n0 + c + 8 * v;
+            if (row_ok && col < args.N) {
+              g[v] = *reinterpret_cast<const uint4*>(args.in0 + base + col);
+              u[v] = *reinterpret_cast<const uint4*>(args.in1 + base + col);
+            } else {
+              g[v] = make_uint4(0u, 0u, 0u, 0u);
+              u[v] = make_uint4(0u, 0u, 0u, 0u);
+            }
+          }
+        };
+        load_gu(0, gc, uc);
+#pragma unroll
+        for (int c = 0; c < T::BN; c += 32) {
+          uint32_t r[32];
+          tmem_ld32(t_row + c, r);
+          if (c + 32 < T::BN) load_gu(c + 32, gn, un);
+          tmem_ld_wait();
+          if (row_ok) {
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+              const int col = ti.n0 + c + 8 * v;
+              if (col >= args.N) continue;
+              float gf[8], uf[8], dg[8], du[8];
+              unpack8(gc[v], gf);
+              unpack8(uc[v], uf);
+#pragma unroll
+              for (int i = 0; i < 8; ++i) {
+                const float f = __uint_as_float(r[8 * v + i]);
+                const float sg = 1.0f / (1.0f + __expf(-gf[i]));
+                dg[i] = f * uf[i] * (sg * (1.0f + gf[i] * (1.0f - sg)));
+                du[i] = f * gf[i] * sg;
+              }
+              *reinterpret_cast<uint4*>(args.out0 + base + col) = pack8(dg);
+              *reinterpret_cast<uint4*>(args.out1 + base + col) = pack8(du);
+            }
+          }
+          if (c + 32 < T::BN) {
+#pragma unroll
+            for (int v = 0; v < 4; ++v) { gc[v] = gn[v]; uc[v] = un[v]; }
+          }
+        }
       } else {
-        // single accumulator, 256 columns
+        // single accumulator, 256 columns, plain (optionally row-scaled) store
         bool row_ok;
         int64_t base;
         if constexpr (K == Kind::WgradDown) {
@@ -437,26 +486,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (col >= args.N) continue;
             float f[8];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) f[i] = __uint_as_float(r[8 * v + i]);
-            if constexpr (K == Kind::DownDgrad) {
-              float gf[8], uf[8], dg[8], du[8];
-              unpack8(*reinterpret_cast<const uint4*>(args.in0 + base + col), gf);
-              unpack8(*reinterpret_cast<const uint4*>(args.in1 + base + col), uf);
-#pragma unroll
-              for (int i = 0; i < 8; ++i) {
-                const float sg = 1.0f / (1.0f + __expf(-gf[i]));
-                dg[i] = f[i] * uf[i] * (sg * (1.0f + gf[i] * (1.0f - sg)));
-                du[i] = f[i] * gf[i] * sg;
-              }
-              *reinterpret_cast<uint4*>(args.out0 + base + col) = pack8(dg);
-              *reinterpret_cast<uint4*>(args.out1 + base + col) = pack8(du);
-            } else {
-              if constexpr (K == Kind::DownFwd) {
-#pragma unroll
-                for (int i = 0; i < 8; ++i) f[i] *= scale;
-              }
-              *reinterpret_cast<uint4*>(args.out0 + base + col) = pack8(f);
-            }
+            for (int i = 0; i < 8; ++i) f[i] = __uint_as_float(r[8 * v + i]) * scale;
+            *reinterpret_cast<uint4*>(args.out0 + base + col) = pack8(f);
           }
         }
       }
