@@ -74,11 +74,16 @@ typedef struct CUstream_st* moe_stream_t; /* the same handle as cudaStream_t */
  *             An id outside [0, E) raises MOE_ERR_DEVICE_INDEX (the slot's
  *             weight is written as 0).
  *  logits     [T, E] fp32 out        topk_idx [T, k] int32 out    topk_w [T, k] fp32 out
- * Limits: 1 <= k <= min(E, 32); E <= 1024.
+ *  ws         moe_workspace_size(MOE_WS_ROUTE, ...) bytes, 256-byte aligned:
+ *             W_r split into three bf16 parts (hi + mid + lo reproduce the fp32
+ *             value) so the logits run on the tensor cores from exact products
+ *             with fp32 accumulation.
+ * Limits: 1 <= k <= min(E, 32); E <= 1024; d a multiple of 8.
  * ------------------------------------------------------------------------ */
 int moe_route(const moe_bf16* x, const float* w_router, const float* bias,
               const int32_t* forced_idx, int64_t T, int d, int E, int k,
-              float* logits, int32_t* topk_idx, float* topk_w, moe_stream_t stream);
+              float* logits, int32_t* topk_idx, float* topk_w,
+              void* ws, size_t ws_bytes, moe_stream_t stream);
 
 /* ------------------------------------------------------------------------
  * moe_permute — the padded expert-grouped layout and the gather into it.
@@ -231,6 +236,7 @@ int moe_route_bwd(const float* d_topk_w, const float* topk_w, const int32_t* top
  * ------------------------------------------------------------------------ */
 #define MOE_WS_PERMUTE   1
 #define MOE_WS_ROUTE_BWD 2
+#define MOE_WS_ROUTE     3
 size_t moe_workspace_size(int which, int64_t T, int d, int E, int k, int align);
 
 /* Smallest valid R_cap: T*k + E*(align-1). */

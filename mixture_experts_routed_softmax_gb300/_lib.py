@@ -16,7 +16,7 @@ _I = ctypes.c_int
 _SZ = ctypes.c_size_t
 
 SIGNATURES = {
-    "moe_route": (_I, [_P, _P, _P, _P, _I64, _I, _I, _I, _P, _P, _P, _P]),
+    "moe_route": (_I, [_P, _P, _P, _P, _I64, _I, _I, _I, _P, _P, _P, _P, _SZ, _P]),
     "moe_permute": (_I, [_P, _I64, _I, _I, _I, _P, _I, _I64, _P, _P, _P, _P, _P, _P, _SZ, _P]),
     "moe_permute_noalloc": (_I, [_P, _I64, _I, _I, _I, _P, _I, _I64, _P, _P, _P, _P, _P, _P]),
     "moe_expert_fwd": (_I, [_P, _P, _P, _I, _I, _I, _I64, _P, _P, _P, _P, _P, _P, _P, _P]),
@@ -45,6 +45,7 @@ MOE_ERR_DEVICE_TIMEOUT = 6
 
 MOE_WS_PERMUTE = 1
 MOE_WS_ROUTE_BWD = 2
+MOE_WS_ROUTE = 3
 
 KERNELS = {
     "router_logits": 1, "topk": 2, "permute": 3, "gateup_fwd": 4, "down_fwd": 5,

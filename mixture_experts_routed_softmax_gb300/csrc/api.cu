@@ -88,6 +88,7 @@ size_t moe_workspace_size(int which, int64_t T, int d, int E, int k, int align) 
   switch (which) {
     case MOE_WS_PERMUTE: return permute_ws_bytes(T, k, E);
     case MOE_WS_ROUTE_BWD: return (align > 0) ? route_bwd_ws_bytes(T, d, E, k, align) : 0;
+    case MOE_WS_ROUTE: return route_ws_bytes(d, E);
     default: return 0;
   }
 }
@@ -166,16 +167,20 @@ int moe_timer_read(float* total_ms, int* launches) {
 
 int moe_route(const moe_bf16* x, const float* w_router, const float* bias,
               const int32_t* forced_idx, int64_t T, int d, int E, int k, float* logits,
-              int32_t* topk_idx, float* topk_w, moe_stream_t stream) {
+              int32_t* topk_idx, float* topk_w, void* ws, size_t ws_bytes,
+              moe_stream_t stream) {
   if (!x || !w_router || !logits || !topk_idx || !topk_w) return MOE_ERR_ARG;
   if (T < 0 || d <= 0 || E <= 0 || k <= 0 || k > E) return MOE_ERR_ARG;
   if (k > kMaxTopK || E > kMaxExperts || d % 8 != 0) return MOE_ERR_UNSUPPORTED;
+  if (T >= ((int64_t)1 << 31)) return MOE_ERR_UNSUPPORTED;
   if (!aligned16(x)) return MOE_ERR_ARG;
+  if (!ws || ws_bytes < route_ws_bytes(d, E) || (reinterpret_cast<uintptr_t>(ws) & 255u))
+    return MOE_ERR_ARG;
   if (T == 0) return MOE_OK;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   int* st = device_status_ptr();
   if (!st) return MOE_ERR_CUDA;
-  cudaError_t e = launch_router_logits(x, w_router, bias, T, d, E, logits, s);
+  cudaError_t e = launch_router_logits(x, w_router, bias, T, d, E, logits, ws, st, s);
   if (e == cudaSuccess) e = launch_topk(logits, forced_idx, T, E, k, topk_idx, topk_w, st, s);
   return cuda_code(e);
 }

@@ -37,15 +37,17 @@
 
 namespace moe {
 
-enum class Kind { GateUpFwd, DownFwd, DownDgrad, GateUpDgrad, WgradDown, WgradGateUp };
+enum class Kind { GateUpFwd, DownFwd, DownDgrad, GateUpDgrad, WgradDown, WgradGateUp, RouterLogits };
 
 template <Kind K>
 struct Tr {
   static constexpr bool dual = (K == Kind::GateUpFwd || K == Kind::WgradGateUp);
   static constexpr bool two_seg = (K == Kind::GateUpDgrad);
   static constexpr bool kgrouped = (K == Kind::WgradDown || K == Kind::WgradGateUp);
+  static constexpr bool dense = (K == Kind::RouterLogits);   // one group of M rows
   static constexpr bool a_mn = kgrouped;                                   // A is M-contiguous
-  static constexpr bool b_mn = (K == Kind::GateUpFwd || K == Kind::DownFwd || kgrouped);
+  static constexpr bool b_mn =
+      (K == Kind::GateUpFwd || K == Kind::DownFwd || kgrouped || K == Kind::RouterLogits);
   static constexpr int BN = dual ? 128 : 256;                              // per accumulator
   static constexpr int kernel_id =
       K == Kind::GateUpFwd ? MOE_KERNEL_GATEUP_FWD
@@ -53,7 +55,8 @@ struct Tr {
       : K == Kind::DownDgrad ? MOE_KERNEL_DOWN_DGRAD
       : K == Kind::GateUpDgrad ? MOE_KERNEL_GATEUP_DGRAD
       : K == Kind::WgradDown ? MOE_KERNEL_WGRAD_DOWN
-                             : MOE_KERNEL_WGRAD_GATEUP;
+      : K == Kind::WgradGateUp ? MOE_KERNEL_WGRAD_GATEUP
+                               : MOE_KERNEL_ROUTER_LOGITS;
 };
 
 constexpr int BM = 128;            // tile rows (TMEM lanes)
@@ -77,6 +80,11 @@ struct GemmArgs {
   const moe_bf16* in0;
   const moe_bf16* in1;
   const float* row_w;
+  // RouterLogits: fp32 output, bias, number of K segments and the K offset of each in B
+  float* outf;
+  const float* bias;
+  int nseg;
+  int seg_koff;
   int* status;
 };
 
@@ -96,7 +104,13 @@ __device__ __forceinline__ void decode_tile(int tile, const GemmArgs& a, const i
   const int nt = tile % nN;
   const int mt = tile / nN;
   ti.n0 = nt * T::BN;
-  if constexpr (T::kgrouped) {
+  if constexpr (T::dense) {
+    ti.e = 0;
+    ti.m0 = (int64_t)mt * BM;
+    ti.row_end = a.M;
+    ti.kbeg = 0;
+    ti.nk = a.nk_seg * a.nseg;
+  } else if constexpr (T::kgrouped) {
     const int nM = (a.M + BM - 1) / BM;
     ti.e = mt / nM;
     ti.m0 = (int64_t)(mt % nM) * BM;
@@ -173,7 +187,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_relinquish();
   }
   // M-grouped tile table: tstart[e] = sum_{e'<e} ceil(L_e' / BM)
-  if constexpr (!T::kgrouped) {
+  if constexpr (!T::kgrouped && !T::dense) {
     for (int e = threadIdx.x; e < args.E; e += kThreads) {
       const int64_t L = args.offsets[e + 1] - args.offsets[e];
       tstart[e + 1] = (int)((L + BM - 1) / BM);
@@ -204,6 +218,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   int total;
   if constexpr (T::kgrouped) {
     total = args.E * ((args.M + BM - 1) / BM) * nN;
+  } else if constexpr (T::dense) {
+    total = ((args.M + BM - 1) / BM) * nN;
   } else {
     total = tstart[args.E] * nN;
   }
@@ -245,6 +261,15 @@ __global__ void __launch_bounds__(kThreads, 1)
               if constexpr (T::dual)
                 tma_load_2d(sB1 + j * (BK * 128), &mapB1, fb, ti.n0 + 64 * j, row0);
             }
+          } else if constexpr (T::dense) {
+            // K segment s of B starts at row s * seg_koff; A is the same in every segment
+            const int seg = ks / args.nk_seg;
+            const int kk = (ks - seg * args.nk_seg) * BK;
+            tma_load_2d(sA, &mapA0, fb, kk, (int)ti.m0);
+#pragma unroll
+            for (int j = 0; j < T::BN / 64; ++j)
+              tma_load_2d(sB0 + j * (BK * 128), &mapB0, fb, ti.n0 + 64 * j,
+                          seg * args.seg_koff + kk);
           } else {
             const int seg = (T::two_seg && ks >= args.nk_seg) ? 1 : 0;
             const int kk = (ks - seg * args.nk_seg) * BK;
@@ -409,6 +434,21 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
         }
+      } else if constexpr (K == Kind::RouterLogits) {
+        const bool row_ok = row < args.M;
+        float* orow = args.outf + row * args.N;
+#pragma unroll 1
+        for (int c = 0; c < T::BN; c += 32) {
+          uint32_t r[32];
+          tmem_ld32(t_row + c, r);
+          tmem_ld_wait();
+          if (!row_ok) continue;
+#pragma unroll 8
+          for (int i = 0; i < 32; ++i) {
+            const int col = ti.n0 + c + i;
+            if (col < args.N) orow[col] = __uint_as_float(r[i]) + (args.bias ? args.bias[col] : 0.f);
+          }
+        }
       } else if constexpr (K == Kind::DownDgrad) {
         // dG = dA * U * silu'(G), dU = dA * silu(G); the saved G, U of chunk c+1
         // are loaded while chunk c is computed
@@ -566,10 +606,11 @@ static cudaError_t launch_kind(const CUtensorMap& a0, const CUtensorMap& a1,
   int64_t grid = num_sms();
   if (tiles_upper < grid) grid = tiles_upper;
   if (grid < 1) grid = 1;
-  timer_before(Tr<K>::kernel_id, s);
+  // the router's timer brackets its weight split and this GEMM (route.cu)
+  if constexpr (K != Kind::RouterLogits) timer_before(Tr<K>::kernel_id, s);
   grouped_gemm_kernel<K><<<(unsigned)grid, kThreads, kSmemBytes, s>>>(a0, a1, b0, b1, args);
   note_launches(1);
-  timer_after(Tr<K>::kernel_id, s);
+  if constexpr (K != Kind::RouterLogits) timer_after(Tr<K>::kernel_id, s);
   return cudaGetLastError();
 }
 
@@ -580,6 +621,28 @@ static GemmArgs base_args(const GroupedDims& g, int* status) {
   a.R_cap = g.R_cap;
   a.status = status;
   return a;
+}
+
+// logits[T, E] = x[T, d] . (W_hi + W_mid + W_lo) + b, the three bf16 parts
+// stacked along K in w_split [3d, E8] (E8 = E rounded up to 8)
+cudaError_t launch_router_gemm(const moe_bf16* x, const moe_bf16* w_split, const float* bias,
+                               int64_t T, int d, int E, int E8, float* logits, int* status,
+                               cudaStream_t s) {
+  CUtensorMap a0, b0;
+  if (!map2d(&a0, x, d, T, BM) || !map2d(&b0, w_split, E8, 3 * (uint64_t)d, BK))
+    return cudaErrorInvalidValue;
+  GemmArgs a{};
+  a.E = 1;
+  a.M = (int)T;
+  a.N = E;
+  a.nk_seg = (d + BK - 1) / BK;
+  a.nseg = 3;
+  a.seg_koff = d;
+  a.outf = logits;
+  a.bias = bias;
+  a.status = status;
+  const int64_t tiles = ((T + BM - 1) / BM) * ((E + 255) / 256);
+  return launch_kind<Kind::RouterLogits>(a0, a0, b0, b0, a, tiles, s);
 }
 
 static int64_t mgrouped_tiles_upper(const GroupedDims& g, int N, int BN) {

@@ -15,82 +15,51 @@
 namespace moe {
 
 // ---------------------------------------------------------------------------
-// logits[T, E] = x[T, d] (bf16) . W_r[d, E] (fp32) + b, fp32 accumulation in
-// k order. A 64x64 output tile per CTA, 16-deep k slices staged in shared
-// memory, a 4x4 register micro-tile per thread.
+// logits[T, E] = x[T, d] (bf16) . W_r[d, E] (fp32) + b on the tensor cores.
+// W_r is split exactly into three bf16 parts, W_hi + W_mid + W_lo (8 + 8 + 8
+// significant bits: the fp32 value to within its last bit); a bf16 x bf16
+// product is exact in fp32, so x . W_r accumulates in fp32 from exact
+// products, as a CUDA-core fp32 dot product would. The parts are stacked
+// along K in the workspace, [3d, E8] with E8 = E rounded up to 8 (16-byte
+// rows for TMA), and one grouped-GEMM launch reduces over all 3d rows.
 // ---------------------------------------------------------------------------
-constexpr int kRBM = 64, kRBN = 64, kRBK = 16;
+static inline int round8(int v) { return (v + 7) & ~7; }
 
-__global__ void __launch_bounds__(256) router_logits_kernel(const moe_bf16* __restrict__ x,
-                                                            const float* __restrict__ wr,
-                                                            const float* __restrict__ bias,
-                                                            int64_t T, int d, int E,
-                                                            float* __restrict__ logits) {
-  __shared__ float xs[kRBK][kRBM + 4];
-  __shared__ float ws[kRBK][kRBN + 4];
-  const int tid = threadIdx.x;
-  const int tx = tid % 16, ty = tid / 16;
-  const int64_t m0 = (int64_t)blockIdx.y * kRBM;
-  const int n0 = blockIdx.x * kRBN;
-  float acc[4][4] = {};
-  // loader coordinates: x tile 64 rows x 16 k (4 bf16 per thread); w tile 16 k x 64 cols
-  const int xr = tid / 4, xk = (tid % 4) * 4;
-  const int wk = tid / 16, wc = (tid % 16) * 4;
-  for (int k0 = 0; k0 < d; k0 += kRBK) {
-    {
-      const int64_t row = m0 + xr;
-      const int kk = k0 + xk;
-      float v[4] = {0.f, 0.f, 0.f, 0.f};
-      if (row < T && kk < d) {  // d is a multiple of 8, so the 4-group is whole
-        const uint2 raw = *reinterpret_cast<const uint2*>(x + row * d + kk);
-        v[0] = bf16_lo(raw.x); v[1] = bf16_hi(raw.x); v[2] = bf16_lo(raw.y); v[3] = bf16_hi(raw.y);
-      }
-#pragma unroll
-      for (int i = 0; i < 4; ++i) xs[xk + i][xr] = v[i];
-    }
-    {
-      const int kk = k0 + wk;
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int c = n0 + wc + i;
-        ws[wk][wc + i] = (kk < d && c < E) ? wr[(int64_t)kk * E + c] : 0.f;
-      }
-    }
-    __syncthreads();
-#pragma unroll
-    for (int kk = 0; kk < kRBK; ++kk) {
-      float a[4], b[4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) a[i] = xs[kk][ty * 4 + i];
-#pragma unroll
-      for (int j = 0; j < 4; ++j) b[j] = ws[kk][tx * 4 + j];
-#pragma unroll
-      for (int i = 0; i < 4; ++i)
-#pragma unroll
-        for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
-    }
-    __syncthreads();
-  }
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int64_t row = m0 + ty * 4 + i;
-    if (row >= T) continue;
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int c = n0 + tx * 4 + j;
-      if (c < E) logits[row * E + c] = acc[i][j] + (bias ? bias[c] : 0.f);
-    }
-  }
+size_t route_ws_bytes(int d, int E) {
+  return ((size_t)3 * d * round8(E) * 2 + 255) & ~(size_t)255;
+}
+
+__global__ void split_router_weight_kernel(const float* __restrict__ wr, int d, int E, int E8,
+                                           moe_bf16* __restrict__ w_split) {
+  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= (int64_t)d * E8) return;
+  const int row = (int)(i / E8), e = (int)(i % E8);
+  const float w = (e < E) ? wr[(int64_t)row * E + e] : 0.f;
+  const __nv_bfloat16 hi = __float2bfloat16_rn(w);
+  const float r1 = w - __bfloat162float(hi);
+  const __nv_bfloat16 mid = __float2bfloat16_rn(r1);
+  const float r2 = r1 - __bfloat162float(mid);
+  const __nv_bfloat16 lo = __float2bfloat16_rn(r2);
+  const int64_t plane = (int64_t)d * E8;
+  w_split[i] = __bfloat16_as_ushort(hi);
+  w_split[plane + i] = __bfloat16_as_ushort(mid);
+  w_split[2 * plane + i] = __bfloat16_as_ushort(lo);
 }
 
 cudaError_t launch_router_logits(const moe_bf16* x, const float* w_router, const float* bias,
-                                 int64_t T, int d, int E, float* logits, cudaStream_t s) {
-  dim3 grid((E + kRBN - 1) / kRBN, (unsigned)((T + kRBM - 1) / kRBM));
+                                 int64_t T, int d, int E, float* logits, void* ws, int* status,
+                                 cudaStream_t s) {
+  const int E8 = round8(E);
+  moe_bf16* w_split = static_cast<moe_bf16*>(ws);
+  const int64_t n = (int64_t)d * E8;
   timer_before(MOE_KERNEL_ROUTER_LOGITS, s);
-  router_logits_kernel<<<grid, 256, 0, s>>>(x, w_router, bias, T, d, E, logits);
+  split_router_weight_kernel<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(w_router, d, E, E8,
+                                                                        w_split);
   note_launches(1);
+  cudaError_t e = cudaGetLastError();
+  if (e == cudaSuccess) e = launch_router_gemm(x, w_split, bias, T, d, E, E8, logits, status, s);
   timer_after(MOE_KERNEL_ROUTER_LOGITS, s);
-  return cudaGetLastError();
+  return e;
 }
 
 // ---------------------------------------------------------------------------

@@ -45,6 +45,7 @@ class Buffers:
     yp: torch.Tensor
     y: torch.Tensor
     ws_permute: torch.Tensor
+    ws_route: torch.Tensor
     # backward
     dyp: Optional[torch.Tensor] = None
     dg: Optional[torch.Tensor] = None
@@ -112,6 +113,9 @@ class MoELayer:
             yp=torch.empty(R, d, dtype=BF16, **kw),
             y=torch.empty(T, d, dtype=BF16, **kw),
             ws_permute=torch.empty(max(ws_p, 256), dtype=torch.uint8, **kw),
+            ws_route=torch.empty(
+                int(self.lib.moe_workspace_size(_lib.MOE_WS_ROUTE, T, d, E, k, self.align)),
+                dtype=torch.uint8, **kw),
         )
         if backward:
             ws_r = int(self.lib.moe_workspace_size(_lib.MOE_WS_ROUTE_BWD, T, d, E, k, self.align))
@@ -133,7 +137,7 @@ class MoELayer:
     def route(self, x, b: Buffers, forced_idx=None, stream=None):
         _lib.call("moe_route", _p(x), _p(self.w_router), _p(self.bias), _p(forced_idx),
                   b.T, self.d, self.E, self.k, _p(b.logits), _p(b.topk_idx), _p(b.topk_w),
-                  _stream(stream))
+                  _p(b.ws_route), b.ws_route.numel(), _stream(stream))
 
     def permute(self, x, b: Buffers, topk_idx=None, stream=None):
         idx = b.topk_idx if topk_idx is None else topk_idx

@@ -52,13 +52,17 @@ def test_host_argument_checks(lib):
     from mixture_experts_routed_softmax_gb300 import _lib as L
     P = 0x1000  # a non-null, 16-byte aligned stand-in; these calls return before touching it
     # null required pointers
-    assert lib.moe_route(None, P, None, None, 4, 8, 4, 2, P, P, P, None) == L.MOE_ERR_ARG
+    wr = lib.moe_workspace_size(3, 4, 8, 4, 2, 16)
+    assert wr >= 3 * 8 * 8 * 2
+    assert lib.moe_route(None, P, None, None, 4, 8, 4, 2, P, P, P, P, wr, None) == L.MOE_ERR_ARG
     # k > E
-    assert lib.moe_route(P, P, None, None, 4, 8, 4, 5, P, P, P, None) == L.MOE_ERR_ARG
+    assert lib.moe_route(P, P, None, None, 4, 8, 4, 5, P, P, P, P, wr, None) == L.MOE_ERR_ARG
     # d not a multiple of 8
-    assert lib.moe_route(P, P, None, None, 4, 12, 4, 2, P, P, P, None) == L.MOE_ERR_UNSUPPORTED
+    assert lib.moe_route(P, P, None, None, 4, 12, 4, 2, P, P, P, P, wr, None) == L.MOE_ERR_UNSUPPORTED
     # E above the limit
-    assert lib.moe_route(P, P, None, None, 4, 8, 2048, 2, P, P, P, None) == L.MOE_ERR_UNSUPPORTED
+    assert lib.moe_route(P, P, None, None, 4, 8, 2048, 2, P, P, P, P, wr, None) == L.MOE_ERR_UNSUPPORTED
+    # workspace too small
+    assert lib.moe_route(P, P, None, None, 4, 8, 4, 2, P, P, P, P, wr - 1, None) == L.MOE_ERR_ARG
     ws = lib.moe_workspace_size(1, 4, 8, 4, 2, 16)
     cap = lib.moe_row_capacity(4, 2, 4, 16)
     # align not a power of two / out of range
