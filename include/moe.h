@@ -151,6 +151,8 @@ int moe_permute_noalloc(const int32_t* topk_idx, int64_t T, int k, int E, int al
  * Yp = A.W_down[e] (times row_w[r] in fp32 when row_w is given).
  *
  *  xp [R_cap, d] bf16, offsets [E+1] int64 (from moe_permute)
+ *  T, k: tokens and top-k of the routing (T*k pairs; sizes the tile schedule:
+ *        with few rows per expert the gate/up GEMM uses narrower tiles)
  *  w_gate, w_up [E, d, f] bf16;  w_down [E, f, d] bf16
  *  row_w [R_cap] fp32 or NULL (NULL: Yp is the unscaled expert output, the
  *        layout the combine and moe_expert_bwd expect)
@@ -160,7 +162,7 @@ int moe_permute_noalloc(const int32_t* topk_idx, int64_t T, int k, int E, int al
  * Limits: d, f multiples of 8 (16-byte rows for TMA); E <= 1024.
  * ------------------------------------------------------------------------ */
 int moe_expert_fwd(const moe_bf16* xp, const int64_t* offsets, const float* row_w,
-                   int E, int d, int f, int64_t R_cap,
+                   int64_t T, int k, int E, int d, int f, int64_t R_cap,
                    const moe_bf16* w_gate, const moe_bf16* w_up, const moe_bf16* w_down,
                    moe_bf16* g, moe_bf16* u, moe_bf16* a, moe_bf16* yp,
                    moe_stream_t stream);

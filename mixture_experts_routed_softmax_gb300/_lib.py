@@ -19,7 +19,8 @@ SIGNATURES = {
     "moe_route": (_I, [_P, _P, _P, _P, _I64, _I, _I, _I, _P, _P, _P, _P, _SZ, _P]),
     "moe_permute": (_I, [_P, _I64, _I, _I, _I, _P, _I, _I64, _P, _P, _P, _P, _P, _P, _SZ, _P]),
     "moe_permute_noalloc": (_I, [_P, _I64, _I, _I, _I, _P, _I, _I64, _P, _P, _P, _P, _P, _P]),
-    "moe_expert_fwd": (_I, [_P, _P, _P, _I, _I, _I, _I64, _P, _P, _P, _P, _P, _P, _P, _P]),
+    "moe_expert_fwd": (_I, [_P, _P, _P, _I64, _I, _I, _I, _I, _I64, _P, _P, _P, _P, _P, _P, _P,
+                            _P]),
     "moe_combine": (_I, [_P, _P, _P, _I64, _I, _I, _P, _P]),
     "moe_expert_bwd": (_I, [_P, _P, _P, _P, _P, _I64, _I, _I, _I, _I, _I64,
                             _P, _P, _P, _P, _P, _P, _P, _P,

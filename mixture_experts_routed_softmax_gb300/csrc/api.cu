@@ -212,13 +212,15 @@ static int check_expert_dims(int E, int d, int f, int64_t R_cap) {
   return MOE_OK;
 }
 
-int moe_expert_fwd(const moe_bf16* xp, const int64_t* offsets, const float* row_w, int E, int d,
-                   int f, int64_t R_cap, const moe_bf16* w_gate, const moe_bf16* w_up,
-                   const moe_bf16* w_down, moe_bf16* g, moe_bf16* u, moe_bf16* a, moe_bf16* yp,
-                   moe_stream_t stream) {
+int moe_expert_fwd(const moe_bf16* xp, const int64_t* offsets, const float* row_w, int64_t T,
+                   int k, int E, int d, int f, int64_t R_cap, const moe_bf16* w_gate,
+                   const moe_bf16* w_up, const moe_bf16* w_down, moe_bf16* g, moe_bf16* u,
+                   moe_bf16* a, moe_bf16* yp, moe_stream_t stream) {
   if (!xp || !offsets || !w_gate || !w_up || !w_down || !g || !u || !a || !yp) return MOE_ERR_ARG;
+  if (T < 0 || k <= 0 || k > E) return MOE_ERR_ARG;
   int rc = check_expert_dims(E, d, f, R_cap);
   if (rc) return rc;
+  if (R_cap < T * k) return MOE_ERR_CAPACITY;
   for (const void* p : {(const void*)xp, (const void*)w_gate, (const void*)w_up,
                         (const void*)w_down, (const void*)g, (const void*)u, (const void*)a,
                         (const void*)yp})
@@ -226,7 +228,7 @@ int moe_expert_fwd(const moe_bf16* xp, const int64_t* offsets, const float* row_
   int* st = device_status_ptr();
   if (!st) return MOE_ERR_CUDA;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  GroupedDims gd{offsets, E, d, f, R_cap};
+  GroupedDims gd{offsets, E, d, f, R_cap, T * k};
   cudaError_t e = launch_gateup_fwd(gd, xp, w_gate, w_up, g, u, a, st, s);
   if (e == cudaSuccess) e = launch_down_fwd(gd, a, w_down, row_w, yp, st, s);
   return cuda_code(e);
@@ -267,7 +269,7 @@ int moe_expert_bwd(const moe_bf16* dy, const int32_t* src_pair, const int32_t* d
   int* st = device_status_ptr();
   if (!st) return MOE_ERR_CUDA;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  GroupedDims gd{offsets, E, d, f, R_cap};
+  GroupedDims gd{offsets, E, d, f, R_cap, T * k};
   cudaError_t e = launch_combine_bwd(dy, yp, src_pair, topk_w, offsets, T, k, E, d, R_cap, dyp,
                                      d_topk_w, s);
   if (e == cudaSuccess) e = launch_down_dgrad(gd, dyp, w_down, g, u, dg, du, st, s);

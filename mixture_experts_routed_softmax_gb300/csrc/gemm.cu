@@ -37,20 +37,24 @@
 
 namespace moe {
 
-enum class Kind { GateUpFwd, DownFwd, DownDgrad, GateUpDgrad, WgradDown, WgradGateUp, RouterLogits };
+enum class Kind {
+  GateUpFwd, DownFwd, DownDgrad, GateUpDgrad, WgradDown, WgradGateUp, RouterLogits,
+  GateUpFwdNarrow   // GateUpFwd with 64-column tiles, for experts of at most ~128 rows
+};
 
 template <Kind K>
 struct Tr {
-  static constexpr bool dual = (K == Kind::GateUpFwd || K == Kind::WgradGateUp);
+  static constexpr bool gateup_fwd = (K == Kind::GateUpFwd || K == Kind::GateUpFwdNarrow);
+  static constexpr bool dual = (gateup_fwd || K == Kind::WgradGateUp);
   static constexpr bool two_seg = (K == Kind::GateUpDgrad);
   static constexpr bool kgrouped = (K == Kind::WgradDown || K == Kind::WgradGateUp);
   static constexpr bool dense = (K == Kind::RouterLogits);   // one group of M rows
   static constexpr bool a_mn = kgrouped;                                   // A is M-contiguous
   static constexpr bool b_mn =
-      (K == Kind::GateUpFwd || K == Kind::DownFwd || kgrouped || K == Kind::RouterLogits);
-  static constexpr int BN = dual ? 128 : 256;                              // per accumulator
+      (gateup_fwd || K == Kind::DownFwd || kgrouped || K == Kind::RouterLogits);
+  static constexpr int BN = K == Kind::GateUpFwdNarrow ? 64 : dual ? 128 : 256;   // per accumulator
   static constexpr int kernel_id =
-      K == Kind::GateUpFwd ? MOE_KERNEL_GATEUP_FWD
+      gateup_fwd ? MOE_KERNEL_GATEUP_FWD
       : K == Kind::DownFwd ? MOE_KERNEL_DOWN_FWD
       : K == Kind::DownDgrad ? MOE_KERNEL_DOWN_DGRAD
       : K == Kind::GateUpDgrad ? MOE_KERNEL_GATEUP_DGRAD
@@ -229,6 +233,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr uint32_t kIdesc =
       idesc_bf16(BM, T::dual ? 2 * T::BN : T::BN, T::a_mn ? 1 : 0, T::b_mn ? 1 : 0);
   constexpr uint32_t kBBytes = (uint32_t)T::BN * BK * 2;
+  constexpr uint32_t kTxBytes = kABytes + (T::dual ? 2u : 1u) * kBBytes;   // bytes TMA lands per stage
+  static_assert(kTxBytes <= (uint32_t)kStageBytes, "stage overflow");
 
   if (warp == 0) {
     if (lane == 0) {
@@ -249,7 +255,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t sA = s_base + stage * kStageBytes;
           const uint32_t sB0 = sA + kABytes;
           const uint32_t sB1 = sB0 + kBBytes;
-          mbar_arrive_expect_tx(fb, kStageBytes);
+          mbar_arrive_expect_tx(fb, kTxBytes);
           if constexpr (T::kgrouped) {
             const int row0 = (int)(ti.kbeg + (int64_t)ks * BK);
 #pragma unroll
@@ -380,13 +386,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const uint32_t t_row = tmem_base + ((uint32_t)(wq * 32) << 16) + (uint32_t)acc * 256u;
 
-      if constexpr (K == Kind::GateUpFwd) {
+      if constexpr (T::gateup_fwd) {
         const bool row_ok = row < ti.row_end;
 #pragma unroll 1
         for (int c = 0; c < T::BN; c += 32) {
           uint32_t g[32], u[32];
           tmem_ld32(t_row + c, g);
-          tmem_ld32(t_row + 128 + c, u);
+          tmem_ld32(t_row + T::BN + c, u);
           tmem_ld_wait();
           if (row_ok) {
 #pragma unroll
@@ -415,7 +421,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int c = 0; c < T::BN; c += 32) {
           uint32_t g[32], u[32];
           tmem_ld32(t_row + c, g);
-          tmem_ld32(t_row + 128 + c, u);
+          tmem_ld32(t_row + T::BN + c, u);
           tmem_ld_wait();
           if (row_ok) {
 #pragma unroll
@@ -660,6 +666,13 @@ cudaError_t launch_gateup_fwd(const GroupedDims& g, const moe_bf16* xp, const mo
   a.N = g.f;
   a.nk_seg = (g.d + BK - 1) / BK;
   a.out0 = G; a.out1 = U; a.out2 = A;
+  // Few rows per expert (the weight-bound regime): 128-wide tiles leave too few
+  // tiles to fill every SM's last round of weight streaming; halve them.
+  const int64_t rows = (g.P + g.E - 1) / g.E;
+  const int64_t tiles = (int64_t)g.E * ((rows + BM - 1) / BM) * ((g.f + 127) / 128);
+  if (tiles < 8 * (int64_t)num_sms())
+    return launch_kind<Kind::GateUpFwdNarrow>(a0, a0, b0, b1, a,
+                                              mgrouped_tiles_upper(g, g.f, 64), s);
   return launch_kind<Kind::GateUpFwd>(a0, a0, b0, b1, a, mgrouped_tiles_upper(g, g.f, 128), s);
 }
 

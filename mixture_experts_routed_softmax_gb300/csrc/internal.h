@@ -56,6 +56,7 @@ struct GroupedDims {
   const int64_t* offsets;
   int E, d, f;
   int64_t R_cap;
+  int64_t P;        // token-expert pairs (T * k): sizes the tile schedule
 };
 cudaError_t launch_gateup_fwd(const GroupedDims& g, const moe_bf16* xp, const moe_bf16* w_gate,
                               const moe_bf16* w_up, moe_bf16* G, moe_bf16* U, moe_bf16* A,

@@ -146,8 +146,8 @@ class MoELayer:
                   _p(b.xp), _p(b.ws_permute), b.ws_permute.numel(), _stream(stream))
 
     def expert_fwd(self, b: Buffers, row_w=None, stream=None):
-        _lib.call("moe_expert_fwd", _p(b.xp), _p(b.offsets), _p(row_w), self.E, self.d, self.f,
-                  b.R_cap, _p(self.w_gate), _p(self.w_up), _p(self.w_down), _p(b.g), _p(b.u),
+        _lib.call("moe_expert_fwd", _p(b.xp), _p(b.offsets), _p(row_w), b.T, self.k, self.E,
+                  self.d, self.f, b.R_cap, _p(self.w_gate), _p(self.w_up), _p(self.w_down), _p(b.g), _p(b.u),
                   _p(b.a), _p(b.yp), _stream(stream))
 
     def combine(self, rows, b: Buffers, out, weights=True, stream=None):

@@ -75,8 +75,8 @@ def test_host_argument_checks(lib):
     # misaligned activation pointer
     assert lib.moe_permute(P, 4, 2, 4, 16, P + 2, 8, cap, P, P, P, P, P, P, ws, None) == L.MOE_ERR_ARG
     # expert GEMMs: f not a multiple of 8
-    assert lib.moe_expert_fwd(P, P, None, 4, 8, 12, cap, P, P, P, P, P, P, P, None) == L.MOE_ERR_UNSUPPORTED
-    assert lib.moe_expert_fwd(P, None, None, 4, 8, 16, cap, P, P, P, P, P, P, P, None) == L.MOE_ERR_ARG
+    assert lib.moe_expert_fwd(P, P, None, 4, 2, 4, 8, 12, cap, P, P, P, P, P, P, P, None) == L.MOE_ERR_UNSUPPORTED
+    assert lib.moe_expert_fwd(P, None, None, 4, 2, 4, 8, 16, cap, P, P, P, P, P, P, P, None) == L.MOE_ERR_ARG
     # combine: k above the slot limit
     assert lib.moe_combine(P, P, None, 4, 33, 8, P, None) == L.MOE_ERR_UNSUPPORTED
     # route backward: workspace missing

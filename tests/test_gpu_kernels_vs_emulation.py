@@ -26,6 +26,9 @@ CASES = {
     "multi_tile": (520, 392, 520, 8, 3, 128, None, None),
     "skewed_empty": (700, 264, 384, 16, 4, 32, 1.2, 1.5),
     "qwen_like": (1024, 2048, 768, 128, 8, 16, 1.1, 0.2),
+    # enough tiles that the gate/up GEMM keeps its 128-wide tiles (the cases above,
+    # with few rows per expert, run the narrow 64-wide variant)
+    "wide_tiles": (8192, 256, 2048, 16, 2, 128, None, None),
 }
 
 
