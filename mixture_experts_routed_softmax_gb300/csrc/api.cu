@@ -88,7 +88,7 @@ size_t moe_workspace_size(int which, int64_t T, int d, int E, int k, int align) 
   switch (which) {
     case MOE_WS_PERMUTE: return permute_ws_bytes(T, k, E);
     case MOE_WS_ROUTE_BWD: return (align > 0) ? route_bwd_ws_bytes(T, d, E, k, align) : 0;
-    case MOE_WS_ROUTE: return route_ws_bytes(d, E);
+    case MOE_WS_ROUTE: return route_ws_bytes(T, d, E);
     default: return 0;
   }
 }
@@ -174,7 +174,7 @@ int moe_route(const moe_bf16* x, const float* w_router, const float* bias,
   if (k > kMaxTopK || E > kMaxExperts || d % 8 != 0) return MOE_ERR_UNSUPPORTED;
   if (T >= ((int64_t)1 << 31)) return MOE_ERR_UNSUPPORTED;
   if (!aligned16(x)) return MOE_ERR_ARG;
-  if (!ws || ws_bytes < route_ws_bytes(d, E) || (reinterpret_cast<uintptr_t>(ws) & 255u))
+  if (!ws || ws_bytes < route_ws_bytes(T, d, E) || (reinterpret_cast<uintptr_t>(ws) & 255u))
     return MOE_ERR_ARG;
   if (T == 0) return MOE_OK;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);

@@ -42,6 +42,12 @@ enum class Kind {
   GateUpFwdNarrow   // GateUpFwd with 64-column tiles, for experts of at most ~128 rows
 };
 
+constexpr int BM = 128;            // tile rows (TMEM lanes)
+constexpr int BK = 64;             // k per stage: one 128-byte swizzle atom of bf16
+constexpr int kABytes = BM * BK * 2;                      // 16 KiB
+constexpr int kRingBytes = 192 * 1024;                    // the TMA ring: 4 x 48 KiB, 6 x 32 KiB
+constexpr int kMaxStages = 8;
+
 template <Kind K>
 struct Tr {
   static constexpr bool gateup_fwd = (K == Kind::GateUpFwd || K == Kind::GateUpFwdNarrow);
@@ -53,6 +59,10 @@ struct Tr {
   static constexpr bool b_mn =
       (gateup_fwd || K == Kind::DownFwd || kgrouped || K == Kind::RouterLogits);
   static constexpr int BN = K == Kind::GateUpFwdNarrow ? 64 : dual ? 128 : 256;   // per accumulator
+  // bytes TMA lands per stage (A tile + one or two B tiles), and as many stages as fit
+  static constexpr int tx_bytes = kABytes + (dual ? 2 : 1) * BN * BK * 2;
+  static constexpr int stages = kRingBytes / tx_bytes > kMaxStages ? kMaxStages
+                                                                   : kRingBytes / tx_bytes;
   static constexpr int kernel_id =
       gateup_fwd ? MOE_KERNEL_GATEUP_FWD
       : K == Kind::DownFwd ? MOE_KERNEL_DOWN_FWD
@@ -63,14 +73,10 @@ struct Tr {
                                : MOE_KERNEL_ROUTER_LOGITS;
 };
 
-constexpr int BM = 128;            // tile rows (TMEM lanes)
-constexpr int BK = 64;             // k per stage: one 128-byte swizzle atom of bf16
-constexpr int kStages = 4;
-constexpr int kABytes = BM * BK * 2;                      // 16 KiB
-constexpr int kStageBytes = 3 * kABytes;                  // 48 KiB: A + 32 KiB of B
 constexpr int kTmemCols = 512;                            // 2 accumulator buffers x 256 columns
-constexpr int kThreads = 256;
-constexpr int kSmemBytes = kStages * kStageBytes + 1024 /*bars*/ + 4 * (kMaxExperts + 1) + 1024;
+constexpr int kEpiWarps = 8;                              // two warpgroups, each half the columns
+constexpr int kThreads = 128 + 32 * kEpiWarps;
+constexpr int kSmemBytes = kRingBytes + 1024 /*bars*/ + 4 * (kMaxExperts + 1) + 1024;
 
 struct GemmArgs {
   const int64_t* offsets;
@@ -89,6 +95,8 @@ struct GemmArgs {
   const float* bias;
   int nseg;
   int seg_koff;
+  int ksplit;         // RouterLogits: K split into this many chunks (1: write logits + bias)
+  int ksteps_split;   // k-steps per chunk
   int* status;
 };
 
@@ -109,11 +117,16 @@ __device__ __forceinline__ void decode_tile(int tile, const GemmArgs& a, const i
   const int mt = tile / nN;
   ti.n0 = nt * T::BN;
   if constexpr (T::dense) {
-    ti.e = 0;
-    ti.m0 = (int64_t)mt * BM;
+    // tile = (m-tile * nN + n-tile) * ksplit + split; e holds the split
+    const int sp = tile % a.ksplit;
+    const int mn = tile / a.ksplit;
+    ti.e = sp;
+    ti.n0 = (mn % nN) * T::BN;
+    ti.m0 = (int64_t)(mn / nN) * BM;
     ti.row_end = a.M;
-    ti.kbeg = 0;
-    ti.nk = a.nk_seg * a.nseg;
+    ti.kbeg = (int64_t)sp * a.ksteps_split;
+    const int total_steps = a.nk_seg * a.nseg;
+    ti.nk = (int)min((int64_t)a.ksteps_split, (int64_t)total_steps - ti.kbeg);
   } else if constexpr (T::kgrouped) {
     const int nM = (a.M + BM - 1) / BM;
     ti.e = mt / nM;
@@ -152,17 +165,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~(uintptr_t)1023);
   const uint32_t s_base = smem_u32(smem);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kStages * kStageBytes);
-  // bars: full[kStages], empty[kStages], tfull[2], tempty[2], drain
+  constexpr int kStages = T::stages;
+  constexpr int kStageBytes = T::tx_bytes;              // a multiple of 8 KiB: atoms stay aligned
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kRingBytes);
+  // bars: full[kMaxStages], empty[kMaxStages], tfull[2], tempty[2], drain
   const uint32_t bar0 = smem_u32(bars);
   auto full_bar = [&](int s) { return bar0 + 8u * s; };
-  auto empty_bar = [&](int s) { return bar0 + 8u * (kStages + s); };
-  auto tfull_bar = [&](int b) { return bar0 + 8u * (2 * kStages + b); };
-  auto tempty_bar = [&](int b) { return bar0 + 8u * (2 * kStages + 2 + b); };
-  const uint32_t drain_bar = bar0 + 8u * (2 * kStages + 4);
-  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bars + 2 * kStages + 5);
+  auto empty_bar = [&](int s) { return bar0 + 8u * (kMaxStages + s); };
+  auto tfull_bar = [&](int b) { return bar0 + 8u * (2 * kMaxStages + b); };
+  auto tempty_bar = [&](int b) { return bar0 + 8u * (2 * kMaxStages + 2 + b); };
+  const uint32_t drain_bar = bar0 + 8u * (2 * kMaxStages + 4);
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bars + 2 * kMaxStages + 5);
   volatile int* s_abort = reinterpret_cast<volatile int*>(s_tmem + 1);
-  int* tstart = reinterpret_cast<int*>(smem + kStages * kStageBytes + 1024);
+  int* tstart = reinterpret_cast<int*>(smem + kRingBytes + 1024);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -174,7 +189,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(tfull_bar(b), 1);
-      mbar_init(tempty_bar(b), 4);
+      mbar_init(tempty_bar(b), kEpiWarps);
     }
     mbar_init(drain_bar, 1);
     *s_abort = 0;
@@ -223,7 +238,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if constexpr (T::kgrouped) {
     total = args.E * ((args.M + BM - 1) / BM) * nN;
   } else if constexpr (T::dense) {
-    total = ((args.M + BM - 1) / BM) * nN;
+    total = ((args.M + BM - 1) / BM) * nN * args.ksplit;
   } else {
     total = tstart[args.E] * nN;
   }
@@ -233,8 +248,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr uint32_t kIdesc =
       idesc_bf16(BM, T::dual ? 2 * T::BN : T::BN, T::a_mn ? 1 : 0, T::b_mn ? 1 : 0);
   constexpr uint32_t kBBytes = (uint32_t)T::BN * BK * 2;
-  constexpr uint32_t kTxBytes = kABytes + (T::dual ? 2u : 1u) * kBBytes;   // bytes TMA lands per stage
-  static_assert(kTxBytes <= (uint32_t)kStageBytes, "stage overflow");
+  constexpr uint32_t kTxBytes = (uint32_t)T::tx_bytes;
+  static_assert(kStages * kStageBytes <= kRingBytes && kStageBytes % 8192 == 0, "ring layout");
 
   if (warp == 0) {
     if (lane == 0) {
@@ -269,8 +284,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           } else if constexpr (T::dense) {
             // K segment s of B starts at row s * seg_koff; A is the same in every segment
-            const int seg = ks / args.nk_seg;
-            const int kk = (ks - seg * args.nk_seg) * BK;
+            const int kg = (int)ti.kbeg + ks;
+            const int seg = kg / args.nk_seg;
+            const int kk = (kg - seg * args.nk_seg) * BK;
             tma_load_2d(sA, &mapA0, fb, kk, (int)ti.m0);
 #pragma unroll
             for (int j = 0; j < T::BN / 64; ++j)
@@ -357,8 +373,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp >= 4) {
     // ------------------------------------------------------------ epilogue --
-    const int wq = warp - 4;                   // TMEM lane quarter of this warp
+    const int wq = (warp - 4) & 3;             // TMEM lane quarter of this warp
     const int rloc = wq * 32 + lane;           // accumulator row of this thread
+    // the two epilogue warpgroups split each accumulator's columns in halves
+    constexpr int kHalf = T::BN / 2;
+    const int c_lo = ((warp - 4) >> 2) * kHalf, c_hi = c_lo + kHalf;
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
@@ -371,7 +390,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (ti.nk == 0) {
           if (row_ok) {
             const uint4 z = make_uint4(0u, 0u, 0u, 0u);
-            for (int c = 0; c < T::BN; c += 8) {
+            for (int c = c_lo; c < c_hi; c += 8) {
               const int col = ti.n0 + c;
               if (col >= args.N) break;
               const int64_t o = ti.e * estride + row * args.N + col;
@@ -389,7 +408,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if constexpr (T::gateup_fwd) {
         const bool row_ok = row < ti.row_end;
 #pragma unroll 1
-        for (int c = 0; c < T::BN; c += 32) {
+        for (int c = c_lo; c < c_hi; c += 32) {
           uint32_t g[32], u[32];
           tmem_ld32(t_row + c, g);
           tmem_ld32(t_row + T::BN + c, u);
@@ -418,7 +437,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool row_ok = row < args.M;
         const int64_t base = ti.e * (int64_t)args.M * args.N + row * args.N;
 #pragma unroll 1
-        for (int c = 0; c < T::BN; c += 32) {
+        for (int c = c_lo; c < c_hi; c += 32) {
           uint32_t g[32], u[32];
           tmem_ld32(t_row + c, g);
           tmem_ld32(t_row + T::BN + c, u);
@@ -441,18 +460,21 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       } else if constexpr (K == Kind::RouterLogits) {
+        // one split: logits + bias; several: this split's fp32 partial, summed later
         const bool row_ok = row < args.M;
-        float* orow = args.outf + row * args.N;
+        const bool whole = args.ksplit == 1;
+        float* orow = args.outf + ((int64_t)ti.e * args.M + row) * args.N;
 #pragma unroll 1
-        for (int c = 0; c < T::BN; c += 32) {
+        for (int c = c_lo; c < c_hi; c += 32) {
           uint32_t r[32];
           tmem_ld32(t_row + c, r);
           tmem_ld_wait();
           if (!row_ok) continue;
-#pragma unroll 8
+#pragma unroll
           for (int i = 0; i < 32; ++i) {
             const int col = ti.n0 + c + i;
-            if (col < args.N) orow[col] = __uint_as_float(r[i]) + (args.bias ? args.bias[col] : 0.f);
+            if (col < args.N)
+              orow[col] = __uint_as_float(r[i]) + (whole && args.bias ? args.bias[col] : 0.f);
           }
         }
       } else if constexpr (K == Kind::DownDgrad) {
@@ -474,12 +496,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
         };
-        load_gu(0, gc, uc);
+        load_gu(c_lo, gc, uc);
 #pragma unroll
-        for (int c = 0; c < T::BN; c += 32) {
+        for (int c = c_lo; c < c_hi; c += 32) {
           uint32_t r[32];
           tmem_ld32(t_row + c, r);
-          if (c + 32 < T::BN) load_gu(c + 32, gn, un);
+          if (c + 32 < c_hi) load_gu(c + 32, gn, un);
           tmem_ld_wait();
           if (row_ok) {
 #pragma unroll
@@ -500,7 +522,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               *reinterpret_cast<uint4*>(args.out1 + base + col) = pack8(du);
             }
           }
-          if (c + 32 < T::BN) {
+          if (c + 32 < c_hi) {
 #pragma unroll
             for (int v = 0; v < 4; ++v) { gc[v] = gn[v]; uc[v] = un[v]; }
           }
@@ -521,7 +543,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (args.row_w && row_ok) scale = args.row_w[row];
         }
 #pragma unroll 1
-        for (int c = 0; c < T::BN; c += 32) {
+        for (int c = c_lo; c < c_hi; c += 32) {
           uint32_t r[32];
           tmem_ld32(t_row + c, r);
           tmem_ld_wait();
@@ -629,11 +651,25 @@ static GemmArgs base_args(const GroupedDims& g, int* status) {
   return a;
 }
 
+// The number of K chunks the router GEMM splits into: none while the output
+// tiles alone fill half the SMs; else enough chunks to cover the SMs once, at
+// least 4 k-steps per chunk, at most 16.
+int router_ksplit(int64_t T, int d, int E) {
+  const int64_t tiles = ((T + BM - 1) / BM) * ((E + 255) / 256);
+  const int steps = 3 * ((d + BK - 1) / BK);
+  if (2 * tiles >= num_sms()) return 1;
+  int64_t sp = ((int64_t)num_sms() + tiles - 1) / tiles;
+  sp = sp > 16 ? 16 : sp;
+  sp = sp > steps / 4 ? steps / 4 : sp;
+  return sp < 1 ? 1 : (int)sp;
+}
+
 // logits[T, E] = x[T, d] . (W_hi + W_mid + W_lo) + b, the three bf16 parts
-// stacked along K in w_split [3d, E8] (E8 = E rounded up to 8)
+// stacked along K in w_split [3d, E8] (E8 = E rounded up to 8). With ksplit > 1
+// the K range is cut into chunks whose fp32 partials go to out[ksplit][T][E].
 cudaError_t launch_router_gemm(const moe_bf16* x, const moe_bf16* w_split, const float* bias,
-                               int64_t T, int d, int E, int E8, float* logits, int* status,
-                               cudaStream_t s) {
+                               int64_t T, int d, int E, int E8, int ksplit, float* out,
+                               int* status, cudaStream_t s) {
   CUtensorMap a0, b0;
   if (!map2d(&a0, x, d, T, BM) || !map2d(&b0, w_split, E8, 3 * (uint64_t)d, BK))
     return cudaErrorInvalidValue;
@@ -644,10 +680,14 @@ cudaError_t launch_router_gemm(const moe_bf16* x, const moe_bf16* w_split, const
   a.nk_seg = (d + BK - 1) / BK;
   a.nseg = 3;
   a.seg_koff = d;
-  a.outf = logits;
+  const int steps = a.nk_seg * a.nseg;
+  a.ksteps_split = (steps + ksplit - 1) / ksplit;
+  a.ksplit = (steps + a.ksteps_split - 1) / a.ksteps_split;   // no empty chunk
+  if (a.ksplit != ksplit) return cudaErrorInvalidValue;
+  a.outf = out;
   a.bias = bias;
   a.status = status;
-  const int64_t tiles = ((T + BM - 1) / BM) * ((E + 255) / 256);
+  const int64_t tiles = ((T + BM - 1) / BM) * ((E + 255) / 256) * a.ksplit;
   return launch_kind<Kind::RouterLogits>(a0, a0, b0, b0, a, tiles, s);
 }
 

@@ -20,7 +20,7 @@ int* device_status_ptr();
 int num_sms();
 
 // route.cu
-size_t route_ws_bytes(int d, int E);
+size_t route_ws_bytes(int64_t T, int d, int E);
 cudaError_t launch_router_logits(const moe_bf16* x, const float* w_router, const float* bias,
                                  int64_t T, int d, int E, float* logits, void* ws, int* status,
                                  cudaStream_t s);
@@ -49,9 +49,10 @@ cudaError_t launch_combine_bwd(const moe_bf16* dy, const moe_bf16* yp, const int
                                cudaStream_t s);
 
 // gemm.cu (tcgen05 grouped GEMMs)
+int router_ksplit(int64_t T, int d, int E);
 cudaError_t launch_router_gemm(const moe_bf16* x, const moe_bf16* w_split, const float* bias,
-                               int64_t T, int d, int E, int E8, float* logits, int* status,
-                               cudaStream_t s);
+                               int64_t T, int d, int E, int E8, int ksplit, float* out,
+                               int* status, cudaStream_t s);
 struct GroupedDims {
   const int64_t* offsets;
   int E, d, f;

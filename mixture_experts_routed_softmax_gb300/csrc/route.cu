@@ -25,8 +25,22 @@ namespace moe {
 // ---------------------------------------------------------------------------
 static inline int round8(int v) { return (v + 7) & ~7; }
 
-size_t route_ws_bytes(int d, int E) {
-  return ((size_t)3 * d * round8(E) * 2 + 255) & ~(size_t)255;
+static inline size_t al256r(size_t b) { return (b + 255) & ~(size_t)255; }
+
+// workspace: the split weight [3d, E8] bf16, then (split K) fp32 partials [ksplit, T, E]
+size_t route_ws_bytes(int64_t T, int d, int E) {
+  const int sp = router_ksplit(T, d, E);
+  return al256r((size_t)3 * d * round8(E) * 2) + (sp > 1 ? al256r((size_t)sp * T * E * 4) : 0);
+}
+
+// logits = sum of the split-K partials in split order, plus the bias
+__global__ void router_reduce_kernel(const float* __restrict__ part, int ksplit, int64_t n, int E,
+                                     const float* __restrict__ bias, float* __restrict__ logits) {
+  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= n) return;
+  float acc = 0.f;
+  for (int sp = 0; sp < ksplit; ++sp) acc += part[(int64_t)sp * n + i];
+  logits[i] = acc + (bias ? bias[i % E] : 0.f);
 }
 
 __global__ void split_router_weight_kernel(const float* __restrict__ wr, int d, int E, int E8,
@@ -57,7 +71,21 @@ cudaError_t launch_router_logits(const moe_bf16* x, const float* w_router, const
                                                                         w_split);
   note_launches(1);
   cudaError_t e = cudaGetLastError();
-  if (e == cudaSuccess) e = launch_router_gemm(x, w_split, bias, T, d, E, E8, logits, status, s);
+  const int sp = router_ksplit(T, d, E);
+  if (sp == 1) {
+    if (e == cudaSuccess) e = launch_router_gemm(x, w_split, bias, T, d, E, E8, 1, logits, status, s);
+  } else {
+    float* part = reinterpret_cast<float*>(reinterpret_cast<char*>(ws) +
+                                           al256r((size_t)3 * d * E8 * 2));
+    if (e == cudaSuccess) e = launch_router_gemm(x, w_split, bias, T, d, E, E8, sp, part, status, s);
+    if (e == cudaSuccess) {
+      const int64_t nel = T * E;
+      router_reduce_kernel<<<(unsigned)((nel + 255) / 256), 256, 0, s>>>(part, sp, nel, E, bias,
+                                                                         logits);
+      note_launches(1);
+      e = cudaGetLastError();
+    }
+  }
   timer_after(MOE_KERNEL_ROUTER_LOGITS, s);
   return e;
 }
