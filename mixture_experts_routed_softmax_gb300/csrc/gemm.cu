@@ -76,7 +76,11 @@ struct Tr {
 constexpr int kTmemCols = 512;                            // 2 accumulator buffers x 256 columns
 constexpr int kEpiWarps = 8;                              // two warpgroups, each half the columns
 constexpr int kThreads = 128 + 32 * kEpiWarps;
-constexpr int kSmemBytes = kRingBytes + 1024 /*bars*/ + 4 * (kMaxExperts + 1) + 1024;
+// K-grouped kinds stage their bf16 output through shared memory for TMA stores:
+// per epilogue warp, 32 rows x 16 columns of each of up to two outputs (1 KiB each)
+constexpr int kStageOutBytes = kEpiWarps * 2 * 1024;
+constexpr int kTstartBytes = (4 * (kMaxExperts + 1) + 127) & ~127;
+constexpr int kSmemBytes = kRingBytes + 1024 /*bars*/ + kTstartBytes + kStageOutBytes + 1024;
 
 struct GemmArgs {
   const int64_t* offsets;
@@ -159,7 +163,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA0,
                         const __grid_constant__ CUtensorMap mapA1,
                         const __grid_constant__ CUtensorMap mapB0,
-                        const __grid_constant__ CUtensorMap mapB1, const GemmArgs args) {
+                        const __grid_constant__ CUtensorMap mapB1,
+                        const __grid_constant__ CUtensorMap mapO0,
+                        const __grid_constant__ CUtensorMap mapO1, const GemmArgs args) {
   using T = Tr<K>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -178,6 +184,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bars + 2 * kMaxStages + 5);
   volatile int* s_abort = reinterpret_cast<volatile int*>(s_tmem + 1);
   int* tstart = reinterpret_cast<int*>(smem + kRingBytes + 1024);
+  uint8_t* stage_out = smem + kRingBytes + 1024 + kTstartBytes;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -433,29 +440,50 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
         }
-      } else if constexpr (K == Kind::WgradGateUp) {
-        const bool row_ok = row < args.M;
-        const int64_t base = ti.e * (int64_t)args.M * args.N + row * args.N;
+      } else if constexpr (T::kgrouped) {
+        // dW[e] rows m0 + 32 wq .. +32 of this warp: each 16-column slice of each
+        // output is packed to bf16 in shared memory and written by one TMA store
+        // (the tensor map clips rows >= M and columns >= N)
+        uint8_t* stg = stage_out + (warp - 4) * 2048;
+        const uint32_t stg0 = smem_u32(stg);
+        const int mrow = (int)ti.m0 + wq * 32;
 #pragma unroll 1
         for (int c = c_lo; c < c_hi; c += 32) {
           uint32_t g[32], u[32];
           tmem_ld32(t_row + c, g);
-          tmem_ld32(t_row + T::BN + c, u);
+          if constexpr (T::dual) tmem_ld32(t_row + T::BN + c, u);
           tmem_ld_wait();
-          if (row_ok) {
 #pragma unroll
-            for (int v = 0; v < 4; ++v) {
-              const int col = ti.n0 + c + 8 * v;
-              if (col < args.N) {
-                float gf[8], uf[8];
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                  gf[i] = __uint_as_float(g[8 * v + i]);
-                  uf[i] = __uint_as_float(u[8 * v + i]);
-                }
-                *reinterpret_cast<uint4*>(args.out0 + base + col) = pack8(gf);
-                *reinterpret_cast<uint4*>(args.out1 + base + col) = pack8(uf);
-              }
+          for (int h = 0; h < 2; ++h) {
+            if (lane == 0) bulk_wait_read();
+            __syncwarp();
+            uint4* d0 = reinterpret_cast<uint4*>(stg + lane * 32);
+            d0[0] = make_uint4(pack_bf16(__uint_as_float(g[16 * h + 0]), __uint_as_float(g[16 * h + 1])),
+                               pack_bf16(__uint_as_float(g[16 * h + 2]), __uint_as_float(g[16 * h + 3])),
+                               pack_bf16(__uint_as_float(g[16 * h + 4]), __uint_as_float(g[16 * h + 5])),
+                               pack_bf16(__uint_as_float(g[16 * h + 6]), __uint_as_float(g[16 * h + 7])));
+            d0[1] = make_uint4(pack_bf16(__uint_as_float(g[16 * h + 8]), __uint_as_float(g[16 * h + 9])),
+                               pack_bf16(__uint_as_float(g[16 * h + 10]), __uint_as_float(g[16 * h + 11])),
+                               pack_bf16(__uint_as_float(g[16 * h + 12]), __uint_as_float(g[16 * h + 13])),
+                               pack_bf16(__uint_as_float(g[16 * h + 14]), __uint_as_float(g[16 * h + 15])));
+            if constexpr (T::dual) {
+              uint4* d1 = reinterpret_cast<uint4*>(stg + 1024 + lane * 32);
+              d1[0] = make_uint4(pack_bf16(__uint_as_float(u[16 * h + 0]), __uint_as_float(u[16 * h + 1])),
+                                 pack_bf16(__uint_as_float(u[16 * h + 2]), __uint_as_float(u[16 * h + 3])),
+                                 pack_bf16(__uint_as_float(u[16 * h + 4]), __uint_as_float(u[16 * h + 5])),
+                                 pack_bf16(__uint_as_float(u[16 * h + 6]), __uint_as_float(u[16 * h + 7])));
+              d1[1] = make_uint4(pack_bf16(__uint_as_float(u[16 * h + 8]), __uint_as_float(u[16 * h + 9])),
+                                 pack_bf16(__uint_as_float(u[16 * h + 10]), __uint_as_float(u[16 * h + 11])),
+                                 pack_bf16(__uint_as_float(u[16 * h + 12]), __uint_as_float(u[16 * h + 13])),
+                                 pack_bf16(__uint_as_float(u[16 * h + 14]), __uint_as_float(u[16 * h + 15])));
+            }
+            fence_async_smem();
+            __syncwarp();
+            const int col = ti.n0 + c + 16 * h;
+            if (lane == 0 && col < args.N && mrow < args.M) {
+              tma_store_3d(&mapO0, stg0, col, mrow, ti.e);
+              if constexpr (T::dual) tma_store_3d(&mapO1, stg0 + 1024, col, mrow, ti.e);
+              bulk_commit();
             }
           }
         }
@@ -529,15 +557,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       } else {
         // single accumulator, 256 columns, plain (optionally row-scaled) store
-        bool row_ok;
-        int64_t base;
-        if constexpr (K == Kind::WgradDown) {
-          row_ok = row < args.M;
-          base = ti.e * (int64_t)args.M * args.N + row * args.N;
-        } else {
-          row_ok = row < ti.row_end;
-          base = row * args.N;
-        }
+        const bool row_ok = row < ti.row_end;
+        const int64_t base = row * args.N;
         float scale = 1.0f;
         if constexpr (K == Kind::DownFwd) {
           if (args.row_w && row_ok) scale = args.row_w[row];
@@ -563,6 +584,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(tempty_bar(acc));
       if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+    }
+    if constexpr (T::kgrouped) {
+      if (lane == 0) bulk_wait_all();   // the staged stores are done before the CTA exits
+      __syncwarp();
     }
   }
   tc_fence_before();
@@ -620,10 +645,24 @@ static bool map3d(CUtensorMap* m, const void* ptr, uint64_t d0, uint64_t d1, uin
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 3-D bf16 map over [E, M, N] (N innermost) for TMA stores of 32-row x 16-column boxes
+static bool map3d_out(CUtensorMap* m, const void* ptr, uint64_t N, uint64_t M, uint64_t E) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {N, M, E};
+  cuuint64_t strides[2] = {N * 2, N * M * 2};
+  cuuint32_t box[3] = {16, 32, 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box,
+            es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+            CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 template <Kind K>
 static cudaError_t launch_kind(const CUtensorMap& a0, const CUtensorMap& a1,
                                const CUtensorMap& b0, const CUtensorMap& b1, const GemmArgs& args,
-                               int64_t tiles_upper, cudaStream_t s) {
+                               int64_t tiles_upper, cudaStream_t s,
+                               const CUtensorMap* o0 = nullptr, const CUtensorMap* o1 = nullptr) {
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(once, [] {
@@ -636,7 +675,8 @@ static cudaError_t launch_kind(const CUtensorMap& a0, const CUtensorMap& a1,
   if (grid < 1) grid = 1;
   // the router's timer brackets its weight split and this GEMM (route.cu)
   if constexpr (K != Kind::RouterLogits) timer_before(Tr<K>::kernel_id, s);
-  grouped_gemm_kernel<K><<<(unsigned)grid, kThreads, kSmemBytes, s>>>(a0, a1, b0, b1, args);
+  grouped_gemm_kernel<K><<<(unsigned)grid, kThreads, kSmemBytes, s>>>(
+      a0, a1, b0, b1, o0 ? *o0 : a0, o1 ? *o1 : (o0 ? *o0 : a0), args);
   note_launches(1);
   if constexpr (K != Kind::RouterLogits) timer_after(Tr<K>::kernel_id, s);
   return cudaGetLastError();
@@ -762,25 +802,27 @@ cudaError_t launch_gateup_dgrad(const GroupedDims& g, const moe_bf16* dG, const 
 
 cudaError_t launch_wgrad_down(const GroupedDims& g, const moe_bf16* A, const moe_bf16* dyp,
                               moe_bf16* dw_down, int* status, cudaStream_t s) {
-  CUtensorMap a0, b0;
+  CUtensorMap a0, b0, o0;
   // dW_down[e] (f x d) = A_e^T . dYp_e: A read as [K = rows, M = f], B as [K = rows, N = d]
-  if (!map2d(&a0, A, g.f, g.R_cap, BK) || !map2d(&b0, dyp, g.d, g.R_cap, BK))
+  if (!map2d(&a0, A, g.f, g.R_cap, BK) || !map2d(&b0, dyp, g.d, g.R_cap, BK) ||
+      !map3d_out(&o0, dw_down, g.d, g.f, g.E))
     return cudaErrorInvalidValue;
   GemmArgs a = base_args(g, status);
   a.M = g.f;
   a.N = g.d;
   a.out0 = dw_down;
   const int64_t tiles = (int64_t)g.E * ((g.f + BM - 1) / BM) * ((g.d + 255) / 256);
-  return launch_kind<Kind::WgradDown>(a0, a0, b0, b0, a, tiles, s);
+  return launch_kind<Kind::WgradDown>(a0, a0, b0, b0, a, tiles, s, &o0);
 }
 
 cudaError_t launch_wgrad_gateup(const GroupedDims& g, const moe_bf16* xp, const moe_bf16* dG,
                                 const moe_bf16* dU, moe_bf16* dw_gate, moe_bf16* dw_up,
                                 int* status, cudaStream_t s) {
-  CUtensorMap a0, b0, b1;
+  CUtensorMap a0, b0, b1, o0, o1;
   // dW_gate[e] (d x f) = Xp_e^T . dG_e: A read as [K = rows, M = d], B as [K = rows, N = f]
   if (!map2d(&a0, xp, g.d, g.R_cap, BK) || !map2d(&b0, dG, g.f, g.R_cap, BK) ||
-      !map2d(&b1, dU, g.f, g.R_cap, BK))
+      !map2d(&b1, dU, g.f, g.R_cap, BK) || !map3d_out(&o0, dw_gate, g.f, g.d, g.E) ||
+      !map3d_out(&o1, dw_up, g.f, g.d, g.E))
     return cudaErrorInvalidValue;
   GemmArgs a = base_args(g, status);
   a.M = g.d;
@@ -788,7 +830,7 @@ cudaError_t launch_wgrad_gateup(const GroupedDims& g, const moe_bf16* xp, const 
   a.out0 = dw_gate;
   a.out1 = dw_up;
   const int64_t tiles = (int64_t)g.E * ((g.d + BM - 1) / BM) * ((g.f + 127) / 128);
-  return launch_kind<Kind::WgradGateUp>(a0, a0, b0, b1, a, tiles, s);
+  return launch_kind<Kind::WgradGateUp>(a0, a0, b0, b1, a, tiles, s, &o0, &o1);
 }
 
 }  // namespace moe
