@@ -76,9 +76,10 @@ struct Tr {
 constexpr int kTmemCols = 512;                            // 2 accumulator buffers x 256 columns
 constexpr int kEpiWarps = 8;                              // two warpgroups, each half the columns
 constexpr int kThreads = 128 + 32 * kEpiWarps;
-// K-grouped kinds stage their bf16 output through shared memory for TMA stores:
-// per epilogue warp, 32 rows x 16 columns of each of up to two outputs (1 KiB each)
-constexpr int kStageOutBytes = kEpiWarps * 2 * 1024;
+// Epilogues stage their bf16 outputs through shared memory for TMA stores: per
+// epilogue warp, 32 rows x 16 columns of each of up to three outputs (1 KiB each)
+constexpr int kStagePerWarp = 3 * 1024;
+constexpr int kStageOutBytes = kEpiWarps * kStagePerWarp;
 constexpr int kTstartBytes = (4 * (kMaxExperts + 1) + 127) & ~127;
 constexpr int kSmemBytes = kRingBytes + 1024 /*bars*/ + kTstartBytes + kStageOutBytes + 1024;
 
@@ -152,6 +153,50 @@ __device__ __forceinline__ void decode_tile(int tile, const GemmArgs& a, const i
   }
 }
 
+// Writes 32 columns (packed bf16 pairs pk[o][0..15]) of NOUT outputs for this
+// warp's 32 rows. A warp whose rows all belong to the tile's group stages each
+// 16-column slice in shared memory and lets lane 0 issue one TMA store per
+// output (coordinates {col, row} or {col, row, e}; the maps clip at the tensor
+// edge); a warp straddling the group end stores row by row with masks.
+template <int NOUT, bool K3D>
+__device__ __forceinline__ void put_chunk(const uint32_t (&pk)[NOUT][16], uint8_t* stg,
+                                          const CUtensorMap* const* maps, moe_bf16* const* outs,
+                                          bool tma_ok, bool row_ok, int64_t row, int col, int N,
+                                          int row0, int e, int lane) {
+  if (tma_ok) {
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      if (lane == 0) bulk_wait_read();
+      __syncwarp();
+#pragma unroll
+      for (int o = 0; o < NOUT; ++o) {
+        uint4* d = reinterpret_cast<uint4*>(stg + o * 1024 + lane * 32);
+        d[0] = make_uint4(pk[o][8 * h + 0], pk[o][8 * h + 1], pk[o][8 * h + 2], pk[o][8 * h + 3]);
+        d[1] = make_uint4(pk[o][8 * h + 4], pk[o][8 * h + 5], pk[o][8 * h + 6], pk[o][8 * h + 7]);
+      }
+      fence_async_smem();
+      __syncwarp();
+      if (lane == 0 && col + 16 * h < N) {
+#pragma unroll
+        for (int o = 0; o < NOUT; ++o) {
+          if constexpr (K3D) tma_store_3d(maps[o], smem_u32(stg + o * 1024), col + 16 * h, row0, e);
+          else tma_store_2d(maps[o], smem_u32(stg + o * 1024), col + 16 * h, row0);
+        }
+        bulk_commit();
+      }
+    }
+  } else if (row_ok) {
+#pragma unroll
+    for (int v = 0; v < 4; ++v) {
+      if (col + 8 * v >= N) break;
+#pragma unroll
+      for (int o = 0; o < NOUT; ++o)
+        *reinterpret_cast<uint4*>(outs[o] + row * N + col + 8 * v) =
+            make_uint4(pk[o][4 * v + 0], pk[o][4 * v + 1], pk[o][4 * v + 2], pk[o][4 * v + 3]);
+    }
+  }
+}
+
 // bounded wait used on the way out: ignores the abort flag, still time-limited
 __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, int* status) {
   volatile int never = 0;
@@ -165,7 +210,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const __grid_constant__ CUtensorMap mapB0,
                         const __grid_constant__ CUtensorMap mapB1,
                         const __grid_constant__ CUtensorMap mapO0,
-                        const __grid_constant__ CUtensorMap mapO1, const GemmArgs args) {
+                        const __grid_constant__ CUtensorMap mapO1,
+                        const __grid_constant__ CUtensorMap mapO2, const GemmArgs args) {
   using T = Tr<K>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -412,84 +458,54 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const uint32_t t_row = tmem_base + ((uint32_t)(wq * 32) << 16) + (uint32_t)acc * 256u;
 
+      // this warp's 32 rows: all inside the tile's group (or, for dW, stored by
+      // TMA, which clips at M) -> staged TMA stores; else masked row stores
+      const int row0 = (int)(ti.m0 + wq * 32);
+      const bool tma_ok = T::kgrouped ? (row0 < args.M) : ((int64_t)row0 + 32 <= ti.row_end);
+      const bool row_ok = T::kgrouped ? false : (row < ti.row_end);
+      uint8_t* stg = stage_out + (warp - 4) * kStagePerWarp;
+      const CUtensorMap* maps[3] = {&mapO0, &mapO1, &mapO2};
+      moe_bf16* outs[3] = {args.out0, args.out1, args.out2};
       if constexpr (T::gateup_fwd) {
-        const bool row_ok = row < ti.row_end;
 #pragma unroll 1
         for (int c = c_lo; c < c_hi; c += 32) {
           uint32_t g[32], u[32];
           tmem_ld32(t_row + c, g);
           tmem_ld32(t_row + T::BN + c, u);
           tmem_ld_wait();
-          if (row_ok) {
+          uint32_t pk[3][16];
 #pragma unroll
-            for (int v = 0; v < 4; ++v) {
-              const int col = ti.n0 + c + 8 * v;
-              if (col < args.N) {
-                float gf[8], uf[8], af[8];
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                  gf[i] = __uint_as_float(g[8 * v + i]);
-                  uf[i] = __uint_as_float(u[8 * v + i]);
-                  af[i] = gf[i] / (1.0f + __expf(-gf[i])) * uf[i];
-                }
-                const int64_t o = row * args.N + col;
-                *reinterpret_cast<uint4*>(args.out0 + o) = pack8(gf);
-                *reinterpret_cast<uint4*>(args.out1 + o) = pack8(uf);
-                *reinterpret_cast<uint4*>(args.out2 + o) = pack8(af);
-              }
-            }
+          for (int i = 0; i < 16; ++i) {
+            const float g0 = __uint_as_float(g[2 * i]), g1 = __uint_as_float(g[2 * i + 1]);
+            const float u0 = __uint_as_float(u[2 * i]), u1 = __uint_as_float(u[2 * i + 1]);
+            pk[0][i] = pack_bf16(g0, g1);
+            pk[1][i] = pack_bf16(u0, u1);
+            pk[2][i] = pack_bf16(g0 / (1.0f + __expf(-g0)) * u0, g1 / (1.0f + __expf(-g1)) * u1);
           }
+          put_chunk<3, false>(pk, stg, maps, outs, tma_ok, row_ok, row, ti.n0 + c, args.N, row0,
+                              0, lane);
         }
       } else if constexpr (T::kgrouped) {
-        // dW[e] rows m0 + 32 wq .. +32 of this warp: each 16-column slice of each
-        // output is packed to bf16 in shared memory and written by one TMA store
-        // (the tensor map clips rows >= M and columns >= N)
-        uint8_t* stg = stage_out + (warp - 4) * 2048;
-        const uint32_t stg0 = smem_u32(stg);
-        const int mrow = (int)ti.m0 + wq * 32;
+        constexpr int NO = T::dual ? 2 : 1;
 #pragma unroll 1
         for (int c = c_lo; c < c_hi; c += 32) {
           uint32_t g[32], u[32];
           tmem_ld32(t_row + c, g);
           if constexpr (T::dual) tmem_ld32(t_row + T::BN + c, u);
           tmem_ld_wait();
+          uint32_t pk[NO][16];
 #pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            if (lane == 0) bulk_wait_read();
-            __syncwarp();
-            uint4* d0 = reinterpret_cast<uint4*>(stg + lane * 32);
-            d0[0] = make_uint4(pack_bf16(__uint_as_float(g[16 * h + 0]), __uint_as_float(g[16 * h + 1])),
-                               pack_bf16(__uint_as_float(g[16 * h + 2]), __uint_as_float(g[16 * h + 3])),
-                               pack_bf16(__uint_as_float(g[16 * h + 4]), __uint_as_float(g[16 * h + 5])),
-                               pack_bf16(__uint_as_float(g[16 * h + 6]), __uint_as_float(g[16 * h + 7])));
-            d0[1] = make_uint4(pack_bf16(__uint_as_float(g[16 * h + 8]), __uint_as_float(g[16 * h + 9])),
-                               pack_bf16(__uint_as_float(g[16 * h + 10]), __uint_as_float(g[16 * h + 11])),
-                               pack_bf16(__uint_as_float(g[16 * h + 12]), __uint_as_float(g[16 * h + 13])),
-                               pack_bf16(__uint_as_float(g[16 * h + 14]), __uint_as_float(g[16 * h + 15])));
-            if constexpr (T::dual) {
-              uint4* d1 = reinterpret_cast<uint4*>(stg + 1024 + lane * 32);
-              d1[0] = make_uint4(pack_bf16(__uint_as_float(u[16 * h + 0]), __uint_as_float(u[16 * h + 1])),
-                                 pack_bf16(__uint_as_float(u[16 * h + 2]), __uint_as_float(u[16 * h + 3])),
-                                 pack_bf16(__uint_as_float(u[16 * h + 4]), __uint_as_float(u[16 * h + 5])),
-                                 pack_bf16(__uint_as_float(u[16 * h + 6]), __uint_as_float(u[16 * h + 7])));
-              d1[1] = make_uint4(pack_bf16(__uint_as_float(u[16 * h + 8]), __uint_as_float(u[16 * h + 9])),
-                                 pack_bf16(__uint_as_float(u[16 * h + 10]), __uint_as_float(u[16 * h + 11])),
-                                 pack_bf16(__uint_as_float(u[16 * h + 12]), __uint_as_float(u[16 * h + 13])),
-                                 pack_bf16(__uint_as_float(u[16 * h + 14]), __uint_as_float(u[16 * h + 15])));
-            }
-            fence_async_smem();
-            __syncwarp();
-            const int col = ti.n0 + c + 16 * h;
-            if (lane == 0 && col < args.N && mrow < args.M) {
-              tma_store_3d(&mapO0, stg0, col, mrow, ti.e);
-              if constexpr (T::dual) tma_store_3d(&mapO1, stg0 + 1024, col, mrow, ti.e);
-              bulk_commit();
-            }
+          for (int i = 0; i < 16; ++i) {
+            pk[0][i] = pack_bf16(__uint_as_float(g[2 * i]), __uint_as_float(g[2 * i + 1]));
+            if constexpr (T::dual)
+              pk[NO - 1][i] = pack_bf16(__uint_as_float(u[2 * i]), __uint_as_float(u[2 * i + 1]));
           }
+          put_chunk<NO, true>(pk, stg, maps, outs, tma_ok, false, row, ti.n0 + c, args.N, row0,
+                              ti.e, lane);
         }
       } else if constexpr (K == Kind::RouterLogits) {
         // one split: logits + bias; several: this split's fp32 partial, summed later
-        const bool row_ok = row < args.M;
+        const bool in_m = row < args.M;
         const bool whole = args.ksplit == 1;
         float* orow = args.outf + ((int64_t)ti.e * args.M + row) * args.N;
 #pragma unroll 1
@@ -497,7 +513,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint32_t r[32];
           tmem_ld32(t_row + c, r);
           tmem_ld_wait();
-          if (!row_ok) continue;
+          if (!in_m) continue;
 #pragma unroll
           for (int i = 0; i < 32; ++i) {
             const int col = ti.n0 + c + i;
@@ -508,7 +524,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       } else if constexpr (K == Kind::DownDgrad) {
         // dG = dA * U * silu'(G), dU = dA * silu(G); the saved G, U of chunk c+1
         // are loaded while chunk c is computed
-        const bool row_ok = row < ti.row_end;
         const int64_t base = row * args.N;
         uint4 gc[4], uc[4], gn[4], un[4];
         auto load_gu = [&](int c, uint4* g, uint4* u) {
@@ -531,25 +546,27 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_ld32(t_row + c, r);
           if (c + 32 < c_hi) load_gu(c + 32, gn, un);
           tmem_ld_wait();
-          if (row_ok) {
+          uint32_t pk[2][16];
 #pragma unroll
-            for (int v = 0; v < 4; ++v) {
-              const int col = ti.n0 + c + 8 * v;
-              if (col >= args.N) continue;
-              float gf[8], uf[8], dg[8], du[8];
-              unpack8(gc[v], gf);
-              unpack8(uc[v], uf);
+          for (int v = 0; v < 4; ++v) {
+            float gf[8], uf[8], dg[8], du[8];
+            unpack8(gc[v], gf);
+            unpack8(uc[v], uf);
 #pragma unroll
-              for (int i = 0; i < 8; ++i) {
-                const float f = __uint_as_float(r[8 * v + i]);
-                const float sg = 1.0f / (1.0f + __expf(-gf[i]));
-                dg[i] = f * uf[i] * (sg * (1.0f + gf[i] * (1.0f - sg)));
-                du[i] = f * gf[i] * sg;
-              }
-              *reinterpret_cast<uint4*>(args.out0 + base + col) = pack8(dg);
-              *reinterpret_cast<uint4*>(args.out1 + base + col) = pack8(du);
+            for (int i = 0; i < 8; ++i) {
+              const float f = __uint_as_float(r[8 * v + i]);
+              const float sg = 1.0f / (1.0f + __expf(-gf[i]));
+              dg[i] = f * uf[i] * (sg * (1.0f + gf[i] * (1.0f - sg)));
+              du[i] = f * gf[i] * sg;
+            }
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              pk[0][4 * v + i] = pack_bf16(dg[2 * i], dg[2 * i + 1]);
+              pk[1][4 * v + i] = pack_bf16(du[2 * i], du[2 * i + 1]);
             }
           }
+          put_chunk<2, false>(pk, stg, maps, outs, tma_ok, row_ok, row, ti.n0 + c, args.N, row0,
+                              0, lane);
           if (c + 32 < c_hi) {
 #pragma unroll
             for (int v = 0; v < 4; ++v) { gc[v] = gn[v]; uc[v] = un[v]; }
@@ -557,8 +574,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       } else {
         // single accumulator, 256 columns, plain (optionally row-scaled) store
-        const bool row_ok = row < ti.row_end;
-        const int64_t base = row * args.N;
         float scale = 1.0f;
         if constexpr (K == Kind::DownFwd) {
           if (args.row_w && row_ok) scale = args.row_w[row];
@@ -568,16 +583,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint32_t r[32];
           tmem_ld32(t_row + c, r);
           tmem_ld_wait();
-          if (!row_ok) continue;
+          uint32_t pk[1][16];
 #pragma unroll
-          for (int v = 0; v < 4; ++v) {
-            const int col = ti.n0 + c + 8 * v;
-            if (col >= args.N) continue;
-            float f[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) f[i] = __uint_as_float(r[8 * v + i]) * scale;
-            *reinterpret_cast<uint4*>(args.out0 + base + col) = pack8(f);
-          }
+          for (int i = 0; i < 16; ++i)
+            pk[0][i] = pack_bf16(__uint_as_float(r[2 * i]) * scale,
+                                 __uint_as_float(r[2 * i + 1]) * scale);
+          put_chunk<1, false>(pk, stg, maps, outs, tma_ok, row_ok, row, ti.n0 + c, args.N, row0,
+                              0, lane);
         }
       }
       tc_fence_before();
@@ -585,10 +597,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) mbar_arrive(tempty_bar(acc));
       if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
     }
-    if constexpr (T::kgrouped) {
-      if (lane == 0) bulk_wait_all();   // the staged stores are done before the CTA exits
-      __syncwarp();
-    }
+    if (lane == 0) bulk_wait_all();     // the staged stores are done before the CTA exits
+    __syncwarp();
   }
   tc_fence_before();
   __syncthreads();
@@ -645,6 +655,19 @@ static bool map3d(CUtensorMap* m, const void* ptr, uint64_t d0, uint64_t d1, uin
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 2-D bf16 map over a row buffer [R, N] for TMA stores of 32-row x 16-column boxes
+static bool map2d_out(CUtensorMap* m, const void* ptr, uint64_t N, uint64_t R) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {N, R};
+  cuuint64_t strides[1] = {N * 2};
+  cuuint32_t box[2] = {16, 32};
+  cuuint32_t es[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box,
+            es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+            CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // 3-D bf16 map over [E, M, N] (N innermost) for TMA stores of 32-row x 16-column boxes
 static bool map3d_out(CUtensorMap* m, const void* ptr, uint64_t N, uint64_t M, uint64_t E) {
   EncodeTiledFn fn = encode_fn();
@@ -662,7 +685,8 @@ template <Kind K>
 static cudaError_t launch_kind(const CUtensorMap& a0, const CUtensorMap& a1,
                                const CUtensorMap& b0, const CUtensorMap& b1, const GemmArgs& args,
                                int64_t tiles_upper, cudaStream_t s,
-                               const CUtensorMap* o0 = nullptr, const CUtensorMap* o1 = nullptr) {
+                               const CUtensorMap* o0 = nullptr, const CUtensorMap* o1 = nullptr,
+                               const CUtensorMap* o2 = nullptr) {
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(once, [] {
@@ -675,8 +699,9 @@ static cudaError_t launch_kind(const CUtensorMap& a0, const CUtensorMap& a1,
   if (grid < 1) grid = 1;
   // the router's timer brackets its weight split and this GEMM (route.cu)
   if constexpr (K != Kind::RouterLogits) timer_before(Tr<K>::kernel_id, s);
+  const CUtensorMap& m0 = o0 ? *o0 : a0;
   grouped_gemm_kernel<K><<<(unsigned)grid, kThreads, kSmemBytes, s>>>(
-      a0, a1, b0, b1, o0 ? *o0 : a0, o1 ? *o1 : (o0 ? *o0 : a0), args);
+      a0, a1, b0, b1, m0, o1 ? *o1 : m0, o2 ? *o2 : m0, args);
   note_launches(1);
   if constexpr (K != Kind::RouterLogits) timer_after(Tr<K>::kernel_id, s);
   return cudaGetLastError();
@@ -738,9 +763,10 @@ static int64_t mgrouped_tiles_upper(const GroupedDims& g, int N, int BN) {
 cudaError_t launch_gateup_fwd(const GroupedDims& g, const moe_bf16* xp, const moe_bf16* w_gate,
                               const moe_bf16* w_up, moe_bf16* G, moe_bf16* U, moe_bf16* A,
                               int* status, cudaStream_t s) {
-  CUtensorMap a0, b0, b1;
+  CUtensorMap a0, b0, b1, o0, o1, o2;
   if (!map2d(&a0, xp, g.d, g.R_cap, BM) || !map3d(&b0, w_gate, g.f, g.d, g.E, BK) ||
-      !map3d(&b1, w_up, g.f, g.d, g.E, BK))
+      !map3d(&b1, w_up, g.f, g.d, g.E, BK) || !map2d_out(&o0, G, g.f, g.R_cap) ||
+      !map2d_out(&o1, U, g.f, g.R_cap) || !map2d_out(&o2, A, g.f, g.R_cap))
     return cudaErrorInvalidValue;
   GemmArgs a = base_args(g, status);
   a.N = g.f;
@@ -752,52 +778,58 @@ cudaError_t launch_gateup_fwd(const GroupedDims& g, const moe_bf16* xp, const mo
   const int64_t tiles = (int64_t)g.E * ((rows + BM - 1) / BM) * ((g.f + 127) / 128);
   if (tiles < 8 * (int64_t)num_sms())
     return launch_kind<Kind::GateUpFwdNarrow>(a0, a0, b0, b1, a,
-                                              mgrouped_tiles_upper(g, g.f, 64), s);
-  return launch_kind<Kind::GateUpFwd>(a0, a0, b0, b1, a, mgrouped_tiles_upper(g, g.f, 128), s);
+                                              mgrouped_tiles_upper(g, g.f, 64), s, &o0, &o1, &o2);
+  return launch_kind<Kind::GateUpFwd>(a0, a0, b0, b1, a, mgrouped_tiles_upper(g, g.f, 128), s,
+                                      &o0, &o1, &o2);
 }
 
 cudaError_t launch_down_fwd(const GroupedDims& g, const moe_bf16* A, const moe_bf16* w_down,
                             const float* row_w, moe_bf16* yp, int* status, cudaStream_t s) {
-  CUtensorMap a0, b0;
-  if (!map2d(&a0, A, g.f, g.R_cap, BM) || !map3d(&b0, w_down, g.d, g.f, g.E, BK))
+  CUtensorMap a0, b0, o0;
+  if (!map2d(&a0, A, g.f, g.R_cap, BM) || !map3d(&b0, w_down, g.d, g.f, g.E, BK) ||
+      !map2d_out(&o0, yp, g.d, g.R_cap))
     return cudaErrorInvalidValue;
   GemmArgs a = base_args(g, status);
   a.N = g.d;
   a.nk_seg = (g.f + BK - 1) / BK;
   a.out0 = yp;
   a.row_w = row_w;
-  return launch_kind<Kind::DownFwd>(a0, a0, b0, b0, a, mgrouped_tiles_upper(g, g.d, 256), s);
+  return launch_kind<Kind::DownFwd>(a0, a0, b0, b0, a, mgrouped_tiles_upper(g, g.d, 256), s, &o0);
 }
 
 cudaError_t launch_down_dgrad(const GroupedDims& g, const moe_bf16* dyp, const moe_bf16* w_down,
                               const moe_bf16* G, const moe_bf16* U, moe_bf16* dG, moe_bf16* dU,
                               int* status, cudaStream_t s) {
-  CUtensorMap a0, b0;
+  CUtensorMap a0, b0, o0, o1;
   // dA[r, c] = sum_j dyp[r, j] W_down[e][c, j]: B is W_down[e] read as [N = f rows, K = d]
-  if (!map2d(&a0, dyp, g.d, g.R_cap, BM) || !map3d(&b0, w_down, g.d, g.f, g.E, 256))
+  if (!map2d(&a0, dyp, g.d, g.R_cap, BM) || !map3d(&b0, w_down, g.d, g.f, g.E, 256) ||
+      !map2d_out(&o0, dG, g.f, g.R_cap) || !map2d_out(&o1, dU, g.f, g.R_cap))
     return cudaErrorInvalidValue;
   GemmArgs a = base_args(g, status);
   a.N = g.f;
   a.nk_seg = (g.d + BK - 1) / BK;
   a.in0 = G; a.in1 = U;
   a.out0 = dG; a.out1 = dU;
-  return launch_kind<Kind::DownDgrad>(a0, a0, b0, b0, a, mgrouped_tiles_upper(g, g.f, 256), s);
+  return launch_kind<Kind::DownDgrad>(a0, a0, b0, b0, a, mgrouped_tiles_upper(g, g.f, 256), s,
+                                      &o0, &o1);
 }
 
 cudaError_t launch_gateup_dgrad(const GroupedDims& g, const moe_bf16* dG, const moe_bf16* dU,
                                 const moe_bf16* w_gate, const moe_bf16* w_up, moe_bf16* dxp,
                                 int* status, cudaStream_t s) {
-  CUtensorMap a0, a1, b0, b1;
+  CUtensorMap a0, a1, b0, b1, o0;
   // dXp[r, i] = sum_c dG[r, c] W_gate[e][i, c] + dU[r, c] W_up[e][i, c]:
   // B is W_gate[e] / W_up[e] read as [N = d rows, K = f]
   if (!map2d(&a0, dG, g.f, g.R_cap, BM) || !map2d(&a1, dU, g.f, g.R_cap, BM) ||
-      !map3d(&b0, w_gate, g.f, g.d, g.E, 256) || !map3d(&b1, w_up, g.f, g.d, g.E, 256))
+      !map3d(&b0, w_gate, g.f, g.d, g.E, 256) || !map3d(&b1, w_up, g.f, g.d, g.E, 256) ||
+      !map2d_out(&o0, dxp, g.d, g.R_cap))
     return cudaErrorInvalidValue;
   GemmArgs a = base_args(g, status);
   a.N = g.d;
   a.nk_seg = (g.f + BK - 1) / BK;
   a.out0 = dxp;
-  return launch_kind<Kind::GateUpDgrad>(a0, a1, b0, b1, a, mgrouped_tiles_upper(g, g.d, 256), s);
+  return launch_kind<Kind::GateUpDgrad>(a0, a1, b0, b1, a, mgrouped_tiles_upper(g, g.d, 256), s,
+                                        &o0);
 }
 
 cudaError_t launch_wgrad_down(const GroupedDims& g, const moe_bf16* A, const moe_bf16* dyp,
