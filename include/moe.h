@@ -215,20 +215,25 @@ int moe_expert_bwd(const moe_bf16* dy, const int32_t* src_pair, const int32_t* d
  * [PRL "dispatch.type = mega_moe"] gradients for x through the top-k weights.
  * dl_t,S_j = w_j (dw_j - sum_j' w_j' dw_j') on the selected experts (0
  * elsewhere; the selection is piecewise constant); then
- *   dx[t] += sum_j dl_t,j W_r[:, S_j]        (read-modify-write of bf16 dx,
- *                                             sum in fp32)
+ *   dx[t] += sum_j dl_t,j W_r[:, S_j]        (dxp == NULL: read-modify-write of
+ *                                             bf16 dx, sum in fp32), or
+ *   dx[t]  = sum_j dxp[dst_row[t*k+j]] + sum_j dl_t,j W_r[:, S_j]
+ *                                            (dxp given: the permute's transpose
+ *                                             fused in, fp32, rounded once)
  *   dW_r[:, e] = sum over e's rows of dl * xp[row]   (fp32, fixed order)
  *   dbias[e]   = sum over e's rows of dl             (fp32, fixed order)
  *  d_topk_w, topk_w [T, k] fp32; topk_idx [T, k] int32; w_router [d, E] fp32;
  *  offsets, src_pair, xp from moe_permute (with the same `align`).
- *  dx_inout [T, d] bf16 (added to); dw_router [d, E] fp32 out; dbias [E]
- *  fp32 out or NULL.
+ *  dx_inout [T, d] bf16 (added to, or overwritten when dxp is given);
+ *  dxp [R_cap, d] bf16 or NULL (from moe_expert_bwd); dst_row [T*k] int32
+ *  (required with dxp); dw_router [d, E] fp32 out; dbias [E] fp32 out or NULL.
  *  ws: moe_workspace_size(MOE_WS_ROUTE_BWD, ...) bytes, 256-byte aligned.
  * ------------------------------------------------------------------------ */
 int moe_route_bwd(const float* d_topk_w, const float* topk_w, const int32_t* topk_idx,
                   const float* w_router, const int64_t* offsets, const int32_t* src_pair,
                   const moe_bf16* xp, int64_t T, int d, int E, int k, int align,
-                  moe_bf16* dx_inout, float* dw_router, float* dbias,
+                  moe_bf16* dx_inout, const moe_bf16* dxp, const int32_t* dst_row,
+                  float* dw_router, float* dbias,
                   void* ws, size_t ws_bytes, moe_stream_t stream);
 
 /* ------------------------------------------------------------------------

@@ -26,7 +26,7 @@ SIGNATURES = {
                             _P, _P, _P, _P, _P, _P, _P, _P,
                             _P, _P, _P, _P, _P, _P, _P, _P, _P]),
     "moe_route_bwd": (_I, [_P, _P, _P, _P, _P, _P, _P, _I64, _I, _I, _I, _I,
-                           _P, _P, _P, _P, _SZ, _P]),
+                           _P, _P, _P, _P, _P, _P, _SZ, _P]),
     "moe_workspace_size": (_SZ, [_I, _I64, _I, _I, _I, _I]),
     "moe_row_capacity": (_I64, [_I64, _I, _I, _I]),
     "moe_status": (_I, [_P]),

@@ -30,8 +30,9 @@ size_t route_bwd_ws_bytes(int64_t T, int d, int E, int k, int align);
 cudaError_t launch_route_bwd(const float* d_topk_w, const float* topk_w, const int32_t* topk_idx,
                              const float* w_router, const int64_t* offsets,
                              const int32_t* src_pair, const moe_bf16* xp, int64_t T, int d, int E,
-                             int k, int align, moe_bf16* dx_inout, float* dw_router, float* dbias,
-                             void* ws, cudaStream_t s);
+                             int k, int align, moe_bf16* dx_inout, const moe_bf16* dxp,
+                             const int32_t* dst_row, float* dw_router, float* dbias, void* ws,
+                             cudaStream_t s);
 
 // permute.cu
 size_t permute_ws_bytes(int64_t T, int k, int E);

@@ -182,7 +182,7 @@ cudaError_t launch_topk(const float* logits, const int32_t* forced_idx, int64_t 
 // phase 2 adds each expert's partial rows in row order. No atomics.
 // ---------------------------------------------------------------------------
 constexpr int kRbRows = 128;   // rows of the padded layout per phase-1 CTA
-constexpr int kRbCols = 256;   // columns of d per CTA (128 threads x 2)
+constexpr int kRbCols = 1024;  // columns of d per phase-1 CTA (128 threads x 8)
 
 static inline int seg_unit(int align) { return align < kRbRows ? align : kRbRows; }
 
@@ -211,21 +211,25 @@ __global__ void transpose_f32_kernel(const float* __restrict__ in, int rows, int
   }
 }
 
-// one warp per token: dl for its k slots, and dx[t] += dl . W_r^T
+// one warp per token: dl for its k slots, then dx[t]. With dxp given, dx[t] =
+// sum_j dxp[dst_row[t, j]] + sum_j dl_j W_r[:, e_j] in fp32, written once (the
+// permute transpose fused in); without it, dx[t] += sum_j dl_j W_r[:, e_j].
 __global__ void __launch_bounds__(256) route_bwd_token_kernel(
     const float* __restrict__ d_topk_w, const float* __restrict__ topk_w,
     const int32_t* __restrict__ topk_idx, const float* __restrict__ wrT, int64_t T, int d, int E,
-    int k, float* __restrict__ dl_pair, moe_bf16* __restrict__ dx) {
+    int k, float* __restrict__ dl_pair, moe_bf16* __restrict__ dx,
+    const moe_bf16* __restrict__ dxp, const int32_t* __restrict__ dst_row) {
   const int lane = threadIdx.x & 31;
   const int64_t t = (int64_t)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
   if (t >= T) return;
   float w = 0.f, dw = 0.f;
-  int e = -1;
+  int e = -1, r = -1;
   if (lane < k) {
     w = topk_w[t * k + lane];
     dw = d_topk_w[t * k + lane];
     e = topk_idx[t * k + lane];
     if (e < 0 || e >= E) { e = -1; w = 0.f; dw = 0.f; }
+    if (dxp) r = dst_row[t * k + lane];
   }
   float inner = w * dw;
 #pragma unroll
@@ -238,7 +242,15 @@ __global__ void __launch_bounds__(256) route_bwd_token_kernel(
     const int c = c0 + lane * 8;
     const bool in = c < d;
     float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-    if (in) unpack8(*reinterpret_cast<const uint4*>(dxr + c), acc);
+    if (in && !dxp) unpack8(*reinterpret_cast<const uint4*>(dxr + c), acc);
+    for (int j = 0; j < k; ++j) {
+      const int rj = __shfl_sync(0xFFFFFFFFu, r, j);
+      if (!in || rj < 0) continue;
+      float f[8];
+      unpack8(*reinterpret_cast<const uint4*>(dxp + (int64_t)rj * d + c), f);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) acc[i] += f[i];
+    }
     float add[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
     for (int j = 0; j < k; ++j) {
       const float dlj = __shfl_sync(0xFFFFFFFFu, dl, j);
@@ -267,8 +279,9 @@ __device__ __forceinline__ int expert_of_row(const int64_t* offsets, int E, int6
   return lo;
 }
 
-// phase 1: CTA (b, cb) sums rows [b*128, b*128+128) for columns [cb*256, +256),
-// one partial row per expert segment it meets; slot = segment start / unit.
+// phase 1: CTA (b, cb) sums rows [b*128, b*128+128) for columns [cb*1024, +1024)
+// (8 per thread, 16-byte loads), one partial row per expert segment it meets;
+// slot = segment start / unit.
 __global__ void __launch_bounds__(128) route_bwd_partial_kernel(
     const int64_t* __restrict__ offsets, const int32_t* __restrict__ src_pair,
     const moe_bf16* __restrict__ xp, const float* __restrict__ dl_pair, int E, int d, int unit,
@@ -286,13 +299,14 @@ __global__ void __launch_bounds__(128) route_bwd_partial_kernel(
     s_dl[threadIdx.x] = pr >= 0 ? dl_pair[pr] : 0.f;
   }
   __syncthreads();
-  const int c = blockIdx.y * kRbCols + threadIdx.x * 2;
+  const int c = blockIdx.y * kRbCols + threadIdx.x * 8;
   int64_t r = r_begin;
   while (r < r_end) {
     const int e = expert_of_row(offsets, E, r);
     const int64_t seg_end = min(r_end, offsets[e + 1]);
     const int64_t slot = r / unit;
-    float a0 = 0.f, a1 = 0.f, adb = 0.f;
+    float a[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    float adb = 0.f;
 #pragma unroll 4
     for (int64_t q = r; q < seg_end; ++q) {
       const int i = (int)(q - r_begin);
@@ -300,27 +314,30 @@ __global__ void __launch_bounds__(128) route_bwd_partial_kernel(
       const float dl = s_dl[i];
       adb += dl;
       if (c < d) {
-        const uint32_t v = *reinterpret_cast<const uint32_t*>(xp + q * d + c);
-        a0 = fmaf(dl, bf16_lo(v), a0);
-        a1 = fmaf(dl, bf16_hi(v), a1);
+        float f[8];
+        unpack8(*reinterpret_cast<const uint4*>(xp + q * d + c), f);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) a[j] = fmaf(dl, f[j], a[j]);
       }
     }
     if (c < d) {
-      part[slot * d + c] = a0;
-      part[slot * d + c + 1] = a1;
+      float4* o = reinterpret_cast<float4*>(part + slot * d + c);
+      o[0] = make_float4(a[0], a[1], a[2], a[3]);
+      o[1] = make_float4(a[4], a[5], a[6], a[7]);
     }
     if (blockIdx.y == 0 && threadIdx.x == 0) part_db[slot] = adb;
     r = seg_end;
   }
 }
 
-// phase 2: per expert, add its partial rows in row order.
+// phase 2: per expert, add its partial rows in row order (2 columns per thread).
+constexpr int kRdCols = 256;
 __global__ void __launch_bounds__(128) route_bwd_reduce_kernel(
     const int64_t* __restrict__ offsets, const float* __restrict__ part,
     const float* __restrict__ part_db, int E, int d, int unit, float* __restrict__ dw_router,
     float* __restrict__ dbias) {
   const int e = blockIdx.x;
-  const int c = blockIdx.y * kRbCols + threadIdx.x * 2;
+  const int c = blockIdx.y * kRdCols + threadIdx.x * 2;
   const int64_t g0 = offsets[e], g1 = offsets[e + 1];
   float a0 = 0.f, a1 = 0.f, adb = 0.f;
   int64_t r = g0;
@@ -343,8 +360,9 @@ __global__ void __launch_bounds__(128) route_bwd_reduce_kernel(
 cudaError_t launch_route_bwd(const float* d_topk_w, const float* topk_w, const int32_t* topk_idx,
                              const float* w_router, const int64_t* offsets,
                              const int32_t* src_pair, const moe_bf16* xp, int64_t T, int d, int E,
-                             int k, int align, moe_bf16* dx_inout, float* dw_router, float* dbias,
-                             void* ws, cudaStream_t s) {
+                             int k, int align, moe_bf16* dx_inout, const moe_bf16* dxp,
+                             const int32_t* dst_row, float* dw_router, float* dbias, void* ws,
+                             cudaStream_t s) {
   const int64_t R_cap = T * k + (int64_t)E * (align - 1);
   const int unit = seg_unit(align);
   char* p = static_cast<char*>(ws);
@@ -363,12 +381,12 @@ cudaError_t launch_route_bwd(const float* d_topk_w, const float* topk_w, const i
   if (T > 0)
     route_bwd_token_kernel<<<(unsigned)((T + 7) / 8), 256, 0, s>>>(d_topk_w, topk_w, topk_idx,
                                                                    wrT, T, d, E, k, dl_pair,
-                                                                   dx_inout);
+                                                                   dx_inout, dxp, dst_row);
   const int cblocks = (d + kRbCols - 1) / kRbCols;
   route_bwd_partial_kernel<<<dim3((unsigned)((R_cap + kRbRows - 1) / kRbRows), cblocks), 128, 0,
                              s>>>(offsets, src_pair, xp, dl_pair, E, d, unit, part, part_db);
-  route_bwd_reduce_kernel<<<dim3(E, cblocks), 128, 0, s>>>(offsets, part, part_db, E, d, unit,
-                                                           dw_router, dbias);
+  route_bwd_reduce_kernel<<<dim3(E, (d + kRdCols - 1) / kRdCols), 128, 0, s>>>(
+      offsets, part, part_db, E, d, unit, dw_router, dbias);
   note_launches(T > 0 ? 4 : 3);
   timer_after(MOE_KERNEL_ROUTE_BWD, s);
   return cudaGetLastError();

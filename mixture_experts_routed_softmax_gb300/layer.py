@@ -2,8 +2,8 @@
 
 PyTorch supplies device memory and the stream; every step of the layer runs
 in the library's kernels. Forward: moe_route -> moe_permute -> moe_expert_fwd
--> moe_combine. Backward: moe_expert_bwd -> moe_combine (unweighted, the
-permute's transpose) -> moe_route_bwd.
+-> moe_combine. Backward: moe_expert_bwd -> moe_route_bwd (which also applies
+the permute's transpose to dXp while it writes dx).
 """
 from __future__ import annotations
 
@@ -162,10 +162,13 @@ class MoELayer:
                   _p(b.dyp), _p(b.dg), _p(b.du), _p(b.dxp), _p(b.d_topk_w),
                   _p(b.dw_gate), _p(b.dw_up), _p(b.dw_down), _stream(stream))
 
-    def route_bwd(self, b: Buffers, stream=None):
+    def route_bwd(self, b: Buffers, fused=True, stream=None):
+        """Router backward. fused: dx = permute transpose of dXp + the router's
+        term in one pass; else dx (already holding the permute transpose) += it."""
         _lib.call("moe_route_bwd", _p(b.d_topk_w), _p(b.topk_w), _p(b.topk_idx),
                   _p(self.w_router), _p(b.offsets), _p(b.src_pair), _p(b.xp), b.T, self.d,
-                  self.E, self.k, self.align, _p(b.dx), _p(b.dw_router), _p(b.dbias),
+                  self.E, self.k, self.align, _p(b.dx), _p(b.dxp) if fused else None,
+                  _p(b.dst_row) if fused else None, _p(b.dw_router), _p(b.dbias),
                   _p(b.ws_route_bwd), b.ws_route_bwd.numel(), _stream(stream))
 
     # ------------------------------------------------------ whole layer --
@@ -178,10 +181,10 @@ class MoELayer:
         return b.y
 
     def backward(self, dy, b: Buffers, stream=None):
-        """Gradients of sum(y * dy) into b.dx, b.dw_*, b.dbias, b.d_topk_w."""
+        """Gradients of sum(y * dy) into b.dx, b.dw_*, b.dbias, b.d_topk_w.
+        The permute's transpose runs inside the router backward's dx pass."""
         self.expert_bwd(dy, b, stream)
-        self.combine(b.dxp, b, b.dx, False, stream)
-        self.route_bwd(b, stream)
+        self.route_bwd(b, fused=True, stream=stream)
         return b.dx
 
     def status(self, stream=None) -> int:

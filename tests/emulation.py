@@ -70,7 +70,7 @@ def emulate(inp: dict, idx, k: int, device="cuda", backward=True) -> dict:
         dtw = (dy[tok] * Yu).sum(1).reshape(T, k)
         dl_sel = w * (dtw - (w * dtw).sum(1, keepdim=True))
         dl = torch.zeros(T, E, **f32).scatter_(1, idx, dl_sel)
-        dx = bf(bf(dXp.reshape(T, k, d).sum(1)) + dl @ wr.T)
+        dx = bf(dXp.reshape(T, k, d).sum(1) + dl @ wr.T)     # one rounding (fused pass)
         out.update(dYu=dYp, dG=dG, dU=dU, dXp=dXp, dx=dx, dw_gate=dwg, dw_up=dwu, dw_down=dwd,
                    d_topk_w=dtw, dw_router=x.T @ dl, dbias=dl.sum(0))
     return out

@@ -80,6 +80,9 @@ def test_host_argument_checks(lib):
     # combine: k above the slot limit
     assert lib.moe_combine(P, P, None, 4, 33, 8, P, None) == L.MOE_ERR_UNSUPPORTED
     # route backward: workspace missing
-    assert lib.moe_route_bwd(P, P, P, P, P, P, P, 4, 8, 4, 2, 16, P, P, None, None, 0, None) == L.MOE_ERR_ARG
+    assert lib.moe_route_bwd(P, P, P, P, P, P, P, 4, 8, 4, 2, 16, P, None, None, P, None, None, 0, None) == L.MOE_ERR_ARG
+    # route backward: dxp without dst_row
+    wsb = lib.moe_workspace_size(2, 4, 8, 4, 2, 16)
+    assert lib.moe_route_bwd(P, P, P, P, P, P, P, 4, 8, 4, 2, 16, P, P, None, P, None, P, wsb, None) == L.MOE_ERR_ARG
     # timer: bad kernel id
     assert lib.moe_timer_start(0, 4) == L.MOE_ERR_ARG

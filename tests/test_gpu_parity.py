@@ -116,3 +116,25 @@ def test_bad_forced_index_raises_device_status():
     assert int(b.dst_row[5 * k + 1]) == -1
     assert int(b.counts.sum()) == T * k - 1
     assert layer.status() == 0           # the status word was cleared by the read
+
+
+def test_router_backward_fused_and_separate_dx_agree():
+    """moe_route_bwd writes dx = permute-transpose(dXp) + router term in one
+    pass (fused), or adds the router term to a dx that moe_combine already
+    holds; the two differ only by the second bf16 rounding."""
+    T, d, f, E, k, align = 300, 200, 136, 6, 2, 16
+    wl, inp = _case("dxfuse", T, d, f, E, k, align)
+    layer = _layer(inp, k, align)
+    b, x, dy = gpu_forward_backward(layer, inp)          # fused path (the layer's default)
+    dx_fused = b.dx.float().clone()
+    dw_r = b.dw_router.clone()
+    layer.combine(b.dxp, b, b.dx, weights=False)          # permute transpose into dx
+    torch.cuda.synchronize()
+    dx_expert = b.dx.float().clone()
+    layer.route_bwd(b, fused=False)                        # then dx += router term
+    assert layer.status() == 0
+    dx_sep = b.dx.float()
+    # the separate path rounds the expert part to bf16 before adding the router term
+    bound = 2 ** -7 * (torch.abs(dx_expert) + torch.abs(dx_fused)) + 1e-6
+    assert torch.all(torch.abs(dx_sep - dx_fused) <= bound)
+    assert torch.equal(b.dw_router, dw_r)
