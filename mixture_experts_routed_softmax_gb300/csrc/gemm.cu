@@ -162,7 +162,7 @@ template <int NOUT, bool K3D>
 __device__ __forceinline__ void put_chunk(const uint32_t (&pk)[NOUT][16], uint8_t* stg,
                                           const CUtensorMap* const* maps, moe_bf16* const* outs,
                                           bool tma_ok, bool row_ok, int64_t row, int col, int N,
-                                          int row0, int e, int lane) {
+                                          int row0, int e, int lane, uint64_t policy) {
   if (tma_ok) {
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
@@ -179,8 +179,10 @@ __device__ __forceinline__ void put_chunk(const uint32_t (&pk)[NOUT][16], uint8_
       if (lane == 0 && col + 16 * h < N) {
 #pragma unroll
         for (int o = 0; o < NOUT; ++o) {
-          if constexpr (K3D) tma_store_3d(maps[o], smem_u32(stg + o * 1024), col + 16 * h, row0, e);
-          else tma_store_2d(maps[o], smem_u32(stg + o * 1024), col + 16 * h, row0);
+          if constexpr (K3D)
+            tma_store_3d(maps[o], smem_u32(stg + o * 1024), col + 16 * h, row0, e, policy);
+          else
+            tma_store_2d(maps[o], smem_u32(stg + o * 1024), col + 16 * h, row0, policy);
         }
         bulk_commit();
       }
@@ -307,6 +309,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0) {
     if (lane == 0) {
       // ------------------------------------------------------ producer --
+      const uint64_t pol_w = l2_evict_last();   // expert weights: re-read by every m-tile
       int stage = 0;
       uint32_t phase = 0;
       int fills = 0;
@@ -343,8 +346,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             tma_load_2d(sA, &mapA0, fb, kk, (int)ti.m0);
 #pragma unroll
             for (int j = 0; j < T::BN / 64; ++j)
-              tma_load_2d(sB0 + j * (BK * 128), &mapB0, fb, ti.n0 + 64 * j,
-                          seg * args.seg_koff + kk);
+              tma_load_2d_hint(sB0 + j * (BK * 128), &mapB0, fb, ti.n0 + 64 * j,
+                               seg * args.seg_koff + kk, pol_w);
           } else {
             const int seg = (T::two_seg && ks >= args.nk_seg) ? 1 : 0;
             const int kk = (ks - seg * args.nk_seg) * BK;
@@ -354,12 +357,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             if constexpr (T::b_mn) {
 #pragma unroll
               for (int j = 0; j < T::BN / 64; ++j) {
-                tma_load_3d(sB0 + j * (BK * 128), &mapB0, fb, ti.n0 + 64 * j, kk, ti.e);
+                tma_load_3d_hint(sB0 + j * (BK * 128), &mapB0, fb, ti.n0 + 64 * j, kk, ti.e, pol_w);
                 if constexpr (T::dual)
-                  tma_load_3d(sB1 + j * (BK * 128), &mapB1, fb, ti.n0 + 64 * j, kk, ti.e);
+                  tma_load_3d_hint(sB1 + j * (BK * 128), &mapB1, fb, ti.n0 + 64 * j, kk, ti.e,
+                                   pol_w);
               }
             } else {
-              tma_load_3d(sB0, mB, fb, kk, ti.n0, ti.e);
+              tma_load_3d_hint(sB0, mB, fb, kk, ti.n0, ti.e, pol_w);
             }
           }
           ++fills;
@@ -426,6 +430,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp >= 4) {
     // ------------------------------------------------------------ epilogue --
+    const uint64_t pol_out = l2_evict_first();   // outputs stream through L2
     const int wq = (warp - 4) & 3;             // TMEM lane quarter of this warp
     const int rloc = wq * 32 + lane;           // accumulator row of this thread
     // the two epilogue warpgroups split each accumulator's columns in halves
@@ -483,7 +488,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             pk[2][i] = pack_bf16(g0 / (1.0f + __expf(-g0)) * u0, g1 / (1.0f + __expf(-g1)) * u1);
           }
           put_chunk<3, false>(pk, stg, maps, outs, tma_ok, row_ok, row, ti.n0 + c, args.N, row0,
-                              0, lane);
+                              0, lane, pol_out);
         }
       } else if constexpr (T::kgrouped) {
         constexpr int NO = T::dual ? 2 : 1;
@@ -501,7 +506,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               pk[NO - 1][i] = pack_bf16(__uint_as_float(u[2 * i]), __uint_as_float(u[2 * i + 1]));
           }
           put_chunk<NO, true>(pk, stg, maps, outs, tma_ok, false, row, ti.n0 + c, args.N, row0,
-                              ti.e, lane);
+                              ti.e, lane, pol_out);
         }
       } else if constexpr (K == Kind::RouterLogits) {
         // one split: logits + bias; several: this split's fp32 partial, summed later
@@ -566,7 +571,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
           put_chunk<2, false>(pk, stg, maps, outs, tma_ok, row_ok, row, ti.n0 + c, args.N, row0,
-                              0, lane);
+                              0, lane, pol_out);
           if (c + 32 < c_hi) {
 #pragma unroll
             for (int v = 0; v < 4; ++v) { gc[v] = gn[v]; uc[v] = un[v]; }
@@ -589,7 +594,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             pk[0][i] = pack_bf16(__uint_as_float(r[2 * i]) * scale,
                                  __uint_as_float(r[2 * i + 1]) * scale);
           put_chunk<1, false>(pk, stg, maps, outs, tma_ok, row_ok, row, ti.n0 + c, args.N, row0,
-                              0, lane);
+                              0, lane, pol_out);
         }
       }
       tc_fence_before();
