@@ -77,9 +77,9 @@ constexpr int kTmemCols = 512;                            // 2 accumulator buffe
 constexpr int kEpiWarps = 8;                              // two warpgroups, each half the columns
 constexpr int kThreads = 128 + 32 * kEpiWarps;
 // Epilogues stage their bf16 outputs through shared memory for TMA stores: per
-// epilogue warp, 32 rows x 16 columns of each of up to three outputs (1 KiB each)
-constexpr int kStagePerWarp = 3 * 1024;
-constexpr int kStageOutBytes = kEpiWarps * kStagePerWarp;
+// epilogue warpgroup, 128 rows x 16 columns of each of up to three outputs (4 KiB each)
+constexpr int kStagePerGroup = 3 * 4096;
+constexpr int kStageOutBytes = (kEpiWarps / 4) * kStagePerGroup;
 constexpr int kTstartBytes = (4 * (kMaxExperts + 1) + 127) & ~127;
 constexpr int kSmemBytes = kRingBytes + 1024 /*bars*/ + kTstartBytes + kStageOutBytes + 1024;
 
@@ -153,36 +153,58 @@ __device__ __forceinline__ void decode_tile(int tile, const GemmArgs& a, const i
   }
 }
 
+// Named barrier over one epilogue warpgroup (ids 1 and 2; id 0 is __syncthreads).
+__device__ __forceinline__ void group_sync(int group) {
+  asm volatile("bar.sync %0, 128;" ::"r"(group + 1) : "memory");
+}
+// The same barrier, returning whether every thread of the group passed `ok`:
+// the group decides together whether to go on, so no warp is left waiting at
+// a group barrier that another warp has abandoned.
+__device__ __forceinline__ bool group_all(int group, bool ok) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred pin, pout;\n\t"
+      "setp.ne.u32 pin, %1, 0;\n\t"
+      "bar.red.and.pred pout, %2, 128, pin;\n\t"
+      "selp.u32 %0, 1, 0, pout;\n\t}\n"
+      : "=r"(r)
+      : "r"((uint32_t)ok), "r"(group + 1)
+      : "memory");
+  return r != 0;
+}
+
 // Writes 32 columns (packed bf16 pairs pk[o][0..15]) of NOUT outputs for this
-// warp's 32 rows. A warp whose rows all belong to the tile's group stages each
-// 16-column slice in shared memory and lets lane 0 issue one TMA store per
-// output (coordinates {col, row} or {col, row, e}; the maps clip at the tensor
-// edge); a warp straddling the group end stores row by row with masks.
+// thread's row. When the whole 128-row tile belongs to its group (tile_tma), the
+// warpgroup stages each 16-column slice of each output in shared memory,
+// [128 rows x 16 columns], and one thread issues one TMA store per output
+// (coordinates {col, m0} or {col, m0, e}; the maps clip at the tensor edge).
+// Otherwise every thread stores its own row with masks.
 template <int NOUT, bool K3D>
 __device__ __forceinline__ void put_chunk(const uint32_t (&pk)[NOUT][16], uint8_t* stg,
                                           const CUtensorMap* const* maps, moe_bf16* const* outs,
-                                          bool tma_ok, bool row_ok, int64_t row, int col, int N,
-                                          int row0, int e, int lane, uint64_t policy) {
-  if (tma_ok) {
+                                          bool tile_tma, bool row_ok, int64_t row, int rloc,
+                                          int col, int N, int m0, int e, int group, bool leader,
+                                          uint64_t policy) {
+  if (tile_tma) {
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
-      if (lane == 0) bulk_wait_read();
-      __syncwarp();
+      if (leader) bulk_wait_read();      // the previous slice's stores have read the buffer
+      group_sync(group);
 #pragma unroll
       for (int o = 0; o < NOUT; ++o) {
-        uint4* d = reinterpret_cast<uint4*>(stg + o * 1024 + lane * 32);
+        uint4* d = reinterpret_cast<uint4*>(stg + o * 4096 + rloc * 32);
         d[0] = make_uint4(pk[o][8 * h + 0], pk[o][8 * h + 1], pk[o][8 * h + 2], pk[o][8 * h + 3]);
         d[1] = make_uint4(pk[o][8 * h + 4], pk[o][8 * h + 5], pk[o][8 * h + 6], pk[o][8 * h + 7]);
       }
       fence_async_smem();
-      __syncwarp();
-      if (lane == 0 && col + 16 * h < N) {
+      group_sync(group);
+      if (leader && col + 16 * h < N) {
 #pragma unroll
         for (int o = 0; o < NOUT; ++o) {
           if constexpr (K3D)
-            tma_store_3d(maps[o], smem_u32(stg + o * 1024), col + 16 * h, row0, e, policy);
+            tma_store_3d(maps[o], smem_u32(stg + o * 4096), col + 16 * h, m0, e, policy);
           else
-            tma_store_2d(maps[o], smem_u32(stg + o * 1024), col + 16 * h, row0, policy);
+            tma_store_2d(maps[o], smem_u32(stg + o * 4096), col + 16 * h, m0, policy);
         }
         bulk_commit();
       }
@@ -459,16 +481,18 @@ __global__ void __launch_bounds__(kThreads, 1)
           continue;
         }
       }
-      if (!mbar_wait_bounded(tfull_bar(acc), acc_phase, s_abort, args.status)) break;
+      const bool got = mbar_wait_bounded(tfull_bar(acc), acc_phase, s_abort, args.status);
+      if (!group_all((warp - 4) >> 2, got)) break;
       tc_fence_after();
       const uint32_t t_row = tmem_base + ((uint32_t)(wq * 32) << 16) + (uint32_t)acc * 256u;
 
-      // this warp's 32 rows: all inside the tile's group (or, for dW, stored by
-      // TMA, which clips at M) -> staged TMA stores; else masked row stores
-      const int row0 = (int)(ti.m0 + wq * 32);
-      const bool tma_ok = T::kgrouped ? (row0 < args.M) : ((int64_t)row0 + 32 <= ti.row_end);
+      // the whole 128-row tile inside its group (dW tiles always: TMA clips at M)
+      // -> staged TMA stores by the warpgroup; else masked row stores
+      const int group = (warp - 4) >> 2;
+      const bool leader = (wq == 0 && lane == 0);
+      const bool tile_tma = T::kgrouped || (ti.m0 + BM <= ti.row_end);
       const bool row_ok = T::kgrouped ? false : (row < ti.row_end);
-      uint8_t* stg = stage_out + (warp - 4) * kStagePerWarp;
+      uint8_t* stg = stage_out + group * kStagePerGroup;
       const CUtensorMap* maps[3] = {&mapO0, &mapO1, &mapO2};
       moe_bf16* outs[3] = {args.out0, args.out1, args.out2};
       if constexpr (T::gateup_fwd) {
@@ -487,8 +511,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             pk[1][i] = pack_bf16(u0, u1);
             pk[2][i] = pack_bf16(g0 / (1.0f + __expf(-g0)) * u0, g1 / (1.0f + __expf(-g1)) * u1);
           }
-          put_chunk<3, false>(pk, stg, maps, outs, tma_ok, row_ok, row, ti.n0 + c, args.N, row0,
-                              0, lane, pol_out);
+          put_chunk<3, false>(pk, stg, maps, outs, tile_tma, row_ok, row, rloc, ti.n0 + c, args.N,
+                              (int)ti.m0, 0, group, leader, pol_out);
         }
       } else if constexpr (T::kgrouped) {
         constexpr int NO = T::dual ? 2 : 1;
@@ -505,8 +529,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             if constexpr (T::dual)
               pk[NO - 1][i] = pack_bf16(__uint_as_float(u[2 * i]), __uint_as_float(u[2 * i + 1]));
           }
-          put_chunk<NO, true>(pk, stg, maps, outs, tma_ok, false, row, ti.n0 + c, args.N, row0,
-                              ti.e, lane, pol_out);
+          put_chunk<NO, true>(pk, stg, maps, outs, tile_tma, false, row, rloc, ti.n0 + c, args.N,
+                              (int)ti.m0, ti.e, group, leader, pol_out);
         }
       } else if constexpr (K == Kind::RouterLogits) {
         // one split: logits + bias; several: this split's fp32 partial, summed later
@@ -570,8 +594,8 @@ __global__ void __launch_bounds__(kThreads, 1)
               pk[1][4 * v + i] = pack_bf16(du[2 * i], du[2 * i + 1]);
             }
           }
-          put_chunk<2, false>(pk, stg, maps, outs, tma_ok, row_ok, row, ti.n0 + c, args.N, row0,
-                              0, lane, pol_out);
+          put_chunk<2, false>(pk, stg, maps, outs, tile_tma, row_ok, row, rloc, ti.n0 + c, args.N,
+                              (int)ti.m0, 0, group, leader, pol_out);
           if (c + 32 < c_hi) {
 #pragma unroll
             for (int v = 0; v < 4; ++v) { gc[v] = gn[v]; uc[v] = un[v]; }
@@ -593,8 +617,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int i = 0; i < 16; ++i)
             pk[0][i] = pack_bf16(__uint_as_float(r[2 * i]) * scale,
                                  __uint_as_float(r[2 * i + 1]) * scale);
-          put_chunk<1, false>(pk, stg, maps, outs, tma_ok, row_ok, row, ti.n0 + c, args.N, row0,
-                              0, lane, pol_out);
+          put_chunk<1, false>(pk, stg, maps, outs, tile_tma, row_ok, row, rloc, ti.n0 + c, args.N,
+                              (int)ti.m0, 0, group, leader, pol_out);
         }
       }
       tc_fence_before();
@@ -602,8 +626,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) mbar_arrive(tempty_bar(acc));
       if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
     }
-    if (lane == 0) bulk_wait_all();     // the staged stores are done before the CTA exits
-    __syncwarp();
+    if (wq == 0 && lane == 0) bulk_wait_all();   // the staged stores finish before the CTA exits
   }
   tc_fence_before();
   __syncthreads();
@@ -660,26 +683,26 @@ static bool map3d(CUtensorMap* m, const void* ptr, uint64_t d0, uint64_t d1, uin
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// 2-D bf16 map over a row buffer [R, N] for TMA stores of 32-row x 16-column boxes
+// 2-D bf16 map over a row buffer [R, N] for TMA stores of 128-row x 16-column boxes
 static bool map2d_out(CUtensorMap* m, const void* ptr, uint64_t N, uint64_t R) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
   cuuint64_t dims[2] = {N, R};
   cuuint64_t strides[1] = {N * 2};
-  cuuint32_t box[2] = {16, 32};
+  cuuint32_t box[2] = {16, 128};
   cuuint32_t es[2] = {1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box,
             es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
             CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// 3-D bf16 map over [E, M, N] (N innermost) for TMA stores of 32-row x 16-column boxes
+// 3-D bf16 map over [E, M, N] (N innermost) for TMA stores of 128-row x 16-column boxes
 static bool map3d_out(CUtensorMap* m, const void* ptr, uint64_t N, uint64_t M, uint64_t E) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
   cuuint64_t dims[3] = {N, M, E};
   cuuint64_t strides[2] = {N * 2, N * M * 2};
-  cuuint32_t box[3] = {16, 32, 1};
+  cuuint32_t box[3] = {16, 128, 1};
   cuuint32_t es[3] = {1, 1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box,
             es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
