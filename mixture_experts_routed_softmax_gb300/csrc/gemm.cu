@@ -173,21 +173,21 @@ __device__ __forceinline__ bool group_all(int group, bool ok) {
   return r != 0;
 }
 
-// Writes 32 columns (packed bf16 pairs pk[o][0..15]) of NOUT outputs for this
-// thread's row. When the whole 128-row tile belongs to its group (tile_tma), the
-// warpgroup stages each 16-column slice of each output in shared memory,
-// [128 rows x 16 columns], and one thread issues one TMA store per output
-// (coordinates {col, m0} or {col, m0, e}; the maps clip at the tensor edge).
-// Otherwise every thread stores its own row with masks.
-template <int NOUT, bool K3D>
-__device__ __forceinline__ void put_chunk(const uint32_t (&pk)[NOUT][16], uint8_t* stg,
+// Writes 16*NH columns (packed bf16 pairs pk[o][0..8*NH-1]) of NOUT outputs for
+// this thread's row. When the whole 128-row tile belongs to its group
+// (tile_tma), the warpgroup stages each 16-column slice of each output in
+// shared memory, [128 rows x 16 columns], and one thread issues one TMA store
+// per output (coordinates {col, m0} or {col, m0, e}; the maps clip at the
+// tensor edge). Otherwise every thread stores its own row with masks.
+template <int NOUT, bool K3D, int NH = 2>
+__device__ __forceinline__ void put_chunk(const uint32_t (&pk)[NOUT][8 * NH], uint8_t* stg,
                                           const CUtensorMap* const* maps, moe_bf16* const* outs,
                                           bool tile_tma, bool row_ok, int64_t row, int rloc,
                                           int col, int N, int m0, int e, int group, bool leader,
                                           uint64_t policy) {
   if (tile_tma) {
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
+    for (int h = 0; h < NH; ++h) {
       if (leader) bulk_wait_read();      // the previous slice's stores have read the buffer
       group_sync(group);
 #pragma unroll
@@ -211,7 +211,7 @@ __device__ __forceinline__ void put_chunk(const uint32_t (&pk)[NOUT][16], uint8_
     }
   } else if (row_ok) {
 #pragma unroll
-    for (int v = 0; v < 4; ++v) {
+    for (int v = 0; v < 2 * NH; ++v) {
       if (col + 8 * v >= N) break;
 #pragma unroll
       for (int o = 0; o < NOUT; ++o)
@@ -418,6 +418,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!mbar_wait_bounded(tempty_bar(acc), acc_phase ^ 1u, s_abort, args.status)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + (uint32_t)acc * 256u;
+        // a tile at the right edge multiplies only the columns that exist
+        // (rounded up to the MMA's 16-column step; B rows past N are zero-filled)
+        uint32_t idesc = kIdesc;
+        if constexpr (!T::dual) {
+          const int nv = (args.N - ti.n0 + 15) & ~15;
+          if (nv < T::BN) idesc = idesc_bf16(BM, nv, T::a_mn ? 1 : 0, T::b_mn ? 1 : 0);
+        }
         for (int ks = 0; ks < ti.nk; ++ks) {
           if (!mbar_wait_bounded(full_bar(stage), phase, s_abort, args.status)) {
             ok = false;
@@ -437,7 +444,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint64_t bd0 = T::b_mn ? sdesc_sw128(sB0 + kk * 2048, BK * 128, 1024)
                                          : sdesc_sw128(sB0 + kk * 32, 16, 1024);
             const uint32_t accum = (ks > 0 || kk > 0) ? 1u : 0u;
-            umma_bf16(d_tmem, ad, bd0, kIdesc, accum);
+            umma_bf16(d_tmem, ad, bd0, idesc, accum);
           }
           umma_commit(empty_bar(stage));
           if (++stage == kStages) { stage = 0; phase ^= 1u; }
@@ -481,6 +488,28 @@ __global__ void __launch_bounds__(kThreads, 1)
           continue;
         }
       }
+      const bool row_ok = T::kgrouped ? false : (row < ti.row_end);
+      const int c_end = min(c_hi, args.N - ti.n0);   // columns of this half that exist
+      // DownDgrad: the saved G, U of chunk c+1 are loaded while chunk c is
+      // computed; the first chunk's loads go out before the accumulator is ready
+      const int64_t gu_base = row * args.N;
+      uint4 gc[4], uc[4];
+      auto load_gu = [&](int c, uint4* g, uint4* u) {
+#pragma unroll
+        for (int v = 0; v < 4; ++v) {
+          const int col = ti.n0 + c + 8 * v;
+          if (row_ok && col < args.N) {
+            g[v] = *reinterpret_cast<const uint4*>(args.in0 + gu_base + col);
+            u[v] = *reinterpret_cast<const uint4*>(args.in1 + gu_base + col);
+          } else {
+            g[v] = make_uint4(0u, 0u, 0u, 0u);
+            u[v] = make_uint4(0u, 0u, 0u, 0u);
+          }
+        }
+      };
+      if constexpr (K == Kind::DownDgrad) {
+        if (c_lo < c_end) load_gu(c_lo, gc, uc);
+      }
       const bool got = mbar_wait_bounded(tfull_bar(acc), acc_phase, s_abort, args.status);
       if (!group_all((warp - 4) >> 2, got)) break;
       tc_fence_after();
@@ -491,13 +520,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int group = (warp - 4) >> 2;
       const bool leader = (wq == 0 && lane == 0);
       const bool tile_tma = T::kgrouped || (ti.m0 + BM <= ti.row_end);
-      const bool row_ok = T::kgrouped ? false : (row < ti.row_end);
       uint8_t* stg = stage_out + group * kStagePerGroup;
       const CUtensorMap* maps[3] = {&mapO0, &mapO1, &mapO2};
       moe_bf16* outs[3] = {args.out0, args.out1, args.out2};
       if constexpr (T::gateup_fwd) {
 #pragma unroll 1
-        for (int c = c_lo; c < c_hi; c += 32) {
+        for (int c = c_lo; c < c_end; c += 32) {
           uint32_t g[32], u[32];
           tmem_ld32(t_row + c, g);
           tmem_ld32(t_row + T::BN + c, u);
@@ -509,7 +537,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float u0 = __uint_as_float(u[2 * i]), u1 = __uint_as_float(u[2 * i + 1]);
             pk[0][i] = pack_bf16(g0, g1);
             pk[1][i] = pack_bf16(u0, u1);
-            pk[2][i] = pack_bf16(g0 / (1.0f + __expf(-g0)) * u0, g1 / (1.0f + __expf(-g1)) * u1);
+            pk[2][i] = pack_bf16(__fdividef(g0, 1.0f + __expf(-g0)) * u0,
+                                 __fdividef(g1, 1.0f + __expf(-g1)) * u1);
           }
           put_chunk<3, false>(pk, stg, maps, outs, tile_tma, row_ok, row, rloc, ti.n0 + c, args.N,
                               (int)ti.m0, 0, group, leader, pol_out);
@@ -517,7 +546,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       } else if constexpr (T::kgrouped) {
         constexpr int NO = T::dual ? 2 : 1;
 #pragma unroll 1
-        for (int c = c_lo; c < c_hi; c += 32) {
+        for (int c = c_lo; c < c_end; c += 32) {
           uint32_t g[32], u[32];
           tmem_ld32(t_row + c, g);
           if constexpr (T::dual) tmem_ld32(t_row + T::BN + c, u);
@@ -538,7 +567,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool whole = args.ksplit == 1;
         float* orow = args.outf + ((int64_t)ti.e * args.M + row) * args.N;
 #pragma unroll 1
-        for (int c = c_lo; c < c_hi; c += 32) {
+        for (int c = c_lo; c < c_end; c += 32) {
           uint32_t r[32];
           tmem_ld32(t_row + c, r);
           tmem_ld_wait();
@@ -551,52 +580,43 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       } else if constexpr (K == Kind::DownDgrad) {
-        // dG = dA * U * silu'(G), dU = dA * silu(G); the saved G, U of chunk c+1
-        // are loaded while chunk c is computed
-        const int64_t base = row * args.N;
-        uint4 gc[4], uc[4], gn[4], un[4];
-        auto load_gu = [&](int c, uint4* g, uint4* u) {
-#pragma unroll
-          for (int v = 0; v < 4; ++v) {
-            const int col = ti.n0 + c + 8 * v;
-            if (row_ok && col < args.N) {
-              g[v] = *reinterpret_cast<const uint4*>(args.in0 + base + col);
-              u[v] = *reinterpret_cast<const uint4*>(args.in1 + base + col);
-            } else {
-              g[v] = make_uint4(0u, 0u, 0u, 0u);
-              u[v] = make_uint4(0u, 0u, 0u, 0u);
-            }
-          }
-        };
-        load_gu(c_lo, gc, uc);
-#pragma unroll
-        for (int c = c_lo; c < c_hi; c += 32) {
+        // dG = dA * U * silu'(G), dU = dA * silu(G)
+        uint4 gn[4], un[4];
+#pragma unroll 1
+        for (int c = c_lo; c < c_end; c += 32) {
           uint32_t r[32];
           tmem_ld32(t_row + c, r);
-          if (c + 32 < c_hi) load_gu(c + 32, gn, un);
+          if (c + 32 < c_end) load_gu(c + 32, gn, un);
           tmem_ld_wait();
-          uint32_t pk[2][16];
 #pragma unroll
-          for (int v = 0; v < 4; ++v) {
-            float gf[8], uf[8], dg[8], du[8];
-            unpack8(gc[v], gf);
-            unpack8(uc[v], uf);
+          for (int h = 0; h < 2; ++h) {
+            uint32_t pk[2][8];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-              const float f = __uint_as_float(r[8 * v + i]);
-              const float sg = 1.0f / (1.0f + __expf(-gf[i]));
-              dg[i] = f * uf[i] * (sg * (1.0f + gf[i] * (1.0f - sg)));
-              du[i] = f * gf[i] * sg;
+            for (int w = 0; w < 2; ++w) {
+              const int v = 2 * h + w;
+              float gf[8], uf[8];
+              unpack8(gc[v], gf);
+              unpack8(uc[v], uf);
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                float dg[2], du[2];
+#pragma unroll
+                for (int j = 0; j < 2; ++j) {
+                  const int q = 2 * i + j;
+                  const float f = __uint_as_float(r[8 * v + q]);
+                  const float sg = __fdividef(1.0f, 1.0f + __expf(-gf[q]));
+                  dg[j] = f * uf[q] * (sg * (1.0f + gf[q] * (1.0f - sg)));
+                  du[j] = f * gf[q] * sg;
+                }
+                pk[0][4 * w + i] = pack_bf16(dg[0], dg[1]);
+                pk[1][4 * w + i] = pack_bf16(du[0], du[1]);
+              }
             }
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              pk[0][4 * v + i] = pack_bf16(dg[2 * i], dg[2 * i + 1]);
-              pk[1][4 * v + i] = pack_bf16(du[2 * i], du[2 * i + 1]);
-            }
+            put_chunk<2, false, 1>(pk, stg, maps, outs, tile_tma, row_ok, row, rloc,
+                                   ti.n0 + c + 16 * h, args.N, (int)ti.m0, 0, group, leader,
+                                   pol_out);
           }
-          put_chunk<2, false>(pk, stg, maps, outs, tile_tma, row_ok, row, rloc, ti.n0 + c, args.N,
-                              (int)ti.m0, 0, group, leader, pol_out);
-          if (c + 32 < c_hi) {
+          if (c + 32 < c_end) {
 #pragma unroll
             for (int v = 0; v < 4; ++v) { gc[v] = gn[v]; uc[v] = un[v]; }
           }
@@ -608,7 +628,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (args.row_w && row_ok) scale = args.row_w[row];
         }
 #pragma unroll 1
-        for (int c = c_lo; c < c_hi; c += 32) {
+        for (int c = c_lo; c < c_end; c += 32) {
           uint32_t r[32];
           tmem_ld32(t_row + c, r);
           tmem_ld_wait();
