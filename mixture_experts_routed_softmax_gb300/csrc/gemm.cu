@@ -59,6 +59,10 @@ struct Tr {
   static constexpr bool b_mn =
       (gateup_fwd || K == Kind::DownFwd || kgrouped || K == Kind::RouterLogits);
   static constexpr int BN = K == Kind::GateUpFwdNarrow ? 64 : dual ? 128 : 256;   // per accumulator
+  // tile width chosen per launch (at most BN): the K-major-B kinds, whose B box
+  // is exactly the tile's rows, and the router, whose N is the expert count
+  static constexpr bool var_bn =
+      (K == Kind::DownDgrad || K == Kind::GateUpDgrad || K == Kind::RouterLogits);
   // bytes TMA lands per stage (A tile + one or two B tiles), and as many stages as fit
   static constexpr int tx_bytes = kABytes + (dual ? 2 : 1) * BN * BK * 2;
   static constexpr int stages = kRingBytes / tx_bytes > kMaxStages ? kMaxStages
@@ -102,6 +106,7 @@ struct GemmArgs {
   int seg_koff;
   int ksplit;         // RouterLogits: K split into this many chunks (1: write logits + bias)
   int ksteps_split;   // k-steps per chunk
+  int bn;             // single-accumulator kinds: tile width (multiple of 16, <= 256)
   int* status;
 };
 
@@ -114,19 +119,27 @@ struct TileInfo {
   int64_t kbeg;     // K-grouped: first row of the group
 };
 
+// tile width: BN, or for the var_bn kinds the width the launch chose so that
+// N splits into equal tiles (N = 2880: twelve of 240)
+template <Kind K>
+__device__ __forceinline__ int tile_bn(const GemmArgs& a) {
+  return Tr<K>::var_bn ? a.bn : Tr<K>::BN;
+}
+
 template <Kind K>
 __device__ __forceinline__ void decode_tile(int tile, const GemmArgs& a, const int* tstart,
                                             int nN, TileInfo& ti) {
   using T = Tr<K>;
+  const int bn = tile_bn<K>(a);
   const int nt = tile % nN;
   const int mt = tile / nN;
-  ti.n0 = nt * T::BN;
+  ti.n0 = nt * bn;
   if constexpr (T::dense) {
     // tile = (m-tile * nN + n-tile) * ksplit + split; e holds the split
     const int sp = tile % a.ksplit;
     const int mn = tile / a.ksplit;
     ti.e = sp;
-    ti.n0 = (mn % nN) * T::BN;
+    ti.n0 = (mn % nN) * bn;
     ti.m0 = (int64_t)(mn / nN) * BM;
     ti.row_end = a.M;
     ti.kbeg = (int64_t)sp * a.ksteps_split;
@@ -178,13 +191,14 @@ __device__ __forceinline__ bool group_all(int group, bool ok) {
 // (tile_tma), the warpgroup stages each 16-column slice of each output in
 // shared memory, [128 rows x 16 columns], and one thread issues one TMA store
 // per output (coordinates {col, m0} or {col, m0, e}; the maps clip at the
-// tensor edge). Otherwise every thread stores its own row with masks.
+// tensor edge). Otherwise every thread stores its own row with masks. Columns
+// from lim on (the tile's end, or N) are not written; N is the row stride.
 template <int NOUT, bool K3D, int NH = 2>
 __device__ __forceinline__ void put_chunk(const uint32_t (&pk)[NOUT][8 * NH], uint8_t* stg,
                                           const CUtensorMap* const* maps, moe_bf16* const* outs,
                                           bool tile_tma, bool row_ok, int64_t row, int rloc,
-                                          int col, int N, int m0, int e, int group, bool leader,
-                                          uint64_t policy) {
+                                          int col, int N, int lim, int m0, int e, int group,
+                                          bool leader, uint64_t policy) {
   if (tile_tma) {
 #pragma unroll
     for (int h = 0; h < NH; ++h) {
@@ -198,7 +212,7 @@ __device__ __forceinline__ void put_chunk(const uint32_t (&pk)[NOUT][8 * NH], ui
       }
       fence_async_smem();
       group_sync(group);
-      if (leader && col + 16 * h < N) {
+      if (leader && col + 16 * h < lim) {
 #pragma unroll
         for (int o = 0; o < NOUT; ++o) {
           if constexpr (K3D)
@@ -212,7 +226,7 @@ __device__ __forceinline__ void put_chunk(const uint32_t (&pk)[NOUT][8 * NH], ui
   } else if (row_ok) {
 #pragma unroll
     for (int v = 0; v < 2 * NH; ++v) {
-      if (col + 8 * v >= N) break;
+      if (col + 8 * v >= lim) break;
 #pragma unroll
       for (int o = 0; o < NOUT; ++o)
         *reinterpret_cast<uint4*>(outs[o] + row * N + col + 8 * v) =
@@ -310,7 +324,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem_base = *s_tmem;
 
-  const int nN = (args.N + T::BN - 1) / T::BN;
+  const int bn = tile_bn<K>(args);
+  const int nN = (args.N + bn - 1) / bn;
   int total;
   if constexpr (T::kgrouped) {
     total = args.E * ((args.M + BM - 1) / BM) * nN;
@@ -325,7 +340,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr uint32_t kIdesc =
       idesc_bf16(BM, T::dual ? 2 * T::BN : T::BN, T::a_mn ? 1 : 0, T::b_mn ? 1 : 0);
   constexpr uint32_t kBBytes = (uint32_t)T::BN * BK * 2;
-  constexpr uint32_t kTxBytes = (uint32_t)T::tx_bytes;
+  // B of a var_bn kind: bn rows (K-major) or ceil(bn / 64) 64-column boxes (N-major)
+  const int nbox = (bn + 63) / 64;
+  const uint32_t b_bytes = T::b_mn ? (uint32_t)nbox * (BK * 128) : (uint32_t)bn * (BK * 2);
+  const uint32_t tx_bytes = T::var_bn ? (uint32_t)kABytes + b_bytes : (uint32_t)T::tx_bytes;
   static_assert(kStages * kStageBytes <= kRingBytes && kStageBytes % 8192 == 0, "ring layout");
 
   if (warp == 0) {
@@ -348,7 +366,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t sA = s_base + stage * kStageBytes;
           const uint32_t sB0 = sA + kABytes;
           const uint32_t sB1 = sB0 + kBBytes;
-          mbar_arrive_expect_tx(fb, kTxBytes);
+          mbar_arrive_expect_tx(fb, tx_bytes);
           if constexpr (T::kgrouped) {
             const int row0 = (int)(ti.kbeg + (int64_t)ks * BK);
 #pragma unroll
@@ -368,7 +386,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             tma_load_2d(sA, &mapA0, fb, kk, (int)ti.m0);
 #pragma unroll
             for (int j = 0; j < T::BN / 64; ++j)
-              tma_load_2d_hint(sB0 + j * (BK * 128), &mapB0, fb, ti.n0 + 64 * j,
+              if (j < nbox)
+                tma_load_2d_hint(sB0 + j * (BK * 128), &mapB0, fb, ti.n0 + 64 * j,
                                seg * args.seg_koff + kk, pol_w);
           } else {
             const int seg = (T::two_seg && ks >= args.nk_seg) ? 1 : 0;
@@ -422,8 +441,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         // (rounded up to the MMA's 16-column step; B rows past N are zero-filled)
         uint32_t idesc = kIdesc;
         if constexpr (!T::dual) {
-          const int nv = (args.N - ti.n0 + 15) & ~15;
-          if (nv < T::BN) idesc = idesc_bf16(BM, nv, T::a_mn ? 1 : 0, T::b_mn ? 1 : 0);
+          int nv = (args.N - ti.n0 + 15) & ~15;
+          nv = nv < bn ? nv : bn;
+          if (nv != T::BN) idesc = idesc_bf16(BM, nv, T::a_mn ? 1 : 0, T::b_mn ? 1 : 0);
         }
         for (int ks = 0; ks < ti.nk; ++ks) {
           if (!mbar_wait_bounded(full_bar(stage), phase, s_abort, args.status)) {
@@ -464,7 +484,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int rloc = wq * 32 + lane;           // accumulator row of this thread
     // the two epilogue warpgroups split each accumulator's columns in halves
     constexpr int kHalf = T::BN / 2;
-    const int c_lo = ((warp - 4) >> 2) * kHalf, c_hi = c_lo + kHalf;
+    const int c_lo = ((warp - 4) >> 2) * kHalf;
+    const int c_hi = c_lo + kHalf < bn ? c_lo + kHalf : bn;
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
@@ -490,6 +511,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       const bool row_ok = T::kgrouped ? false : (row < ti.row_end);
       const int c_end = min(c_hi, args.N - ti.n0);   // columns of this half that exist
+      const int col_lim = ti.n0 + c_end;
       // DownDgrad: the saved G, U of chunk c+1 are loaded while chunk c is
       // computed; the first chunk's loads go out before the accumulator is ready
       const int64_t gu_base = row * args.N;
@@ -498,7 +520,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int v = 0; v < 4; ++v) {
           const int col = ti.n0 + c + 8 * v;
-          if (row_ok && col < args.N) {
+          if (row_ok && col < col_lim) {
             g[v] = *reinterpret_cast<const uint4*>(args.in0 + gu_base + col);
             u[v] = *reinterpret_cast<const uint4*>(args.in1 + gu_base + col);
           } else {
@@ -541,7 +563,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                  __fdividef(g1, 1.0f + __expf(-g1)) * u1);
           }
           put_chunk<3, false>(pk, stg, maps, outs, tile_tma, row_ok, row, rloc, ti.n0 + c, args.N,
-                              (int)ti.m0, 0, group, leader, pol_out);
+                              col_lim, (int)ti.m0, 0, group, leader, pol_out);
         }
       } else if constexpr (T::kgrouped) {
         constexpr int NO = T::dual ? 2 : 1;
@@ -559,7 +581,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               pk[NO - 1][i] = pack_bf16(__uint_as_float(u[2 * i]), __uint_as_float(u[2 * i + 1]));
           }
           put_chunk<NO, true>(pk, stg, maps, outs, tile_tma, false, row, rloc, ti.n0 + c, args.N,
-                              (int)ti.m0, ti.e, group, leader, pol_out);
+                              col_lim, (int)ti.m0, ti.e, group, leader, pol_out);
         }
       } else if constexpr (K == Kind::RouterLogits) {
         // one split: logits + bias; several: this split's fp32 partial, summed later
@@ -575,7 +597,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int i = 0; i < 32; ++i) {
             const int col = ti.n0 + c + i;
-            if (col < args.N)
+            if (col < col_lim)
               orow[col] = __uint_as_float(r[i]) + (whole && args.bias ? args.bias[col] : 0.f);
           }
         }
@@ -613,8 +635,8 @@ __global__ void __launch_bounds__(kThreads, 1)
               }
             }
             put_chunk<2, false, 1>(pk, stg, maps, outs, tile_tma, row_ok, row, rloc,
-                                   ti.n0 + c + 16 * h, args.N, (int)ti.m0, 0, group, leader,
-                                   pol_out);
+                                   ti.n0 + c + 16 * h, args.N, col_lim, (int)ti.m0, 0, group,
+                                   leader, pol_out);
           }
           if (c + 32 < c_end) {
 #pragma unroll
@@ -638,7 +660,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             pk[0][i] = pack_bf16(__uint_as_float(r[2 * i]) * scale,
                                  __uint_as_float(r[2 * i + 1]) * scale);
           put_chunk<1, false>(pk, stg, maps, outs, tile_tma, row_ok, row, rloc, ti.n0 + c, args.N,
-                              (int)ti.m0, 0, group, leader, pol_out);
+                              col_lim, (int)ti.m0, 0, group, leader, pol_out);
         }
       }
       tc_fence_before();
@@ -755,6 +777,16 @@ static cudaError_t launch_kind(const CUtensorMap& a0, const CUtensorMap& a1,
   return cudaGetLastError();
 }
 
+// Tile width of a single-accumulator GEMM over N columns: the fewest 256-wide
+// tiles, made equal in width and rounded up to `step` columns: 16 (the MMA's
+// step) when B is K-major, 64 when B is N-major, whose TMA boxes are 64
+// columns wide and stay on 128-byte lines only at multiples of 64.
+static int pick_bn(int N, int step) {
+  const int n = (N + 255) / 256;
+  const int w = (N + n - 1) / n;
+  return (w + step - 1) / step * step;
+}
+
 static GemmArgs base_args(const GroupedDims& g, int* status) {
   GemmArgs a{};
   a.offsets = g.offsets;
@@ -800,11 +832,13 @@ cudaError_t launch_router_gemm(const moe_bf16* x, const moe_bf16* w_split, const
   a.outf = out;
   a.bias = bias;
   a.status = status;
-  const int64_t tiles = ((T + BM - 1) / BM) * ((E + 255) / 256) * a.ksplit;
+  a.bn = pick_bn(E, 64);
+  const int64_t tiles = ((T + BM - 1) / BM) * ((E + a.bn - 1) / a.bn) * a.ksplit;
   return launch_kind<Kind::RouterLogits>(a0, a0, b0, b0, a, tiles, s);
 }
 
 static int64_t mgrouped_tiles_upper(const GroupedDims& g, int N, int BN) {
+  // each expert's rows may end in a partial tile
   return ((g.R_cap + BM - 1) / BM + g.E) * ((N + BN - 1) / BN);
 }
 
@@ -849,8 +883,9 @@ cudaError_t launch_down_dgrad(const GroupedDims& g, const moe_bf16* dyp, const m
                               const moe_bf16* G, const moe_bf16* U, moe_bf16* dG, moe_bf16* dU,
                               int* status, cudaStream_t s) {
   CUtensorMap a0, b0, o0, o1;
+  const int bn = pick_bn(g.f, 16);
   // dA[r, c] = sum_j dyp[r, j] W_down[e][c, j]: B is W_down[e] read as [N = f rows, K = d]
-  if (!map2d(&a0, dyp, g.d, g.R_cap, BM) || !map3d(&b0, w_down, g.d, g.f, g.E, 256) ||
+  if (!map2d(&a0, dyp, g.d, g.R_cap, BM) || !map3d(&b0, w_down, g.d, g.f, g.E, bn) ||
       !map2d_out(&o0, dG, g.f, g.R_cap) || !map2d_out(&o1, dU, g.f, g.R_cap))
     return cudaErrorInvalidValue;
   GemmArgs a = base_args(g, status);
@@ -858,7 +893,8 @@ cudaError_t launch_down_dgrad(const GroupedDims& g, const moe_bf16* dyp, const m
   a.nk_seg = (g.d + BK - 1) / BK;
   a.in0 = G; a.in1 = U;
   a.out0 = dG; a.out1 = dU;
-  return launch_kind<Kind::DownDgrad>(a0, a0, b0, b0, a, mgrouped_tiles_upper(g, g.f, 256), s,
+  a.bn = bn;
+  return launch_kind<Kind::DownDgrad>(a0, a0, b0, b0, a, mgrouped_tiles_upper(g, g.f, bn), s,
                                       &o0, &o1);
 }
 
@@ -866,17 +902,19 @@ cudaError_t launch_gateup_dgrad(const GroupedDims& g, const moe_bf16* dG, const 
                                 const moe_bf16* w_gate, const moe_bf16* w_up, moe_bf16* dxp,
                                 int* status, cudaStream_t s) {
   CUtensorMap a0, a1, b0, b1, o0;
+  const int bn = pick_bn(g.d, 16);
   // dXp[r, i] = sum_c dG[r, c] W_gate[e][i, c] + dU[r, c] W_up[e][i, c]:
   // B is W_gate[e] / W_up[e] read as [N = d rows, K = f]
   if (!map2d(&a0, dG, g.f, g.R_cap, BM) || !map2d(&a1, dU, g.f, g.R_cap, BM) ||
-      !map3d(&b0, w_gate, g.f, g.d, g.E, 256) || !map3d(&b1, w_up, g.f, g.d, g.E, 256) ||
+      !map3d(&b0, w_gate, g.f, g.d, g.E, bn) || !map3d(&b1, w_up, g.f, g.d, g.E, bn) ||
       !map2d_out(&o0, dxp, g.d, g.R_cap))
     return cudaErrorInvalidValue;
   GemmArgs a = base_args(g, status);
   a.N = g.d;
   a.nk_seg = (g.f + BK - 1) / BK;
   a.out0 = dxp;
-  return launch_kind<Kind::GateUpDgrad>(a0, a1, b0, b1, a, mgrouped_tiles_upper(g, g.d, 256), s,
+  a.bn = bn;
+  return launch_kind<Kind::GateUpDgrad>(a0, a1, b0, b1, a, mgrouped_tiles_upper(g, g.d, bn), s,
                                         &o0);
 }
 
