@@ -250,11 +250,12 @@ def run_ours(args, rank, world, local_rank):
         raise RuntimeError(f"device status {status}: {_lib.status_str(status)}")
 
     kernels = STEP_KERNELS if wl.backward else FWD_KERNELS
-    # one profiled step per kernel group (outside the timed region)
+    # three profiled steps per kernel group (outside the timed region)
     per_kernel = {}
     for name in kernels:
-        _lib.call("moe_timer_start", _lib.KERNELS[name], 4)
-        step()
+        _lib.call("moe_timer_start", _lib.KERNELS[name], 8)
+        for _ in range(3):
+            step()
         ms, n = _lib.ctypes.c_float(), _lib.ctypes.c_int()
         _lib.call("moe_timer_read", _lib.ctypes.byref(ms), _lib.ctypes.byref(n))
         per_kernel[name] = ms.value / max(n.value, 1)

@@ -220,10 +220,12 @@ int moe_expert_bwd(const moe_bf16* dy, const int32_t* src_pair, const int32_t* d
  *   dx[t]  = sum_j dxp[dst_row[t*k+j]] + sum_j dl_t,j W_r[:, S_j]
  *                                            (dxp given: the permute's transpose
  *                                             fused in, fp32, rounded once)
- *   dW_r[:, e] = sum over e's rows of dl * xp[row]   (fp32, fixed order)
- *   dbias[e]   = sum over e's rows of dl             (fp32, fixed order)
+ *   dW_r = x^T . dl   (dl as a dense [T, E] matrix; fp32 accumulation of
+ *                      exact products on the tensor cores, fixed order)
+ *   dbias[e] = sum over e's rows of the padded layout of dl (fp32, row order)
  *  d_topk_w, topk_w [T, k] fp32; topk_idx [T, k] int32; w_router [d, E] fp32;
- *  offsets, src_pair, xp from moe_permute (with the same `align`).
+ *  x [T, d] bf16: the layer input (16-byte aligned);
+ *  offsets, src_pair from moe_permute (with the same `align`).
  *  dx_inout [T, d] bf16 (added to, or overwritten when dxp is given);
  *  dxp [R_cap, d] bf16 or NULL (from moe_expert_bwd); dst_row [T*k] int32
  *  (required with dxp); dw_router [d, E] fp32 out; dbias [E] fp32 out or NULL.
@@ -231,7 +233,7 @@ int moe_expert_bwd(const moe_bf16* dy, const int32_t* src_pair, const int32_t* d
  * ------------------------------------------------------------------------ */
 int moe_route_bwd(const float* d_topk_w, const float* topk_w, const int32_t* topk_idx,
                   const float* w_router, const int64_t* offsets, const int32_t* src_pair,
-                  const moe_bf16* xp, int64_t T, int d, int E, int k, int align,
+                  const moe_bf16* x, int64_t T, int d, int E, int k, int align,
                   moe_bf16* dx_inout, const moe_bf16* dxp, const int32_t* dst_row,
                   float* dw_router, float* dbias,
                   void* ws, size_t ws_bytes, moe_stream_t stream);

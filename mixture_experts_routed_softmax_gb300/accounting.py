@@ -61,7 +61,8 @@ def kernel_costs(s: Shape, backward: bool = True) -> dict:
     c["gateup_dgrad"] = (4 * P * f * d, 2 * P * f * 2 + 2 * W1 + P * d * 2)
     c["wgrad_down"] = (2 * P * f * d, P * f * 2 + P * d * 2 + W1)
     c["wgrad_gateup"] = (4 * P * d * f, P * d * 2 + 2 * P * f * 2 + 2 * W1)
-    c["combine_dx"] = (0, P * d * 2 + T * k * 4 + T * d * 2)
+    # the router backward includes the permute's transpose: dXp read once, x
+    # read, dx written once, W_r read and dW_r written, the per-pair scalars
     c["route_bwd"] = (2 * P * d + 2 * P * d,
                       2 * T * d * 2 + P * d * 2 + 2 * d * E * 4 + T * k * 12)
     return c

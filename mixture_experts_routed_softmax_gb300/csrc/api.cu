@@ -281,11 +281,11 @@ int moe_expert_bwd(const moe_bf16* dy, const int32_t* src_pair, const int32_t* d
 
 int moe_route_bwd(const float* d_topk_w, const float* topk_w, const int32_t* topk_idx,
                   const float* w_router, const int64_t* offsets, const int32_t* src_pair,
-                  const moe_bf16* xp, int64_t T, int d, int E, int k, int align,
+                  const moe_bf16* x, int64_t T, int d, int E, int k, int align,
                   moe_bf16* dx_inout, const moe_bf16* dxp, const int32_t* dst_row,
                   float* dw_router, float* dbias, void* ws, size_t ws_bytes,
                   moe_stream_t stream) {
-  if (!d_topk_w || !topk_w || !topk_idx || !w_router || !offsets || !src_pair || !xp ||
+  if (!d_topk_w || !topk_w || !topk_idx || !w_router || !offsets || !src_pair || !x ||
       !dx_inout || !dw_router)
     return MOE_ERR_ARG;
   if (dxp && (!dst_row || !aligned16(dxp))) return MOE_ERR_ARG;
@@ -293,12 +293,14 @@ int moe_route_bwd(const float* d_topk_w, const float* topk_w, const int32_t* top
   if (!is_pow2(align) || align < 16 || align > 256) return MOE_ERR_ARG;
   if (k > kMaxTopK || E > kMaxExperts || d % 8 != 0) return MOE_ERR_UNSUPPORTED;
   if (moe_row_capacity(T, k, E, align) >= ((int64_t)1 << 31)) return MOE_ERR_UNSUPPORTED;
-  if (!aligned16(xp) || !aligned16(dx_inout)) return MOE_ERR_ARG;
+  if (!aligned16(x) || !aligned16(dx_inout)) return MOE_ERR_ARG;
   const size_t need = route_bwd_ws_bytes(T, d, E, k, align);
   if (!ws || ws_bytes < need || (reinterpret_cast<uintptr_t>(ws) & 255u)) return MOE_ERR_ARG;
-  return cuda_code(launch_route_bwd(d_topk_w, topk_w, topk_idx, w_router, offsets, src_pair, xp,
+  int* st = device_status_ptr();
+  if (!st) return MOE_ERR_CUDA;
+  return cuda_code(launch_route_bwd(d_topk_w, topk_w, topk_idx, w_router, offsets, src_pair, x,
                                     T, d, E, k, align, dx_inout, dxp, dst_row, dw_router, dbias,
-                                    ws, reinterpret_cast<cudaStream_t>(stream)));
+                                    ws, st, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 }  // extern "C"

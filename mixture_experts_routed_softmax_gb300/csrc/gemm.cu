@@ -39,6 +39,7 @@ namespace moe {
 
 enum class Kind {
   GateUpFwd, DownFwd, DownDgrad, GateUpDgrad, WgradDown, WgradGateUp, RouterLogits,
+  RouterWgrad,      // dW_r partials = x^T . dl (dl's three bf16 parts side by side in N)
   GateUpFwdNarrow   // GateUpFwd with 64-column tiles, for experts of at most ~128 rows
 };
 
@@ -54,15 +55,14 @@ struct Tr {
   static constexpr bool dual = (gateup_fwd || K == Kind::WgradGateUp);
   static constexpr bool two_seg = (K == Kind::GateUpDgrad);
   static constexpr bool kgrouped = (K == Kind::WgradDown || K == Kind::WgradGateUp);
-  static constexpr bool dense = (K == Kind::RouterLogits);   // one group of M rows
-  static constexpr bool a_mn = kgrouped;                                   // A is M-contiguous
-  static constexpr bool b_mn =
-      (gateup_fwd || K == Kind::DownFwd || kgrouped || K == Kind::RouterLogits);
+  // one group of M rows, fp32 output (split K: one partial per chunk)
+  static constexpr bool dense = (K == Kind::RouterLogits || K == Kind::RouterWgrad);
+  static constexpr bool a_mn = kgrouped || K == Kind::RouterWgrad;         // A is M-contiguous
+  static constexpr bool b_mn = (gateup_fwd || K == Kind::DownFwd || kgrouped || dense);
   static constexpr int BN = K == Kind::GateUpFwdNarrow ? 64 : dual ? 128 : 256;   // per accumulator
   // tile width chosen per launch (at most BN): the K-major-B kinds, whose B box
   // is exactly the tile's rows, and the router, whose N is the expert count
-  static constexpr bool var_bn =
-      (K == Kind::DownDgrad || K == Kind::GateUpDgrad || K == Kind::RouterLogits);
+  static constexpr bool var_bn = (K == Kind::DownDgrad || K == Kind::GateUpDgrad || dense);
   // bytes TMA lands per stage (A tile + one or two B tiles), and as many stages as fit
   static constexpr int tx_bytes = kABytes + (dual ? 2 : 1) * BN * BK * 2;
   static constexpr int stages = kRingBytes / tx_bytes > kMaxStages ? kMaxStages
@@ -74,6 +74,7 @@ struct Tr {
       : K == Kind::GateUpDgrad ? MOE_KERNEL_GATEUP_DGRAD
       : K == Kind::WgradDown ? MOE_KERNEL_WGRAD_DOWN
       : K == Kind::WgradGateUp ? MOE_KERNEL_WGRAD_GATEUP
+      : K == Kind::RouterWgrad ? MOE_KERNEL_ROUTE_BWD
                                : MOE_KERNEL_ROUTER_LOGITS;
 };
 
@@ -383,7 +384,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int kg = (int)ti.kbeg + ks;
             const int seg = kg / args.nk_seg;
             const int kk = (kg - seg * args.nk_seg) * BK;
-            tma_load_2d(sA, &mapA0, fb, kk, (int)ti.m0);
+            if constexpr (T::a_mn) {
+#pragma unroll
+              for (int i = 0; i < BM / 64; ++i)
+                tma_load_2d(sA + i * (BK * 128), &mapA0, fb, (int)ti.m0 + 64 * i, kk);
+            } else {
+              tma_load_2d(sA, &mapA0, fb, kk, (int)ti.m0);
+            }
 #pragma unroll
             for (int j = 0; j < T::BN / 64; ++j)
               if (j < nbox)
@@ -583,8 +590,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           put_chunk<NO, true>(pk, stg, maps, outs, tile_tma, false, row, rloc, ti.n0 + c, args.N,
                               col_lim, (int)ti.m0, ti.e, group, leader, pol_out);
         }
-      } else if constexpr (K == Kind::RouterLogits) {
-        // one split: logits + bias; several: this split's fp32 partial, summed later
+      } else if constexpr (T::dense) {
+        // one split: the result (+ bias); several: this split's fp32 partial, summed later
         const bool in_m = row < args.M;
         const bool whole = args.ksplit == 1;
         float* orow = args.outf + ((int64_t)ti.e * args.M + row) * args.N;
@@ -767,13 +774,13 @@ static cudaError_t launch_kind(const CUtensorMap& a0, const CUtensorMap& a1,
   int64_t grid = num_sms();
   if (tiles_upper < grid) grid = tiles_upper;
   if (grid < 1) grid = 1;
-  // the router's timer brackets its weight split and this GEMM (route.cu)
-  if constexpr (K != Kind::RouterLogits) timer_before(Tr<K>::kernel_id, s);
+  // the router's timers bracket these GEMMs with their other kernels (route.cu)
+  if constexpr (!Tr<K>::dense) timer_before(Tr<K>::kernel_id, s);
   const CUtensorMap& m0 = o0 ? *o0 : a0;
   grouped_gemm_kernel<K><<<(unsigned)grid, kThreads, kSmemBytes, s>>>(
       a0, a1, b0, b1, m0, o1 ? *o1 : m0, o2 ? *o2 : m0, args);
   note_launches(1);
-  if constexpr (K != Kind::RouterLogits) timer_after(Tr<K>::kernel_id, s);
+  if constexpr (!Tr<K>::dense) timer_after(Tr<K>::kernel_id, s);
   return cudaGetLastError();
 }
 
@@ -796,17 +803,25 @@ static GemmArgs base_args(const GroupedDims& g, int* status) {
   return a;
 }
 
-// The number of K chunks the router GEMM splits into: none while the output
-// tiles alone fill half the SMs; else enough chunks to cover the SMs once, at
-// least 4 k-steps per chunk, at most 16.
-int router_ksplit(int64_t T, int d, int E) {
-  const int64_t tiles = ((T + BM - 1) / BM) * ((E + 255) / 256);
-  const int steps = 3 * ((d + BK - 1) / BK);
-  if (2 * tiles >= num_sms()) return 1;
-  int64_t sp = ((int64_t)num_sms() + tiles - 1) / tiles;
+// K chunks for a GEMM of `tiles` output tiles over `steps` k-steps: none while
+// the tiles alone fill half the SMs; else as many as fit the SMs in one round,
+// at least min_steps k-steps per chunk, at most 16 chunks, and normalised so
+// that ceil(steps / chunk length) chunks of ceil(steps / chunks) steps are all
+// non-empty.
+static int ksplit_for(int64_t tiles, int64_t steps, int min_steps) {
+  if (steps <= 0 || tiles <= 0 || 2 * tiles >= num_sms()) return 1;
+  int64_t sp = (int64_t)num_sms() / tiles;   // one round of CTAs
   sp = sp > 16 ? 16 : sp;
-  sp = sp > steps / 4 ? steps / 4 : sp;
-  return sp < 1 ? 1 : (int)sp;
+  sp = sp > steps / min_steps ? steps / min_steps : sp;
+  if (sp < 1) return 1;
+  const int64_t len = (steps + sp - 1) / sp;
+  return (int)((steps + len - 1) / len);
+}
+
+// The number of K chunks the router GEMM splits into (at least 4 k-steps each).
+int router_ksplit(int64_t T, int d, int E) {
+  const int bn = pick_bn(E, 64);
+  return ksplit_for(((T + BM - 1) / BM) * ((E + bn - 1) / bn), 3 * ((d + BK - 1) / BK), 4);
 }
 
 // logits[T, E] = x[T, d] . (W_hi + W_mid + W_lo) + b, the three bf16 parts
@@ -835,6 +850,38 @@ cudaError_t launch_router_gemm(const moe_bf16* x, const moe_bf16* w_split, const
   a.bn = pick_bn(E, 64);
   const int64_t tiles = ((T + BM - 1) / BM) * ((E + a.bn - 1) / a.bn) * a.ksplit;
   return launch_kind<Kind::RouterLogits>(a0, a0, b0, b0, a, tiles, s);
+}
+
+// The number of K chunks of the router-weight gradient GEMM (at least 8 k-steps each).
+int router_wgrad_ksplit(int64_t T, int d, int N3) {
+  const int bn = pick_bn(N3, 64);
+  return ksplit_for((int64_t)((d + BM - 1) / BM) * ((N3 + bn - 1) / bn), (T + BK - 1) / BK, 8);
+}
+
+// part[s][d][N3] = sum over the tokens of chunk s of x[t, :]^T dl3[t, :]: the
+// gradient of the router weight with dl's three bf16 parts side by side in N
+// (dl3 [T, N3] bf16, N3 = 3 * E8); the chunks and parts are summed later.
+cudaError_t launch_router_wgrad_gemm(const moe_bf16* x, const moe_bf16* dl3, int64_t T, int d,
+                                     int N3, int ksplit, float* part, int* status,
+                                     cudaStream_t s) {
+  if (T == 0) return cudaMemsetAsync(part, 0, (size_t)ksplit * d * N3 * 4, s);
+  CUtensorMap a0, b0;
+  if (!map2d(&a0, x, d, T, BK) || !map2d(&b0, dl3, N3, T, BK)) return cudaErrorInvalidValue;
+  GemmArgs a{};
+  a.E = 1;
+  a.M = d;
+  a.N = N3;
+  a.nk_seg = (int)((T + BK - 1) / BK);
+  a.nseg = 1;
+  a.seg_koff = 0;
+  a.ksteps_split = (a.nk_seg + ksplit - 1) / ksplit;
+  a.ksplit = (a.nk_seg + a.ksteps_split - 1) / a.ksteps_split;   // no empty chunk
+  if (a.ksplit != ksplit) return cudaErrorInvalidValue;
+  a.outf = part;
+  a.status = status;
+  a.bn = pick_bn(N3, 64);
+  const int64_t tiles = (int64_t)((d + BM - 1) / BM) * ((N3 + a.bn - 1) / a.bn) * a.ksplit;
+  return launch_kind<Kind::RouterWgrad>(a0, a0, b0, b0, a, tiles, s);
 }
 
 static int64_t mgrouped_tiles_upper(const GroupedDims& g, int N, int BN) {

@@ -29,10 +29,10 @@ cudaError_t launch_topk(const float* logits, const int32_t* forced_idx, int64_t 
 size_t route_bwd_ws_bytes(int64_t T, int d, int E, int k, int align);
 cudaError_t launch_route_bwd(const float* d_topk_w, const float* topk_w, const int32_t* topk_idx,
                              const float* w_router, const int64_t* offsets,
-                             const int32_t* src_pair, const moe_bf16* xp, int64_t T, int d, int E,
+                             const int32_t* src_pair, const moe_bf16* x, int64_t T, int d, int E,
                              int k, int align, moe_bf16* dx_inout, const moe_bf16* dxp,
                              const int32_t* dst_row, float* dw_router, float* dbias, void* ws,
-                             cudaStream_t s);
+                             int* status, cudaStream_t s);
 
 // permute.cu
 size_t permute_ws_bytes(int64_t T, int k, int E);
@@ -51,6 +51,10 @@ cudaError_t launch_combine_bwd(const moe_bf16* dy, const moe_bf16* yp, const int
 
 // gemm.cu (tcgen05 grouped GEMMs)
 int router_ksplit(int64_t T, int d, int E);
+int router_wgrad_ksplit(int64_t T, int d, int N3);
+cudaError_t launch_router_wgrad_gemm(const moe_bf16* x, const moe_bf16* dl3, int64_t T, int d,
+                                     int N3, int ksplit, float* part, int* status,
+                                     cudaStream_t s);
 cudaError_t launch_router_gemm(const moe_bf16* x, const moe_bf16* w_split, const float* bias,
                                int64_t T, int d, int E, int E8, int ksplit, float* out,
                                int* status, cudaStream_t s);

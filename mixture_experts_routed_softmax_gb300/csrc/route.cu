@@ -9,6 +9,8 @@
 // full softmax denominator cancels, so selecting on the logits and taking
 // the softmax over the selected ones gives the same weights without ties
 // created by rounding of exp.
+#include <algorithm>
+
 #include "common.cuh"
 #include "internal.h"
 
@@ -100,6 +102,7 @@ __device__ __forceinline__ bool ranks_above(float va, int ia, float vb, int ib) 
   return va > vb || (va == vb && ia < ib);
 }
 
+template <int NV>   // logits per lane: 32 * NV >= E
 __global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ logits,
                                                    const int32_t* __restrict__ forced, int64_t T,
                                                    int E, int k, int32_t* __restrict__ topk_idx,
@@ -119,9 +122,9 @@ __global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ log
       else raise_status(status, MOE_ERR_DEVICE_INDEX);
     }
   } else {
-    float v[kMaxExperts / 32];
+    float v[NV];
 #pragma unroll
-    for (int i = 0; i < kMaxExperts / 32; ++i) {
+    for (int i = 0; i < NV; ++i) {
       const int e = lane + 32 * i;
       v[i] = (e < E) ? lrow[e] : -INFINITY;
     }
@@ -130,7 +133,7 @@ __global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ log
       float bv = -INFINITY;
       int bi = 0x7FFFFFFF;
 #pragma unroll
-      for (int i = 0; i < kMaxExperts / 32; ++i) {
+      for (int i = 0; i < NV; ++i) {
         const int e = lane + 32 * i;
         if (e < E && !((taken >> i) & 1u) && ranks_above(v[i], e, bv, bi)) {
           bv = v[i];
@@ -166,7 +169,20 @@ cudaError_t launch_topk(const float* logits, const int32_t* forced_idx, int64_t 
   const int warps = 8;
   dim3 grid((unsigned)((T + warps - 1) / warps));
   timer_before(MOE_KERNEL_TOPK, s);
-  topk_kernel<<<grid, warps * 32, 0, s>>>(logits, forced_idx, T, E, k, topk_idx, topk_w, status);
+  const int nv = (E + 31) / 32;
+  if (nv <= 1)
+    topk_kernel<1><<<grid, warps * 32, 0, s>>>(logits, forced_idx, T, E, k, topk_idx, topk_w, status);
+  else if (nv <= 2)
+    topk_kernel<2><<<grid, warps * 32, 0, s>>>(logits, forced_idx, T, E, k, topk_idx, topk_w, status);
+  else if (nv <= 4)
+    topk_kernel<4><<<grid, warps * 32, 0, s>>>(logits, forced_idx, T, E, k, topk_idx, topk_w, status);
+  else if (nv <= 8)
+    topk_kernel<8><<<grid, warps * 32, 0, s>>>(logits, forced_idx, T, E, k, topk_idx, topk_w, status);
+  else if (nv <= 16)
+    topk_kernel<16><<<grid, warps * 32, 0, s>>>(logits, forced_idx, T, E, k, topk_idx, topk_w, status);
+  else
+    topk_kernel<kMaxExperts / 32><<<grid, warps * 32, 0, s>>>(logits, forced_idx, T, E, k,
+                                                              topk_idx, topk_w, status);
   note_launches(1);
   timer_after(MOE_KERNEL_TOPK, s);
   return cudaGetLastError();
@@ -174,25 +190,27 @@ cudaError_t launch_topk(const float* logits, const int32_t* forced_idx, int64_t 
 
 // ---------------------------------------------------------------------------
 // Router backward.
-//   dl_t,j = w_j (dw_j - sum_j' w_j' dw_j')  on the selected slots
+//   dl_t,j = w_j (dw_j - sum_j' w_j' dw_j')  on the selected slots (0 elsewhere)
 //   dx[t] += sum_j dl_t,j W_r[:, e_j]
-//   dW_r[:, e] = sum over e's rows of dl * xp[row];  db[e] = sum of dl
-// The last two are fixed-order two-phase sums: phase 1 sums each (128-row
-// block) n (expert group) segment of the padded layout into a partial row,
-// phase 2 adds each expert's partial rows in row order. No atomics.
+//   dW_r = x^T . dl  (dl as a dense [T, E] matrix)   db = column sums of dl
+// dW_r runs on the tensor cores like the forward logits: dl is split exactly
+// into three bf16 parts, laid side by side in a dense [T, 3 E8] matrix, and one
+// grouped-GEMM launch (split K, fixed-order reduce) forms x^T . [hi | mid | lo];
+// a bf16 x bf16 product is exact in fp32, so this is an fp32 accumulation of
+// exact products. db sums dl over each expert's rows of the padded layout in
+// row order. No atomics.
 // ---------------------------------------------------------------------------
-constexpr int kRbRows = 128;   // rows of the padded layout per phase-1 CTA
-constexpr int kRbCols = 1024;  // columns of d per phase-1 CTA (128 threads x 8)
-
-static inline int seg_unit(int align) { return align < kRbRows ? align : kRbRows; }
-
 static inline size_t al256(size_t b) { return (b + 255) & ~(size_t)255; }
+static inline int n3_of(int E) { return 3 * round8(E); }
 
+// workspace: W_r^T [E, d] fp32 | dl per pair [T*k] fp32 | dl3 [T, 3 E8] bf16 |
+// the GEMM's split-K partials [ksplit, d, 3 E8] fp32
 size_t route_bwd_ws_bytes(int64_t T, int d, int E, int k, int align) {
-  const int64_t R_cap = T * k + (int64_t)E * (align - 1);
-  const int64_t slots = (R_cap + seg_unit(align) - 1) / seg_unit(align);
-  return al256((size_t)E * d * 4) + al256((size_t)T * k * 4) + al256((size_t)slots * d * 4) +
-         al256((size_t)slots * 4);
+  (void)align;
+  const int N3 = n3_of(E);
+  const int sp = router_wgrad_ksplit(T, d, N3);
+  return al256((size_t)E * d * 4) + al256((size_t)T * k * 4) + al256((size_t)T * N3 * 2) +
+         al256((size_t)sp * d * N3 * 4);
 }
 
 __global__ void transpose_f32_kernel(const float* __restrict__ in, int rows, int cols,
@@ -211,14 +229,18 @@ __global__ void transpose_f32_kernel(const float* __restrict__ in, int rows, int
   }
 }
 
-// one warp per token: dl for its k slots, then dx[t]. With dxp given, dx[t] =
+// one warp per token: dl for its k slots (to dl_pair, and as three bf16 parts
+// into the token's dense row of dl3), then dx[t]. With dxp given, dx[t] =
 // sum_j dxp[dst_row[t, j]] + sum_j dl_j W_r[:, e_j] in fp32, written once (the
 // permute transpose fused in); without it, dx[t] += sum_j dl_j W_r[:, e_j].
-__global__ void __launch_bounds__(256) route_bwd_token_kernel(
+// The dxp rows of up to four slots are loaded together; few registers, so that
+// many warps per SM keep enough loads in flight.
+__global__ void __launch_bounds__(256, 4) route_bwd_token_kernel(
     const float* __restrict__ d_topk_w, const float* __restrict__ topk_w,
     const int32_t* __restrict__ topk_idx, const float* __restrict__ wrT, int64_t T, int d, int E,
-    int k, float* __restrict__ dl_pair, moe_bf16* __restrict__ dx,
-    const moe_bf16* __restrict__ dxp, const int32_t* __restrict__ dst_row) {
+    int E8, int k, float* __restrict__ dl_pair, moe_bf16* __restrict__ dl3,
+    moe_bf16* __restrict__ dx, const moe_bf16* __restrict__ dxp,
+    const int32_t* __restrict__ dst_row) {
   const int lane = threadIdx.x & 31;
   const int64_t t = (int64_t)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
   if (t >= T) return;
@@ -236,6 +258,23 @@ __global__ void __launch_bounds__(256) route_bwd_token_kernel(
   for (int off = 16; off > 0; off >>= 1) inner += __shfl_xor_sync(0xFFFFFFFFu, inner, off);
   const float dl = w * (dw - inner);
   if (lane < k) dl_pair[t * k + lane] = dl;
+
+  // dense dl row: zeros, then the three parts of each slot at columns p E8 + e
+  const int N3 = 3 * E8;
+  moe_bf16* drow = dl3 + t * N3;
+  for (int c = lane * 8; c < N3; c += 256)
+    *reinterpret_cast<uint4*>(drow + c) = make_uint4(0u, 0u, 0u, 0u);
+  __syncwarp();
+  if (lane < k && e >= 0) {
+    const __nv_bfloat16 hi = __float2bfloat16_rn(dl);
+    const float r1 = dl - __bfloat162float(hi);
+    const __nv_bfloat16 mid = __float2bfloat16_rn(r1);
+    const __nv_bfloat16 lo = __float2bfloat16_rn(r1 - __bfloat162float(mid));
+    drow[e] = __bfloat16_as_ushort(hi);
+    drow[E8 + e] = __bfloat16_as_ushort(mid);
+    drow[2 * E8 + e] = __bfloat16_as_ushort(lo);
+  }
+
   moe_bf16* dxr = dx + t * d;
   // every lane runs the same number of iterations: the shuffles need the whole warp
   for (int c0 = 0; c0 < d; c0 += 256) {
@@ -243,13 +282,25 @@ __global__ void __launch_bounds__(256) route_bwd_token_kernel(
     const bool in = c < d;
     float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
     if (in && !dxp) unpack8(*reinterpret_cast<const uint4*>(dxr + c), acc);
-    for (int j = 0; j < k; ++j) {
-      const int rj = __shfl_sync(0xFFFFFFFFu, r, j);
-      if (!in || rj < 0) continue;
-      float f[8];
-      unpack8(*reinterpret_cast<const uint4*>(dxp + (int64_t)rj * d + c), f);
+    if (dxp) {
+      for (int j0 = 0; j0 < k; j0 += 4) {
+        uint4 v[4];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) acc[i] += f[i];
+        for (int q = 0; q < 4; ++q) {
+          const int j = j0 + q;
+          const int rj = __shfl_sync(0xFFFFFFFFu, r, j & 31);
+          v[q] = (in && j < k && rj >= 0)
+                     ? *reinterpret_cast<const uint4*>(dxp + (int64_t)rj * d + c)
+                     : make_uint4(0u, 0u, 0u, 0u);
+        }
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          float f[8];
+          unpack8(v[q], f);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) acc[i] += f[i];
+        }
+      }
     }
     float add[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
     for (int j = 0; j < k; ++j) {
@@ -269,127 +320,81 @@ __global__ void __launch_bounds__(256) route_bwd_token_kernel(
   }
 }
 
-__device__ __forceinline__ int expert_of_row(const int64_t* offsets, int E, int64_t r) {
-  // largest e with offsets[e] <= r (offsets non-decreasing, offsets[0] = 0)
-  int lo = 0, hi = E;  // answer in [lo, hi)
-  while (hi - lo > 1) {
-    const int mid = (lo + hi) >> 1;
-    if (offsets[mid] <= r) lo = mid; else hi = mid;
-  }
-  return lo;
-}
-
-// phase 1: CTA (b, cb) sums rows [b*128, b*128+128) for columns [cb*1024, +1024)
-// (8 per thread, 16-byte loads), one partial row per expert segment it meets;
-// slot = segment start / unit.
-__global__ void __launch_bounds__(128) route_bwd_partial_kernel(
+// blockIdx.y == 0: dW_r[i, e] = sum over the K chunks s, in order, of
+// part[s][i][e] + part[s][i][E8 + e] + part[s][i][2 E8 + e];
+// blockIdx.y == 1: one warp per expert, db[e] = sum of dl over e's rows of the
+// padded layout (lane-strided in row order, then a fixed shuffle tree).
+__global__ void __launch_bounds__(256) route_bwd_reduce_kernel(
+    const float* __restrict__ part, int ksplit, int d, int E, int E8,
     const int64_t* __restrict__ offsets, const int32_t* __restrict__ src_pair,
-    const moe_bf16* __restrict__ xp, const float* __restrict__ dl_pair, int E, int d, int unit,
-    float* __restrict__ part, float* __restrict__ part_db) {
-  __shared__ float s_dl[kRbRows];     // dl of each row's pair, 0 for padding rows
-  __shared__ int s_real[kRbRows];
-  const int64_t r_begin = (int64_t)blockIdx.x * kRbRows;
-  const int64_t R_pad = offsets[E];
-  if (r_begin >= R_pad) return;
-  const int64_t r_end = min(r_begin + kRbRows, R_pad);
-  {
-    const int64_t q = r_begin + threadIdx.x;
-    const int pr = (q < r_end) ? src_pair[q] : -1;
-    s_real[threadIdx.x] = pr >= 0;
-    s_dl[threadIdx.x] = pr >= 0 ? dl_pair[pr] : 0.f;
-  }
-  __syncthreads();
-  const int c = blockIdx.y * kRbCols + threadIdx.x * 8;
-  int64_t r = r_begin;
-  while (r < r_end) {
-    const int e = expert_of_row(offsets, E, r);
-    const int64_t seg_end = min(r_end, offsets[e + 1]);
-    const int64_t slot = r / unit;
-    float a[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-    float adb = 0.f;
-#pragma unroll 4
-    for (int64_t q = r; q < seg_end; ++q) {
-      const int i = (int)(q - r_begin);
-      if (!s_real[i]) continue;
-      const float dl = s_dl[i];
-      adb += dl;
-      if (c < d) {
-        float f[8];
-        unpack8(*reinterpret_cast<const uint4*>(xp + q * d + c), f);
+    const float* __restrict__ dl_pair, float* __restrict__ dw_router, float* __restrict__ dbias) {
+  if (blockIdx.y == 0) {
+    const int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (idx >= (int64_t)d * E) return;
+    const int i = (int)(idx / E), e = (int)(idx % E);
+    const int N3 = 3 * E8;
+    float a = 0.f;
+    for (int s = 0; s < ksplit; ++s) {
+      const float* q = part + ((int64_t)s * d + i) * N3 + e;
+      a += q[0] + q[E8] + q[2 * E8];
+    }
+    dw_router[idx] = a;
+  } else {
+    const int lane = threadIdx.x & 31;
+    const int e = blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
+    if (e >= E) return;
+    const int64_t g0 = offsets[e], g1 = offsets[e + 1];
+    float a = 0.f;
+    for (int64_t r = g0 + lane; r < g1; r += 32) {
+      const int p = src_pair[r];
+      if (p >= 0) a += dl_pair[p];
+    }
 #pragma unroll
-        for (int j = 0; j < 8; ++j) a[j] = fmaf(dl, f[j], a[j]);
-      }
-    }
-    if (c < d) {
-      float4* o = reinterpret_cast<float4*>(part + slot * d + c);
-      o[0] = make_float4(a[0], a[1], a[2], a[3]);
-      o[1] = make_float4(a[4], a[5], a[6], a[7]);
-    }
-    if (blockIdx.y == 0 && threadIdx.x == 0) part_db[slot] = adb;
-    r = seg_end;
+    for (int off = 16; off > 0; off >>= 1) a += __shfl_xor_sync(0xFFFFFFFFu, a, off);
+    if (lane == 0) dbias[e] = a;
   }
-}
-
-// phase 2: per expert, add its partial rows in row order (2 columns per thread).
-constexpr int kRdCols = 256;
-__global__ void __launch_bounds__(128) route_bwd_reduce_kernel(
-    const int64_t* __restrict__ offsets, const float* __restrict__ part,
-    const float* __restrict__ part_db, int E, int d, int unit, float* __restrict__ dw_router,
-    float* __restrict__ dbias) {
-  const int e = blockIdx.x;
-  const int c = blockIdx.y * kRdCols + threadIdx.x * 2;
-  const int64_t g0 = offsets[e], g1 = offsets[e + 1];
-  float a0 = 0.f, a1 = 0.f, adb = 0.f;
-  int64_t r = g0;
-  while (r < g1) {
-    const int64_t slot = r / unit;
-    if (c < d) {
-      a0 += part[slot * d + c];
-      a1 += part[slot * d + c + 1];
-    }
-    adb += part_db[slot];
-    r = min(g1, (r / kRbRows + 1) * kRbRows);  // next 128-row block boundary
-  }
-  if (c < d) {
-    dw_router[(int64_t)c * E + e] = a0;
-    dw_router[(int64_t)(c + 1) * E + e] = a1;
-  }
-  if (dbias && blockIdx.y == 0 && threadIdx.x == 0) dbias[e] = adb;
 }
 
 cudaError_t launch_route_bwd(const float* d_topk_w, const float* topk_w, const int32_t* topk_idx,
                              const float* w_router, const int64_t* offsets,
-                             const int32_t* src_pair, const moe_bf16* xp, int64_t T, int d, int E,
+                             const int32_t* src_pair, const moe_bf16* x, int64_t T, int d, int E,
                              int k, int align, moe_bf16* dx_inout, const moe_bf16* dxp,
                              const int32_t* dst_row, float* dw_router, float* dbias, void* ws,
-                             cudaStream_t s) {
-  const int64_t R_cap = T * k + (int64_t)E * (align - 1);
-  const int unit = seg_unit(align);
+                             int* status, cudaStream_t s) {
+  (void)align;
+  const int E8 = round8(E);
+  const int N3 = n3_of(E);
+  const int sp = router_wgrad_ksplit(T, d, N3);
   char* p = static_cast<char*>(ws);
   float* wrT = reinterpret_cast<float*>(p);
   p += al256((size_t)E * d * 4);
   float* dl_pair = reinterpret_cast<float*>(p);
   p += al256((size_t)T * k * 4);
-  const int64_t slots = (R_cap + unit - 1) / unit;
+  moe_bf16* dl3 = reinterpret_cast<moe_bf16*>(p);
+  p += al256((size_t)T * N3 * 2);
   float* part = reinterpret_cast<float*>(p);
-  p += al256((size_t)slots * d * 4);
-  float* part_db = reinterpret_cast<float*>(p);
 
   timer_before(MOE_KERNEL_ROUTE_BWD, s);
   transpose_f32_kernel<<<dim3((E + 31) / 32, (d + 31) / 32), dim3(32, 8), 0, s>>>(w_router, d, E,
                                                                                   wrT);
-  if (T > 0)
-    route_bwd_token_kernel<<<(unsigned)((T + 7) / 8), 256, 0, s>>>(d_topk_w, topk_w, topk_idx,
-                                                                   wrT, T, d, E, k, dl_pair,
-                                                                   dx_inout, dxp, dst_row);
-  const int cblocks = (d + kRbCols - 1) / kRbCols;
-  route_bwd_partial_kernel<<<dim3((unsigned)((R_cap + kRbRows - 1) / kRbRows), cblocks), 128, 0,
-                             s>>>(offsets, src_pair, xp, dl_pair, E, d, unit, part, part_db);
-  route_bwd_reduce_kernel<<<dim3(E, (d + kRdCols - 1) / kRdCols), 128, 0, s>>>(
-      offsets, part, part_db, E, d, unit, dw_router, dbias);
-  note_launches(T > 0 ? 4 : 3);
+  note_launches(1);
+  if (T > 0) {
+    route_bwd_token_kernel<<<(unsigned)((T + 7) / 8), 256, 0, s>>>(
+        d_topk_w, topk_w, topk_idx, wrT, T, d, E, E8, k, dl_pair, dl3, dx_inout, dxp, dst_row);
+    note_launches(1);
+  }
+  cudaError_t err = cudaGetLastError();
+  if (err == cudaSuccess) err = launch_router_wgrad_gemm(x, dl3, T, d, N3, sp, part, status, s);
+  if (err == cudaSuccess) {
+    const int64_t n = (int64_t)d * E;
+    const unsigned gx = (unsigned)std::max<int64_t>((n + 255) / 256, (E + 7) / 8);
+    route_bwd_reduce_kernel<<<dim3(gx, dbias ? 2 : 1), 256, 0, s>>>(
+        part, sp, d, E, E8, offsets, src_pair, dl_pair, dw_router, dbias);
+    note_launches(1);
+    err = cudaGetLastError();
+  }
   timer_after(MOE_KERNEL_ROUTE_BWD, s);
-  return cudaGetLastError();
+  return err;
 }
 
 }  // namespace moe

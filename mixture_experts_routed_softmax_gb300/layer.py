@@ -59,6 +59,8 @@ class Buffers:
     dw_router: Optional[torch.Tensor] = None
     dbias: Optional[torch.Tensor] = None
     ws_route_bwd: Optional[torch.Tensor] = None
+    # the input of the last forward (the router backward reads it)
+    x: Optional[torch.Tensor] = None
 
 
 class MoELayer:
@@ -162,18 +164,21 @@ class MoELayer:
                   _p(b.dyp), _p(b.dg), _p(b.du), _p(b.dxp), _p(b.d_topk_w),
                   _p(b.dw_gate), _p(b.dw_up), _p(b.dw_down), _stream(stream))
 
-    def route_bwd(self, b: Buffers, fused=True, stream=None):
+    def route_bwd(self, b: Buffers, fused=True, stream=None, x=None):
         """Router backward. fused: dx = permute transpose of dXp + the router's
-        term in one pass; else dx (already holding the permute transpose) += it."""
+        term in one pass; else dx (already holding the permute transpose) += it.
+        x: the layer input (default: the one the last forward recorded in b)."""
+        x = b.x if x is None else x
         _lib.call("moe_route_bwd", _p(b.d_topk_w), _p(b.topk_w), _p(b.topk_idx),
-                  _p(self.w_router), _p(b.offsets), _p(b.src_pair), _p(b.xp), b.T, self.d,
+                  _p(self.w_router), _p(b.offsets), _p(b.src_pair), _p(x), b.T, self.d,
                   self.E, self.k, self.align, _p(b.dx), _p(b.dxp) if fused else None,
                   _p(b.dst_row) if fused else None, _p(b.dw_router), _p(b.dbias),
                   _p(b.ws_route_bwd), b.ws_route_bwd.numel(), _stream(stream))
 
     # ------------------------------------------------------ whole layer --
     def forward(self, x, b: Buffers, forced_idx=None, stream=None):
-        """y = layer(x) into b.y; every intermediate stays in ``b``."""
+        """y = layer(x) into b.y; every intermediate stays in ``b`` (x by reference)."""
+        b.x = x
         self.route(x, b, forced_idx, stream)
         self.permute(x, b, None, stream)
         self.expert_fwd(b, None, stream)
