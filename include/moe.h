@@ -36,6 +36,11 @@
  *   - Return codes below; MOE_ERR_ARG etc. are detected on the host before
  *     anything is enqueued. MOE_ERR_DEVICE_* are raised by kernels into a
  *     per-device status word and reported by moe_status().
+ *   - Tuning: the expert GEMMs run some kinds as two-CTA clusters (one
+ *     M = 256 tensor-core MMA over two SMs) where that is faster; the
+ *     environment variable MOE_GEMM_PAIRS=0 or 1, read once per process,
+ *     turns that off or on for every grouped GEMM. Results agree either way
+ *     within rounding of the same fp32 accumulation.
  */
 #ifndef MOE_GB300_H
 #define MOE_GB300_H

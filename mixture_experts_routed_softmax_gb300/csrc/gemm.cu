@@ -78,6 +78,17 @@ struct Tr {
                                : MOE_KERNEL_ROUTER_LOGITS;
 };
 
+// Shared-memory ring per CTA: one A tile and all of B's tile (or, in a CTA
+// pair, this CTA's half of B's columns) per stage, as many stages as fit.
+template <Kind K, bool PAIR>
+struct Geo {
+  using T = Tr<K>;
+  static constexpr int b_bytes = (T::dual ? 2 : 1) * T::BN * BK * 2 / (PAIR ? 2 : 1);
+  static constexpr int stage_bytes = kABytes + b_bytes;
+  static constexpr int stages =
+      kRingBytes / stage_bytes > kMaxStages ? kMaxStages : kRingBytes / stage_bytes;
+};
+
 constexpr int kTmemCols = 512;                            // 2 accumulator buffers x 256 columns
 constexpr int kEpiWarps = 8;                              // two warpgroups, each half the columns
 constexpr int kThreads = 128 + 32 * kEpiWarps;
@@ -127,10 +138,13 @@ __device__ __forceinline__ int tile_bn(const GemmArgs& a) {
   return Tr<K>::var_bn ? a.bn : Tr<K>::BN;
 }
 
-template <Kind K>
+// A CTA pair (PAIR) takes 256-row tiles: rank 0 the first 128 rows, rank 1
+// the next 128 (past the group's end: computed, not stored).
+template <Kind K, bool PAIR>
 __device__ __forceinline__ void decode_tile(int tile, const GemmArgs& a, const int* tstart,
-                                            int nN, TileInfo& ti) {
+                                            int nN, int rank, TileInfo& ti) {
   using T = Tr<K>;
+  constexpr int TM = PAIR ? 2 * BM : BM;
   const int bn = tile_bn<K>(a);
   const int nt = tile % nN;
   const int mt = tile / nN;
@@ -147,9 +161,9 @@ __device__ __forceinline__ void decode_tile(int tile, const GemmArgs& a, const i
     const int total_steps = a.nk_seg * a.nseg;
     ti.nk = (int)min((int64_t)a.ksteps_split, (int64_t)total_steps - ti.kbeg);
   } else if constexpr (T::kgrouped) {
-    const int nM = (a.M + BM - 1) / BM;
+    const int nM = (a.M + TM - 1) / TM;
     ti.e = mt / nM;
-    ti.m0 = (int64_t)(mt % nM) * BM;
+    ti.m0 = (int64_t)(mt % nM) * TM + rank * BM;
     ti.kbeg = a.offsets[ti.e];
     ti.row_end = a.offsets[ti.e + 1] - ti.kbeg;
     ti.nk = (int)((ti.row_end + BK - 1) / BK);
@@ -160,7 +174,7 @@ __device__ __forceinline__ void decode_tile(int tile, const GemmArgs& a, const i
       if (tstart[mid] <= mt) lo = mid; else hi = mid;
     }
     ti.e = lo;
-    ti.m0 = a.offsets[lo] + (int64_t)(mt - tstart[lo]) * BM;
+    ti.m0 = a.offsets[lo] + (int64_t)(mt - tstart[lo]) * TM + rank * BM;
     ti.row_end = a.offsets[lo + 1];
     ti.kbeg = 0;
     ti.nk = a.nk_seg * (T::two_seg ? 2 : 1);
@@ -242,7 +256,7 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, int* s
   mbar_wait_bounded(bar, parity, &never, status);
 }
 
-template <Kind K>
+template <Kind K, bool PAIR>
 __global__ void __launch_bounds__(kThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA0,
                         const __grid_constant__ CUtensorMap mapA1,
@@ -252,12 +266,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const __grid_constant__ CUtensorMap mapO1,
                         const __grid_constant__ CUtensorMap mapO2, const GemmArgs args) {
   using T = Tr<K>;
+  using G = Geo<K, PAIR>;
+  static_assert(!PAIR || (!T::dense && K != Kind::GateUpFwdNarrow), "pairs: grouped kinds");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~(uintptr_t)1023);
   const uint32_t s_base = smem_u32(smem);
-  constexpr int kStages = T::stages;
-  constexpr int kStageBytes = T::tx_bytes;              // a multiple of 8 KiB: atoms stay aligned
+  constexpr int kStages = G::stages;
+  constexpr int kStageBytes = G::stage_bytes;           // a multiple of 8 KiB: atoms stay aligned
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kRingBytes);
   // bars: full[kMaxStages], empty[kMaxStages], tfull[2], tempty[2], drain
   const uint32_t bar0 = smem_u32(bars);
@@ -273,6 +289,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  // CTA pair: rank 0 issues the MMAs and owns the barriers both CTAs' loads
+  // and epilogues report to
+  const int rank = PAIR ? (int)cluster_ctarank() : 0;
+  const bool rank0 = rank == 0;
+  // this CTA's (or pair's) first tile and the tile stride, read where used
+  // (no register held across the kernel)
+#define GEMM_CID (PAIR ? (int)(blockIdx.x >> 1) : (int)blockIdx.x)
+#define GEMM_NCL (PAIR ? (int)(gridDim.x >> 1) : (int)gridDim.x)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -281,7 +305,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(tfull_bar(b), 1);
-      mbar_init(tempty_bar(b), kEpiWarps);
+      mbar_init(tempty_bar(b), PAIR ? 2 * kEpiWarps : kEpiWarps);
     }
     mbar_init(drain_bar, 1);
     *s_abort = 0;
@@ -294,14 +318,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (T::dual || T::two_seg) tma_prefetch_desc(&mapB1);
   }
   if (warp == 2) {
-    tmem_alloc(smem_u32(s_tmem), kTmemCols);
-    tmem_relinquish();
+    if constexpr (PAIR) {
+      tmem_alloc_pair(smem_u32(s_tmem), kTmemCols);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(smem_u32(s_tmem), kTmemCols);
+      tmem_relinquish();
+    }
   }
-  // M-grouped tile table: tstart[e] = sum_{e'<e} ceil(L_e' / BM)
+  // M-grouped tile table: tstart[e] = sum_{e'<e} ceil(L_e' / tile rows)
+  constexpr int TM = PAIR ? 2 * BM : BM;
   if constexpr (!T::kgrouped && !T::dense) {
     for (int e = threadIdx.x; e < args.E; e += kThreads) {
       const int64_t L = args.offsets[e + 1] - args.offsets[e];
-      tstart[e + 1] = (int)((L + BM - 1) / BM);
+      tstart[e + 1] = (int)((L + TM - 1) / TM);
     }
     __syncthreads();
     if (warp == 3) {
@@ -322,6 +352,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
+  if constexpr (PAIR) cluster_sync();   // the peer's barriers are initialised
   tc_fence_after();
   const uint32_t tmem_base = *s_tmem;
 
@@ -329,7 +360,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int nN = (args.N + bn - 1) / bn;
   int total;
   if constexpr (T::kgrouped) {
-    total = args.E * ((args.M + BM - 1) / BM) * nN;
+    total = args.E * ((args.M + TM - 1) / TM) * nN;
   } else if constexpr (T::dense) {
     total = ((args.M + BM - 1) / BM) * nN * args.ksplit;
   } else {
@@ -338,13 +369,21 @@ __global__ void __launch_bounds__(kThreads, 1)
   // dual kinds: the two B tiles sit side by side in shared memory ([B0 | B1],
   // 64-column chunks at a fixed stride), so one N = 256 MMA fills both
   // accumulators (columns 0-127 and 128-255) and the A tile is read once
+  // (a pair: one M = 256 MMA, B's columns split between the two CTAs; for the
+  // dual kinds rank 0 holds B0 and rank 1 B1)
   constexpr uint32_t kIdesc =
-      idesc_bf16(BM, T::dual ? 2 * T::BN : T::BN, T::a_mn ? 1 : 0, T::b_mn ? 1 : 0);
+      idesc_bf16(TM, T::dual ? 2 * T::BN : T::BN, T::a_mn ? 1 : 0, T::b_mn ? 1 : 0);
   constexpr uint32_t kBBytes = (uint32_t)T::BN * BK * 2;
-  // B of a var_bn kind: bn rows (K-major) or ceil(bn / 64) 64-column boxes (N-major)
+  // B of a var_bn kind: bn rows (K-major) or ceil(bn / 64) 64-column boxes (N-major);
+  // in a pair each CTA loads bn / 2 rows (K-major) or two boxes (N-major)
   const int nbox = (bn + 63) / 64;
-  const uint32_t b_bytes = T::b_mn ? (uint32_t)nbox * (BK * 128) : (uint32_t)bn * (BK * 2);
-  const uint32_t tx_bytes = T::var_bn ? (uint32_t)kABytes + b_bytes : (uint32_t)T::tx_bytes;
+  uint32_t b_bytes;
+  if constexpr (PAIR)
+    b_bytes = (T::dual || T::b_mn) ? 2u * (BK * 128) : (uint32_t)(bn / 2) * (BK * 2);
+  else
+    b_bytes = T::b_mn ? (uint32_t)nbox * (BK * 128) : (uint32_t)bn * (BK * 2);
+  const uint32_t tx_bytes =
+      (PAIR || T::var_bn) ? (uint32_t)kABytes + b_bytes : (uint32_t)G::stage_bytes;
   static_assert(kStages * kStageBytes <= kRingBytes && kStageBytes % 8192 == 0, "ring layout");
 
   if (warp == 0) {
@@ -355,9 +394,57 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t phase = 0;
       int fills = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+      if constexpr (PAIR) {
+        // each CTA loads its A rows and its share of B's columns into its own
+        // ring; the bytes are counted on rank 0's full barrier, which rank 0
+        // arms for both
+        for (int tile = GEMM_CID; tile < total && ok; tile += GEMM_NCL) {
+          TileInfo ti;
+          decode_tile<K, PAIR>(tile, args, tstart, nN, rank, ti);
+          int nv = (args.N - ti.n0 + 15) & ~15;   // the columns the pair multiplies
+          nv = nv < bn ? nv : bn;
+          const int bcol = T::dual ? ti.n0 : ti.n0 + rank * (nv >> 1);
+          const void* mBd = (T::dual && rank) ? (const void*)&mapB1 : (const void*)&mapB0;
+          for (int ks = 0; ks < ti.nk; ++ks) {
+            if (!mbar_wait_bounded(empty_bar(stage), phase ^ 1u, s_abort, args.status)) {
+              ok = false;
+              break;
+            }
+            const uint32_t fb = full_bar(stage);
+            const uint32_t fbl = rank0 ? fb : mapa_shared(fb, 0);
+            const uint32_t sA = s_base + stage * kStageBytes;
+            const uint32_t sB = sA + kABytes;
+            if (rank0) mbar_arrive_expect_tx(fb, 2u * tx_bytes);
+            if constexpr (T::kgrouped) {
+              const int row0 = (int)(ti.kbeg + (int64_t)ks * BK);
+#pragma unroll
+              for (int i = 0; i < BM / 64; ++i)
+                tma_load_2d_pair(sA + i * (BK * 128), &mapA0, fbl, (int)ti.m0 + 64 * i, row0);
+#pragma unroll
+              for (int j = 0; j < 2; ++j)
+                tma_load_2d_pair(sB + j * (BK * 128), mBd, fbl, bcol + 64 * j, row0);
+            } else {
+              const int seg = (T::two_seg && ks >= args.nk_seg) ? 1 : 0;
+              const int kk = (ks - seg * args.nk_seg) * BK;
+              const void* mA = seg ? (const void*)&mapA1 : (const void*)&mapA0;
+              const void* mB = seg ? (const void*)&mapB1 : (const void*)&mapB0;
+              tma_load_2d_pair(sA, mA, fbl, kk, (int)ti.m0);
+              if constexpr (T::b_mn) {
+#pragma unroll
+                for (int j = 0; j < 2; ++j)
+                  tma_load_3d_pair(sB + j * (BK * 128), mBd, fbl, bcol + 64 * j, kk, ti.e, pol_w);
+              } else {
+                tma_load_3d_pair(sB, mB, fbl, kk, bcol, ti.e, pol_w);
+              }
+            }
+            ++fills;
+            if (++stage == kStages) { stage = 0; phase ^= 1u; }
+          }
+        }
+      } else {
+      for (int tile = GEMM_CID; tile < total && ok; tile += GEMM_NCL) {
         TileInfo ti;
-        decode_tile<K>(tile, args, tstart, nN, ti);
+        decode_tile<K, PAIR>(tile, args, tstart, nN, 0, ti);
         for (int ks = 0; ks < ti.nk; ++ks) {
           if (!mbar_wait_bounded(empty_bar(stage), phase ^ 1u, s_abort, args.status)) {
             ok = false;
@@ -418,28 +505,37 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (++stage == kStages) { stage = 0; phase ^= 1u; }
         }
       }
+      }
       if (*s_abort) {
         // let the copies already issued land before the CTA's shared memory goes away
-        const int outstanding = fills < kStages ? fills : kStages;
-        int st = stage;
-        uint32_t ph = phase;
-        for (int i = 0; i < outstanding; ++i) {
-          if (--st < 0) { st = kStages - 1; ph ^= 1u; }
-          drain_wait(full_bar(st), ph, args.status);
+        if (!PAIR || rank0) {
+          const int outstanding = fills < kStages ? fills : kStages;
+          int st = stage;
+          uint32_t ph = phase;
+          for (int i = 0; i < outstanding; ++i) {
+            if (--st < 0) { st = kStages - 1; ph ^= 1u; }
+            drain_wait(full_bar(st), ph, args.status);
+          }
+        } else {
+          // rank 1's copies report to rank 0's barriers: give them a fixed,
+          // generous time to land instead
+          const uint64_t t0 = global_ns();
+          while (global_ns() - t0 < 200000ull) {
+          }
         }
       }
     }
   } else if (warp == 1) {
-    if (lane == 0) {
+    if (lane == 0 && rank0) {
       // ---------------------------------------------------------- MMA --
       int stage = 0;
       uint32_t phase = 0;
       int acc = 0;
       uint32_t acc_phase = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+      for (int tile = GEMM_CID; tile < total && ok; tile += GEMM_NCL) {
         TileInfo ti;
-        decode_tile<K>(tile, args, tstart, nN, ti);
+        decode_tile<K, PAIR>(tile, args, tstart, nN, 0, ti);
         if (ti.nk == 0) continue;
         if (!mbar_wait_bounded(tempty_bar(acc), acc_phase ^ 1u, s_abort, args.status)) break;
         tc_fence_after();
@@ -450,7 +546,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if constexpr (!T::dual) {
           int nv = (args.N - ti.n0 + 15) & ~15;
           nv = nv < bn ? nv : bn;
-          if (nv != T::BN) idesc = idesc_bf16(BM, nv, T::a_mn ? 1 : 0, T::b_mn ? 1 : 0);
+          if (nv != T::BN) idesc = idesc_bf16(TM, nv, T::a_mn ? 1 : 0, T::b_mn ? 1 : 0);
         }
         for (int ks = 0; ks < ti.nk; ++ks) {
           if (!mbar_wait_bounded(full_bar(stage), phase, s_abort, args.status)) {
@@ -471,17 +567,32 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint64_t bd0 = T::b_mn ? sdesc_sw128(sB0 + kk * 2048, BK * 128, 1024)
                                          : sdesc_sw128(sB0 + kk * 32, 16, 1024);
             const uint32_t accum = (ks > 0 || kk > 0) ? 1u : 0u;
-            umma_bf16(d_tmem, ad, bd0, idesc, accum);
+            if constexpr (PAIR)
+              umma_bf16_pair(d_tmem, ad, bd0, idesc, accum);
+            else
+              umma_bf16(d_tmem, ad, bd0, idesc, accum);
           }
-          umma_commit(empty_bar(stage));
+          if constexpr (PAIR)
+            umma_commit_pair(empty_bar(stage), 3);   // the slot is free in both CTAs
+          else
+            umma_commit(empty_bar(stage));
           if (++stage == kStages) { stage = 0; phase ^= 1u; }
         }
         if (!ok) break;
-        umma_commit(tfull_bar(acc));
+        if constexpr (PAIR)
+          umma_commit_pair(tfull_bar(acc), 3);
+        else
+          umma_commit(tfull_bar(acc));
         if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
       }
       // every MMA issued by this thread has finished before tensor memory is freed
-      umma_commit(drain_bar);
+      if constexpr (PAIR)
+        umma_commit_pair(drain_bar, 3);
+      else
+        umma_commit(drain_bar);
+      drain_wait(drain_bar, 0, args.status);
+    } else if (PAIR && lane == 0) {
+      // rank 1: rank 0's MMAs write this CTA's tensor memory; they finish first
       drain_wait(drain_bar, 0, args.status);
     }
   } else if (warp >= 4) {
@@ -495,9 +606,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int c_hi = c_lo + kHalf < bn ? c_lo + kHalf : bn;
     int acc = 0;
     uint32_t acc_phase = 0;
-    for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
+    for (int tile = GEMM_CID; tile < total; tile += GEMM_NCL) {
       TileInfo ti;
-      decode_tile<K>(tile, args, tstart, nN, ti);
+      decode_tile<K, PAIR>(tile, args, tstart, nN, rank, ti);
       const int64_t row = ti.m0 + rloc;
       if constexpr (T::kgrouped) {
         const bool row_ok = row < args.M;
@@ -548,7 +659,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // -> staged TMA stores by the warpgroup; else masked row stores
       const int group = (warp - 4) >> 2;
       const bool leader = (wq == 0 && lane == 0);
-      const bool tile_tma = T::kgrouped || (ti.m0 + BM <= ti.row_end);
+      const bool tile_tma = T::kgrouped ? ti.m0 < args.M : ti.m0 + BM <= ti.row_end;
       uint8_t* stg = stage_out + group * kStagePerGroup;
       const CUtensorMap* maps[3] = {&mapO0, &mapO1, &mapO2};
       moe_bf16* outs[3] = {args.out0, args.out1, args.out2};
@@ -672,15 +783,28 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(tempty_bar(acc));
+      if (lane == 0) {
+        if (PAIR && !rank0)
+          mbar_arrive_cluster(mapa_shared(tempty_bar(acc), 0));   // rank 0's MMA waits on it
+        else
+          mbar_arrive(tempty_bar(acc));
+      }
       if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
     }
     if (wq == 0 && lane == 0) bulk_wait_all();   // the staged stores finish before the CTA exits
   }
   tc_fence_before();
   __syncthreads();
+  if constexpr (PAIR) cluster_sync();   // no remote arrival or copy is still to come
   tc_fence_after();
-  if (warp == 2) tmem_dealloc(tmem_base, kTmemCols);
+  if (warp == 2) {
+    if constexpr (PAIR)
+      tmem_dealloc_pair(tmem_base, kTmemCols);
+    else
+      tmem_dealloc(tmem_base, kTmemCols);
+  }
+#undef GEMM_CID
+#undef GEMM_NCL
 }
 
 // ------------------------------------------------------------------ host --
@@ -758,7 +882,10 @@ static bool map3d_out(CUtensorMap* m, const void* ptr, uint64_t N, uint64_t M, u
             CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <Kind K>
+// tiles_upper: an upper bound on the kernel's tiles (pair tiles for PAIR). A
+// persistent grid: one CTA per SM, or for PAIR one two-CTA cluster per pair of
+// SMs that can hold one at a time.
+template <Kind K, bool PAIR>
 static cudaError_t launch_kind(const CUtensorMap& a0, const CUtensorMap& a1,
                                const CUtensorMap& b0, const CUtensorMap& b1, const GemmArgs& args,
                                int64_t tiles_upper, cudaStream_t s,
@@ -766,23 +893,83 @@ static cudaError_t launch_kind(const CUtensorMap& a0, const CUtensorMap& a1,
                                const CUtensorMap* o2 = nullptr) {
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
+  static int units = 0;
   std::call_once(once, [] {
-    attr_err = cudaFuncSetAttribute(grouped_gemm_kernel<K>,
+    attr_err = cudaFuncSetAttribute(grouped_gemm_kernel<K, PAIR>,
                                     cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    units = num_sms();
+    if (PAIR && attr_err == cudaSuccess) {
+      cudaLaunchConfig_t cfg = {};
+      cudaLaunchAttribute at[1];
+      at[0].id = cudaLaunchAttributeClusterDimension;
+      at[0].val.clusterDim.x = 2;
+      at[0].val.clusterDim.y = 1;
+      at[0].val.clusterDim.z = 1;
+      cfg.gridDim = dim3((unsigned)(num_sms() & ~1));
+      cfg.blockDim = dim3(kThreads);
+      cfg.dynamicSmemBytes = kSmemBytes;
+      cfg.attrs = at;
+      cfg.numAttrs = 1;
+      int n = 0;
+      if (cudaOccupancyMaxActiveClusters(&n, grouped_gemm_kernel<K, PAIR>, &cfg) != cudaSuccess ||
+          n < 1) {
+        cudaGetLastError();
+        n = num_sms() / 2;
+      }
+      units = n;
+    }
   });
   if (attr_err != cudaSuccess) return attr_err;
-  int64_t grid = num_sms();
+  int64_t grid = units;
   if (tiles_upper < grid) grid = tiles_upper;
   if (grid < 1) grid = 1;
   // the router's timers bracket these GEMMs with their other kernels (route.cu)
   if constexpr (!Tr<K>::dense) timer_before(Tr<K>::kernel_id, s);
   const CUtensorMap& m0 = o0 ? *o0 : a0;
-  grouped_gemm_kernel<K><<<(unsigned)grid, kThreads, kSmemBytes, s>>>(
-      a0, a1, b0, b1, m0, o1 ? *o1 : m0, o2 ? *o2 : m0, args);
+  const CUtensorMap& m1 = o1 ? *o1 : m0;
+  const CUtensorMap& m2 = o2 ? *o2 : m0;
+  if constexpr (PAIR) {
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = 2;
+    at[0].val.clusterDim.y = 1;
+    at[0].val.clusterDim.z = 1;
+    cfg.gridDim = dim3((unsigned)(2 * grid));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.stream = s;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    cudaLaunchKernelEx(&cfg, grouped_gemm_kernel<K, PAIR>, a0, a1, b0, b1, m0, m1, m2, args);
+  } else {
+    grouped_gemm_kernel<K, PAIR><<<(unsigned)grid, kThreads, kSmemBytes, s>>>(a0, a1, b0, b1, m0,
+                                                                             m1, m2, args);
+  }
   note_launches(1);
   if constexpr (!Tr<K>::dense) timer_after(Tr<K>::kernel_id, s);
   return cudaGetLastError();
 }
+
+// CTA pairs (M = 256 MMAs over two SMs: half the B traffic per SM, a deeper
+// ring) for the M-grouped kinds when the experts average at least 1024 rows,
+// where 256-row tiles waste little (the down dgrad excepted, below). Not by
+// default for the K-grouped weight gradients: their rows (d or f, e.g.
+// 2880 = 11.25 x 256) leave a mostly empty last 256-row tile.
+// MOE_GEMM_PAIRS=0 or 1 in the environment turns pairs off or on for every
+// grouped kind (a tuning and testing knob; the results are the same).
+static int pairs_env() {
+  static const int v = [] {
+    const char* e = getenv("MOE_GEMM_PAIRS");
+    return (e && (e[0] == '0' || e[0] == '1')) ? e[0] - '0' : -1;
+  }();
+  return v;
+}
+static bool pairs_mgrouped(const GroupedDims& g) {
+  const int e = pairs_env();
+  return e >= 0 ? e == 1 : g.P >= (int64_t)1024 * g.E;
+}
+static bool pairs_kgrouped() { return pairs_env() == 1; }
 
 // Tile width of a single-accumulator GEMM over N columns: the fewest 256-wide
 // tiles, made equal in width and rounded up to `step` columns: 16 (the MMA's
@@ -849,7 +1036,7 @@ cudaError_t launch_router_gemm(const moe_bf16* x, const moe_bf16* w_split, const
   a.status = status;
   a.bn = pick_bn(E, 64);
   const int64_t tiles = ((T + BM - 1) / BM) * ((E + a.bn - 1) / a.bn) * a.ksplit;
-  return launch_kind<Kind::RouterLogits>(a0, a0, b0, b0, a, tiles, s);
+  return launch_kind<Kind::RouterLogits, false>(a0, a0, b0, b0, a, tiles, s);
 }
 
 // The number of K chunks of the router-weight gradient GEMM (at least 8 k-steps each).
@@ -881,12 +1068,12 @@ cudaError_t launch_router_wgrad_gemm(const moe_bf16* x, const moe_bf16* dl3, int
   a.status = status;
   a.bn = pick_bn(N3, 64);
   const int64_t tiles = (int64_t)((d + BM - 1) / BM) * ((N3 + a.bn - 1) / a.bn) * a.ksplit;
-  return launch_kind<Kind::RouterWgrad>(a0, a0, b0, b0, a, tiles, s);
+  return launch_kind<Kind::RouterWgrad, false>(a0, a0, b0, b0, a, tiles, s);
 }
 
-static int64_t mgrouped_tiles_upper(const GroupedDims& g, int N, int BN) {
+static int64_t mgrouped_tiles_upper(const GroupedDims& g, int N, int BN, int TM = BM) {
   // each expert's rows may end in a partial tile
-  return ((g.R_cap + BM - 1) / BM + g.E) * ((N + BN - 1) / BN);
+  return ((g.R_cap + TM - 1) / TM + g.E) * ((N + BN - 1) / BN);
 }
 
 cudaError_t launch_gateup_fwd(const GroupedDims& g, const moe_bf16* xp, const moe_bf16* w_gate,
@@ -906,10 +1093,13 @@ cudaError_t launch_gateup_fwd(const GroupedDims& g, const moe_bf16* xp, const mo
   const int64_t rows = (g.P + g.E - 1) / g.E;
   const int64_t tiles = (int64_t)g.E * ((rows + BM - 1) / BM) * ((g.f + 127) / 128);
   if (tiles < 8 * (int64_t)num_sms())
-    return launch_kind<Kind::GateUpFwdNarrow>(a0, a0, b0, b1, a,
-                                              mgrouped_tiles_upper(g, g.f, 64), s, &o0, &o1, &o2);
-  return launch_kind<Kind::GateUpFwd>(a0, a0, b0, b1, a, mgrouped_tiles_upper(g, g.f, 128), s,
-                                      &o0, &o1, &o2);
+    return launch_kind<Kind::GateUpFwdNarrow, false>(
+        a0, a0, b0, b1, a, mgrouped_tiles_upper(g, g.f, 64), s, &o0, &o1, &o2);
+  if (pairs_mgrouped(g))
+    return launch_kind<Kind::GateUpFwd, true>(
+        a0, a0, b0, b1, a, mgrouped_tiles_upper(g, g.f, 128, 2 * BM), s, &o0, &o1, &o2);
+  return launch_kind<Kind::GateUpFwd, false>(a0, a0, b0, b1, a, mgrouped_tiles_upper(g, g.f, 128),
+                                             s, &o0, &o1, &o2);
 }
 
 cudaError_t launch_down_fwd(const GroupedDims& g, const moe_bf16* A, const moe_bf16* w_down,
@@ -923,7 +1113,11 @@ cudaError_t launch_down_fwd(const GroupedDims& g, const moe_bf16* A, const moe_b
   a.nk_seg = (g.f + BK - 1) / BK;
   a.out0 = yp;
   a.row_w = row_w;
-  return launch_kind<Kind::DownFwd>(a0, a0, b0, b0, a, mgrouped_tiles_upper(g, g.d, 256), s, &o0);
+  if (pairs_mgrouped(g))
+    return launch_kind<Kind::DownFwd, true>(a0, a0, b0, b0, a,
+                                            mgrouped_tiles_upper(g, g.d, 256, 2 * BM), s, &o0);
+  return launch_kind<Kind::DownFwd, false>(a0, a0, b0, b0, a, mgrouped_tiles_upper(g, g.d, 256), s,
+                                           &o0);
 }
 
 cudaError_t launch_down_dgrad(const GroupedDims& g, const moe_bf16* dyp, const moe_bf16* w_down,
@@ -931,8 +1125,12 @@ cudaError_t launch_down_dgrad(const GroupedDims& g, const moe_bf16* dyp, const m
                               int* status, cudaStream_t s) {
   CUtensorMap a0, b0, o0, o1;
   const int bn = pick_bn(g.f, 16);
+  // no pairs by default: this kernel is bound by its epilogue (G and U read,
+  // dG and dU written), which pairs do not shorten
+  const bool pair = pairs_env() == 1;
   // dA[r, c] = sum_j dyp[r, j] W_down[e][c, j]: B is W_down[e] read as [N = f rows, K = d]
-  if (!map2d(&a0, dyp, g.d, g.R_cap, BM) || !map3d(&b0, w_down, g.d, g.f, g.E, bn) ||
+  // (a pair's CTAs load bn / 2 rows each)
+  if (!map2d(&a0, dyp, g.d, g.R_cap, BM) || !map3d(&b0, w_down, g.d, g.f, g.E, pair ? bn / 2 : bn) ||
       !map2d_out(&o0, dG, g.f, g.R_cap) || !map2d_out(&o1, dU, g.f, g.R_cap))
     return cudaErrorInvalidValue;
   GemmArgs a = base_args(g, status);
@@ -941,8 +1139,11 @@ cudaError_t launch_down_dgrad(const GroupedDims& g, const moe_bf16* dyp, const m
   a.in0 = G; a.in1 = U;
   a.out0 = dG; a.out1 = dU;
   a.bn = bn;
-  return launch_kind<Kind::DownDgrad>(a0, a0, b0, b0, a, mgrouped_tiles_upper(g, g.f, bn), s,
-                                      &o0, &o1);
+  if (pair)
+    return launch_kind<Kind::DownDgrad, true>(a0, a0, b0, b0, a,
+                                              mgrouped_tiles_upper(g, g.f, bn, 2 * BM), s, &o0, &o1);
+  return launch_kind<Kind::DownDgrad, false>(a0, a0, b0, b0, a, mgrouped_tiles_upper(g, g.f, bn),
+                                             s, &o0, &o1);
 }
 
 cudaError_t launch_gateup_dgrad(const GroupedDims& g, const moe_bf16* dG, const moe_bf16* dU,
@@ -950,10 +1151,12 @@ cudaError_t launch_gateup_dgrad(const GroupedDims& g, const moe_bf16* dG, const 
                                 int* status, cudaStream_t s) {
   CUtensorMap a0, a1, b0, b1, o0;
   const int bn = pick_bn(g.d, 16);
+  const bool pair = pairs_mgrouped(g);
+  const int brows = pair ? bn / 2 : bn;   // a pair's CTAs load bn / 2 rows of B each
   // dXp[r, i] = sum_c dG[r, c] W_gate[e][i, c] + dU[r, c] W_up[e][i, c]:
   // B is W_gate[e] / W_up[e] read as [N = d rows, K = f]
   if (!map2d(&a0, dG, g.f, g.R_cap, BM) || !map2d(&a1, dU, g.f, g.R_cap, BM) ||
-      !map3d(&b0, w_gate, g.f, g.d, g.E, bn) || !map3d(&b1, w_up, g.f, g.d, g.E, bn) ||
+      !map3d(&b0, w_gate, g.f, g.d, g.E, brows) || !map3d(&b1, w_up, g.f, g.d, g.E, brows) ||
       !map2d_out(&o0, dxp, g.d, g.R_cap))
     return cudaErrorInvalidValue;
   GemmArgs a = base_args(g, status);
@@ -961,8 +1164,11 @@ cudaError_t launch_gateup_dgrad(const GroupedDims& g, const moe_bf16* dG, const 
   a.nk_seg = (g.f + BK - 1) / BK;
   a.out0 = dxp;
   a.bn = bn;
-  return launch_kind<Kind::GateUpDgrad>(a0, a1, b0, b1, a, mgrouped_tiles_upper(g, g.d, bn), s,
-                                        &o0);
+  if (pair)
+    return launch_kind<Kind::GateUpDgrad, true>(a0, a1, b0, b1, a,
+                                                mgrouped_tiles_upper(g, g.d, bn, 2 * BM), s, &o0);
+  return launch_kind<Kind::GateUpDgrad, false>(a0, a1, b0, b1, a, mgrouped_tiles_upper(g, g.d, bn),
+                                               s, &o0);
 }
 
 cudaError_t launch_wgrad_down(const GroupedDims& g, const moe_bf16* A, const moe_bf16* dyp,
@@ -976,8 +1182,13 @@ cudaError_t launch_wgrad_down(const GroupedDims& g, const moe_bf16* A, const moe
   a.M = g.f;
   a.N = g.d;
   a.out0 = dw_down;
-  const int64_t tiles = (int64_t)g.E * ((g.f + BM - 1) / BM) * ((g.d + 255) / 256);
-  return launch_kind<Kind::WgradDown>(a0, a0, b0, b0, a, tiles, s, &o0);
+  const int64_t nN = (g.d + 255) / 256;
+  if (pairs_kgrouped())
+    return launch_kind<Kind::WgradDown, true>(a0, a0, b0, b0, a,
+                                              (int64_t)g.E * ((g.f + 2 * BM - 1) / (2 * BM)) * nN,
+                                              s, &o0);
+  return launch_kind<Kind::WgradDown, false>(a0, a0, b0, b0, a,
+                                             (int64_t)g.E * ((g.f + BM - 1) / BM) * nN, s, &o0);
 }
 
 cudaError_t launch_wgrad_gateup(const GroupedDims& g, const moe_bf16* xp, const moe_bf16* dG,
@@ -994,8 +1205,13 @@ cudaError_t launch_wgrad_gateup(const GroupedDims& g, const moe_bf16* xp, const 
   a.N = g.f;
   a.out0 = dw_gate;
   a.out1 = dw_up;
-  const int64_t tiles = (int64_t)g.E * ((g.d + BM - 1) / BM) * ((g.f + 127) / 128);
-  return launch_kind<Kind::WgradGateUp>(a0, a0, b0, b1, a, tiles, s, &o0, &o1);
+  const int64_t nN = (g.f + 127) / 128;
+  if (pairs_kgrouped())
+    return launch_kind<Kind::WgradGateUp, true>(
+        a0, a0, b0, b1, a, (int64_t)g.E * ((g.d + 2 * BM - 1) / (2 * BM)) * nN, s, &o0, &o1);
+  return launch_kind<Kind::WgradGateUp, false>(a0, a0, b0, b1, a,
+                                               (int64_t)g.E * ((g.d + BM - 1) / BM) * nN, s, &o0,
+                                               &o1);
 }
 
 }  // namespace moe
