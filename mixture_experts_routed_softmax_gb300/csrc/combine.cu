@@ -32,14 +32,27 @@ __global__ void __launch_bounds__(256) combine_kernel(const moe_bf16* __restrict
   for (int v0 = 0; v0 < nv; v0 += 32) {
     const int v = v0 + lane;
     float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-    for (int j = 0; j < k; ++j) {
-      const int32_t r = __shfl_sync(0xFFFFFFFFu, my_r, j);
-      const float wj = __shfl_sync(0xFFFFFFFFu, my_w, j);
-      if (r < 0 || v >= nv) continue;
-      float f[8];
-      unpack8(reinterpret_cast<const uint4*>(rows + (int64_t)r * d)[v], f);
+    // the rows of up to four slots are loaded together, then summed in slot order
+    for (int j0 = 0; j0 < k; j0 += 4) {
+      uint4 rv[4];
+      float wv[4];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) acc[i] = fmaf(wj, f[i], acc[i]);
+      for (int q = 0; q < 4; ++q) {
+        const int j = j0 + q;
+        const int32_t r = __shfl_sync(0xFFFFFFFFu, my_r, j & 31);
+        wv[q] = __shfl_sync(0xFFFFFFFFu, my_w, j & 31);
+        const bool ok = j < k && r >= 0 && v < nv;
+        rv[q] = ok ? reinterpret_cast<const uint4*>(rows + (int64_t)r * d)[v]
+                   : make_uint4(0u, 0u, 0u, 0u);
+        if (!ok) wv[q] = 0.f;
+      }
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        float f[8];
+        unpack8(rv[q], f);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) acc[i] = fmaf(wv[q], f[i], acc[i]);
+      }
     }
     if (v < nv) dst[v] = pack8(acc);
   }
@@ -78,16 +91,28 @@ __global__ void __launch_bounds__(256) combine_bwd_kernel(
   const uint4* g = reinterpret_cast<const uint4*>(dy + t * d);
   const uint4* y = reinterpret_cast<const uint4*>(yp + r * d);
   float dot = 0.f;
-  for (int v = lane; v < nv; v += 32) {
-    float a[8], b[8], o[8];
-    unpack8(g[v], a);
-    unpack8(y[v], b);
+  // four 16-byte pieces of each row in flight per lane, then used in order
+  for (int v0 = lane; v0 < nv; v0 += 128) {
+    uint4 gv[4], yv[4];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      dot = fmaf(a[i], b[i], dot);
-      o[i] = w * a[i];
+    for (int u = 0; u < 4; ++u) {
+      const int v = v0 + 32 * u;
+      if (v < nv) { gv[u] = g[v]; yv[u] = y[v]; }
     }
-    out[v] = pack8(o);
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int v = v0 + 32 * u;
+      if (v >= nv) break;
+      float a[8], b[8], o[8];
+      unpack8(gv[u], a);
+      unpack8(yv[u], b);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        dot = fmaf(a[i], b[i], dot);
+        o[i] = w * a[i];
+      }
+      out[v] = pack8(o);
+    }
   }
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) dot += __shfl_xor_sync(0xFFFFFFFFu, dot, off);

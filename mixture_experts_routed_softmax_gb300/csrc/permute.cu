@@ -183,7 +183,16 @@ __global__ void __launch_bounds__(256) permute_gather_kernel(
   if (real) {
     const int64_t t = src_pair[r] / k;
     const uint4* src = reinterpret_cast<const uint4*>(x + t * d);
-    for (int v = lane; v < nv; v += 32) dst[v] = src[v];
+    // four 16-byte pieces in flight per lane
+    for (int v0 = lane; v0 < nv; v0 += 128) {
+      uint4 c[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        if (v0 + 32 * u < nv) c[u] = src[v0 + 32 * u];
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        if (v0 + 32 * u < nv) dst[v0 + 32 * u] = c[u];
+    }
   } else {
     if (lane == 0) src_pair[r] = -1;
     for (int v = lane; v < nv; v += 32) dst[v] = make_uint4(0u, 0u, 0u, 0u);
