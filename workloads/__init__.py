@@ -94,6 +94,9 @@ CONFIGS = {
 # for ncu captures, whose replays save and restore device memory
 CONFIGS["gptoss20b_T4096"] = Workload("gptoss20b_T4096", T=4096, d=2880, f=2880, E=32, k=4,
                                       note="GPT-OSS-20B-shaped layer, one 4096-token sequence")
+# half the bench batch (2 x 4096 tokens, 1024 rows per expert): a profiling size
+CONFIGS["gptoss20b_T8192"] = Workload("gptoss20b_T8192", T=8192, d=2880, f=2880, E=32, k=4,
+                                      note="GPT-OSS-20B-shaped layer, batch 2 x 4096")
 for _T in (128, 512, 1024, 2048):
     CONFIGS[f"smallm_T{_T}"] = Workload(
         f"smallm_T{_T}", T=_T, d=2048, f=768, E=128, k=8, backward=False,
