@@ -269,7 +269,7 @@ int moe_expert_bwd(const moe_bf16* dy, const int32_t* src_pair, const int32_t* d
   int* st = device_status_ptr();
   if (!st) return MOE_ERR_CUDA;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  GroupedDims gd{offsets, E, d, f, R_cap, T * k};
+  GroupedDims gd{offsets, E, d, f, R_cap, T * k, src_pair};
   cudaError_t e = launch_combine_bwd(dy, yp, src_pair, topk_w, offsets, T, k, E, d, R_cap, dyp,
                                      d_topk_w, s);
   if (e == cudaSuccess) e = launch_down_dgrad(gd, dyp, w_down, g, u, dg, du, st, s);

@@ -119,6 +119,7 @@ struct GemmArgs {
   int ksplit;         // RouterLogits: K split into this many chunks (1: write logits + bias)
   int ksteps_split;   // k-steps per chunk
   int bn;             // single-accumulator kinds: tile width (multiple of 16, <= 256)
+  const int32_t* src_pair;   // K-grouped: pair of each layout row (-1: padding), or NULL
   int* status;
 };
 
@@ -165,7 +166,9 @@ __device__ __forceinline__ void decode_tile(int tile, const GemmArgs& a, const i
     ti.e = mt / nM;
     ti.m0 = (int64_t)(mt % nM) * TM + rank * BM;
     ti.kbeg = a.offsets[ti.e];
-    ti.row_end = a.offsets[ti.e + 1] - ti.kbeg;
+    // the reduction stops after the expert's real rows (rounded up to the MMA's
+    // 16-row step; the padding rows are zero in both operands)
+    ti.row_end = tstart[ti.e];
     ti.nk = (int)((ti.row_end + BK - 1) / BK);
   } else {
     int lo = 0, hi = a.E;  // largest e with tstart[e] <= mt
@@ -324,6 +327,25 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else {
       tmem_alloc(smem_u32(s_tmem), kTmemCols);
       tmem_relinquish();
+    }
+  }
+  // K-grouped: tstart[e] = the rows of expert e the reduction runs over: its
+  // real rows rounded up to 16 (the real rows come first in the group, then
+  // the padding, whose src_pair is -1), or the whole group without src_pair
+  if constexpr (T::kgrouped) {
+    for (int e = threadIdx.x; e < args.E; e += kThreads) {
+      const int64_t g0 = args.offsets[e], g1 = args.offsets[e + 1];
+      int64_t n = g1 - g0;
+      if (args.src_pair) {
+        int64_t lo = g0, hi = g1;   // the first padding row is in [lo, hi]
+        while (lo < hi) {
+          const int64_t mid = (lo + hi) >> 1;
+          if (args.src_pair[mid] >= 0) lo = mid + 1; else hi = mid;
+        }
+        n = ((lo - g0) + 15) & ~(int64_t)15;
+        if (n > g1 - g0) n = g1 - g0;
+      }
+      tstart[e] = (int)n;
     }
   }
   // M-grouped tile table: tstart[e] = sum_{e'<e} ceil(L_e' / tile rows)
@@ -986,6 +1008,7 @@ static GemmArgs base_args(const GroupedDims& g, int* status) {
   a.offsets = g.offsets;
   a.E = g.E;
   a.R_cap = g.R_cap;
+  a.src_pair = g.src_pair;
   a.status = status;
   return a;
 }

@@ -63,6 +63,9 @@ struct GroupedDims {
   int E, d, f;
   int64_t R_cap;
   int64_t P;        // token-expert pairs (T * k): sizes the tile schedule
+  // the pair held by each row of the layout (-1: padding), or NULL: lets the
+  // K-grouped weight gradients stop each expert's reduction at its real rows
+  const int32_t* src_pair = nullptr;
 };
 cudaError_t launch_gateup_fwd(const GroupedDims& g, const moe_bf16* xp, const moe_bf16* w_gate,
                               const moe_bf16* w_up, moe_bf16* G, moe_bf16* U, moe_bf16* A,
