@@ -22,7 +22,8 @@
  * Conventions shared by every entry point:
  *   - moe_bf16 is the raw 16-bit pattern of a bfloat16.
  *   - Every pointer is a DEVICE pointer unless stated otherwise; every buffer
- *     is owned by the caller. No entry point allocates, frees or
+ *     is owned by the caller. A pointer to an array sized by T (x, dy, y, dx,
+ *     logits, the [T, k] arrays, dst_row) may be NULL when T = 0. No entry point allocates, frees or
  *     synchronises device memory (moe_status and the timer read are the only
  *     calls that synchronise). All work is enqueued on `stream` in order.
  *   - Matrices are row-major and densely packed.

@@ -169,7 +169,7 @@ int moe_route(const moe_bf16* x, const float* w_router, const float* bias,
               const int32_t* forced_idx, int64_t T, int d, int E, int k, float* logits,
               int32_t* topk_idx, float* topk_w, void* ws, size_t ws_bytes,
               moe_stream_t stream) {
-  if (!x || !w_router || !logits || !topk_idx || !topk_w) return MOE_ERR_ARG;
+  if (!w_router || (T > 0 && (!x || !logits || !topk_idx || !topk_w))) return MOE_ERR_ARG;
   if (T < 0 || d <= 0 || E <= 0 || k <= 0 || k > E) return MOE_ERR_ARG;
   if (k > kMaxTopK || E > kMaxExperts || d % 8 != 0) return MOE_ERR_UNSUPPORTED;
   if (T >= ((int64_t)1 << 31)) return MOE_ERR_UNSUPPORTED;
@@ -189,7 +189,8 @@ int moe_permute(const int32_t* topk_idx, int64_t T, int k, int E, int align, con
                 int d, int64_t R_cap, int32_t* counts, int64_t* offsets, int32_t* dst_row,
                 int32_t* src_pair, moe_bf16* xp, void* ws, size_t ws_bytes,
                 moe_stream_t stream) {
-  if (!topk_idx || !x || !counts || !offsets || !dst_row || !src_pair || !xp) return MOE_ERR_ARG;
+  if (!counts || !offsets || !src_pair || !xp || (T > 0 && (!topk_idx || !x || !dst_row)))
+    return MOE_ERR_ARG;
   if (T < 0 || k <= 0 || E <= 0 || d <= 0 || k > E) return MOE_ERR_ARG;
   if (!is_pow2(align) || align < 16 || align > 256) return MOE_ERR_ARG;
   if (E > kMaxExperts || d % 8 != 0) return MOE_ERR_UNSUPPORTED;
@@ -236,7 +237,7 @@ int moe_expert_fwd(const moe_bf16* xp, const int64_t* offsets, const float* row_
 
 int moe_combine(const moe_bf16* rows, const int32_t* dst_row, const float* topk_w, int64_t T,
                 int k, int d, moe_bf16* out, moe_stream_t stream) {
-  if (!rows || !dst_row || !out) return MOE_ERR_ARG;
+  if (!rows || (T > 0 && (!dst_row || !out))) return MOE_ERR_ARG;
   if (T < 0 || k <= 0 || d <= 0) return MOE_ERR_ARG;
   if (k > kMaxTopK || d % 8 != 0) return MOE_ERR_UNSUPPORTED;
   if (!aligned16(rows) || !aligned16(out)) return MOE_ERR_ARG;
@@ -252,9 +253,9 @@ int moe_expert_bwd(const moe_bf16* dy, const int32_t* src_pair, const int32_t* d
                    const moe_bf16* w_gate, const moe_bf16* w_up, const moe_bf16* w_down,
                    moe_bf16* dyp, moe_bf16* dg, moe_bf16* du, moe_bf16* dxp, float* d_topk_w,
                    moe_bf16* dw_gate, moe_bf16* dw_up, moe_bf16* dw_down, moe_stream_t stream) {
-  if (!dy || !src_pair || !dst_row || !topk_w || !offsets || !xp || !g || !u || !a || !yp ||
-      !w_gate || !w_up || !w_down || !dyp || !dg || !du || !dxp || !d_topk_w || !dw_gate ||
-      !dw_up || !dw_down)
+  if (!src_pair || !offsets || !xp || !g || !u || !a || !yp || !w_gate || !w_up || !w_down ||
+      !dyp || !dg || !du || !dxp || !dw_gate || !dw_up || !dw_down ||
+      (T > 0 && (!dy || !dst_row || !topk_w || !d_topk_w)))
     return MOE_ERR_ARG;
   if (T < 0 || k <= 0 || k > E) return MOE_ERR_ARG;
   int rc = check_expert_dims(E, d, f, R_cap);
@@ -285,10 +286,10 @@ int moe_route_bwd(const float* d_topk_w, const float* topk_w, const int32_t* top
                   moe_bf16* dx_inout, const moe_bf16* dxp, const int32_t* dst_row,
                   float* dw_router, float* dbias, void* ws, size_t ws_bytes,
                   moe_stream_t stream) {
-  if (!d_topk_w || !topk_w || !topk_idx || !w_router || !offsets || !src_pair || !x ||
-      !dx_inout || !dw_router)
+  if (!w_router || !offsets || !src_pair || !dw_router ||
+      (T > 0 && (!d_topk_w || !topk_w || !topk_idx || !x || !dx_inout)))
     return MOE_ERR_ARG;
-  if (dxp && (!dst_row || !aligned16(dxp))) return MOE_ERR_ARG;
+  if (dxp && ((T > 0 && !dst_row) || !aligned16(dxp))) return MOE_ERR_ARG;
   if (T < 0 || d <= 0 || E <= 0 || k <= 0 || k > E) return MOE_ERR_ARG;
   if (!is_pow2(align) || align < 16 || align > 256) return MOE_ERR_ARG;
   if (k > kMaxTopK || E > kMaxExperts || d % 8 != 0) return MOE_ERR_UNSUPPORTED;

@@ -44,7 +44,8 @@ extern "C" int moe_permute_noalloc(const int32_t* topk_idx, int64_t T, int k, in
                                    const moe_bf16* x, int d, int64_t R_cap, int32_t* counts,
                                    int64_t* offsets, int32_t* dst_row, int32_t* src_pair,
                                    moe_bf16* xp, moe_stream_t stream) {
-  if (!topk_idx || !x || !counts || !offsets || !dst_row || !src_pair || !xp) return MOE_ERR_ARG;
+  if (!counts || !offsets || !src_pair || !xp || (T > 0 && (!topk_idx || !x || !dst_row)))
+    return MOE_ERR_ARG;
   if (T < 0 || k <= 0 || E <= 0 || d <= 0 || k > E) return MOE_ERR_ARG;
   if (!is_pow2(align) || align < 16 || align > 256) return MOE_ERR_ARG;
   if (E > moe::kMaxExperts || d % 8 != 0) return MOE_ERR_UNSUPPORTED;

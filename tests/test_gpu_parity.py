@@ -138,3 +138,24 @@ def test_router_backward_fused_and_separate_dx_agree():
     bound = 2 ** -7 * (torch.abs(dx_expert) + torch.abs(dx_fused)) + 1e-6
     assert torch.all(torch.abs(dx_sep - dx_fused) <= bound)
     assert torch.equal(b.dw_router, dw_r)
+
+
+def test_empty_batch():
+    """T = 0: every call succeeds (the T-sized arrays are empty), the layout
+    is all padding-free zeros, and every gradient of the empty batch is 0."""
+    T, d, f, E, k, align = 0, 128, 256, 8, 2, 16
+    wl, inp = _case("tiny", 64, d, f, E, k, align)     # weights only; the batch is empty
+    layer = _layer(inp, k, align)
+    b = layer.buffers(T)
+    x = torch.empty(0, d, dtype=torch.bfloat16, device="cuda")
+    dy = torch.empty(0, d, dtype=torch.bfloat16, device="cuda")
+    for buf in (b.dw_gate, b.dw_up, b.dw_down, b.dw_router, b.dbias):
+        buf.fill_(7.0)                                 # must be overwritten with zeros
+    layer.forward(x, b)
+    layer.backward(dy, b)
+    assert layer.status() == 0
+    assert b.y.shape == (0, d) and b.dx.shape == (0, d)
+    assert int(b.counts.abs().sum()) == 0 and int(b.offsets.abs().sum()) == 0
+    assert torch.all(b.src_pair == -1)
+    for name in ("dw_gate", "dw_up", "dw_down", "dw_router", "dbias"):
+        assert torch.count_nonzero(getattr(b, name)).item() == 0, name
