@@ -426,6 +426,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           int nv = (args.N - ti.n0 + 15) & ~15;   // the columns the pair multiplies
           nv = nv < bn ? nv : bn;
           const int bcol = T::dual ? ti.n0 : ti.n0 + rank * (nv >> 1);
+          // rank 1's half of a group's last 256-row tile may lie wholly past the
+          // group: its A rows then come from past the tensor's end (zero-filled,
+          // no memory traffic) instead of from the next group
+          const int arow = (!T::kgrouped && ti.m0 >= ti.row_end) ? (int)args.R_cap : (int)ti.m0;
           const void* mBd = (T::dual && rank) ? (const void*)&mapB1 : (const void*)&mapB0;
           for (int ks = 0; ks < ti.nk; ++ks) {
             if (!mbar_wait_bounded(empty_bar(stage), phase ^ 1u, s_abort, args.status)) {
@@ -450,7 +454,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               const int kk = (ks - seg * args.nk_seg) * BK;
               const void* mA = seg ? (const void*)&mapA1 : (const void*)&mapA0;
               const void* mB = seg ? (const void*)&mapB1 : (const void*)&mapB0;
-              tma_load_2d_pair(sA, mA, fbl, kk, (int)ti.m0);
+              tma_load_2d_pair(sA, mA, fbl, kk, arow);
               if constexpr (T::b_mn) {
 #pragma unroll
                 for (int j = 0; j < 2; ++j)
