@@ -468,69 +468,70 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       } else {
-      for (int tile = GEMM_CID; tile < total && ok; tile += GEMM_NCL) {
-        TileInfo ti;
-        decode_tile<K, PAIR>(tile, args, tstart, nN, 0, ti);
-        for (int ks = 0; ks < ti.nk; ++ks) {
-          if (!mbar_wait_bounded(empty_bar(stage), phase ^ 1u, s_abort, args.status)) {
-            ok = false;
-            break;
-          }
-          const uint32_t fb = full_bar(stage);
-          const uint32_t sA = s_base + stage * kStageBytes;
-          const uint32_t sB0 = sA + kABytes;
-          const uint32_t sB1 = sB0 + kBBytes;
-          mbar_arrive_expect_tx(fb, tx_bytes);
-          if constexpr (T::kgrouped) {
-            const int row0 = (int)(ti.kbeg + (int64_t)ks * BK);
-#pragma unroll
-            for (int i = 0; i < BM / 64; ++i)
-              tma_load_2d(sA + i * (BK * 128), &mapA0, fb, (int)ti.m0 + 64 * i, row0);
-#pragma unroll
-            for (int j = 0; j < T::BN / 64; ++j) {
-              tma_load_2d(sB0 + j * (BK * 128), &mapB0, fb, ti.n0 + 64 * j, row0);
-              if constexpr (T::dual)
-                tma_load_2d(sB1 + j * (BK * 128), &mapB1, fb, ti.n0 + 64 * j, row0);
+        for (int tile = GEMM_CID; tile < total && ok; tile += GEMM_NCL) {
+          TileInfo ti;
+          decode_tile<K, PAIR>(tile, args, tstart, nN, 0, ti);
+          for (int ks = 0; ks < ti.nk; ++ks) {
+            if (!mbar_wait_bounded(empty_bar(stage), phase ^ 1u, s_abort, args.status)) {
+              ok = false;
+              break;
             }
-          } else if constexpr (T::dense) {
-            // K segment s of B starts at row s * seg_koff; A is the same in every segment
-            const int kg = (int)ti.kbeg + ks;
-            const int seg = kg / args.nk_seg;
-            const int kk = (kg - seg * args.nk_seg) * BK;
-            if constexpr (T::a_mn) {
+            const uint32_t fb = full_bar(stage);
+            const uint32_t sA = s_base + stage * kStageBytes;
+            const uint32_t sB0 = sA + kABytes;
+            const uint32_t sB1 = sB0 + kBBytes;
+            mbar_arrive_expect_tx(fb, tx_bytes);
+            if constexpr (T::kgrouped) {
+              const int row0 = (int)(ti.kbeg + (int64_t)ks * BK);
 #pragma unroll
               for (int i = 0; i < BM / 64; ++i)
-                tma_load_2d(sA + i * (BK * 128), &mapA0, fb, (int)ti.m0 + 64 * i, kk);
-            } else {
-              tma_load_2d(sA, &mapA0, fb, kk, (int)ti.m0);
-            }
-#pragma unroll
-            for (int j = 0; j < T::BN / 64; ++j)
-              if (j < nbox)
-                tma_load_2d_hint(sB0 + j * (BK * 128), &mapB0, fb, ti.n0 + 64 * j,
-                               seg * args.seg_koff + kk, pol_w);
-          } else {
-            const int seg = (T::two_seg && ks >= args.nk_seg) ? 1 : 0;
-            const int kk = (ks - seg * args.nk_seg) * BK;
-            const void* mA = seg ? (const void*)&mapA1 : (const void*)&mapA0;
-            const void* mB = seg ? (const void*)&mapB1 : (const void*)&mapB0;
-            tma_load_2d(sA, mA, fb, kk, (int)ti.m0);
-            if constexpr (T::b_mn) {
+                tma_load_2d(sA + i * (BK * 128), &mapA0, fb, (int)ti.m0 + 64 * i, row0);
 #pragma unroll
               for (int j = 0; j < T::BN / 64; ++j) {
-                tma_load_3d_hint(sB0 + j * (BK * 128), &mapB0, fb, ti.n0 + 64 * j, kk, ti.e, pol_w);
+                tma_load_2d(sB0 + j * (BK * 128), &mapB0, fb, ti.n0 + 64 * j, row0);
                 if constexpr (T::dual)
-                  tma_load_3d_hint(sB1 + j * (BK * 128), &mapB1, fb, ti.n0 + 64 * j, kk, ti.e,
-                                   pol_w);
+                  tma_load_2d(sB1 + j * (BK * 128), &mapB1, fb, ti.n0 + 64 * j, row0);
               }
+            } else if constexpr (T::dense) {
+              // K segment s of B starts at row s * seg_koff; A is the same in every segment
+              const int kg = (int)ti.kbeg + ks;
+              const int seg = kg / args.nk_seg;
+              const int kk = (kg - seg * args.nk_seg) * BK;
+              if constexpr (T::a_mn) {
+#pragma unroll
+                for (int i = 0; i < BM / 64; ++i)
+                  tma_load_2d(sA + i * (BK * 128), &mapA0, fb, (int)ti.m0 + 64 * i, kk);
+              } else {
+                tma_load_2d(sA, &mapA0, fb, kk, (int)ti.m0);
+              }
+#pragma unroll
+              for (int j = 0; j < T::BN / 64; ++j)
+                if (j < nbox)
+                  tma_load_2d_hint(sB0 + j * (BK * 128), &mapB0, fb, ti.n0 + 64 * j,
+                                 seg * args.seg_koff + kk, pol_w);
             } else {
-              tma_load_3d_hint(sB0, mB, fb, kk, ti.n0, ti.e, pol_w);
+              const int seg = (T::two_seg && ks >= args.nk_seg) ? 1 : 0;
+              const int kk = (ks - seg * args.nk_seg) * BK;
+              const void* mA = seg ? (const void*)&mapA1 : (const void*)&mapA0;
+              const void* mB = seg ? (const void*)&mapB1 : (const void*)&mapB0;
+              tma_load_2d(sA, mA, fb, kk, (int)ti.m0);
+              if constexpr (T::b_mn) {
+#pragma unroll
+                for (int j = 0; j < T::BN / 64; ++j) {
+                  tma_load_3d_hint(sB0 + j * (BK * 128), &mapB0, fb, ti.n0 + 64 * j, kk, ti.e,
+                                   pol_w);
+                  if constexpr (T::dual)
+                    tma_load_3d_hint(sB1 + j * (BK * 128), &mapB1, fb, ti.n0 + 64 * j, kk, ti.e,
+                                     pol_w);
+                }
+              } else {
+                tma_load_3d_hint(sB0, mB, fb, kk, ti.n0, ti.e, pol_w);
+              }
             }
+            ++fills;
+            if (++stage == kStages) { stage = 0; phase ^= 1u; }
           }
-          ++fills;
-          if (++stage == kStages) { stage = 0; phase ^= 1u; }
         }
-      }
       }
       if (*s_abort) {
         // let the copies already issued land before the CTA's shared memory goes away
@@ -1157,7 +1158,8 @@ cudaError_t launch_down_dgrad(const GroupedDims& g, const moe_bf16* dyp, const m
   const bool pair = pairs_env() == 1;
   // dA[r, c] = sum_j dyp[r, j] W_down[e][c, j]: B is W_down[e] read as [N = f rows, K = d]
   // (a pair's CTAs load bn / 2 rows each)
-  if (!map2d(&a0, dyp, g.d, g.R_cap, BM) || !map3d(&b0, w_down, g.d, g.f, g.E, pair ? bn / 2 : bn) ||
+  if (!map2d(&a0, dyp, g.d, g.R_cap, BM) ||
+      !map3d(&b0, w_down, g.d, g.f, g.E, pair ? bn / 2 : bn) ||
       !map2d_out(&o0, dG, g.f, g.R_cap) || !map2d_out(&o1, dU, g.f, g.R_cap))
     return cudaErrorInvalidValue;
   GemmArgs a = base_args(g, status);
@@ -1167,8 +1169,8 @@ cudaError_t launch_down_dgrad(const GroupedDims& g, const moe_bf16* dyp, const m
   a.out0 = dG; a.out1 = dU;
   a.bn = bn;
   if (pair)
-    return launch_kind<Kind::DownDgrad, true>(a0, a0, b0, b0, a,
-                                              mgrouped_tiles_upper(g, g.f, bn, 2 * BM), s, &o0, &o1);
+    return launch_kind<Kind::DownDgrad, true>(
+        a0, a0, b0, b0, a, mgrouped_tiles_upper(g, g.f, bn, 2 * BM), s, &o0, &o1);
   return launch_kind<Kind::DownDgrad, false>(a0, a0, b0, b0, a, mgrouped_tiles_upper(g, g.f, bn),
                                              s, &o0, &o1);
 }
