@@ -61,6 +61,8 @@ def parse_args(argv=None):
     ap.add_argument("--ref-tokens", type=int, default=1,
                     help="tokens per step of the reference (oracle) arm")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--graph", action="store_true",
+                    help="launch each timed step as one captured CUDA graph (launch-bound sizes)")
     return ap.parse_args(argv)
 
 
@@ -264,25 +266,64 @@ def run_ours(args, rank, world, local_rank):
 
     # ------------------------------------------------------ timed region --
     stream = torch.cuda.current_stream()
-    _lib.call("moe_timer_start", _lib.KERNELS[dominant], args.steps * 2)
+    run = step
+    graph_launches = 0
+    if args.graph:
+        # the whole step captured once (its kernels become graph nodes) and
+        # replayed; the library's launch counter sees the capture only
+        g = torch.cuda.CUDAGraph()
+        c0 = int(lib.moe_kernel_launches())
+        with torch.cuda.graph(g):
+            step()
+        graph_launches = int(lib.moe_kernel_launches()) - c0
+        torch.cuda.synchronize()
+        run = g.replay
+        for _ in range(3):
+            run()
+    else:
+        _lib.call("moe_timer_start", _lib.KERNELS[dominant], args.steps * 2)
+    # A step that moves less than four L2s of data would find its weights in
+    # L2 again on the next step: then L2 is flushed (a write of twice its
+    # size) between steps, outside each step's own pair of events.
+    l2_bytes = torch.cuda.get_device_properties(dev).L2_cache_size
+    step_bytes = accounting.totals(accounting.Shape(T=wl.T, d=wl.d, f=wl.f, E=wl.E, k=wl.k,
+                                                    E_active=int((b.counts > 0).sum())),
+                                   wl.backward)[1]
+    flush = step_bytes < 4 * l2_bytes
+    flush_buf = torch.empty(2 * l2_bytes, dtype=torch.uint8, device=dev) if flush else None
     sampler = ClockSampler(local_rank).start()
     launches0 = int(lib.moe_kernel_launches())
     barrier()
     torch.cuda.synchronize()
     ev0 = torch.cuda.Event(enable_timing=True)
     ev1 = torch.cuda.Event(enable_timing=True)
-    ev0.record(stream)
-    for _ in range(args.steps):
-        step()
-    ev1.record(stream)
-    torch.cuda.synchronize()
-    barrier()
-    elapsed_ms = ev0.elapsed_time(ev1)
-    launches = int(lib.moe_kernel_launches()) - launches0
+    if flush:
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(args.steps)]
+        for e0, e1 in evs:
+            flush_buf.zero_()
+            e0.record(stream)
+            run()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        barrier()
+        elapsed_ms = sum(e0.elapsed_time(e1) for e0, e1 in evs)
+    else:
+        ev0.record(stream)
+        for _ in range(args.steps):
+            run()
+        ev1.record(stream)
+        torch.cuda.synchronize()
+        barrier()
+        elapsed_ms = ev0.elapsed_time(ev1)
+    launches = int(lib.moe_kernel_launches()) - launches0 + graph_launches * args.steps
     clocks = sampler.stop()
-    ms, n = _lib.ctypes.c_float(), _lib.ctypes.c_int()
-    _lib.call("moe_timer_read", _lib.ctypes.byref(ms), _lib.ctypes.byref(n))
-    dom_ms = ms.value / max(n.value, 1)
+    if args.graph:
+        dom_ms = per_kernel[dominant]        # from the single-kernel timer steps above
+    else:
+        ms, n = _lib.ctypes.c_float(), _lib.ctypes.c_int()
+        _lib.call("moe_timer_read", _lib.ctypes.byref(ms), _lib.ctypes.byref(n))
+        dom_ms = ms.value / max(n.value, 1)
     status = layer.status()
     if status != 0:
         raise RuntimeError(f"device status {status}: {_lib.status_str(status)}")
@@ -393,7 +434,10 @@ def run_ours(args, rank, world, local_rank):
         "config": {"workload": f"{wl.name}: {wl.note}", "T": wl.T, "d": wl.d, "f": wl.f,
                    "E": wl.E, "k": wl.k, "align": wl.align, "backward": wl.backward,
                    "tau": inp.get("tau"), "seed": wl.seed,
-                   "l2": "inputs larger than L2 (no flush): one step moves several GB",
+                   "l2": ("L2 flushed between timed steps (a step moves less than four L2s)"
+                          if flush else
+                          "inputs larger than L2 (no flush): one step moves several GB"),
+                   "graph": bool(args.graph),
                    "parallelism": f"replicas x{world}"},
         "roofline": roof,
         "layer_roofline": {"flops": F, "bytes": B, "t_roof_ms": t_roof * 1e3,

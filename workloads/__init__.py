@@ -101,6 +101,12 @@ for _T in (128, 512, 1024, 2048):
     CONFIGS[f"smallm_T{_T}"] = Workload(
         f"smallm_T{_T}", T=_T, d=2048, f=768, E=128, k=8, backward=False,
         note="small-M weight-bound sweep, forward only")
+# decode: one and eight tokens through the same layer shape (every selected
+# expert's weights streamed for one or two rows)
+for _T in (1, 8):
+    CONFIGS[f"decode_T{_T}"] = Workload(
+        f"decode_T{_T}", T=_T, d=2048, f=768, E=128, k=8, align=16, backward=False,
+        note="decode, forward only")
 
 
 def zipf_tau(name: str) -> float:
