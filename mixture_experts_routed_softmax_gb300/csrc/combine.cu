@@ -11,57 +11,57 @@
 
 namespace moe {
 
-// out[t] = sum_j w[t, j] * rows[dst_row[t*k + j]]  (slot order, fp32), one warp per token
+// out[t] = sum_j w[t, j] * rows[dst_row[t*k + j]]  (slot order, fp32); one warp
+// per (token, 256 columns), so a handful of tokens still spreads over many warps
 __global__ void __launch_bounds__(256) combine_kernel(const moe_bf16* __restrict__ rows,
                                                       const int32_t* __restrict__ dst_row,
                                                       const float* __restrict__ topk_w,
                                                       int64_t T, int k, int d,
                                                       moe_bf16* __restrict__ out) {
   const int lane = threadIdx.x & 31;
-  const int64_t t = (int64_t)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
-  if (t >= T) return;
+  const int nv = d / 8;
+  const int nchunk = (nv + 31) / 32;
+  const int64_t w = (int64_t)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
+  if (w >= T * nchunk) return;
+  const int64_t t = w / nchunk;
+  const int v = (int)(w - t * nchunk) * 32 + lane;
   int32_t my_r = -1;
   float my_w = 0.f;
   if (lane < k) {
     my_r = dst_row[t * k + lane];
     my_w = topk_w ? topk_w[t * k + lane] : 1.f;
   }
-  const int nv = d / 8;
-  uint4* dst = reinterpret_cast<uint4*>(out + t * d);
-  // every lane runs the same number of iterations: the shuffles need the whole warp
-  for (int v0 = 0; v0 < nv; v0 += 32) {
-    const int v = v0 + lane;
-    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-    // the rows of up to four slots are loaded together, then summed in slot order
-    for (int j0 = 0; j0 < k; j0 += 4) {
-      uint4 rv[4];
-      float wv[4];
+  float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  // the rows of up to four slots are loaded together, then summed in slot order
+  for (int j0 = 0; j0 < k; j0 += 4) {
+    uint4 rv[4];
+    float wv[4];
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const int j = j0 + q;
-        const int32_t r = __shfl_sync(0xFFFFFFFFu, my_r, j & 31);
-        wv[q] = __shfl_sync(0xFFFFFFFFu, my_w, j & 31);
-        const bool ok = j < k && r >= 0 && v < nv;
-        rv[q] = ok ? reinterpret_cast<const uint4*>(rows + (int64_t)r * d)[v]
-                   : make_uint4(0u, 0u, 0u, 0u);
-        if (!ok) wv[q] = 0.f;
-      }
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        float f[8];
-        unpack8(rv[q], f);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) acc[i] = fmaf(wv[q], f[i], acc[i]);
-      }
+    for (int q = 0; q < 4; ++q) {
+      const int j = j0 + q;
+      const int32_t r = __shfl_sync(0xFFFFFFFFu, my_r, j & 31);
+      wv[q] = __shfl_sync(0xFFFFFFFFu, my_w, j & 31);
+      const bool ok = j < k && r >= 0 && v < nv;
+      rv[q] = ok ? reinterpret_cast<const uint4*>(rows + (int64_t)r * d)[v]
+                 : make_uint4(0u, 0u, 0u, 0u);
+      if (!ok) wv[q] = 0.f;
     }
-    if (v < nv) dst[v] = pack8(acc);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      float f[8];
+      unpack8(rv[q], f);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) acc[i] = fmaf(wv[q], f[i], acc[i]);
+    }
   }
+  if (v < nv) reinterpret_cast<uint4*>(out + t * d)[v] = pack8(acc);
 }
 
 cudaError_t launch_combine(const moe_bf16* rows, const int32_t* dst_row, const float* topk_w,
                            int64_t T, int k, int d, moe_bf16* out, cudaStream_t s) {
   timer_before(MOE_KERNEL_COMBINE, s);
-  combine_kernel<<<(unsigned)((T + 7) / 8), 256, 0, s>>>(rows, dst_row, topk_w, T, k, d, out);
+  const int64_t warps = T * (((int64_t)d / 8 + 31) / 32);
+  combine_kernel<<<(unsigned)((warps + 7) / 8), 256, 0, s>>>(rows, dst_row, topk_w, T, k, d, out);
   note_launches(1);
   timer_after(MOE_KERNEL_COMBINE, s);
   return cudaGetLastError();

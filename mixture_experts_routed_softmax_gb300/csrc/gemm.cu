@@ -58,8 +58,10 @@ struct Tr {
   // one group of M rows, fp32 output (split K: one partial per chunk)
   static constexpr bool dense = (K == Kind::RouterLogits || K == Kind::RouterWgrad);
   static constexpr bool a_mn = kgrouped || K == Kind::RouterWgrad;         // A is M-contiguous
-  static constexpr bool b_mn = (gateup_fwd || K == Kind::DownFwd || kgrouped || dense);
-  static constexpr int BN = K == Kind::GateUpFwdNarrow ? 64 : dual ? 128 : 256;   // per accumulator
+  static constexpr bool down_fwd = (K == Kind::DownFwd);
+  static constexpr bool narrow = (K == Kind::GateUpFwdNarrow);
+  static constexpr bool b_mn = (gateup_fwd || down_fwd || kgrouped || dense);
+  static constexpr int BN = narrow ? 64 : dual ? 128 : 256;   // per accumulator
   // tile width chosen per launch (at most BN): the K-major-B kinds, whose B box
   // is exactly the tile's rows, and the router, whose N is the expert count
   static constexpr bool var_bn = (K == Kind::DownDgrad || K == Kind::GateUpDgrad || dense);
@@ -69,7 +71,7 @@ struct Tr {
                                                                    : kRingBytes / tx_bytes;
   static constexpr int kernel_id =
       gateup_fwd ? MOE_KERNEL_GATEUP_FWD
-      : K == Kind::DownFwd ? MOE_KERNEL_DOWN_FWD
+      : down_fwd ? MOE_KERNEL_DOWN_FWD
       : K == Kind::DownDgrad ? MOE_KERNEL_DOWN_DGRAD
       : K == Kind::GateUpDgrad ? MOE_KERNEL_GATEUP_DGRAD
       : K == Kind::WgradDown ? MOE_KERNEL_WGRAD_DOWN
@@ -270,7 +272,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const __grid_constant__ CUtensorMap mapO2, const GemmArgs args) {
   using T = Tr<K>;
   using G = Geo<K, PAIR>;
-  static_assert(!PAIR || (!T::dense && K != Kind::GateUpFwdNarrow), "pairs: grouped kinds");
+  static_assert(!PAIR || (!T::dense && !T::narrow), "pairs: grouped kinds");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~(uintptr_t)1023);
@@ -789,9 +791,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       } else {
-        // single accumulator, 256 columns, plain (optionally row-scaled) store
+        // single accumulator, plain (optionally row-scaled) store
         float scale = 1.0f;
-        if constexpr (K == Kind::DownFwd) {
+        if constexpr (T::down_fwd) {
           if (args.row_w && row_ok) scale = args.row_w[row];
         }
 #pragma unroll 1

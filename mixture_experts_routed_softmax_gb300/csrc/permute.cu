@@ -154,6 +154,66 @@ __global__ void permute_scatter_kernel(const int32_t* __restrict__ idx, int64_t 
   src_pair[dst] = (int32_t)p;
 }
 
+// A few pairs (decode): hist, scan and scatter in one CTA of 1024 threads.
+// Thread e counts expert e's pairs, the padded sizes are scanned as above,
+// and pair p's rank is the number of earlier pairs with its expert — the same
+// layout as the four-kernel path.
+constexpr int kSmallPairs = 256;
+__global__ void __launch_bounds__(1024) permute_small_kernel(
+    const int32_t* __restrict__ idx, int64_t P, int E, int align, int32_t* __restrict__ counts,
+    int64_t* __restrict__ offsets, int32_t* __restrict__ dst_row,
+    int32_t* __restrict__ src_pair, int* status) {
+  __shared__ int32_t s_idx[kSmallPairs];
+  __shared__ int64_t warp_tot[32];
+  __shared__ int64_t s_off[1024];
+  const int tid = threadIdx.x;
+  const int lane = tid & 31, w = tid >> 5;
+  for (int p = tid; p < P; p += blockDim.x) s_idx[p] = valid_expert(idx, p, P, E, status);
+  __syncthreads();
+  int64_t n = 0;
+  if (tid < E)
+    for (int p = 0; p < P; ++p) n += (s_idx[p] == tid);
+  const int64_t padded = (tid < E) ? ((n + align - 1) / align) * align : 0;
+  int64_t incl = padded;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int64_t o = __shfl_up_sync(0xFFFFFFFFu, incl, off);
+    if (lane >= off) incl += o;
+  }
+  if (lane == 31) warp_tot[w] = incl;
+  __syncthreads();
+  if (w == 0) {
+    int64_t v = warp_tot[lane];
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int64_t o = __shfl_up_sync(0xFFFFFFFFu, v, off);
+      if (lane >= off) v += o;
+    }
+    warp_tot[lane] = v;
+  }
+  __syncthreads();
+  const int64_t excl = incl - padded + (w > 0 ? warp_tot[w - 1] : 0);
+  s_off[tid] = excl;
+  if (tid < E) {
+    counts[tid] = (int32_t)n;
+    offsets[tid] = excl;
+  }
+  if (tid == E - 1) offsets[E] = excl + padded;
+  __syncthreads();
+  for (int p = tid; p < P; p += blockDim.x) {
+    const int e = s_idx[p];
+    if (e < 0) {
+      dst_row[p] = -1;
+      continue;
+    }
+    int rank = 0;
+    for (int q = 0; q < p; ++q) rank += (s_idx[q] == e);
+    const int32_t dst = (int32_t)(s_off[e] + rank);
+    dst_row[p] = dst;
+    src_pair[dst] = (int32_t)p;
+  }
+}
+
 __device__ __forceinline__ int expert_of_row_p(const int64_t* offsets, int E, int64_t r) {
   int lo = 0, hi = E;
   while (hi - lo > 1) {
@@ -214,16 +274,23 @@ cudaError_t launch_permute(const int32_t* topk_idx, int64_t T, int k, int E, int
                                          (int)hist_smem);
   if (err != cudaSuccess) return err;
   timer_before(MOE_KERNEL_PERMUTE, s);
-  if (P > 0)
-    permute_hist_kernel<<<(unsigned)nblk, kHistWarps * 32, hist_smem, s>>>(
-        topk_idx, P, E, blk_count, rank_in_blk, status);
-  permute_scan_kernel<<<1, 1024, 0, s>>>(blk_count, nblk, E, align, counts, offsets);
-  if (P > 0)
-    permute_scatter_kernel<<<(unsigned)((P + 255) / 256), 256, 0, s>>>(
-        topk_idx, P, E, blk_count, rank_in_blk, dst_row, src_pair);
+  int launches = 2;
+  if (P > 0 && P <= kSmallPairs) {
+    permute_small_kernel<<<1, 1024, 0, s>>>(topk_idx, P, E, align, counts, offsets, dst_row,
+                                            src_pair, status);
+  } else {
+    if (P > 0)
+      permute_hist_kernel<<<(unsigned)nblk, kHistWarps * 32, hist_smem, s>>>(
+          topk_idx, P, E, blk_count, rank_in_blk, status);
+    permute_scan_kernel<<<1, 1024, 0, s>>>(blk_count, nblk, E, align, counts, offsets);
+    if (P > 0)
+      permute_scatter_kernel<<<(unsigned)((P + 255) / 256), 256, 0, s>>>(
+          topk_idx, P, E, blk_count, rank_in_blk, dst_row, src_pair);
+    launches = P > 0 ? 4 : 2;
+  }
   permute_gather_kernel<<<(unsigned)((R_cap + 7) / 8), 256, 0, s>>>(x, d, k, offsets, counts, E,
                                                                     R_cap, src_pair, xp);
-  note_launches(P > 0 ? 4 : 2);
+  note_launches(launches);
   timer_after(MOE_KERNEL_PERMUTE, s);
   return cudaGetLastError();
 }

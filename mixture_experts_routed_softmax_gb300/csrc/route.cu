@@ -62,9 +62,59 @@ __global__ void split_router_weight_kernel(const float* __restrict__ wr, int d, 
   w_split[2 * plane + i] = __bfloat16_as_ushort(lo);
 }
 
+// A few tokens (decode): logits on the CUDA cores, one block per (token, eight
+// experts). Thread i accumulates rows i, i + 256, ... of x_t . W_r[:, e0:e0+8]
+// in fp32 (the products of a bf16 and an fp32 value), then the block adds the
+// 256 partial sums in a fixed tree order. No weight split, no split K.
+constexpr int kRouterSimtMaxT = 32;
+constexpr int kRouterSimtCols = 8;
+__global__ void __launch_bounds__(256) router_simt_kernel(const moe_bf16* __restrict__ x,
+                                                          const float* __restrict__ w_router,
+                                                          const float* __restrict__ bias, int d,
+                                                          int E, float* __restrict__ logits) {
+  __shared__ float part[kRouterSimtCols][256];
+  const int64_t t = blockIdx.y;
+  const int e0 = blockIdx.x * kRouterSimtCols;
+  const int ne = min(kRouterSimtCols, E - e0);
+  float acc[kRouterSimtCols];
+#pragma unroll
+  for (int j = 0; j < kRouterSimtCols; ++j) acc[j] = 0.f;
+  const moe_bf16* xr = x + t * d;
+  for (int i = threadIdx.x; i < d; i += 256) {
+    const float xv = __bfloat162float(__ushort_as_bfloat16(xr[i]));
+    const float* wr = w_router + (int64_t)i * E + e0;
+#pragma unroll
+    for (int j = 0; j < kRouterSimtCols; ++j)
+      if (j < ne) acc[j] = fmaf(xv, wr[j], acc[j]);
+  }
+#pragma unroll
+  for (int j = 0; j < kRouterSimtCols; ++j) part[j][threadIdx.x] = acc[j];
+  __syncthreads();
+  for (int w = 128; w > 0; w >>= 1) {
+    if (threadIdx.x < w) {
+#pragma unroll
+      for (int j = 0; j < kRouterSimtCols; ++j)
+        part[j][threadIdx.x] += part[j][threadIdx.x + w];
+    }
+    __syncthreads();
+  }
+  if (threadIdx.x < ne)
+    logits[t * E + e0 + threadIdx.x] =
+        part[threadIdx.x][0] + (bias ? bias[e0 + threadIdx.x] : 0.f);
+}
+
 cudaError_t launch_router_logits(const moe_bf16* x, const float* w_router, const float* bias,
                                  int64_t T, int d, int E, float* logits, void* ws, int* status,
                                  cudaStream_t s) {
+  if (T <= kRouterSimtMaxT) {
+    timer_before(MOE_KERNEL_ROUTER_LOGITS, s);
+    router_simt_kernel<<<dim3((unsigned)((E + kRouterSimtCols - 1) / kRouterSimtCols),
+                             (unsigned)T),
+                        256, 0, s>>>(x, w_router, bias, d, E, logits);
+    note_launches(1);
+    timer_after(MOE_KERNEL_ROUTER_LOGITS, s);
+    return cudaGetLastError();
+  }
   const int E8 = round8(E);
   moe_bf16* w_split = static_cast<moe_bf16*>(ws);
   const int64_t n = (int64_t)d * E8;
