@@ -80,12 +80,21 @@ __global__ void __launch_bounds__(256) router_simt_kernel(const moe_bf16* __rest
 #pragma unroll
   for (int j = 0; j < kRouterSimtCols; ++j) acc[j] = 0.f;
   const moe_bf16* xr = x + t * d;
-  for (int i = threadIdx.x; i < d; i += 256) {
-    const float xv = __bfloat162float(__ushort_as_bfloat16(xr[i]));
-    const float* wr = w_router + (int64_t)i * E + e0;
+  // four rows' loads in flight before their products are added (in row order)
+  for (int i0 = threadIdx.x; i0 < d; i0 += 4 * 256) {
+    float xv[4], wv[4][kRouterSimtCols];
 #pragma unroll
-    for (int j = 0; j < kRouterSimtCols; ++j)
-      if (j < ne) acc[j] = fmaf(xv, wr[j], acc[j]);
+    for (int u = 0; u < 4; ++u) {
+      const int i = i0 + 256 * u;
+      xv[u] = i < d ? __bfloat162float(__ushort_as_bfloat16(xr[i])) : 0.f;
+      const float* wr = w_router + (int64_t)i * E + e0;
+#pragma unroll
+      for (int j = 0; j < kRouterSimtCols; ++j) wv[u][j] = (i < d && j < ne) ? wr[j] : 0.f;
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+#pragma unroll
+      for (int j = 0; j < kRouterSimtCols; ++j) acc[j] = fmaf(xv[u], wv[u][j], acc[j]);
   }
 #pragma unroll
   for (int j = 0; j < kRouterSimtCols; ++j) part[j][threadIdx.x] = acc[j];
