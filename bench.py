@@ -61,6 +61,9 @@ def parse_args(argv=None):
     ap.add_argument("--ref-tokens", type=int, default=1,
                     help="tokens per step of the reference (oracle) arm")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--path", choices=["auto", "general", "decode"], default="auto",
+                    help="decode: the one-launch forward (moe_decode_fwd); auto picks it for "
+                         "forward-only workloads of at most 8 tokens")
     ap.add_argument("--graph", action="store_true",
                     help="launch each timed step as one captured CUDA graph (launch-bound sizes)")
     return ap.parse_args(argv)
@@ -235,15 +238,29 @@ def run_ours(args, rank, world, local_rank):
         wl = wl.with_(align=args.align)
     inp = workloads.generate(wl, with_dy=wl.backward)
     layer = MoELayer.from_inputs(inp, wl.k, wl.align, device=dev)
-    b = layer.buffers(wl.T, backward=wl.backward)
+    decode = args.path == "decode" or (args.path == "auto" and not wl.backward and wl.T <= 8)
+    if decode and (wl.backward or wl.T > 8):
+        raise SystemExit("the decode path runs forward-only workloads of at most 8 tokens")
+    if decode:
+        new_buffers = lambda: layer.decode_buffers(wl.T)  # noqa: E731
+        fwd = layer.decode_fwd
+    else:
+        new_buffers = lambda: layer.buffers(wl.T, backward=wl.backward)  # noqa: E731
+        fwd = layer.forward
+    b = new_buffers()
     x = inp["x"].to(dev)
     dy = inp["dy"].to(dev) if wl.backward else None
     lib = _lib.load()
 
     def step():
-        layer.forward(x, b)
+        fwd(x, b)
         if wl.backward:
             layer.backward(dy, b)
+
+    def active_experts():
+        if decode:
+            return int(torch.unique(b.topk_idx).numel())
+        return int((b.counts > 0).sum())
 
     for _ in range(max(args.warmup, 3)):
         step()
@@ -251,7 +268,7 @@ def run_ours(args, rank, world, local_rank):
     if status != 0:
         raise RuntimeError(f"device status {status}: {_lib.status_str(status)}")
 
-    kernels = STEP_KERNELS if wl.backward else FWD_KERNELS
+    kernels = ["decode"] if decode else (STEP_KERNELS if wl.backward else FWD_KERNELS)
     # three profiled steps per kernel group (outside the timed region)
     per_kernel = {}
     for name in kernels:
@@ -286,9 +303,12 @@ def run_ours(args, rank, world, local_rank):
     # L2 again on the next step: then L2 is flushed (a write of twice its
     # size) between steps, outside each step's own pair of events.
     l2_bytes = torch.cuda.get_device_properties(dev).L2_cache_size
-    step_bytes = accounting.totals(accounting.Shape(T=wl.T, d=wl.d, f=wl.f, E=wl.E, k=wl.k,
-                                                    E_active=int((b.counts > 0).sum())),
-                                   wl.backward)[1]
+    shape = accounting.Shape(T=wl.T, d=wl.d, f=wl.f, E=wl.E, k=wl.k, E_active=active_experts())
+    if decode:
+        costs = {"decode": accounting.decode_costs(shape)}
+    else:
+        costs = accounting.kernel_costs(shape, wl.backward)
+    step_bytes = sum(c[1] for c in costs.values())
     flush = step_bytes < 4 * l2_bytes
     flush_buf = torch.empty(2 * l2_bytes, dtype=torch.uint8, device=dev) if flush else None
     sampler = ClockSampler(local_rank).start()
@@ -344,7 +364,7 @@ def run_ours(args, rank, world, local_rank):
         dx_h = [torch.empty_like(inp["x"]).pin_memory() for _ in range(2)] if wl.backward else None
         bi = x_h.numel() * 2 + (dy_h.numel() * 2 if wl.backward else 0)
         bo = y_h[0].numel() * 2 + (dx_h[0].numel() * 2 if wl.backward else 0)
-        bufs = [b, layer.buffers(wl.T, backward=wl.backward)]
+        bufs = [b, new_buffers()]
         xs = [torch.empty_like(x) for _ in range(2)]
         dys = [torch.empty_like(dy) for _ in range(2)] if wl.backward else None
         up = torch.cuda.Stream(device=dev)       # host -> device
@@ -373,7 +393,7 @@ def run_ours(args, rank, world, local_rank):
             j = i & 1
             stream.wait_event(h2d[j])            # step i's inputs are in set j
             stream.wait_event(d2h[j])            # step i-2's results have left set j
-            layer.forward(xs[j], bufs[j])
+            fwd(xs[j], bufs[j])
             if wl.backward:
                 layer.backward(dys[j], bufs[j])
             done[j].record(stream)
@@ -397,10 +417,6 @@ def run_ours(args, rank, world, local_rank):
                "overlap": "uploads and downloads on two copy streams, two buffer sets"}
 
     # ----------------------------------------------------------- roofline --
-    counts = b.counts.cpu()
-    shape = accounting.Shape(T=wl.T, d=wl.d, f=wl.f, E=wl.E, k=wl.k,
-                             E_active=int((counts > 0).sum()))
-    costs = accounting.kernel_costs(shape, wl.backward)
     peaks = load_peaks()
     key = "combine" if dominant == "combine" else dominant
     fl, by = costs[key]
@@ -423,7 +439,8 @@ def run_ours(args, rank, world, local_rank):
     roof["traffic"] = recorded_traffic(dominant, args.config)
 
     ms_per_step = max_ms / args.steps
-    F, B = accounting.totals(shape, wl.backward)
+    F = sum(c[0] for c in costs.values())
+    B = sum(c[1] for c in costs.values())
     t_roof = accounting.roofline_seconds(F, B, peaks["bf16_tflops"], peaks["hbm_gbs"])
     value = world * wl.T * args.steps / (max_ms / 1e3)
 
@@ -438,6 +455,7 @@ def run_ours(args, rank, world, local_rank):
                           if flush else
                           "inputs larger than L2 (no flush): one step moves several GB"),
                    "graph": bool(args.graph),
+                   "path": "decode (one launch)" if decode else "general",
                    "parallelism": f"replicas x{world}"},
         "roofline": roof,
         "layer_roofline": {"flops": F, "bytes": B, "t_roof_ms": t_roof * 1e3,

@@ -245,6 +245,37 @@ int moe_route_bwd(const float* d_topk_w, const float* topk_w, const int32_t* top
                   void* ws, size_t ws_bytes, moe_stream_t stream);
 
 /* ------------------------------------------------------------------------
+ * moe_decode_fwd — the whole forward for a handful of tokens (decode), in one
+ * cooperative kernel.
+ * [HALO §Levers that do not help here] small-M experts are bound by reading
+ * their weights; [PLLM §Runtime architecture] top-k routing. For T <= 8 the
+ * general path's seven launches cost more than the work: this call computes
+ * the same forward as moe_route + moe_permute + moe_expert_fwd + moe_combine
+ * (row_w == NULL) in one launch whose phases are separated by grid barriers:
+ * router logits (fp32 dot products), top-k with renormalised weights (ties ->
+ * lower index), then per selected expert the gate/up and down products of
+ * every token routed to it (one read of its weights), A = silu(G)*U and the
+ * expert outputs kept in fp32, and y[t] = sum_j w[t,j] * (expert output) in
+ * slot order, rounded to bf16 once.
+ *  x [T, d] bf16; w_router [d, E] fp32; bias [E] fp32 or NULL;
+ *  forced_idx [T, k] int32 or NULL (as in moe_route: ids outside [0, E) raise
+ *  MOE_ERR_DEVICE_INDEX and the pair is dropped);
+ *  w_gate, w_up [E, d, f] bf16; w_down [E, f, d] bf16;
+ *  logits [T, E] fp32, topk_idx [T, k] int32, topk_w [T, k] fp32, y [T, d]
+ *  bf16 out.
+ *  ws: moe_decode_workspace_size(T, d, f, k) bytes, 256-byte aligned.
+ * Limits: T <= 8 (else MOE_ERR_UNSUPPORTED; T = 0 does nothing), d and f
+ * multiples of 64, k <= 32, E <= 1024. Needs a device that supports
+ * cooperative launch with one CTA per SM.
+ * ------------------------------------------------------------------------ */
+int moe_decode_fwd(const moe_bf16* x, const float* w_router, const float* bias,
+                   const int32_t* forced_idx, int64_t T, int d, int f, int E, int k,
+                   const moe_bf16* w_gate, const moe_bf16* w_up, const moe_bf16* w_down,
+                   float* logits, int32_t* topk_idx, float* topk_w, moe_bf16* y,
+                   void* ws, size_t ws_bytes, moe_stream_t stream);
+size_t moe_decode_workspace_size(int64_t T, int d, int f, int k);
+
+/* ------------------------------------------------------------------------
  * Workspace sizes (bytes) for the calls that take `ws`. Any 256-byte-aligned
  * device buffer of at least this size works; its contents need no
  * initialisation and are scratch after the call.
@@ -285,6 +316,7 @@ const char* moe_status_str(int code);
 #define MOE_KERNEL_WGRAD_DOWN    10
 #define MOE_KERNEL_WGRAD_GATEUP  11
 #define MOE_KERNEL_ROUTE_BWD     12
+#define MOE_KERNEL_DECODE        13
 int moe_timer_start(int kernel, int max_launches);
 int moe_timer_read(float* total_ms, int* launches);
 

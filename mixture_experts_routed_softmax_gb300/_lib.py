@@ -27,6 +27,9 @@ SIGNATURES = {
                             _P, _P, _P, _P, _P, _P, _P, _P, _P]),
     "moe_route_bwd": (_I, [_P, _P, _P, _P, _P, _P, _P, _I64, _I, _I, _I, _I,
                            _P, _P, _P, _P, _P, _P, _SZ, _P]),
+    "moe_decode_fwd": (_I, [_P, _P, _P, _P, _I64, _I, _I, _I, _I, _P, _P, _P,
+                            _P, _P, _P, _P, _P, _SZ, _P]),
+    "moe_decode_workspace_size": (_SZ, [_I64, _I, _I, _I]),
     "moe_workspace_size": (_SZ, [_I, _I64, _I, _I, _I, _I]),
     "moe_row_capacity": (_I64, [_I64, _I, _I, _I]),
     "moe_status": (_I, [_P]),
@@ -52,6 +55,7 @@ KERNELS = {
     "router_logits": 1, "topk": 2, "permute": 3, "gateup_fwd": 4, "down_fwd": 5,
     "combine": 6, "combine_bwd": 7, "down_dgrad": 8, "gateup_dgrad": 9,
     "wgrad_down": 10, "wgrad_gateup": 11, "route_bwd": 12,
+    "decode": 13,
 }
 
 _lib = None

@@ -68,6 +68,17 @@ def kernel_costs(s: Shape, backward: bool = True) -> dict:
     return c
 
 
+def decode_costs(s: Shape) -> tuple[int, int]:
+    """(flops, bytes) of the one-launch decode forward: the router and every
+    pair's three expert products; x, W_r, logits, top-k, y and the three
+    weight matrices of each selected expert, each moved once (the per-pair
+    fp32 intermediates stay on chip or in L2)."""
+    P, T, d, f, E, k = s.P, s.T, s.d, s.f, s.E, s.k
+    fl = 2 * T * d * E + 6 * P * d * f
+    by = T * d * 2 + d * E * 4 + T * E * 4 + T * k * 8 + 3 * s.E_active * d * f * 2 + T * d * 2
+    return fl, by
+
+
 def totals(s: Shape, backward: bool = True) -> tuple[int, int]:
     fl = by = 0
     for f_, b_ in kernel_costs(s, backward).values():

@@ -122,7 +122,7 @@ int moe_status(moe_stream_t stream) {
 }
 
 int moe_timer_start(int kernel, int max_launches) {
-  if (kernel < MOE_KERNEL_ROUTER_LOGITS || kernel > MOE_KERNEL_ROUTE_BWD || max_launches <= 0)
+  if (kernel < MOE_KERNEL_ROUTER_LOGITS || kernel > MOE_KERNEL_DECODE || max_launches <= 0)
     return MOE_ERR_ARG;
   std::lock_guard<std::mutex> lock(g_timer.mu);
   if (g_timer.kernel != 0) return MOE_ERR_ARG;
@@ -278,6 +278,35 @@ int moe_expert_bwd(const moe_bf16* dy, const int32_t* src_pair, const int32_t* d
   if (e == cudaSuccess) e = launch_wgrad_down(gd, a, dyp, dw_down, st, s);
   if (e == cudaSuccess) e = launch_wgrad_gateup(gd, xp, dg, du, dw_gate, dw_up, st, s);
   return cuda_code(e);
+}
+
+size_t moe_decode_workspace_size(int64_t T, int d, int f, int k) {
+  if (T < 0 || d <= 0 || f <= 0 || k <= 0) return 0;
+  return decode_ws_bytes(T, d, f, k);
+}
+
+int moe_decode_fwd(const moe_bf16* x, const float* w_router, const float* bias,
+                   const int32_t* forced_idx, int64_t T, int d, int f, int E, int k,
+                   const moe_bf16* w_gate, const moe_bf16* w_up, const moe_bf16* w_down,
+                   float* logits, int32_t* topk_idx, float* topk_w, moe_bf16* y,
+                   void* ws, size_t ws_bytes, moe_stream_t stream) {
+  if (!w_router || !w_gate || !w_up || !w_down ||
+      (T > 0 && (!x || !logits || !topk_idx || !topk_w || !y)))
+    return MOE_ERR_ARG;
+  if (T < 0 || d <= 0 || f <= 0 || E <= 0 || k <= 0 || k > E) return MOE_ERR_ARG;
+  if (T > 8 || k > kMaxTopK || E > kMaxExperts || d % 64 != 0 || f % 64 != 0)
+    return MOE_ERR_UNSUPPORTED;
+  for (const void* p : {(const void*)x, (const void*)w_gate, (const void*)w_up,
+                        (const void*)w_down, (const void*)y})
+    if (!aligned16(p)) return MOE_ERR_ARG;
+  if (T == 0) return MOE_OK;
+  if (!ws || ws_bytes < decode_ws_bytes(T, d, f, k) || (reinterpret_cast<uintptr_t>(ws) & 255u))
+    return MOE_ERR_ARG;
+  int* st = device_status_ptr();
+  if (!st) return MOE_ERR_CUDA;
+  return cuda_code(launch_decode_fwd(x, w_router, bias, forced_idx, (int)T, d, f, E, k, w_gate,
+                                     w_up, w_down, logits, topk_idx, topk_w, y, ws, st,
+                                     reinterpret_cast<cudaStream_t>(stream)));
 }
 
 int moe_route_bwd(const float* d_topk_w, const float* topk_w, const int32_t* topk_idx,

@@ -50,6 +50,13 @@ cudaError_t launch_combine_bwd(const moe_bf16* dy, const moe_bf16* yp, const int
                                cudaStream_t s);
 
 // gemm.cu (tcgen05 grouped GEMMs)
+size_t decode_ws_bytes(int64_t T, int d, int f, int k);
+cudaError_t launch_decode_fwd(const moe_bf16* x, const float* w_router, const float* bias,
+                              const int32_t* forced, int T, int d, int f, int E, int k,
+                              const moe_bf16* w_gate, const moe_bf16* w_up,
+                              const moe_bf16* w_down, float* logits, int32_t* topk_idx,
+                              float* topk_w, moe_bf16* y, void* ws, int* status,
+                              cudaStream_t s);
 int router_ksplit(int64_t T, int d, int E);
 int router_wgrad_ksplit(int64_t T, int d, int N3);
 cudaError_t launch_router_wgrad_gemm(const moe_bf16* x, const moe_bf16* dl3, int64_t T, int d,

@@ -13,6 +13,7 @@
 
 #include "common.cuh"
 #include "internal.h"
+#include "topk.cuh"
 
 namespace moe {
 
@@ -152,15 +153,8 @@ cudaError_t launch_router_logits(const moe_bf16* x, const float* w_router, const
 }
 
 // ---------------------------------------------------------------------------
-// Top-k and weights: one warp per token. Each lane keeps the logits of
-// experts lane, lane+32, ... in registers; k rounds of a warp arg-max pick the
-// slots in descending order (equal values: lower index first). Slot j's lane
-// then computes exp(l_j - l_0) and the warp sums them.
+// Top-k and weights: one warp per token (topk.cuh).
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ bool ranks_above(float va, int ia, float vb, int ib) {
-  return va > vb || (va == vb && ia < ib);
-}
-
 template <int NV>   // logits per lane: 32 * NV >= E
 __global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ logits,
                                                    const int32_t* __restrict__ forced, int64_t T,
@@ -169,58 +163,8 @@ __global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ log
   const int lane = threadIdx.x & 31;
   const int64_t t = (int64_t)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
   if (t >= T) return;
-  const float* lrow = logits + t * E;
-  float my_v = -INFINITY;  // slot `lane`'s logit (lanes < k)
-  int my_i = 0;
-  bool valid = true;
-  if (forced) {
-    if (lane < k) {
-      my_i = forced[t * k + lane];
-      valid = (my_i >= 0 && my_i < E);
-      if (valid) my_v = lrow[my_i];
-      else raise_status(status, MOE_ERR_DEVICE_INDEX);
-    }
-  } else {
-    float v[NV];
-#pragma unroll
-    for (int i = 0; i < NV; ++i) {
-      const int e = lane + 32 * i;
-      v[i] = (e < E) ? lrow[e] : -INFINITY;
-    }
-    uint32_t taken = 0;
-    for (int j = 0; j < k; ++j) {
-      float bv = -INFINITY;
-      int bi = 0x7FFFFFFF;
-#pragma unroll
-      for (int i = 0; i < NV; ++i) {
-        const int e = lane + 32 * i;
-        if (e < E && !((taken >> i) & 1u) && ranks_above(v[i], e, bv, bi)) {
-          bv = v[i];
-          bi = e;
-        }
-      }
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) {
-        const float ov = __shfl_xor_sync(0xFFFFFFFFu, bv, off);
-        const int oi = __shfl_xor_sync(0xFFFFFFFFu, bi, off);
-        if (ranks_above(ov, oi, bv, bi)) { bv = ov; bi = oi; }
-      }
-      if (bi != 0x7FFFFFFF && (bi & 31) == lane) taken |= 1u << (bi >> 5);
-      if (lane == j) { my_v = bv; my_i = (bi == 0x7FFFFFFF) ? 0 : bi; }
-    }
-  }
-  // renormalised softmax over the k slots
-  float m = (lane < k && valid) ? my_v : -INFINITY;
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, off));
-  float ex = (lane < k && valid) ? expf(my_v - m) : 0.f;
-  float sum = ex;
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xFFFFFFFFu, sum, off);
-  if (lane < k) {
-    topk_idx[t * k + lane] = my_i;
-    topk_w[t * k + lane] = sum > 0.f ? ex / sum : 0.f;
-  }
+  topk_warp<NV>(logits + t * E, forced ? forced + t * k : nullptr, E, k, lane, topk_idx + t * k,
+                topk_w + t * k, status);
 }
 
 cudaError_t launch_topk(const float* logits, const int32_t* forced_idx, int64_t T, int E, int k,

@@ -192,6 +192,35 @@ class MoELayer:
         self.route_bwd(b, fused=True, stream=stream)
         return b.dx
 
+    # ------------------------------------------------------------ decode --
+    def decode_buffers(self, T: int) -> Buffers:
+        """Buffers for decode_fwd: logits, top-k, y and the decode workspace."""
+        E, d, k = self.E, self.d, self.k
+        kw = dict(device=self.device)
+        ws = int(self.lib.moe_decode_workspace_size(T, d, self.f, k))
+        none = torch.empty(0, **kw)
+        return Buffers(
+            T=T, R_cap=0,
+            logits=torch.empty(T, E, dtype=torch.float32, **kw),
+            topk_idx=torch.empty(T, k, dtype=torch.int32, **kw),
+            topk_w=torch.empty(T, k, dtype=torch.float32, **kw),
+            counts=none, offsets=none, dst_row=none, src_pair=none, xp=none, g=none,
+            u=none, a=none, yp=none,
+            y=torch.empty(T, d, dtype=BF16, **kw),
+            ws_permute=torch.empty(max(ws, 256), dtype=torch.uint8, **kw),
+            ws_route=none,
+        )
+
+    def decode_fwd(self, x, b: Buffers, forced_idx=None, stream=None):
+        """The whole forward of T <= 8 tokens in one launch (moe_decode_fwd);
+        b from decode_buffers(T). Fills b.logits, b.topk_idx, b.topk_w, b.y."""
+        b.x = x
+        _lib.call("moe_decode_fwd", _p(x), _p(self.w_router), _p(self.bias), _p(forced_idx),
+                  b.T, self.d, self.f, self.E, self.k, _p(self.w_gate), _p(self.w_up),
+                  _p(self.w_down), _p(b.logits), _p(b.topk_idx), _p(b.topk_w), _p(b.y),
+                  _p(b.ws_permute), b.ws_permute.numel(), _stream(stream))
+        return b.y
+
     def status(self, stream=None) -> int:
         """Synchronise and read (and clear) the device status word."""
         return int(self.lib.moe_status(_stream(stream)))

@@ -29,7 +29,8 @@ def lib():
 def test_header_declares_the_layer_calls():
     names = declared_functions()
     for n in ("moe_route", "moe_permute", "moe_expert_fwd", "moe_expert_bwd", "moe_combine",
-              "moe_route_bwd", "moe_workspace_size", "moe_status", "moe_status_str"):
+              "moe_route_bwd", "moe_decode_fwd", "moe_decode_workspace_size",
+              "moe_workspace_size", "moe_status", "moe_status_str"):
         assert n in names
 
 
@@ -84,5 +85,18 @@ def test_host_argument_checks(lib):
     # route backward: dxp without dst_row
     wsb = lib.moe_workspace_size(2, 4, 8, 4, 2, 16)
     assert lib.moe_route_bwd(P, P, P, P, P, P, P, 4, 8, 4, 2, 16, P, P, None, P, None, P, wsb, None) == L.MOE_ERR_ARG
+    # decode: T above 8, d not a multiple of 64, k > E, null x, workspace too small
+    wd = lib.moe_decode_workspace_size(2, 128, 64, 2)
+    assert wd >= 256 + 2 * 2 * (128 + 64) * 4
+    dec = lambda T, d, f, E, k, x=P, ws=wd: lib.moe_decode_fwd(  # noqa: E731
+        x, P, None, None, T, d, f, E, k, P, P, P, P, P, P, P, P, ws, None)
+    assert dec(9, 128, 64, 4, 2) == L.MOE_ERR_UNSUPPORTED
+    assert dec(2, 96, 64, 4, 2) == L.MOE_ERR_UNSUPPORTED
+    assert dec(2, 128, 72, 4, 2) == L.MOE_ERR_UNSUPPORTED
+    assert dec(2, 128, 64, 4, 5) == L.MOE_ERR_ARG
+    assert dec(2, 128, 64, 4, 2, x=None) == L.MOE_ERR_ARG
+    assert dec(2, 128, 64, 4, 2, ws=wd - 1) == L.MOE_ERR_ARG
+    assert dec(0, 128, 64, 4, 2, x=None) == L.MOE_OK      # nothing to do
     # timer: bad kernel id
     assert lib.moe_timer_start(0, 4) == L.MOE_ERR_ARG
+    assert lib.moe_timer_start(L.KERNELS["decode"] + 1, 4) == L.MOE_ERR_ARG

@@ -90,3 +90,12 @@ def test_reference_arm_other_ranks_exit_quietly():
                           "--config", "tiny", "--steps", "1", "--warmup", "0"],
                          capture_output=True, text=True, timeout=600, cwd=ROOT, env=env)
     assert res.returncode == 0 and res.stdout.strip() == ""
+
+
+def test_decode_costs_match_the_forward_arithmetic():
+    from mixture_experts_routed_softmax_gb300 import accounting as acc
+    s = acc.Shape(T=8, d=2048, f=768, E=128, k=8, E_active=52)
+    fl, by = acc.decode_costs(s)
+    assert fl == acc.totals(s, backward=False)[0]       # the same products, one launch
+    w = 3 * 52 * 2048 * 768 * 2
+    assert w < by < w + 2 * 2**20                       # weights dominate; the rest is small
