@@ -200,10 +200,21 @@ def oracle_sample(inp: dict, wl, tokens: int) -> float:
 
 # ------------------------------------------------------------- traffic --
 
-def csrc_digest() -> str:
-    h = hashlib.sha256()
+# The source files that define each kernel (its translation unit and the
+# device-code header it includes); a recorded ncu figure stays valid while
+# these bytes are unchanged.
+_GEMM_SOURCES = ("gemm.cu", "common.cuh")
+KERNEL_SOURCES = {name: _GEMM_SOURCES for name in (
+    "gateup_fwd", "down_fwd", "down_dgrad", "gateup_dgrad", "wgrad_down", "wgrad_gateup")}
+
+
+def kernel_digest(kernel: str) -> str:
+    """sha256 (first 16 hex digits) of the kernel's source files; all of csrc/
+    for a kernel with no entry in KERNEL_SOURCES."""
     base = os.path.join(ROOT, "mixture_experts_routed_softmax_gb300", "csrc")
-    for f in sorted(os.listdir(base)):
+    files = KERNEL_SOURCES.get(kernel) or tuple(sorted(os.listdir(base)))
+    h = hashlib.sha256()
+    for f in files:
         with open(os.path.join(base, f), "rb") as fh:
             h.update(f.encode() + b"\0" + fh.read())
     return h.hexdigest()[:16]
@@ -217,8 +228,8 @@ def recorded_traffic(kernel: str, config: str):
         return None
     text = open(path).read()
     m = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", text)
-    s = re.search(r"csrc_sha256_16:\s*([0-9a-f]+)", text)
-    if not m or not s or s.group(1) != csrc_digest():
+    s = re.search(r"kernel_sources_sha256_16:\s*([0-9a-f]+)", text)
+    if not m or not s or s.group(1) != kernel_digest(kernel):
         return None
     return float(m.group(1))
 
