@@ -253,27 +253,33 @@ int moe_route_bwd(const float* d_topk_w, const float* topk_w, const int32_t* top
  * the same forward as moe_route + moe_permute + moe_expert_fwd + moe_combine
  * (row_w == NULL) in one launch whose phases are separated by grid barriers:
  * router logits (fp32 dot products), top-k with renormalised weights (ties ->
- * lower index), then per selected expert the gate/up and down products of
- * every token routed to it (one read of its weights), A = silu(G)*U and the
- * expert outputs kept in fp32, and y[t] = sum_j w[t,j] * (expert output) in
- * slot order, rounded to bf16 once.
+ * lower index), then the gate/up and down products of every selected expert
+ * with every token routed to it (each weight row read once, the rows of all
+ * selected experts split evenly over every warp of the GPU), A = silu(G)*U
+ * and the expert outputs kept in fp32, and y[t] = sum_j w[t,j] * (expert
+ * output) in slot order, rounded to bf16 once. Two calls on one GPU give
+ * bitwise equal results.
  *  x [T, d] bf16; w_router [d, E] fp32; bias [E] fp32 or NULL;
  *  forced_idx [T, k] int32 or NULL (as in moe_route: ids outside [0, E) raise
  *  MOE_ERR_DEVICE_INDEX and the pair is dropped);
  *  w_gate, w_up [E, d, f] bf16; w_down [E, f, d] bf16;
  *  logits [T, E] fp32, topk_idx [T, k] int32, topk_w [T, k] fp32, y [T, d]
  *  bf16 out.
- *  ws: moe_decode_workspace_size(T, d, f, k) bytes, 256-byte aligned.
+ *  ws: moe_decode_workspace_size(T, d, f, E, k) bytes, 256-byte aligned. The
+ *  size depends on the current device's SM count: query it with the device
+ *  that will run the call current.
  * Limits: T <= 8 (else MOE_ERR_UNSUPPORTED; T = 0 does nothing), d and f
- * multiples of 64, k <= 32, E <= 1024. Needs a device that supports
- * cooperative launch with one CTA per SM.
+ * multiples of 64, d <= 8192, f <= 16384, k <= 32, E <= 1024. Needs a device
+ * that supports cooperative launch with one CTA of 512 threads and 200 KiB of
+ * shared memory per SM.
  * ------------------------------------------------------------------------ */
 int moe_decode_fwd(const moe_bf16* x, const float* w_router, const float* bias,
                    const int32_t* forced_idx, int64_t T, int d, int f, int E, int k,
                    const moe_bf16* w_gate, const moe_bf16* w_up, const moe_bf16* w_down,
                    float* logits, int32_t* topk_idx, float* topk_w, moe_bf16* y,
                    void* ws, size_t ws_bytes, moe_stream_t stream);
-size_t moe_decode_workspace_size(int64_t T, int d, int f, int k);
+/* 0 for arguments the call rejects (T outside [0, 8], a size <= 0). */
+size_t moe_decode_workspace_size(int64_t T, int d, int f, int E, int k);
 
 /* ------------------------------------------------------------------------
  * Workspace sizes (bytes) for the calls that take `ws`. Any 256-byte-aligned

@@ -29,7 +29,7 @@ SIGNATURES = {
                            _P, _P, _P, _P, _P, _P, _SZ, _P]),
     "moe_decode_fwd": (_I, [_P, _P, _P, _P, _I64, _I, _I, _I, _I, _P, _P, _P,
                             _P, _P, _P, _P, _P, _SZ, _P]),
-    "moe_decode_workspace_size": (_SZ, [_I64, _I, _I, _I]),
+    "moe_decode_workspace_size": (_SZ, [_I64, _I, _I, _I, _I]),
     "moe_workspace_size": (_SZ, [_I, _I64, _I, _I, _I, _I]),
     "moe_row_capacity": (_I64, [_I64, _I, _I, _I]),
     "moe_status": (_I, [_P]),

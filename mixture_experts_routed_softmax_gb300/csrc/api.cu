@@ -280,9 +280,9 @@ int moe_expert_bwd(const moe_bf16* dy, const int32_t* src_pair, const int32_t* d
   return cuda_code(e);
 }
 
-size_t moe_decode_workspace_size(int64_t T, int d, int f, int k) {
-  if (T < 0 || d <= 0 || f <= 0 || k <= 0) return 0;
-  return decode_ws_bytes(T, d, f, k);
+size_t moe_decode_workspace_size(int64_t T, int d, int f, int E, int k) {
+  if (T < 0 || T > kDecodeMaxT || d <= 0 || f <= 0 || E <= 0 || k <= 0) return 0;
+  return decode_ws_bytes(T, d, f, E, k);
 }
 
 int moe_decode_fwd(const moe_bf16* x, const float* w_router, const float* bias,
@@ -294,13 +294,14 @@ int moe_decode_fwd(const moe_bf16* x, const float* w_router, const float* bias,
       (T > 0 && (!x || !logits || !topk_idx || !topk_w || !y)))
     return MOE_ERR_ARG;
   if (T < 0 || d <= 0 || f <= 0 || E <= 0 || k <= 0 || k > E) return MOE_ERR_ARG;
-  if (T > 8 || k > kMaxTopK || E > kMaxExperts || d % 64 != 0 || f % 64 != 0)
+  if (T > kDecodeMaxT || k > kMaxTopK || E > kMaxExperts || d % 64 != 0 || f % 64 != 0 ||
+      d > kDecodeMaxD || f > kDecodeMaxF)
     return MOE_ERR_UNSUPPORTED;
   for (const void* p : {(const void*)x, (const void*)w_gate, (const void*)w_up,
                         (const void*)w_down, (const void*)y})
     if (!aligned16(p)) return MOE_ERR_ARG;
   if (T == 0) return MOE_OK;
-  if (!ws || ws_bytes < decode_ws_bytes(T, d, f, k) || (reinterpret_cast<uintptr_t>(ws) & 255u))
+  if (!ws || ws_bytes < decode_ws_bytes(T, d, f, E, k) || (reinterpret_cast<uintptr_t>(ws) & 255u))
     return MOE_ERR_ARG;
   int* st = device_status_ptr();
   if (!st) return MOE_ERR_CUDA;

@@ -50,7 +50,10 @@ cudaError_t launch_combine_bwd(const moe_bf16* dy, const moe_bf16* yp, const int
                                cudaStream_t s);
 
 // gemm.cu (tcgen05 grouped GEMMs)
-size_t decode_ws_bytes(int64_t T, int d, int f, int k);
+constexpr int kDecodeMaxT = 8;        // tokens of one decode call
+constexpr int kDecodeMaxD = 8192;     // x is kept in shared memory
+constexpr int kDecodeMaxF = 16384;
+size_t decode_ws_bytes(int64_t T, int d, int f, int E, int k);
 cudaError_t launch_decode_fwd(const moe_bf16* x, const float* w_router, const float* bias,
                               const int32_t* forced, int T, int d, int f, int E, int k,
                               const moe_bf16* w_gate, const moe_bf16* w_up,

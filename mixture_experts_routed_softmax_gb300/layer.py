@@ -197,7 +197,7 @@ class MoELayer:
         """Buffers for decode_fwd: logits, top-k, y and the decode workspace."""
         E, d, k = self.E, self.d, self.k
         kw = dict(device=self.device)
-        ws = int(self.lib.moe_decode_workspace_size(T, d, self.f, k))
+        ws = int(self.lib.moe_decode_workspace_size(T, d, self.f, self.E, k))
         none = torch.empty(0, **kw)
         return Buffers(
             T=T, R_cap=0,

@@ -86,13 +86,15 @@ def test_host_argument_checks(lib):
     wsb = lib.moe_workspace_size(2, 4, 8, 4, 2, 16)
     assert lib.moe_route_bwd(P, P, P, P, P, P, P, 4, 8, 4, 2, 16, P, P, None, P, None, P, wsb, None) == L.MOE_ERR_ARG
     # decode: T above 8, d not a multiple of 64, k > E, null x, workspace too small
-    wd = lib.moe_decode_workspace_size(2, 128, 64, 2)
-    assert wd >= 256 + 2 * 2 * (128 + 64) * 4
+    wd = lib.moe_decode_workspace_size(2, 128, 64, 4, 2)
+    assert wd >= 256 + 2 * 2 * 64 * 4          # at least the barrier word and A
+    assert lib.moe_decode_workspace_size(9, 128, 64, 4, 2) == 0
     dec = lambda T, d, f, E, k, x=P, ws=wd: lib.moe_decode_fwd(  # noqa: E731
         x, P, None, None, T, d, f, E, k, P, P, P, P, P, P, P, P, ws, None)
     assert dec(9, 128, 64, 4, 2) == L.MOE_ERR_UNSUPPORTED
     assert dec(2, 96, 64, 4, 2) == L.MOE_ERR_UNSUPPORTED
     assert dec(2, 128, 72, 4, 2) == L.MOE_ERR_UNSUPPORTED
+    assert dec(2, 8256, 64, 4, 2) == L.MOE_ERR_UNSUPPORTED   # d above 8192
     assert dec(2, 128, 64, 4, 5) == L.MOE_ERR_ARG
     assert dec(2, 128, 64, 4, 2, x=None) == L.MOE_ERR_ARG
     assert dec(2, 128, 64, 4, 2, ws=wd - 1) == L.MOE_ERR_ARG
