@@ -62,8 +62,9 @@ def parse_args(argv=None):
                     help="tokens per step of the reference (oracle) arm")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--path", choices=["auto", "general", "decode"], default="auto",
-                    help="decode: the one-launch forward (moe_decode_fwd); auto picks it for "
-                         "forward-only workloads of at most 8 tokens")
+                    help="decode: the one-launch forward (moe_decode_fwd), forward-only "
+                         "workloads of at most 8 tokens; auto: the general path, measured "
+                         "faster than the one-launch forward at every decode size")
     ap.add_argument("--graph", action="store_true",
                     help="launch each timed step as one captured CUDA graph (launch-bound sizes)")
     return ap.parse_args(argv)
@@ -249,7 +250,7 @@ def run_ours(args, rank, world, local_rank):
         wl = wl.with_(align=args.align)
     inp = workloads.generate(wl, with_dy=wl.backward)
     layer = MoELayer.from_inputs(inp, wl.k, wl.align, device=dev)
-    decode = args.path == "decode" or (args.path == "auto" and not wl.backward and wl.T <= 8)
+    decode = args.path == "decode"
     if decode and (wl.backward or wl.T > 8):
         raise SystemExit("the decode path runs forward-only workloads of at most 8 tokens")
     if decode:

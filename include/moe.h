@@ -258,7 +258,8 @@ int moe_route_bwd(const float* d_topk_w, const float* topk_w, const int32_t* top
  * selected experts split evenly over every warp of the GPU), A = silu(G)*U
  * and the expert outputs kept in fp32, and y[t] = sum_j w[t,j] * (expert
  * output) in slot order, rounded to bf16 once. Two calls on one GPU give
- * bitwise equal results.
+ * bitwise equal results. The general path (the four calls above) is faster
+ * on GB300 at the decode sizes measured; this call is the one-launch form.
  *  x [T, d] bf16; w_router [d, E] fp32; bias [E] fp32 or NULL;
  *  forced_idx [T, k] int32 or NULL (as in moe_route: ids outside [0, E) raise
  *  MOE_ERR_DEVICE_INDEX and the pair is dropped);
@@ -269,9 +270,10 @@ int moe_route_bwd(const float* d_topk_w, const float* topk_w, const int32_t* top
  *  size depends on the current device's SM count: query it with the device
  *  that will run the call current.
  * Limits: T <= 8 (else MOE_ERR_UNSUPPORTED; T = 0 does nothing), d and f
- * multiples of 64, d <= 8192, f <= 16384, k <= 32, E <= 1024. Needs a device
- * that supports cooperative launch with one CTA of 512 threads and 200 KiB of
- * shared memory per SM.
+ * multiples of 64, d <= 8192, f <= 16384, each cut into equal column blocks of
+ * at most 4096 (else MOE_ERR_UNSUPPORTED), k <= 32, E <= 1024. Needs a device
+ * that supports cooperative launch with one CTA of 544 threads and about
+ * 200 KiB of shared memory per SM, and at most 256 SMs (else MOE_ERR_CUDA).
  * ------------------------------------------------------------------------ */
 int moe_decode_fwd(const moe_bf16* x, const float* w_router, const float* bias,
                    const int32_t* forced_idx, int64_t T, int d, int f, int E, int k,

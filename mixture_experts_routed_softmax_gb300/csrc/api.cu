@@ -295,7 +295,7 @@ int moe_decode_fwd(const moe_bf16* x, const float* w_router, const float* bias,
     return MOE_ERR_ARG;
   if (T < 0 || d <= 0 || f <= 0 || E <= 0 || k <= 0 || k > E) return MOE_ERR_ARG;
   if (T > kDecodeMaxT || k > kMaxTopK || E > kMaxExperts || d % 64 != 0 || f % 64 != 0 ||
-      d > kDecodeMaxD || f > kDecodeMaxF)
+      d > kDecodeMaxD || f > kDecodeMaxF || !decode_shape_ok(d, f))
     return MOE_ERR_UNSUPPORTED;
   for (const void* p : {(const void*)x, (const void*)w_gate, (const void*)w_up,
                         (const void*)w_down, (const void*)y})

@@ -54,6 +54,7 @@ constexpr int kDecodeMaxT = 8;        // tokens of one decode call
 constexpr int kDecodeMaxD = 8192;     // x is kept in shared memory
 constexpr int kDecodeMaxF = 16384;
 size_t decode_ws_bytes(int64_t T, int d, int f, int E, int k);
+bool decode_shape_ok(int d, int f);   // rows cut into equal column blocks of whole octets
 cudaError_t launch_decode_fwd(const moe_bf16* x, const float* w_router, const float* bias,
                               const int32_t* forced, int T, int d, int f, int E, int k,
                               const moe_bf16* w_gate, const moe_bf16* w_up,
