@@ -95,6 +95,7 @@ def test_host_argument_checks(lib):
     assert dec(2, 96, 64, 4, 2) == L.MOE_ERR_UNSUPPORTED
     assert dec(2, 128, 72, 4, 2) == L.MOE_ERR_UNSUPPORTED
     assert dec(2, 8256, 64, 4, 2) == L.MOE_ERR_UNSUPPORTED   # d above 8192
+    assert dec(2, 128, 8320, 4, 2) == L.MOE_ERR_UNSUPPORTED  # f not cut into equal 8-column blocks
     assert dec(2, 128, 64, 4, 5) == L.MOE_ERR_ARG
     assert dec(2, 128, 64, 4, 2, x=None) == L.MOE_ERR_ARG
     assert dec(2, 128, 64, 4, 2, ws=wd - 1) == L.MOE_ERR_ARG

@@ -4,8 +4,9 @@ oracle.
 Free routing: logits within tolerance, top-k indices exact up to near-ties.
 Then the oracle's selection forced on the GPU: indices exact, weights and y
 within the bf16 bar. Cases span one to eight tokens, ragged expert counts
-(E not a multiple of 32), k = 1 and k = 32 (256 pairs), E = 1024, several
-64-column units in d and f, and the decode workloads' full layer shape.
+(E not a multiple of 32), k = 1 and k = 32 (256 pairs), E = 1024, narrow rows
+(several warp groups per row lane set), rows wider than 4096 columns (two
+column blocks), and the decode workloads' full layer shape.
 Caller-chosen ids that repeat an expert, an id out of range, two runs
 bitwise equal and T = 0 are covered separately.
 """
@@ -28,6 +29,8 @@ CASES = {
     "eight_wide_E": (8, 320, 256, 160, 6),
     "k32_E1024": (8, 64, 128, 1024, 32),
     "layer_shape_T8": (8, 2048, 768, 16, 8),
+    # rows wider than 4096 columns: each phase cuts them into two column blocks
+    "two_column_blocks": (2, 4160, 4224, 4, 2),
 }
 
 
