@@ -180,6 +180,9 @@ int moe_route(const moe_bf16* x, const float* w_router, const float* bias,
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   int* st = device_status_ptr();
   if (!st) return MOE_ERR_CUDA;
+  if (route_is_small(T))
+    return cuda_code(launch_route_small(x, w_router, bias, forced_idx, T, d, E, k, logits,
+                                        topk_idx, topk_w, ws, st, s));
   cudaError_t e = launch_router_logits(x, w_router, bias, T, d, E, logits, ws, st, s);
   if (e == cudaSuccess) e = launch_topk(logits, forced_idx, T, E, k, topk_idx, topk_w, st, s);
   return cuda_code(e);

@@ -21,6 +21,12 @@ int num_sms();
 
 // route.cu
 size_t route_ws_bytes(int64_t T, int d, int E);
+// up to 32 tokens: routing on the CUDA cores, logits and top-k in two launches
+inline bool route_is_small(int64_t T) { return T <= 32; }
+cudaError_t launch_route_small(const moe_bf16* x, const float* w_router, const float* bias,
+                               const int32_t* forced, int64_t T, int d, int E, int k,
+                               float* logits, int32_t* topk_idx, float* topk_w, void* ws,
+                               int* status, cudaStream_t s);
 cudaError_t launch_router_logits(const moe_bf16* x, const float* w_router, const float* bias,
                                  int64_t T, int d, int E, float* logits, void* ws, int* status,
                                  cudaStream_t s);

@@ -30,10 +30,30 @@ static inline int round8(int v) { return (v + 7) & ~7; }
 
 static inline size_t al256r(size_t b) { return (b + 255) & ~(size_t)255; }
 
-// workspace: the split weight [3d, E8] bf16, then (split K) fp32 partials [ksplit, T, E]
+// A few tokens (decode) take the CUDA cores in two launches: row-slice partial
+// dot products, then one CTA per token that adds them, writes the logits and
+// takes the top-k. The slices: at most kSmallSlices per 128 experts.
+constexpr int kRouterSmallMaxT = 32;   // route_is_small
+constexpr int kSmallTok = 8;        // tokens a CTA of the partial kernel multiplies
+constexpr int kSmallCols = 128;     // experts a CTA covers: 4 per lane
+constexpr int kSmallSlices = 16;
+constexpr int kSmallWarps = 8;
+
+static inline int small_slice_rows(int d) {
+  const int n = (d + 63) / 64 < kSmallSlices ? (d + 63) / 64 : kSmallSlices;
+  const int rs = (d + n - 1) / n;
+  return (rs + kSmallWarps - 1) / kSmallWarps * kSmallWarps;   // whole rows per warp
+}
+
+// workspace: the split weight [3d, E8] bf16, then (split K) fp32 partials
+// [ksplit, T, E]; a few tokens use it for their row-slice partials instead
 size_t route_ws_bytes(int64_t T, int d, int E) {
   const int sp = router_ksplit(T, d, E);
-  return al256r((size_t)3 * d * round8(E) * 2) + (sp > 1 ? al256r((size_t)sp * T * E * 4) : 0);
+  const size_t big = al256r((size_t)3 * d * round8(E) * 2) + (sp > 1 ? al256r((size_t)sp * T * E * 4) : 0);
+  if (T > kRouterSmallMaxT) return big;
+  const int rs = small_slice_rows(d), ns = (d + rs - 1) / rs;
+  const size_t small = al256r((size_t)ns * T * E * 4);
+  return big > small ? big : small;
 }
 
 // logits = sum of the split-K partials in split order, plus the bias
@@ -63,68 +83,144 @@ __global__ void split_router_weight_kernel(const float* __restrict__ wr, int d, 
   w_split[2 * plane + i] = __bfloat16_as_ushort(lo);
 }
 
-// A few tokens (decode): logits on the CUDA cores, one block per (token, eight
-// experts). Thread i accumulates rows i, i + 256, ... of x_t . W_r[:, e0:e0+8]
-// in fp32 (the products of a bf16 and an fp32 value), then the block adds the
-// 256 partial sums in a fixed tree order. No weight split, no split K.
-constexpr int kRouterSimtMaxT = 32;
-constexpr int kRouterSimtCols = 8;
-__global__ void __launch_bounds__(256) router_simt_kernel(const moe_bf16* __restrict__ x,
-                                                          const float* __restrict__ w_router,
-                                                          const float* __restrict__ bias, int d,
-                                                          int E, float* __restrict__ logits) {
-  __shared__ float part[kRouterSimtCols][256];
-  const int64_t t = blockIdx.y;
-  const int e0 = blockIdx.x * kRouterSimtCols;
-  const int ne = min(kRouterSimtCols, E - e0);
-  float acc[kRouterSimtCols];
+// Partial logits of a few tokens: CTA (chunk, slice, token group) multiplies
+// rows [slice * rs, slice * rs + rs) of W_r[:, chunk * 128 : + 128] with up to
+// eight tokens. Each warp takes rs / 8 consecutive rows, a lane four experts
+// (16-byte loads, eight rows' loads in flight), in fp32 from exact products of
+// bf16 and fp32 values; the warps' sums meet in shared memory in warp order.
+// part: [ns, T, E].
+__global__ void __launch_bounds__(kSmallWarps * 32) router_small_partial_kernel(
+    const moe_bf16* __restrict__ x, const float* __restrict__ w_router, int64_t T, int d, int E,
+    int rs, float* __restrict__ part) {
+  __shared__ float4 red[kSmallWarps][kSmallTok][32];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int e0 = blockIdx.x * kSmallCols + 4 * lane;
+  const int slice = blockIdx.y, t0 = blockIdx.z * kSmallTok;
+  const int nt = (int)(T - t0 < kSmallTok ? T - t0 : kSmallTok);
+  const int rpw = rs / kSmallWarps;
+  const int r0 = slice * rs + warp * rpw;
+  const bool vec = (E % 4) == 0 && (reinterpret_cast<uintptr_t>(w_router) & 15u) == 0;
+  float acc[kSmallTok][4];
 #pragma unroll
-  for (int j = 0; j < kRouterSimtCols; ++j) acc[j] = 0.f;
-  const moe_bf16* xr = x + t * d;
-  // four rows' loads in flight before their products are added (in row order)
-  for (int i0 = threadIdx.x; i0 < d; i0 += 4 * 256) {
-    float xv[4], wv[4][kRouterSimtCols];
+  for (int t = 0; t < kSmallTok; ++t) acc[t][0] = acc[t][1] = acc[t][2] = acc[t][3] = 0.f;
+  for (int rb = 0; rb < rpw; rb += 8) {
+    float4 wv[8];
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const int i = i0 + 256 * u;
-      xv[u] = i < d ? __bfloat162float(__ushort_as_bfloat16(xr[i])) : 0.f;
-      const float* wr = w_router + (int64_t)i * E + e0;
-#pragma unroll
-      for (int j = 0; j < kRouterSimtCols; ++j) wv[u][j] = (i < d && j < ne) ? wr[j] : 0.f;
+    for (int u = 0; u < 8; ++u) {
+      const int i = r0 + rb + u;
+      wv[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (rb + u < rpw && i < d) {
+        const float* src = w_router + (int64_t)i * E + e0;
+        if (vec && e0 + 3 < E) {
+          wv[u] = __ldg(reinterpret_cast<const float4*>(src));
+        } else {
+          if (e0 < E) wv[u].x = __ldg(src);
+          if (e0 + 1 < E) wv[u].y = __ldg(src + 1);
+          if (e0 + 2 < E) wv[u].z = __ldg(src + 2);
+          if (e0 + 3 < E) wv[u].w = __ldg(src + 3);
+        }
+      }
     }
 #pragma unroll
-    for (int u = 0; u < 4; ++u)
+    for (int u = 0; u < 8; ++u) {
+      const int i = r0 + rb + u;
+      if (rb + u >= rpw || i >= d) break;
 #pragma unroll
-      for (int j = 0; j < kRouterSimtCols; ++j) acc[j] = fmaf(xv[u], wv[u][j], acc[j]);
+      for (int t = 0; t < kSmallTok; ++t) {
+        if (t < nt) {
+          const float xv = __bfloat162float(__ushort_as_bfloat16(x[(t0 + t) * (int64_t)d + i]));
+          acc[t][0] = fmaf(xv, wv[u].x, acc[t][0]);
+          acc[t][1] = fmaf(xv, wv[u].y, acc[t][1]);
+          acc[t][2] = fmaf(xv, wv[u].z, acc[t][2]);
+          acc[t][3] = fmaf(xv, wv[u].w, acc[t][3]);
+        }
+      }
+    }
   }
 #pragma unroll
-  for (int j = 0; j < kRouterSimtCols; ++j) part[j][threadIdx.x] = acc[j];
+  for (int t = 0; t < kSmallTok; ++t)
+    red[warp][t][lane] = make_float4(acc[t][0], acc[t][1], acc[t][2], acc[t][3]);
   __syncthreads();
-  for (int w = 128; w > 0; w >>= 1) {
-    if (threadIdx.x < w) {
+  for (int o = threadIdx.x; o < nt * kSmallCols; o += blockDim.x) {
+    const int t = o / kSmallCols, col = o % kSmallCols, e = blockIdx.x * kSmallCols + col;
+    if (e >= E) continue;
+    float sum = 0.f;
 #pragma unroll
-      for (int j = 0; j < kRouterSimtCols; ++j)
-        part[j][threadIdx.x] += part[j][threadIdx.x + w];
-    }
-    __syncthreads();
+    for (int w = 0; w < kSmallWarps; ++w) sum += reinterpret_cast<const float*>(&red[w][t][0])[col];
+    part[((int64_t)slice * T + t0 + t) * E + e] = sum;
   }
-  if (threadIdx.x < ne)
-    logits[t * E + e0 + threadIdx.x] =
-        part[threadIdx.x][0] + (bias ? bias[e0 + threadIdx.x] : 0.f);
 }
 
+// One CTA per token: logits = the slices' partials in slice order + bias, then
+// the top-k with renormalised weights (topk.cuh) on them.
+template <int NV>
+__global__ void __launch_bounds__(256) router_small_topk_kernel(
+    const float* __restrict__ part, int ns, int64_t T, int E, int k,
+    const float* __restrict__ bias, const int32_t* __restrict__ forced,
+    float* __restrict__ logits, int32_t* __restrict__ topk_idx, float* __restrict__ topk_w,
+    int* status) {
+  __shared__ float lrow[kMaxExperts];
+  const int64_t t = blockIdx.x;
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    float sum = 0.f;
+    for (int s0 = 0; s0 < ns; s0 += 8) {
+      float v[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u)
+        v[u] = s0 + u < ns ? __ldg(part + ((int64_t)(s0 + u) * T + t) * E + e) : 0.f;
+#pragma unroll
+      for (int u = 0; u < 8; ++u) sum += v[u];
+    }
+    sum += bias ? bias[e] : 0.f;
+    lrow[e] = sum;
+    logits[t * E + e] = sum;
+  }
+  __syncthreads();
+  if (threadIdx.x < 32)
+    topk_warp<NV>(lrow, forced ? forced + t * k : nullptr, E, k, threadIdx.x, topk_idx + t * k,
+                  topk_w + t * k, status);
+}
+
+template <int NV>
+static void launch_small_topk(const float* part, int ns, int64_t T, int E, int k,
+                              const float* bias, const int32_t* forced, float* logits,
+                              int32_t* topk_idx, float* topk_w, int* status, cudaStream_t s) {
+  router_small_topk_kernel<NV><<<(unsigned)T, 256, 0, s>>>(part, ns, T, E, k, bias, forced, logits,
+                                                           topk_idx, topk_w, status);
+}
+
+// The whole routing of a few tokens: two launches (partials; logits + top-k).
+cudaError_t launch_route_small(const moe_bf16* x, const float* w_router, const float* bias,
+                               const int32_t* forced, int64_t T, int d, int E, int k,
+                               float* logits, int32_t* topk_idx, float* topk_w, void* ws,
+                               int* status, cudaStream_t s) {
+  const int rs = small_slice_rows(d), ns = (d + rs - 1) / rs;
+  float* part = static_cast<float*>(ws);
+  const dim3 grid((unsigned)((E + kSmallCols - 1) / kSmallCols), (unsigned)ns,
+                  (unsigned)((T + kSmallTok - 1) / kSmallTok));
+  timer_before(MOE_KERNEL_ROUTER_LOGITS, s);
+  router_small_partial_kernel<<<grid, kSmallWarps * 32, 0, s>>>(x, w_router, T, d, E, rs, part);
+  note_launches(1);
+  timer_after(MOE_KERNEL_ROUTER_LOGITS, s);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  timer_before(MOE_KERNEL_TOPK, s);
+  const int nv = (E + 31) / 32;
+  if (nv <= 1) launch_small_topk<1>(part, ns, T, E, k, bias, forced, logits, topk_idx, topk_w, status, s);
+  else if (nv <= 2) launch_small_topk<2>(part, ns, T, E, k, bias, forced, logits, topk_idx, topk_w, status, s);
+  else if (nv <= 4) launch_small_topk<4>(part, ns, T, E, k, bias, forced, logits, topk_idx, topk_w, status, s);
+  else if (nv <= 8) launch_small_topk<8>(part, ns, T, E, k, bias, forced, logits, topk_idx, topk_w, status, s);
+  else if (nv <= 16) launch_small_topk<16>(part, ns, T, E, k, bias, forced, logits, topk_idx, topk_w, status, s);
+  else launch_small_topk<kMaxExperts / 32>(part, ns, T, E, k, bias, forced, logits, topk_idx, topk_w, status, s);
+  note_launches(1);
+  timer_after(MOE_KERNEL_TOPK, s);
+  return cudaGetLastError();
+}
+
+// Many tokens: logits on the tensor cores (the top-k is its own launch).
 cudaError_t launch_router_logits(const moe_bf16* x, const float* w_router, const float* bias,
                                  int64_t T, int d, int E, float* logits, void* ws, int* status,
                                  cudaStream_t s) {
-  if (T <= kRouterSimtMaxT) {
-    timer_before(MOE_KERNEL_ROUTER_LOGITS, s);
-    router_simt_kernel<<<dim3((unsigned)((E + kRouterSimtCols - 1) / kRouterSimtCols),
-                             (unsigned)T),
-                        256, 0, s>>>(x, w_router, bias, d, E, logits);
-    note_launches(1);
-    timer_after(MOE_KERNEL_ROUTER_LOGITS, s);
-    return cudaGetLastError();
-  }
   const int E8 = round8(E);
   moe_bf16* w_split = static_cast<moe_bf16*>(ws);
   const int64_t n = (int64_t)d * E8;

@@ -37,6 +37,8 @@ CASES = {
     "k_equals_E": (64, 64, 64, 4, 4, 16, None, None),
     "one_token": (1, 128, 128, 8, 2, 16, None, None),
     "seven_tokens": (7, 96, 160, 8, 3, 256, None, None),
+    # three groups of eight tokens in the few-token router, E not a multiple of 4
+    "twentyfour_tokens": (24, 160, 192, 12, 3, 16, None, None),
     "wide_E": (256, 128, 64, 160, 6, 16, 1.1, 0.8),
 }
 
