@@ -30,7 +30,6 @@
 //   D   down products over W_down in the same way (groups: segment, column
 //       block of d); each stage's copy also brings its rows of A
 //   |
-//   |
 //   E1  the expert output of every pair = its group's partials (fixed order)
 //   |
 //   E   y[t] = sum_j w[t, j] * (expert output of pair (t, j)) in slot order,
