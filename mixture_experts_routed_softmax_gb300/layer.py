@@ -58,6 +58,8 @@ class Buffers:
     dw_down: Optional[torch.Tensor] = None
     dw_router: Optional[torch.Tensor] = None
     dbias: Optional[torch.Tensor] = None
+    # the one-launch decode forward's workspace (decode_buffers)
+    ws_decode: Optional[torch.Tensor] = None
     ws_route_bwd: Optional[torch.Tensor] = None
     # the input of the last forward (the router backward reads it)
     x: Optional[torch.Tensor] = None
@@ -207,8 +209,8 @@ class MoELayer:
             counts=none, offsets=none, dst_row=none, src_pair=none, xp=none, g=none,
             u=none, a=none, yp=none,
             y=torch.empty(T, d, dtype=BF16, **kw),
-            ws_permute=torch.empty(max(ws, 256), dtype=torch.uint8, **kw),
-            ws_route=none,
+            ws_permute=none, ws_route=none,
+            ws_decode=torch.empty(max(ws, 256), dtype=torch.uint8, **kw),
         )
 
     def decode_fwd(self, x, b: Buffers, forced_idx=None, stream=None):
@@ -218,7 +220,7 @@ class MoELayer:
         _lib.call("moe_decode_fwd", _p(x), _p(self.w_router), _p(self.bias), _p(forced_idx),
                   b.T, self.d, self.f, self.E, self.k, _p(self.w_gate), _p(self.w_up),
                   _p(self.w_down), _p(b.logits), _p(b.topk_idx), _p(b.topk_w), _p(b.y),
-                  _p(b.ws_permute), b.ws_permute.numel(), _stream(stream))
+                  _p(b.ws_decode), b.ws_decode.numel(), _stream(stream))
         return b.y
 
     def status(self, stream=None) -> int:
