@@ -83,7 +83,10 @@ typedef struct CUstream_st* moe_stream_t; /* the same handle as cudaStream_t */
  *  ws         moe_workspace_size(MOE_WS_ROUTE, ...) bytes, 256-byte aligned:
  *             W_r split into three bf16 parts (hi + mid + lo reproduce the fp32
  *             value) so the logits run on the tensor cores from exact products
- *             with fp32 accumulation.
+ *             with fp32 accumulation; for T <= 32 the logits run on the CUDA
+ *             cores instead (fp32 products of the bf16 and fp32 values, summed
+ *             in row slices, then the slices in order) and ws holds the
+ *             slices' partial sums.
  * Limits: 1 <= k <= min(E, 32); E <= 1024; d a multiple of 8.
  * ------------------------------------------------------------------------ */
 int moe_route(const moe_bf16* x, const float* w_router, const float* bias,
