@@ -40,6 +40,8 @@ CASES = {
     # three groups of eight tokens in the few-token router, E not a multiple of 4
     "twentyfour_tokens": (24, 160, 192, 12, 3, 16, None, None),
     "wide_E": (256, 128, 64, 160, 6, 16, 1.1, 0.8),
+    # the largest routing the ABI takes: 1024 experts, top-32 (most experts empty)
+    "max_E_and_k": (96, 64, 64, 1024, 32, 16, None, None),
 }
 
 
