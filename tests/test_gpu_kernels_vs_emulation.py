@@ -11,7 +11,6 @@ difference within 2e-3.
 """
 import numpy as np
 import pytest
-import torch
 
 import workloads
 from emulation import emulate
