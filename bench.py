@@ -482,7 +482,7 @@ def run_ours(args, rank, world, local_rank):
         "clocks": clocks,
         "e2e": e2e,
     }
-    if rank == 0 and not args.no_cpu_baseline:
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:   # the oracle beside N = 1 only
         tokens = min(args.cpu_tokens, wl.T)
         secs = oracle_sample(inp, wl, tokens)
         out["cpu_baseline"] = {"value": tokens / secs, "unit": UNIT, "cores": blas_threads(),
