@@ -154,10 +154,12 @@ int moe_permute_noalloc(const int32_t* topk_idx, int64_t T, int k, int E, int al
 /* ------------------------------------------------------------------------
  * moe_expert_fwd — grouped gate/up GEMM with fused SwiGLU, grouped down GEMM.
  * [HALO §Levers that help] one grouped expert matmul instead of a loop, fused
- * GLU; [PRL "Kept expert activations"] G and U are kept for backward.
+ * GLU; [PRL "Kept expert activations"] G and U are kept for backward (in
+ * fp32, so the backward's SwiGLU gradient starts from unrounded values).
  * Per expert e on its rows:  G = Xp.W_gate[e], U = Xp.W_up[e] (fp32
  * accumulation in tensor memory), A = silu(G)*U from the fp32 accumulators,
- * Yp = A.W_down[e] (times row_w[r] in fp32 when row_w is given).
+ * Yp = A.W_down[e] (times row_w[r] in fp32 when row_w is given), kept in
+ * fp32 so the combine's gather-sum rounds each output once.
  *
  *  xp [R_cap, d] bf16, offsets [E+1] int64 (from moe_permute)
  *  T, k: tokens and top-k of the routing (T*k pairs; sizes the tile schedule:
@@ -165,7 +167,8 @@ int moe_permute_noalloc(const int32_t* topk_idx, int64_t T, int k, int E, int al
  *  w_gate, w_up [E, d, f] bf16;  w_down [E, f, d] bf16
  *  row_w [R_cap] fp32 or NULL (NULL: Yp is the unscaled expert output, the
  *        layout the combine and moe_expert_bwd expect)
- *  g, u, a [R_cap, f] bf16 out;  yp [R_cap, d] bf16 out
+ *  g, u [R_cap, f] fp32 out;  a [R_cap, f] bf16 out (the down GEMM's operand);
+ *  yp [R_cap, d] fp32 out
  * Rows of every group, padding included, are written; padding rows come out
  * 0 because their xp rows are 0. Rows >= offsets[E] are not written.
  * Limits: d, f multiples of 8 (16-byte rows for TMA); E <= 1024.
@@ -173,7 +176,7 @@ int moe_permute_noalloc(const int32_t* topk_idx, int64_t T, int k, int E, int al
 int moe_expert_fwd(const moe_bf16* xp, const int64_t* offsets, const float* row_w,
                    int64_t T, int k, int E, int d, int f, int64_t R_cap,
                    const moe_bf16* w_gate, const moe_bf16* w_up, const moe_bf16* w_down,
-                   moe_bf16* g, moe_bf16* u, moe_bf16* a, moe_bf16* yp,
+                   float* g, float* u, moe_bf16* a, float* yp,
                    moe_stream_t stream);
 
 /* ------------------------------------------------------------------------
@@ -182,10 +185,10 @@ int moe_expert_fwd(const moe_bf16* xp, const int64_t* offsets, const float* row_
  * rows[dst_row[t*k+j]], accumulated in fp32 in slot order, rounded once to
  * bf16. With topk_w == NULL the weights are 1: that is the permute's
  * transpose (dx_t = sum_j dXp[dst_row]) used in backward.
- *  rows [R_cap, d] bf16 in;  dst_row [T*k] int32;  topk_w [T, k] fp32 or NULL
- *  out  [T, d] bf16 out
+ *  rows [R_cap, d] fp32 in (Yp or dXp);  dst_row [T*k] int32;
+ *  topk_w [T, k] fp32 or NULL;  out [T, d] bf16 out
  * ------------------------------------------------------------------------ */
-int moe_combine(const moe_bf16* rows, const int32_t* dst_row, const float* topk_w,
+int moe_combine(const float* rows, const int32_t* dst_row, const float* topk_w,
                 int64_t T, int k, int d, moe_bf16* out, moe_stream_t stream);
 
 /* ------------------------------------------------------------------------
@@ -194,30 +197,40 @@ int moe_combine(const moe_bf16* rows, const int32_t* dst_row, const float* topk_
  * [PRL "FP8 routed experts"] grouped dgrad and wgrad; [PRL "FP8 Mega MoE"]
  * K-grouped wgrad; [PRL "dispatch.type = mega_moe"] gradient of the top-k
  * weights. Steps:
- *   combine transpose:  dyp[r] = w(p) * dy[t(p)] (0 on padding rows),
- *                       d_topk_w[p] = <dy[t(p)], yp[r]>   (fp32, yp unscaled)
- *   down dgrad:         dA = dyp . W_down[e]^T, and in the same epilogue
- *                       dg = dA * U * silu'(G), du = dA * silu(G)
- *   gate/up dgrad:      dxp = dg . W_gate[e]^T + du . W_up[e]^T  (one K = 2f sum)
+ *   combine transpose:  dyg[r] = dy[t(p)] (the gathered rows, an exact copy),
+ *                       dyp[r] = w(p) * dy[t(p)] (bf16), both 0 on padding rows
+ *   down dgrad:         dAu = dyg . W_down[e]^T (fp32 accumulator), and in its
+ *                       epilogue dA = w(p) * dAu (so dA carries no bf16
+ *                       rounding of w * dy), dg = dA * U * silu'(G),
+ *                       du = dA * silu(G), and d_topk_w[p] = <dy[t(p)], Yu> as
+ *                       <dAu, silu(G) * U> from the fp32 G and U (the expert
+ *                       output of the unrounded A), summed over the column
+ *                       tiles in a fixed order
+ *   gate/up dgrad:      dxp = dg . W_gate[e]^T + du . W_up[e]^T  (one K = 2f
+ *                       sum, stored in fp32 so dx is rounded once)
  *   K-grouped wgrad:    dW_down[e] = A_e^T . dyp_e, dW_gate[e] = Xp_e^T . dg_e,
  *                       dW_up[e] = Xp_e^T . du_e   (an empty expert gets zeros)
  *  dy [T, d] bf16; src_pair [R_cap], dst_row [T*k] int32; topk_w [T, k] fp32;
- *  offsets [E+1]; xp, g, u, a, yp as written by moe_permute / moe_expert_fwd
- *  (row_w == NULL); weights as in moe_expert_fwd.
- *  Outputs: dyp [R_cap, d], dg, du [R_cap, f], dxp [R_cap, d] bf16 (row
- *  buffers, caller-owned, may be reused after the call); d_topk_w [T, k]
- *  fp32 (pairs dropped from the layout get no value); dw_gate, dw_up
- *  [E, d, f], dw_down [E, f, d] bf16 (overwritten).
+ *  offsets [E+1]; xp, a (bf16), g, u (fp32) as written by moe_permute /
+ *  moe_expert_fwd; weights as in moe_expert_fwd.
+ *  ws: moe_expert_bwd_workspace_size(R_cap, f) bytes, 256-byte aligned (the
+ *  top-k weight gradient's per-tile partials; scratch after the call).
+ *  Outputs (row buffers, caller-owned, may be reused after the call):
+ *  dyg, dyp [R_cap, d] bf16; dg, du [R_cap, f] bf16; dxp [R_cap, d] fp32;
+ *  d_topk_w [T, k] fp32 (pairs dropped from the layout get no value);
+ *  dw_gate, dw_up [E, d, f], dw_down [E, f, d] bf16 (overwritten).
  * ------------------------------------------------------------------------ */
 int moe_expert_bwd(const moe_bf16* dy, const int32_t* src_pair, const int32_t* dst_row,
                    const float* topk_w, const int64_t* offsets,
                    int64_t T, int k, int E, int d, int f, int64_t R_cap,
-                   const moe_bf16* xp, const moe_bf16* g, const moe_bf16* u,
-                   const moe_bf16* a, const moe_bf16* yp,
+                   const moe_bf16* xp, const float* g, const float* u, const moe_bf16* a,
                    const moe_bf16* w_gate, const moe_bf16* w_up, const moe_bf16* w_down,
-                   moe_bf16* dyp, moe_bf16* dg, moe_bf16* du, moe_bf16* dxp,
+                   moe_bf16* dyg, moe_bf16* dyp, moe_bf16* dg, moe_bf16* du, float* dxp,
                    float* d_topk_w, moe_bf16* dw_gate, moe_bf16* dw_up, moe_bf16* dw_down,
-                   moe_stream_t stream);
+                   void* ws, size_t ws_bytes, moe_stream_t stream);
+/* Workspace bytes of moe_expert_bwd for R_cap rows of ffn width f (0 for a
+ * size <= 0). */
+size_t moe_expert_bwd_workspace_size(int64_t R_cap, int f);
 
 /* ------------------------------------------------------------------------
  * moe_route_bwd — backward of the router.
@@ -236,14 +249,14 @@ int moe_expert_bwd(const moe_bf16* dy, const int32_t* src_pair, const int32_t* d
  *  x [T, d] bf16: the layer input (16-byte aligned);
  *  offsets, src_pair from moe_permute (with the same `align`).
  *  dx_inout [T, d] bf16 (added to, or overwritten when dxp is given);
- *  dxp [R_cap, d] bf16 or NULL (from moe_expert_bwd); dst_row [T*k] int32
+ *  dxp [R_cap, d] fp32 or NULL (from moe_expert_bwd); dst_row [T*k] int32
  *  (required with dxp); dw_router [d, E] fp32 out; dbias [E] fp32 out or NULL.
  *  ws: moe_workspace_size(MOE_WS_ROUTE_BWD, ...) bytes, 256-byte aligned.
  * ------------------------------------------------------------------------ */
 int moe_route_bwd(const float* d_topk_w, const float* topk_w, const int32_t* topk_idx,
                   const float* w_router, const int64_t* offsets, const int32_t* src_pair,
                   const moe_bf16* x, int64_t T, int d, int E, int k, int align,
-                  moe_bf16* dx_inout, const moe_bf16* dxp, const int32_t* dst_row,
+                  moe_bf16* dx_inout, const float* dxp, const int32_t* dst_row,
                   float* dw_router, float* dbias,
                   void* ws, size_t ws_bytes, moe_stream_t stream);
 

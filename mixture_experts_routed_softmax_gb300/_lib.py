@@ -23,8 +23,9 @@ SIGNATURES = {
                             _P]),
     "moe_combine": (_I, [_P, _P, _P, _I64, _I, _I, _P, _P]),
     "moe_expert_bwd": (_I, [_P, _P, _P, _P, _P, _I64, _I, _I, _I, _I, _I64,
-                            _P, _P, _P, _P, _P, _P, _P, _P,
-                            _P, _P, _P, _P, _P, _P, _P, _P, _P]),
+                            _P, _P, _P, _P, _P, _P, _P,
+                            _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
+    "moe_expert_bwd_workspace_size": (_SZ, [_I64, _I]),
     "moe_route_bwd": (_I, [_P, _P, _P, _P, _P, _P, _P, _I64, _I, _I, _I, _I,
                            _P, _P, _P, _P, _P, _P, _SZ, _P]),
     "moe_decode_fwd": (_I, [_P, _P, _P, _P, _I64, _I, _I, _I, _I, _P, _P, _P,

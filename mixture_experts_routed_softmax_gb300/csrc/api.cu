@@ -218,8 +218,8 @@ static int check_expert_dims(int E, int d, int f, int64_t R_cap) {
 
 int moe_expert_fwd(const moe_bf16* xp, const int64_t* offsets, const float* row_w, int64_t T,
                    int k, int E, int d, int f, int64_t R_cap, const moe_bf16* w_gate,
-                   const moe_bf16* w_up, const moe_bf16* w_down, moe_bf16* g, moe_bf16* u,
-                   moe_bf16* a, moe_bf16* yp, moe_stream_t stream) {
+                   const moe_bf16* w_up, const moe_bf16* w_down, float* g, float* u,
+                   moe_bf16* a, float* yp, moe_stream_t stream) {
   if (!xp || !offsets || !w_gate || !w_up || !w_down || !g || !u || !a || !yp) return MOE_ERR_ARG;
   if (T < 0 || k <= 0 || k > E) return MOE_ERR_ARG;
   int rc = check_expert_dims(E, d, f, R_cap);
@@ -238,7 +238,7 @@ int moe_expert_fwd(const moe_bf16* xp, const int64_t* offsets, const float* row_
   return cuda_code(e);
 }
 
-int moe_combine(const moe_bf16* rows, const int32_t* dst_row, const float* topk_w, int64_t T,
+int moe_combine(const float* rows, const int32_t* dst_row, const float* topk_w, int64_t T,
                 int k, int d, moe_bf16* out, moe_stream_t stream) {
   if (!rows || (T > 0 && (!dst_row || !out))) return MOE_ERR_ARG;
   if (T < 0 || k <= 0 || d <= 0) return MOE_ERR_ARG;
@@ -251,36 +251,48 @@ int moe_combine(const moe_bf16* rows, const int32_t* dst_row, const float* topk_
 
 int moe_expert_bwd(const moe_bf16* dy, const int32_t* src_pair, const int32_t* dst_row,
                    const float* topk_w, const int64_t* offsets, int64_t T, int k, int E, int d,
-                   int f, int64_t R_cap, const moe_bf16* xp, const moe_bf16* g,
-                   const moe_bf16* u, const moe_bf16* a, const moe_bf16* yp,
+                   int f, int64_t R_cap, const moe_bf16* xp, const float* g,
+                   const float* u, const moe_bf16* a,
                    const moe_bf16* w_gate, const moe_bf16* w_up, const moe_bf16* w_down,
-                   moe_bf16* dyp, moe_bf16* dg, moe_bf16* du, moe_bf16* dxp, float* d_topk_w,
-                   moe_bf16* dw_gate, moe_bf16* dw_up, moe_bf16* dw_down, moe_stream_t stream) {
-  if (!src_pair || !offsets || !xp || !g || !u || !a || !yp || !w_gate || !w_up || !w_down ||
-      !dyp || !dg || !du || !dxp || !dw_gate || !dw_up || !dw_down ||
+                   moe_bf16* dyg, moe_bf16* dyp, moe_bf16* dg, moe_bf16* du, float* dxp,
+                   float* d_topk_w, moe_bf16* dw_gate, moe_bf16* dw_up, moe_bf16* dw_down,
+                   void* ws, size_t ws_bytes, moe_stream_t stream) {
+  if (!src_pair || !offsets || !xp || !g || !u || !a || !w_gate || !w_up || !w_down ||
+      !dyg || !dyp || !dg || !du || !dxp || !dw_gate || !dw_up || !dw_down ||
       (T > 0 && (!dy || !dst_row || !topk_w || !d_topk_w)))
     return MOE_ERR_ARG;
   if (T < 0 || k <= 0 || k > E) return MOE_ERR_ARG;
   int rc = check_expert_dims(E, d, f, R_cap);
   if (rc) return rc;
   if (R_cap < T * k) return MOE_ERR_CAPACITY;
+  if (!ws || ws_bytes < moe_expert_bwd_workspace_size(R_cap, f) ||
+      (reinterpret_cast<uintptr_t>(ws) & 255u))
+    return MOE_ERR_ARG;
   for (const void* p : {(const void*)dy, (const void*)xp, (const void*)g, (const void*)u,
-                        (const void*)a, (const void*)yp, (const void*)w_gate, (const void*)w_up,
-                        (const void*)w_down, (const void*)dyp, (const void*)dg, (const void*)du,
-                        (const void*)dxp, (const void*)dw_gate, (const void*)dw_up,
+                        (const void*)a, (const void*)w_gate, (const void*)w_up,
+                        (const void*)w_down, (const void*)dyg, (const void*)dyp, (const void*)dg,
+                        (const void*)du, (const void*)dxp, (const void*)dw_gate, (const void*)dw_up,
                         (const void*)dw_down})
     if (!aligned16(p)) return MOE_ERR_ARG;
   int* st = device_status_ptr();
   if (!st) return MOE_ERR_CUDA;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   GroupedDims gd{offsets, E, d, f, R_cap, T * k, src_pair};
-  cudaError_t e = launch_combine_bwd(dy, yp, src_pair, topk_w, offsets, T, k, E, d, R_cap, dyp,
-                                     d_topk_w, s);
-  if (e == cudaSuccess) e = launch_down_dgrad(gd, dyp, w_down, g, u, dg, du, st, s);
+  float* part = static_cast<float*>(ws);
+  cudaError_t e = launch_combine_bwd(dy, src_pair, topk_w, offsets, k, E, d, R_cap, dyg, dyp, s);
+  if (e == cudaSuccess)
+    e = launch_down_dgrad(gd, dyg, topk_w, w_down, g, u, dg, du, part, st, s);
+  if (e == cudaSuccess)
+    e = launch_dtw_finalize(part, down_dgrad_dtw_slots(f), dst_row, T * k, d_topk_w, s);
   if (e == cudaSuccess) e = launch_gateup_dgrad(gd, dg, du, w_gate, w_up, dxp, st, s);
   if (e == cudaSuccess) e = launch_wgrad_down(gd, a, dyp, dw_down, st, s);
   if (e == cudaSuccess) e = launch_wgrad_gateup(gd, xp, dg, du, dw_gate, dw_up, st, s);
   return cuda_code(e);
+}
+
+size_t moe_expert_bwd_workspace_size(int64_t R_cap, int f) {
+  if (R_cap <= 0 || f <= 0) return 0;
+  return (size_t)R_cap * down_dgrad_dtw_slots(f) * sizeof(float);
 }
 
 size_t moe_decode_workspace_size(int64_t T, int d, int f, int E, int k) {
@@ -316,7 +328,7 @@ int moe_decode_fwd(const moe_bf16* x, const float* w_router, const float* bias,
 int moe_route_bwd(const float* d_topk_w, const float* topk_w, const int32_t* topk_idx,
                   const float* w_router, const int64_t* offsets, const int32_t* src_pair,
                   const moe_bf16* x, int64_t T, int d, int E, int k, int align,
-                  moe_bf16* dx_inout, const moe_bf16* dxp, const int32_t* dst_row,
+                  moe_bf16* dx_inout, const float* dxp, const int32_t* dst_row,
                   float* dw_router, float* dbias, void* ws, size_t ws_bytes,
                   moe_stream_t stream) {
   if (!w_router || !offsets || !src_pair || !dw_router ||

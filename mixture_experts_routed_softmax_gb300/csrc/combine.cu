@@ -11,9 +11,10 @@
 
 namespace moe {
 
-// out[t] = sum_j w[t, j] * rows[dst_row[t*k + j]]  (slot order, fp32); one warp
-// per (token, 256 columns), so a handful of tokens still spreads over many warps
-__global__ void __launch_bounds__(256) combine_kernel(const moe_bf16* __restrict__ rows,
+// out[t] = sum_j w[t, j] * rows[dst_row[t*k + j]]  (fp32 rows, slot order, fp32
+// sum, rounded to bf16 once); one warp per (token, 256 columns), so a handful
+// of tokens still spreads over many warps
+__global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ rows,
                                                       const int32_t* __restrict__ dst_row,
                                                       const float* __restrict__ topk_w,
                                                       int64_t T, int k, int d,
@@ -32,9 +33,10 @@ __global__ void __launch_bounds__(256) combine_kernel(const moe_bf16* __restrict
     my_w = topk_w ? topk_w[t * k + lane] : 1.f;
   }
   float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-  // the rows of up to four slots are loaded together, then summed in slot order
+  // the 8-column pieces of up to four slots' rows are loaded together, then
+  // summed in slot order
   for (int j0 = 0; j0 < k; j0 += 4) {
-    uint4 rv[4];
+    float4 rv[4][2];
     float wv[4];
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
@@ -42,22 +44,27 @@ __global__ void __launch_bounds__(256) combine_kernel(const moe_bf16* __restrict
       const int32_t r = __shfl_sync(0xFFFFFFFFu, my_r, j & 31);
       wv[q] = __shfl_sync(0xFFFFFFFFu, my_w, j & 31);
       const bool ok = j < k && r >= 0 && v < nv;
-      rv[q] = ok ? reinterpret_cast<const uint4*>(rows + (int64_t)r * d)[v]
-                 : make_uint4(0u, 0u, 0u, 0u);
-      if (!ok) wv[q] = 0.f;
+      if (ok) {
+        const float4* src = reinterpret_cast<const float4*>(rows + (int64_t)r * d) + 2 * v;
+        rv[q][0] = src[0];
+        rv[q][1] = src[1];
+      } else {
+        rv[q][0] = rv[q][1] = make_float4(0.f, 0.f, 0.f, 0.f);
+        wv[q] = 0.f;
+      }
     }
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
-      float f[8];
-      unpack8(rv[q], f);
-#pragma unroll
-      for (int i = 0; i < 8; ++i) acc[i] = fmaf(wv[q], f[i], acc[i]);
+      acc[0] = fmaf(wv[q], rv[q][0].x, acc[0]); acc[1] = fmaf(wv[q], rv[q][0].y, acc[1]);
+      acc[2] = fmaf(wv[q], rv[q][0].z, acc[2]); acc[3] = fmaf(wv[q], rv[q][0].w, acc[3]);
+      acc[4] = fmaf(wv[q], rv[q][1].x, acc[4]); acc[5] = fmaf(wv[q], rv[q][1].y, acc[5]);
+      acc[6] = fmaf(wv[q], rv[q][1].z, acc[6]); acc[7] = fmaf(wv[q], rv[q][1].w, acc[7]);
     }
   }
   if (v < nv) reinterpret_cast<uint4*>(out + t * d)[v] = pack8(acc);
 }
 
-cudaError_t launch_combine(const moe_bf16* rows, const int32_t* dst_row, const float* topk_w,
+cudaError_t launch_combine(const float* rows, const int32_t* dst_row, const float* topk_w,
                            int64_t T, int k, int d, moe_bf16* out, cudaStream_t s) {
   timer_before(MOE_KERNEL_COMBINE, s);
   const int64_t warps = T * (((int64_t)d / 8 + 31) / 32);
@@ -67,69 +74,92 @@ cudaError_t launch_combine(const moe_bf16* rows, const int32_t* dst_row, const f
   return cudaGetLastError();
 }
 
-// Transpose of the weighted combine, one warp per row r of the layout:
-//   dyp[r] = w(p) * dy[t(p)],  d_topk_w[p] = <dy[t(p)], yp[r]>  (fp32)
-// with p = src_pair[r]; padding rows get dyp = 0. Rows >= offsets[E] are
-// not touched.
+// Transpose of the weighted combine, one warp per row r of the layout, with
+// p = src_pair[r] and t its token:
+//   dyg[r] = dy[t]                 (the gathered upstream gradient, unscaled:
+//                                   the down dgrad's operand; the score is
+//                                   applied there to the fp32 accumulator)
+//   dyp[r] = w(p) * dy[t]          (bf16: the weight gradient's operand)
+// Padding rows get dyg = dyp = 0. Rows >= offsets[E] are not touched. The
+// gradient of the top-k weights, <dy[t], Yu>, is taken in the down dgrad's
+// epilogue instead, where dy . W_down^T and the unrounded A meet.
 __global__ void __launch_bounds__(256) combine_bwd_kernel(
-    const moe_bf16* __restrict__ dy, const moe_bf16* __restrict__ yp,
-    const int32_t* __restrict__ src_pair, const float* __restrict__ topk_w,
-    const int64_t* __restrict__ offsets, int k, int E, int d, int64_t R_cap,
-    moe_bf16* __restrict__ dyp, float* __restrict__ d_topk_w) {
+    const moe_bf16* __restrict__ dy, const int32_t* __restrict__ src_pair,
+    const float* __restrict__ topk_w, const int64_t* __restrict__ offsets, int k, int E, int d,
+    int64_t R_cap, moe_bf16* __restrict__ dyg, moe_bf16* __restrict__ dyp) {
   const int lane = threadIdx.x & 31;
   const int64_t r = (int64_t)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
   if (r >= R_cap || r >= offsets[E]) return;
   const int nv = d / 8;
-  uint4* out = reinterpret_cast<uint4*>(dyp + r * d);
+  uint4* outg = reinterpret_cast<uint4*>(dyg + r * d);
+  uint4* outp = reinterpret_cast<uint4*>(dyp + r * d);
   const int32_t p = src_pair[r];
   if (p < 0) {
-    for (int v = lane; v < nv; v += 32) out[v] = make_uint4(0u, 0u, 0u, 0u);
+    for (int v = lane; v < nv; v += 32) {
+      outg[v] = make_uint4(0u, 0u, 0u, 0u);
+      outp[v] = make_uint4(0u, 0u, 0u, 0u);
+    }
     return;
   }
   const int64_t t = p / k;
   const float w = topk_w[p];
   const uint4* g = reinterpret_cast<const uint4*>(dy + t * d);
-  const uint4* y = reinterpret_cast<const uint4*>(yp + r * d);
-  float dot = 0.f;
-  // four 16-byte pieces of each row in flight per lane, then used in order
+  // four 8-column pieces of the row in flight per lane
   for (int v0 = lane; v0 < nv; v0 += 128) {
-    uint4 gv[4], yv[4];
+    uint4 gv[4];
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
       const int v = v0 + 32 * u;
-      if (v < nv) { gv[u] = g[v]; yv[u] = y[v]; }
+      if (v < nv) gv[u] = g[v];
     }
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
       const int v = v0 + 32 * u;
       if (v >= nv) break;
-      float a[8], b[8], o[8];
+      float a[8], o[8];
       unpack8(gv[u], a);
-      unpack8(yv[u], b);
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        dot = fmaf(a[i], b[i], dot);
-        o[i] = w * a[i];
-      }
-      out[v] = pack8(o);
+      for (int i = 0; i < 8; ++i) o[i] = w * a[i];
+      outg[v] = gv[u];
+      outp[v] = pack8(o);
     }
   }
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) dot += __shfl_xor_sync(0xFFFFFFFFu, dot, off);
-  if (lane == 0) d_topk_w[p] = dot;
 }
 
-cudaError_t launch_combine_bwd(const moe_bf16* dy, const moe_bf16* yp, const int32_t* src_pair,
-                               const float* topk_w, const int64_t* offsets, int64_t T, int k,
-                               int E, int d, int64_t R_cap, moe_bf16* dyp, float* d_topk_w,
-                               cudaStream_t s) {
-  (void)T;
+cudaError_t launch_combine_bwd(const moe_bf16* dy, const int32_t* src_pair, const float* topk_w,
+                               const int64_t* offsets, int k, int E, int d, int64_t R_cap,
+                               moe_bf16* dyg, moe_bf16* dyp, cudaStream_t s) {
   timer_before(MOE_KERNEL_COMBINE_BWD, s);
-  combine_bwd_kernel<<<(unsigned)((R_cap + 7) / 8), 256, 0, s>>>(dy, yp, src_pair, topk_w,
-                                                                 offsets, k, E, d, R_cap, dyp,
-                                                                 d_topk_w);
+  combine_bwd_kernel<<<(unsigned)((R_cap + 7) / 8), 256, 0, s>>>(dy, src_pair, topk_w, offsets,
+                                                                 k, E, d, R_cap, dyg, dyp);
   note_launches(1);
   timer_after(MOE_KERNEL_COMBINE_BWD, s);
+  return cudaGetLastError();
+}
+
+// d_topk_w[p] = sum_{s < slots} part[dst_row[p]][s], in slot order (the down
+// dgrad's per-tile partials of <dy . W_down^T, A>); pairs dropped from the
+// layout (dst_row = -1) are left untouched.
+__global__ void __launch_bounds__(256) dtw_finalize_kernel(const float* __restrict__ part,
+                                                           int slots,
+                                                           const int32_t* __restrict__ dst_row,
+                                                           int64_t P, float* __restrict__ d_topk_w) {
+  const int64_t p = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (p >= P) return;
+  const int32_t r = dst_row[p];
+  if (r < 0) return;
+  const float* q = part + (int64_t)r * slots;
+  float a = 0.f;
+  for (int s = 0; s < slots; ++s) a += q[s];
+  d_topk_w[p] = a;
+}
+
+cudaError_t launch_dtw_finalize(const float* part, int slots, const int32_t* dst_row, int64_t P,
+                                float* d_topk_w, cudaStream_t s) {
+  if (P == 0) return cudaSuccess;
+  dtw_finalize_kernel<<<(unsigned)((P + 255) / 256), 256, 0, s>>>(part, slots, dst_row, P,
+                                                                  d_topk_w);
+  note_launches(1);
   return cudaGetLastError();
 }
 

@@ -4,24 +4,30 @@
 // a per-expert loop, with the GLU fused. prime-rl PR #3885 (DeepSeek-V4.1
 // Flash perf work), §Changes: grouped forward, dgrad and wgrad GEMMs ("FP8
 // routed experts"), the weight gradient as a K-grouped GEMM and the bf16
-// gate/up output kept for backward ("FP8 Mega MoE"), tasks ordered
-// expert-major so each expert's weights are read about once.
+// gate/up output kept for backward ("FP8 Mega MoE").
 //
 // One persistent, warp-specialised kernel template serves all six GEMMs:
-//   warp 0     TMA producer: tiles of A and B into a 4-stage shared-memory ring
-//   warp 1     MMA issuer: tcgen05.mma 128 x N x 16 (bf16 in, fp32 in tensor
-//              memory), two accumulator buffers so the epilogue of one tile
-//              overlaps the main loop of the next
-//   warp 2     tensor-memory allocator
-//   warps 4-7  epilogue: tcgen05.ld of the accumulator (one row per thread),
-//              the fused element-wise step, bf16 stores with row/col masks
+//   warp 0      TMA producer: tiles of A and B into a shared-memory ring of
+//               as many stages as fit 192 KiB (4 of 48 KiB, 6 of 32 KiB)
+//   warp 1      MMA issuer: tcgen05.mma 128 x N x 16 (bf16 in, fp32 in tensor
+//               memory), two accumulator buffers so the epilogue of one tile
+//               overlaps the main loop of the next
+//   warp 2      tensor-memory allocator
+//   warps 4-11  epilogue, two warpgroups (each half of the tile's columns):
+//               tcgen05.ld of the accumulator (one row per thread), the fused
+//               element-wise step, TMA stores staged through a 3-slot ring
 // Kinds:
 //   GateUpFwd    [G | U] = Xp . [W_gate[e] | W_up[e]]  (two accumulators),
-//                epilogue A = silu(G) * U, stores G, U, A       (M-grouped)
-//   DownFwd      Yp = A . W_down[e]  (optionally * row_w)       (M-grouped)
-//   DownDgrad    dA = dYp . W_down[e]^T, epilogue dG = dA*U*silu'(G),
-//                dU = dA*silu(G)                                (M-grouped)
-//   GateUpDgrad  dXp = dG . W_gate[e]^T + dU . W_up[e]^T (two K segments)
+//                epilogue A = silu(G) * U; stores G, U (fp32, for the
+//                backward's SwiGLU gradient) and A (bf16)      (M-grouped)
+//   DownFwd      Yp = A . W_down[e]  (optionally * row_w), fp32  (M-grouped)
+//   DownDgrad    dAu = dY[t(r)] . W_down[e]^T from the unscaled gathered rows
+//                of dY; epilogue dA = w(r) * dAu (the pair's score on the
+//                fp32 accumulator), dG = dA*U*silu'(G), dU = dA*silu(G), and
+//                the row's share of the top-k weight gradient
+//                <dAu, silu(G)*U> (= <dY, A.W_down> with A unrounded), one
+//                fp32 partial per (n-tile, column half)         (M-grouped)
+//   GateUpDgrad  dXp = dG . W_gate[e]^T + dU . W_up[e]^T (two K segments), fp32
 //   WgradDown    dW_down[e] = A_e^T . dYp_e                     (K-grouped)
 //   WgradGateUp  dW_gate[e] = Xp_e^T . dG_e, dW_up[e] = Xp_e^T . dU_e
 // "M-grouped": expert e's output rows are its rows [offsets[e], offsets[e+1])
@@ -94,11 +100,16 @@ struct Geo {
 constexpr int kTmemCols = 512;                            // 2 accumulator buffers x 256 columns
 constexpr int kEpiWarps = 8;                              // two warpgroups, each half the columns
 constexpr int kThreads = 128 + 32 * kEpiWarps;
-// Epilogues stage their bf16 outputs through shared memory for TMA stores: per
-// epilogue warpgroup, 128 rows x 16 columns of each of up to three outputs (4 KiB each)
-constexpr int kStagePerGroup = 3 * 4096;
+// Epilogues stage their outputs through shared memory for TMA stores: per
+// epilogue warpgroup a ring of kStgSlots slots, each [128 rows x 32 bytes]
+// (16 bf16 or 8 fp32 columns of one output)
+constexpr int kStgSlots = 3;
+constexpr int kSlotBytes = 128 * 32;
+constexpr int kStagePerGroup = kStgSlots * kSlotBytes;
 constexpr int kStageOutBytes = (kEpiWarps / 4) * kStagePerGroup;
-constexpr int kTstartBytes = (4 * (kMaxExperts + 1) + 127) & ~127;
+// the tile table, rounded up so the staging slots after it sit on 1 KiB
+// boundaries (the 32-byte swizzle pattern is taken from address bits 4-7)
+constexpr int kTstartBytes = (4 * (kMaxExperts + 1) + 1023) & ~1023;
 constexpr int kSmemBytes = kRingBytes + 1024 /*bars*/ + kTstartBytes + kStageOutBytes + 1024;
 
 struct GemmArgs {
@@ -107,12 +118,15 @@ struct GemmArgs {
   int M, N;        // K-grouped: per-expert output is M x N. M-grouped: N output columns
   int nk_seg;      // M-grouped: k-steps per K segment
   int64_t R_cap;
-  moe_bf16* out0;
-  moe_bf16* out1;
-  moe_bf16* out2;
-  const moe_bf16* in0;
-  const moe_bf16* in1;
+  void* out0;      // bf16, or fp32 (G, U of GateUpFwd; DownFwd; GateUpDgrad)
+  void* out1;
+  void* out2;
+  const float* in0;          // DownDgrad: the saved G, U (fp32)
+  const float* in1;
   const float* row_w;
+  const float* pair_w;       // DownDgrad: the score of each pair ([T*k], via src_pair)
+  float* dtw_part;           // DownDgrad: [R_cap][dtw_slots] partials of the top-k weight grad
+  int dtw_slots;             // 2 per n-tile (one per epilogue warpgroup)
   // RouterLogits: fp32 output, bias, number of K segments and the K offset of each in B
   float* outf;
   const float* bias;
@@ -121,7 +135,7 @@ struct GemmArgs {
   int ksplit;         // RouterLogits: K split into this many chunks (1: write logits + bias)
   int ksteps_split;   // k-steps per chunk
   int bn;             // single-accumulator kinds: tile width (multiple of 16, <= 256)
-  const int32_t* src_pair;   // K-grouped: pair of each layout row (-1: padding), or NULL
+  const int32_t* src_pair;   // pair of each layout row (-1: padding): K-grouped (or NULL), DownDgrad
   int* status;
 };
 
@@ -206,52 +220,83 @@ __device__ __forceinline__ bool group_all(int group, bool ok) {
   return r != 0;
 }
 
-// Writes 16*NH columns (packed bf16 pairs pk[o][0..8*NH-1]) of NOUT outputs for
-// this thread's row. When the whole 128-row tile belongs to its group
-// (tile_tma), the warpgroup stages each 16-column slice of each output in
-// shared memory, [128 rows x 16 columns], and one thread issues one TMA store
-// per output (coordinates {col, m0} or {col, m0, e}; the maps clip at the
-// tensor edge). Otherwise every thread stores its own row with masks. Columns
-// from lim on (the tile's end, or N) are not written; N is the row stride.
-template <int NOUT, bool K3D, int NH = 2>
-__device__ __forceinline__ void put_chunk(const uint32_t (&pk)[NOUT][8 * NH], uint8_t* stg,
-                                          const CUtensorMap* const* maps, moe_bf16* const* outs,
-                                          bool tile_tma, bool row_ok, int64_t row, int rloc,
-                                          int col, int N, int lim, int m0, int e, int group,
-                                          bool leader, uint64_t policy) {
+// Writes one 32-byte slice (16 bf16 or 8 fp32 columns, v[o][0..1]) of each of
+// NOUT outputs for this thread's row. When the whole 128-row tile belongs to
+// its group (tile_tma), the warpgroup stages the slices in shared memory, one
+// slot of [128 rows x 32 bytes] per output, and one thread issues one TMA
+// store per slot (coordinates {col, m0} or {col, m0, e}; the maps clip at
+// the tensor edge), each its own bulk group. The slots rotate through a ring
+// of kStgSlots, advancing only with stores issued, so a slot is written again
+// as soon as the store that last used it has read it, while the later stores
+// are still in flight. Rows are
+// stored with the maps' 32-byte swizzle (the two 16-byte halves of rows 4-7
+// of every 8 swapped), so the warp's shared-memory writes hit distinct banks.
+// Otherwise every thread stores its own row with masks. Columns from lim on
+// (the tile's end, or N) are not written; N is the row stride; esz[o] the
+// element size of output o (every output's slice starts at column col).
+template <int NOUT, bool K3D>
+__device__ __forceinline__ void put_slice(const uint4 (&v)[NOUT][2], uint8_t* stg, int& slot,
+                                          const CUtensorMap* const* maps, uint8_t* const* outs,
+                                          const int* esz, bool tile_tma, bool row_ok, int64_t row,
+                                          int rloc, int col, int N, int lim, int m0, int e,
+                                          int group, bool leader, uint64_t policy) {
+  static_assert(NOUT <= kStgSlots, "one slot per output");
   if (tile_tma) {
+    // the stores that last used these NOUT slots have read them
+    if (leader) bulk_wait_read_n<kStgSlots - NOUT>();
+    group_sync(group);
+    const int sw = ((rloc >> 2) & 1) * 16;
 #pragma unroll
-    for (int h = 0; h < NH; ++h) {
-      if (leader) bulk_wait_read();      // the previous slice's stores have read the buffer
-      group_sync(group);
+    for (int o = 0; o < NOUT; ++o) {
+      int so = slot + o;
+      so = so >= kStgSlots ? so - kStgSlots : so;
+      uint8_t* d = stg + so * kSlotBytes + rloc * 32;
+      *reinterpret_cast<uint4*>(d + sw) = v[o][0];
+      *reinterpret_cast<uint4*>(d + (16 - sw)) = v[o][1];
+    }
+    fence_async_smem();
+    group_sync(group);
+    if (leader && col < lim) {
 #pragma unroll
       for (int o = 0; o < NOUT; ++o) {
-        uint4* d = reinterpret_cast<uint4*>(stg + o * 4096 + rloc * 32);
-        d[0] = make_uint4(pk[o][8 * h + 0], pk[o][8 * h + 1], pk[o][8 * h + 2], pk[o][8 * h + 3]);
-        d[1] = make_uint4(pk[o][8 * h + 4], pk[o][8 * h + 5], pk[o][8 * h + 6], pk[o][8 * h + 7]);
-      }
-      fence_async_smem();
-      group_sync(group);
-      if (leader && col + 16 * h < lim) {
-#pragma unroll
-        for (int o = 0; o < NOUT; ++o) {
-          if constexpr (K3D)
-            tma_store_3d(maps[o], smem_u32(stg + o * 4096), col + 16 * h, m0, e, policy);
-          else
-            tma_store_2d(maps[o], smem_u32(stg + o * 4096), col + 16 * h, m0, policy);
-        }
+        int so = slot + o;
+        so = so >= kStgSlots ? so - kStgSlots : so;
+        const uint32_t src = smem_u32(stg + so * kSlotBytes);
+        if constexpr (K3D)
+          tma_store_3d(maps[o], src, col, m0, e, policy);
+        else
+          tma_store_2d(maps[o], src, col, m0, policy);
         bulk_commit();
       }
     }
+    // the ring advances with the stores actually issued (col and lim are the
+    // same in every thread of the warpgroup), so the slot rewritten next was
+    // last read by the store kStgSlots commits back
+    if (col < lim) {
+      slot += NOUT;
+      slot = slot >= kStgSlots ? slot - kStgSlots : slot;
+    }
   } else if (row_ok) {
 #pragma unroll
-    for (int v = 0; v < 2 * NH; ++v) {
-      if (col + 8 * v >= lim) break;
+    for (int o = 0; o < NOUT; ++o) {
+      const int per16 = 16 / esz[o];   // columns per 16-byte piece
 #pragma unroll
-      for (int o = 0; o < NOUT; ++o)
-        *reinterpret_cast<uint4*>(outs[o] + row * N + col + 8 * v) =
-            make_uint4(pk[o][4 * v + 0], pk[o][4 * v + 1], pk[o][4 * v + 2], pk[o][4 * v + 3]);
+      for (int h = 0; h < 2; ++h) {
+        const int c = col + per16 * h;
+        if (c < lim) *reinterpret_cast<uint4*>(outs[o] + (row * N + c) * esz[o]) = v[o][h];
+      }
     }
+  }
+}
+
+// the 16-byte halves of a 32-byte slice of packed bf16 pairs pk[8 * h .. 8 * h + 7]
+template <int NOUT, int W>
+__device__ __forceinline__ void slice_of(const uint32_t (&pk)[NOUT][W], int h,
+                                         uint4 (&v)[NOUT][2]) {
+#pragma unroll
+  for (int o = 0; o < NOUT; ++o) {
+    v[o][0] = make_uint4(pk[o][8 * h + 0], pk[o][8 * h + 1], pk[o][8 * h + 2], pk[o][8 * h + 3]);
+    v[o][1] = make_uint4(pk[o][8 * h + 4], pk[o][8 * h + 5], pk[o][8 * h + 6], pk[o][8 * h + 7]);
   }
 }
 
@@ -633,6 +678,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr int kHalf = T::BN / 2;
     const int c_lo = ((warp - 4) >> 2) * kHalf;
     const int c_hi = c_lo + kHalf < bn ? c_lo + kHalf : bn;
+    const int group = (warp - 4) >> 2;
+    const bool leader = (wq == 0 && lane == 0);
+    uint8_t* stg = stage_out + group * kStagePerGroup;
+    int slot = 0;   // next staging slot: the same in every thread of the warpgroup
+    const CUtensorMap* maps[3] = {&mapO0, &mapO1, &mapO2};
+    uint8_t* outs[3] = {static_cast<uint8_t*>(args.out0), static_cast<uint8_t*>(args.out1),
+                        static_cast<uint8_t*>(args.out2)};
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int tile = GEMM_CID; tile < total; tile += GEMM_NCL) {
@@ -649,8 +701,9 @@ __global__ void __launch_bounds__(kThreads, 1)
               const int col = ti.n0 + c;
               if (col >= args.N) break;
               const int64_t o = ti.e * estride + row * args.N + col;
-              *reinterpret_cast<uint4*>(args.out0 + o) = z;
-              if constexpr (T::dual) *reinterpret_cast<uint4*>(args.out1 + o) = z;
+              reinterpret_cast<uint4*>(static_cast<moe_bf16*>(args.out0) + o)[0] = z;
+              if constexpr (T::dual)
+                reinterpret_cast<uint4*>(static_cast<moe_bf16*>(args.out1) + o)[0] = z;
             }
           }
           continue;
@@ -659,58 +712,81 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool row_ok = T::kgrouped ? false : (row < ti.row_end);
       const int c_end = min(c_hi, args.N - ti.n0);   // columns of this half that exist
       const int col_lim = ti.n0 + c_end;
-      // DownDgrad: the saved G, U of chunk c+1 are loaded while chunk c is
-      // computed; the first chunk's loads go out before the accumulator is ready
+      // DownDgrad: the saved G, U of the next 16 columns are loaded while the
+      // current ones are computed; the first loads and the row's score go out
+      // before the accumulator is ready
       const int64_t gu_base = row * args.N;
-      uint4 gc[4], uc[4];
-      auto load_gu = [&](int c, uint4* g, uint4* u) {
+      float4 gc[4], uc[4];
+      auto load_gu = [&](int c, float4* g, float4* u) {   // 16 fp32 columns of G and U
 #pragma unroll
         for (int v = 0; v < 4; ++v) {
-          const int col = ti.n0 + c + 8 * v;
+          const int col = ti.n0 + c + 4 * v;
           if (row_ok && col < col_lim) {
-            g[v] = *reinterpret_cast<const uint4*>(args.in0 + gu_base + col);
-            u[v] = *reinterpret_cast<const uint4*>(args.in1 + gu_base + col);
+            g[v] = *reinterpret_cast<const float4*>(args.in0 + gu_base + col);
+            u[v] = *reinterpret_cast<const float4*>(args.in1 + gu_base + col);
           } else {
-            g[v] = make_uint4(0u, 0u, 0u, 0u);
-            u[v] = make_uint4(0u, 0u, 0u, 0u);
+            g[v] = make_float4(0.f, 0.f, 0.f, 0.f);
+            u[v] = make_float4(0.f, 0.f, 0.f, 0.f);
           }
         }
       };
+      float rscale = 1.0f;
       if constexpr (K == Kind::DownDgrad) {
+        rscale = 0.0f;
+        if (row_ok) {
+          const int32_t p = args.src_pair[row];
+          if (p >= 0) rscale = args.pair_w[p];
+        }
         if (c_lo < c_end) load_gu(c_lo, gc, uc);
+      } else if constexpr (T::down_fwd) {
+        if (args.row_w && row_ok) rscale = args.row_w[row];
       }
       const bool got = mbar_wait_bounded(tfull_bar(acc), acc_phase, s_abort, args.status);
-      if (!group_all((warp - 4) >> 2, got)) break;
+      if (!group_all(group, got)) break;
       tc_fence_after();
       const uint32_t t_row = tmem_base + ((uint32_t)(wq * 32) << 16) + (uint32_t)acc * 256u;
 
       // the whole 128-row tile inside its group (dW tiles always: TMA clips at M)
       // -> staged TMA stores by the warpgroup; else masked row stores
-      const int group = (warp - 4) >> 2;
-      const bool leader = (wq == 0 && lane == 0);
       const bool tile_tma = T::kgrouped ? ti.m0 < args.M : ti.m0 + BM <= ti.row_end;
-      uint8_t* stg = stage_out + group * kStagePerGroup;
-      const CUtensorMap* maps[3] = {&mapO0, &mapO1, &mapO2};
-      moe_bf16* outs[3] = {args.out0, args.out1, args.out2};
       if constexpr (T::gateup_fwd) {
+        // G, U fp32 in 8-column slices, A bf16 in 16-column slices (each
+        // with the first of every two G / U slices)
+        constexpr int es[3] = {4, 4, 2};
 #pragma unroll 1
         for (int c = c_lo; c < c_end; c += 32) {
           uint32_t g[32], u[32];
           tmem_ld32(t_row + c, g);
           tmem_ld32(t_row + T::BN + c, u);
           tmem_ld_wait();
-          uint32_t pk[3][16];
+          uint32_t pa[16];
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
             const float g0 = __uint_as_float(g[2 * i]), g1 = __uint_as_float(g[2 * i + 1]);
             const float u0 = __uint_as_float(u[2 * i]), u1 = __uint_as_float(u[2 * i + 1]);
-            pk[0][i] = pack_bf16(g0, g1);
-            pk[1][i] = pack_bf16(u0, u1);
-            pk[2][i] = pack_bf16(__fdividef(g0, 1.0f + __expf(-g0)) * u0,
-                                 __fdividef(g1, 1.0f + __expf(-g1)) * u1);
+            pa[i] = pack_bf16(__fdividef(g0, 1.0f + __expf(-g0)) * u0,
+                              __fdividef(g1, 1.0f + __expf(-g1)) * u1);
           }
-          put_chunk<3, false>(pk, stg, maps, outs, tile_tma, row_ok, row, rloc, ti.n0 + c, args.N,
-                              col_lim, (int)ti.m0, 0, group, leader, pol_out);
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            uint4 v[3][2];
+            v[0][0] = make_uint4(g[8 * q + 0], g[8 * q + 1], g[8 * q + 2], g[8 * q + 3]);
+            v[0][1] = make_uint4(g[8 * q + 4], g[8 * q + 5], g[8 * q + 6], g[8 * q + 7]);
+            v[1][0] = make_uint4(u[8 * q + 0], u[8 * q + 1], u[8 * q + 2], u[8 * q + 3]);
+            v[1][1] = make_uint4(u[8 * q + 4], u[8 * q + 5], u[8 * q + 6], u[8 * q + 7]);
+            const int col = ti.n0 + c + 8 * q;
+            if ((q & 1) == 0) {
+              const int h = q >> 1;
+              v[2][0] = make_uint4(pa[8 * h + 0], pa[8 * h + 1], pa[8 * h + 2], pa[8 * h + 3]);
+              v[2][1] = make_uint4(pa[8 * h + 4], pa[8 * h + 5], pa[8 * h + 6], pa[8 * h + 7]);
+              put_slice<3, false>(v, stg, slot, maps, outs, es, tile_tma, row_ok, row, rloc, col,
+                                  args.N, col_lim, (int)ti.m0, 0, group, leader, pol_out);
+            } else {
+              uint4 w2[2][2] = {{v[0][0], v[0][1]}, {v[1][0], v[1][1]}};
+              put_slice<2, false>(w2, stg, slot, maps, outs, es, tile_tma, row_ok, row, rloc,
+                                  col, args.N, col_lim, (int)ti.m0, 0, group, leader, pol_out);
+            }
+          }
         }
       } else if constexpr (T::kgrouped) {
         constexpr int NO = T::dual ? 2 : 1;
@@ -727,8 +803,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             if constexpr (T::dual)
               pk[NO - 1][i] = pack_bf16(__uint_as_float(u[2 * i]), __uint_as_float(u[2 * i + 1]));
           }
-          put_chunk<NO, true>(pk, stg, maps, outs, tile_tma, false, row, rloc, ti.n0 + c, args.N,
-                              col_lim, (int)ti.m0, ti.e, group, leader, pol_out);
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            uint4 v[NO][2];
+            slice_of<NO, 16>(pk, h, v);
+            constexpr int es[2] = {2, 2};
+            put_slice<NO, true>(v, stg, slot, maps, outs, es, tile_tma, false, row, rloc,
+                                ti.n0 + c + 16 * h, args.N, col_lim, (int)ti.m0, ti.e, group,
+                                leader, pol_out);
+          }
         }
       } else if constexpr (T::dense) {
         // one split: the result (+ bias); several: this split's fp32 partial, summed later
@@ -749,65 +832,81 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       } else if constexpr (K == Kind::DownDgrad) {
-        // dG = dA * U * silu'(G), dU = dA * silu(G)
-        uint4 gn[4], un[4];
+        // dA = w * acc; dG = dA * U * silu'(G), dU = dA * silu(G), 16 columns
+        // at a time, the next 16 columns' G and U loaded while these are computed
+        constexpr int es[2] = {2, 2};
+        float4 gn[4], un[4];
+        float dtw = 0.0f;   // this row's <dAu, silu(G) U> over this warpgroup's columns
 #pragma unroll 1
         for (int c = c_lo; c < c_end; c += 32) {
           uint32_t r[32];
           tmem_ld32(t_row + c, r);
-          if (c + 32 < c_end) load_gu(c + 32, gn, un);
+          if (c + 16 < c_end) load_gu(c + 16, gn, un);
           tmem_ld_wait();
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
+            const float gf[16] = {gc[0].x, gc[0].y, gc[0].z, gc[0].w, gc[1].x, gc[1].y,
+                                  gc[1].z, gc[1].w, gc[2].x, gc[2].y, gc[2].z, gc[2].w,
+                                  gc[3].x, gc[3].y, gc[3].z, gc[3].w};
+            const float uf[16] = {uc[0].x, uc[0].y, uc[0].z, uc[0].w, uc[1].x, uc[1].y,
+                                  uc[1].z, uc[1].w, uc[2].x, uc[2].y, uc[2].z, uc[2].w,
+                                  uc[3].x, uc[3].y, uc[3].z, uc[3].w};
             uint32_t pk[2][8];
 #pragma unroll
-            for (int w = 0; w < 2; ++w) {
-              const int v = 2 * h + w;
-              float gf[8], uf[8];
-              unpack8(gc[v], gf);
-              unpack8(uc[v], uf);
+            for (int i = 0; i < 8; ++i) {
+              float dg[2], du[2];
 #pragma unroll
-              for (int i = 0; i < 4; ++i) {
-                float dg[2], du[2];
-#pragma unroll
-                for (int j = 0; j < 2; ++j) {
-                  const int q = 2 * i + j;
-                  const float f = __uint_as_float(r[8 * v + q]);
-                  const float sg = __fdividef(1.0f, 1.0f + __expf(-gf[q]));
-                  dg[j] = f * uf[q] * (sg * (1.0f + gf[q] * (1.0f - sg)));
-                  du[j] = f * gf[q] * sg;
-                }
-                pk[0][4 * w + i] = pack_bf16(dg[0], dg[1]);
-                pk[1][4 * w + i] = pack_bf16(du[0], du[1]);
+              for (int j = 0; j < 2; ++j) {
+                const int q = 2 * i + j;
+                const float au = __uint_as_float(r[16 * h + q]);
+                const float f = au * rscale;
+                const float sg = __fdividef(1.0f, 1.0f + __expf(-gf[q]));
+                const float sl = gf[q] * sg;   // silu(G)
+                // only the tile's real columns: past them the accumulator was
+                // never written (the MMA's N stops at the tile width) and the
+                // G, U registers may hold the previous half
+                if (ti.n0 + c + 16 * h + q < col_lim) dtw = fmaf(au, sl * uf[q], dtw);
+                dg[j] = f * uf[q] * (sg * (1.0f + gf[q] * (1.0f - sg)));
+                du[j] = f * sl;
               }
+              pk[0][i] = pack_bf16(dg[0], dg[1]);
+              pk[1][i] = pack_bf16(du[0], du[1]);
             }
-            put_chunk<2, false, 1>(pk, stg, maps, outs, tile_tma, row_ok, row, rloc,
-                                   ti.n0 + c + 16 * h, args.N, col_lim, (int)ti.m0, 0, group,
-                                   leader, pol_out);
-          }
-          if (c + 32 < c_end) {
 #pragma unroll
             for (int v = 0; v < 4; ++v) { gc[v] = gn[v]; uc[v] = un[v]; }
+            if (h == 0 && c + 32 < c_end) load_gu(c + 32, gn, un);
+            uint4 vv[2][2];
+            slice_of<2, 8>(pk, 0, vv);
+            put_slice<2, false>(vv, stg, slot, maps, outs, es, tile_tma, row_ok, row, rloc,
+                                ti.n0 + c + 16 * h, args.N, col_lim, (int)ti.m0, 0, group,
+                                leader, pol_out);
           }
         }
+        if (row_ok)
+          args.dtw_part[row * args.dtw_slots + 2 * (ti.n0 / bn) + group] = dtw;
       } else {
-        // single accumulator, plain (optionally row-scaled) store
-        float scale = 1.0f;
-        if constexpr (T::down_fwd) {
-          if (args.row_w && row_ok) scale = args.row_w[row];
-        }
+        // single accumulator, fp32 output (DownFwd optionally row-scaled): 8-column slices
 #pragma unroll 1
         for (int c = c_lo; c < c_end; c += 32) {
           uint32_t r[32];
           tmem_ld32(t_row + c, r);
           tmem_ld_wait();
-          uint32_t pk[1][16];
 #pragma unroll
-          for (int i = 0; i < 16; ++i)
-            pk[0][i] = pack_bf16(__uint_as_float(r[2 * i]) * scale,
-                                 __uint_as_float(r[2 * i + 1]) * scale);
-          put_chunk<1, false>(pk, stg, maps, outs, tile_tma, row_ok, row, rloc, ti.n0 + c, args.N,
-                              col_lim, (int)ti.m0, 0, group, leader, pol_out);
+          for (int q = 0; q < 4; ++q) {
+            uint4 v[1][2];
+            v[0][0] = make_uint4(__float_as_uint(__uint_as_float(r[8 * q + 0]) * rscale),
+                                 __float_as_uint(__uint_as_float(r[8 * q + 1]) * rscale),
+                                 __float_as_uint(__uint_as_float(r[8 * q + 2]) * rscale),
+                                 __float_as_uint(__uint_as_float(r[8 * q + 3]) * rscale));
+            v[0][1] = make_uint4(__float_as_uint(__uint_as_float(r[8 * q + 4]) * rscale),
+                                 __float_as_uint(__uint_as_float(r[8 * q + 5]) * rscale),
+                                 __float_as_uint(__uint_as_float(r[8 * q + 6]) * rscale),
+                                 __float_as_uint(__uint_as_float(r[8 * q + 7]) * rscale));
+            constexpr int es[1] = {4};
+            put_slice<1, false>(v, stg, slot, maps, outs, es, tile_tma, row_ok, row, rloc,
+                                ti.n0 + c + 8 * q, args.N, col_lim, (int)ti.m0, 0, group,
+                                leader, pol_out);
+          }
         }
       }
       tc_fence_before();
@@ -885,20 +984,23 @@ static bool map3d(CUtensorMap* m, const void* ptr, uint64_t d0, uint64_t d1, uin
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// 2-D bf16 map over a row buffer [R, N] for TMA stores of 128-row x 16-column boxes
-static bool map2d_out(CUtensorMap* m, const void* ptr, uint64_t N, uint64_t R) {
+// Maps for the epilogues' TMA stores: boxes of 128 rows x 32 bytes (16 bf16 or
+// 8 fp32 columns) with the 32-byte swizzle the staging slots are written in.
+// 2-D over a row buffer [R, N]; esz = 2 (bf16) or 4 (fp32).
+static bool map2d_out(CUtensorMap* m, const void* ptr, uint64_t N, uint64_t R, int esz = 2) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
   cuuint64_t dims[2] = {N, R};
-  cuuint64_t strides[1] = {N * 2};
-  cuuint32_t box[2] = {16, 128};
+  cuuint64_t strides[1] = {N * (uint64_t)esz};
+  cuuint32_t box[2] = {(cuuint32_t)(32 / esz), 128};
   cuuint32_t es[2] = {1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box,
-            es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-            CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  return fn(m, esz == 4 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+            const_cast<void*>(ptr), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_32B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// 3-D bf16 map over [E, M, N] (N innermost) for TMA stores of 128-row x 16-column boxes
+// 3-D bf16 map over [E, M, N] (N innermost), same boxes
 static bool map3d_out(CUtensorMap* m, const void* ptr, uint64_t N, uint64_t M, uint64_t E) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
@@ -907,7 +1009,7 @@ static bool map3d_out(CUtensorMap* m, const void* ptr, uint64_t N, uint64_t M, u
   cuuint32_t box[3] = {16, 128, 1};
   cuuint32_t es[3] = {1, 1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box,
-            es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+            es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_32B,
             CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -1107,12 +1209,12 @@ static int64_t mgrouped_tiles_upper(const GroupedDims& g, int N, int BN, int TM 
 }
 
 cudaError_t launch_gateup_fwd(const GroupedDims& g, const moe_bf16* xp, const moe_bf16* w_gate,
-                              const moe_bf16* w_up, moe_bf16* G, moe_bf16* U, moe_bf16* A,
+                              const moe_bf16* w_up, float* G, float* U, moe_bf16* A,
                               int* status, cudaStream_t s) {
   CUtensorMap a0, b0, b1, o0, o1, o2;
   if (!map2d(&a0, xp, g.d, g.R_cap, BM) || !map3d(&b0, w_gate, g.f, g.d, g.E, BK) ||
-      !map3d(&b1, w_up, g.f, g.d, g.E, BK) || !map2d_out(&o0, G, g.f, g.R_cap) ||
-      !map2d_out(&o1, U, g.f, g.R_cap) || !map2d_out(&o2, A, g.f, g.R_cap))
+      !map3d(&b1, w_up, g.f, g.d, g.E, BK) || !map2d_out(&o0, G, g.f, g.R_cap, 4) ||
+      !map2d_out(&o1, U, g.f, g.R_cap, 4) || !map2d_out(&o2, A, g.f, g.R_cap))
     return cudaErrorInvalidValue;
   GemmArgs a = base_args(g, status);
   a.N = g.f;
@@ -1133,10 +1235,10 @@ cudaError_t launch_gateup_fwd(const GroupedDims& g, const moe_bf16* xp, const mo
 }
 
 cudaError_t launch_down_fwd(const GroupedDims& g, const moe_bf16* A, const moe_bf16* w_down,
-                            const float* row_w, moe_bf16* yp, int* status, cudaStream_t s) {
+                            const float* row_w, float* yp, int* status, cudaStream_t s) {
   CUtensorMap a0, b0, o0;
   if (!map2d(&a0, A, g.f, g.R_cap, BM) || !map3d(&b0, w_down, g.d, g.f, g.E, BK) ||
-      !map2d_out(&o0, yp, g.d, g.R_cap))
+      !map2d_out(&o0, yp, g.d, g.R_cap, 4))
     return cudaErrorInvalidValue;
   GemmArgs a = base_args(g, status);
   a.N = g.d;
@@ -1150,17 +1252,26 @@ cudaError_t launch_down_fwd(const GroupedDims& g, const moe_bf16* A, const moe_b
                                            &o0);
 }
 
-cudaError_t launch_down_dgrad(const GroupedDims& g, const moe_bf16* dyp, const moe_bf16* w_down,
-                              const moe_bf16* G, const moe_bf16* U, moe_bf16* dG, moe_bf16* dU,
-                              int* status, cudaStream_t s) {
+// Partial slots per row of the down dgrad's top-k weight gradient: one per
+// n-tile and epilogue warpgroup.
+int down_dgrad_dtw_slots(int f) {
+  const int bn = pick_bn(f, 16);
+  return 2 * ((f + bn - 1) / bn);
+}
+
+cudaError_t launch_down_dgrad(const GroupedDims& g, const moe_bf16* dyg, const float* pair_w,
+                              const moe_bf16* w_down, const float* G, const float* U,
+                              moe_bf16* dG, moe_bf16* dU, float* dtw_part, int* status,
+                              cudaStream_t s) {
   CUtensorMap a0, b0, o0, o1;
   const int bn = pick_bn(g.f, 16);
   // no pairs by default: this kernel is bound by its epilogue (G and U read,
   // dG and dU written), which pairs do not shorten
   const bool pair = pairs_env() == 1;
-  // dA[r, c] = sum_j dyp[r, j] W_down[e][c, j]: B is W_down[e] read as [N = f rows, K = d]
-  // (a pair's CTAs load bn / 2 rows each)
-  if (!map2d(&a0, dyp, g.d, g.R_cap, BM) ||
+  // dA[r, c] = w(r) sum_j dyg[r, j] W_down[e][c, j]: B is W_down[e] read as
+  // [N = f rows, K = d] (a pair's CTAs load bn / 2 rows each)
+  if (!g.src_pair) return cudaErrorInvalidValue;
+  if (!map2d(&a0, dyg, g.d, g.R_cap, BM) ||
       !map3d(&b0, w_down, g.d, g.f, g.E, pair ? bn / 2 : bn) ||
       !map2d_out(&o0, dG, g.f, g.R_cap) || !map2d_out(&o1, dU, g.f, g.R_cap))
     return cudaErrorInvalidValue;
@@ -1169,6 +1280,9 @@ cudaError_t launch_down_dgrad(const GroupedDims& g, const moe_bf16* dyp, const m
   a.nk_seg = (g.d + BK - 1) / BK;
   a.in0 = G; a.in1 = U;
   a.out0 = dG; a.out1 = dU;
+  a.pair_w = pair_w;
+  a.dtw_part = dtw_part;
+  a.dtw_slots = down_dgrad_dtw_slots(g.f);
   a.bn = bn;
   if (pair)
     return launch_kind<Kind::DownDgrad, true>(
@@ -1178,7 +1292,7 @@ cudaError_t launch_down_dgrad(const GroupedDims& g, const moe_bf16* dyp, const m
 }
 
 cudaError_t launch_gateup_dgrad(const GroupedDims& g, const moe_bf16* dG, const moe_bf16* dU,
-                                const moe_bf16* w_gate, const moe_bf16* w_up, moe_bf16* dxp,
+                                const moe_bf16* w_gate, const moe_bf16* w_up, float* dxp,
                                 int* status, cudaStream_t s) {
   CUtensorMap a0, a1, b0, b1, o0;
   const int bn = pick_bn(g.d, 16);
@@ -1188,7 +1302,7 @@ cudaError_t launch_gateup_dgrad(const GroupedDims& g, const moe_bf16* dG, const 
   // B is W_gate[e] / W_up[e] read as [N = d rows, K = f]
   if (!map2d(&a0, dG, g.f, g.R_cap, BM) || !map2d(&a1, dU, g.f, g.R_cap, BM) ||
       !map3d(&b0, w_gate, g.f, g.d, g.E, brows) || !map3d(&b1, w_up, g.f, g.d, g.E, brows) ||
-      !map2d_out(&o0, dxp, g.d, g.R_cap))
+      !map2d_out(&o0, dxp, g.d, g.R_cap, 4))
     return cudaErrorInvalidValue;
   GemmArgs a = base_args(g, status);
   a.N = g.d;

@@ -36,7 +36,7 @@ size_t route_bwd_ws_bytes(int64_t T, int d, int E, int k, int align);
 cudaError_t launch_route_bwd(const float* d_topk_w, const float* topk_w, const int32_t* topk_idx,
                              const float* w_router, const int64_t* offsets,
                              const int32_t* src_pair, const moe_bf16* x, int64_t T, int d, int E,
-                             int k, int align, moe_bf16* dx_inout, const moe_bf16* dxp,
+                             int k, int align, moe_bf16* dx_inout, const float* dxp,
                              const int32_t* dst_row, float* dw_router, float* dbias, void* ws,
                              int* status, cudaStream_t s);
 
@@ -48,12 +48,14 @@ cudaError_t launch_permute(const int32_t* topk_idx, int64_t T, int k, int E, int
                            void* ws, int* status, cudaStream_t s);
 
 // combine.cu
-cudaError_t launch_combine(const moe_bf16* rows, const int32_t* dst_row, const float* topk_w,
+cudaError_t launch_combine(const float* rows, const int32_t* dst_row, const float* topk_w,
                            int64_t T, int k, int d, moe_bf16* out, cudaStream_t s);
-cudaError_t launch_combine_bwd(const moe_bf16* dy, const moe_bf16* yp, const int32_t* src_pair,
-                               const float* topk_w, const int64_t* offsets, int64_t T, int k,
-                               int E, int d, int64_t R_cap, moe_bf16* dyp, float* d_topk_w,
-                               cudaStream_t s);
+cudaError_t launch_combine_bwd(const moe_bf16* dy, const int32_t* src_pair, const float* topk_w,
+                               const int64_t* offsets, int k, int E, int d, int64_t R_cap,
+                               moe_bf16* dyg, moe_bf16* dyp, cudaStream_t s);
+// d_topk_w[p] = sum over the slots, in order, of part[dst_row[p]][slot]
+cudaError_t launch_dtw_finalize(const float* part, int slots, const int32_t* dst_row, int64_t P,
+                                float* d_topk_w, cudaStream_t s);
 
 // gemm.cu (tcgen05 grouped GEMMs)
 constexpr int kDecodeMaxT = 8;        // tokens of one decode call
@@ -81,19 +83,22 @@ struct GroupedDims {
   int64_t R_cap;
   int64_t P;        // token-expert pairs (T * k): sizes the tile schedule
   // the pair held by each row of the layout (-1: padding), or NULL: lets the
-  // K-grouped weight gradients stop each expert's reduction at its real rows
+  // K-grouped weight gradients stop each expert's reduction at its real rows;
+  // the down dgrad needs it (it finds each row's score through it)
   const int32_t* src_pair = nullptr;
 };
 cudaError_t launch_gateup_fwd(const GroupedDims& g, const moe_bf16* xp, const moe_bf16* w_gate,
-                              const moe_bf16* w_up, moe_bf16* G, moe_bf16* U, moe_bf16* A,
+                              const moe_bf16* w_up, float* G, float* U, moe_bf16* A,
                               int* status, cudaStream_t s);
 cudaError_t launch_down_fwd(const GroupedDims& g, const moe_bf16* A, const moe_bf16* w_down,
-                            const float* row_w, moe_bf16* yp, int* status, cudaStream_t s);
-cudaError_t launch_down_dgrad(const GroupedDims& g, const moe_bf16* dyp, const moe_bf16* w_down,
-                              const moe_bf16* G, const moe_bf16* U, moe_bf16* dG, moe_bf16* dU,
-                              int* status, cudaStream_t s);
+                            const float* row_w, float* yp, int* status, cudaStream_t s);
+int down_dgrad_dtw_slots(int f);
+cudaError_t launch_down_dgrad(const GroupedDims& g, const moe_bf16* dyg, const float* pair_w,
+                              const moe_bf16* w_down, const float* G, const float* U,
+                              moe_bf16* dG, moe_bf16* dU, float* dtw_part, int* status,
+                              cudaStream_t s);
 cudaError_t launch_gateup_dgrad(const GroupedDims& g, const moe_bf16* dG, const moe_bf16* dU,
-                                const moe_bf16* w_gate, const moe_bf16* w_up, moe_bf16* dxp,
+                                const moe_bf16* w_gate, const moe_bf16* w_up, float* dxp,
                                 int* status, cudaStream_t s);
 cudaError_t launch_wgrad_down(const GroupedDims& g, const moe_bf16* A, const moe_bf16* dyp,
                               moe_bf16* dw_down, int* status, cudaStream_t s);

@@ -329,16 +329,16 @@ __global__ void transpose_f32_kernel(const float* __restrict__ in, int rows, int
 }
 
 // one warp per token: dl for its k slots (to dl_pair, and as three bf16 parts
-// into the token's dense row of dl3), then dx[t]. With dxp given, dx[t] =
-// sum_j dxp[dst_row[t, j]] + sum_j dl_j W_r[:, e_j] in fp32, written once (the
-// permute transpose fused in); without it, dx[t] += sum_j dl_j W_r[:, e_j].
-// The dxp rows of up to four slots are loaded together; few registers, so that
-// many warps per SM keep enough loads in flight.
+// into the token's dense row of dl3), then dx[t]. With dxp (fp32 rows) given,
+// dx[t] = sum_j dxp[dst_row[t, j]] + sum_j dl_j W_r[:, e_j] in fp32, rounded to
+// bf16 once (the permute transpose fused in); without it, dx[t] += sum_j dl_j
+// W_r[:, e_j]. The dxp rows of up to four slots are loaded together; few
+// registers, so that many warps per SM keep enough loads in flight.
 __global__ void __launch_bounds__(256, 4) route_bwd_token_kernel(
     const float* __restrict__ d_topk_w, const float* __restrict__ topk_w,
     const int32_t* __restrict__ topk_idx, const float* __restrict__ wrT, int64_t T, int d, int E,
     int E8, int k, float* __restrict__ dl_pair, moe_bf16* __restrict__ dl3,
-    moe_bf16* __restrict__ dx, const moe_bf16* __restrict__ dxp,
+    moe_bf16* __restrict__ dx, const float* __restrict__ dxp,
     const int32_t* __restrict__ dst_row) {
   const int lane = threadIdx.x & 31;
   const int64_t t = (int64_t)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
@@ -383,21 +383,23 @@ __global__ void __launch_bounds__(256, 4) route_bwd_token_kernel(
     if (in && !dxp) unpack8(*reinterpret_cast<const uint4*>(dxr + c), acc);
     if (dxp) {
       for (int j0 = 0; j0 < k; j0 += 4) {
-        uint4 v[4];
+        float4 v[4][2];
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
           const int j = j0 + q;
           const int rj = __shfl_sync(0xFFFFFFFFu, r, j & 31);
-          v[q] = (in && j < k && rj >= 0)
-                     ? *reinterpret_cast<const uint4*>(dxp + (int64_t)rj * d + c)
-                     : make_uint4(0u, 0u, 0u, 0u);
+          if (in && j < k && rj >= 0) {
+            const float4* src = reinterpret_cast<const float4*>(dxp + (int64_t)rj * d + c);
+            v[q][0] = src[0];
+            v[q][1] = src[1];
+          } else {
+            v[q][0] = v[q][1] = make_float4(0.f, 0.f, 0.f, 0.f);
+          }
         }
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
-          float f[8];
-          unpack8(v[q], f);
-#pragma unroll
-          for (int i = 0; i < 8; ++i) acc[i] += f[i];
+          acc[0] += v[q][0].x; acc[1] += v[q][0].y; acc[2] += v[q][0].z; acc[3] += v[q][0].w;
+          acc[4] += v[q][1].x; acc[5] += v[q][1].y; acc[6] += v[q][1].z; acc[7] += v[q][1].w;
         }
       }
     }
@@ -457,7 +459,7 @@ __global__ void __launch_bounds__(256) route_bwd_reduce_kernel(
 cudaError_t launch_route_bwd(const float* d_topk_w, const float* topk_w, const int32_t* topk_idx,
                              const float* w_router, const int64_t* offsets,
                              const int32_t* src_pair, const moe_bf16* x, int64_t T, int d, int E,
-                             int k, int align, moe_bf16* dx_inout, const moe_bf16* dxp,
+                             int k, int align, moe_bf16* dx_inout, const float* dxp,
                              const int32_t* dst_row, float* dw_router, float* dbias, void* ws,
                              int* status, cudaStream_t s) {
   (void)align;

@@ -47,6 +47,7 @@ class Buffers:
     ws_permute: torch.Tensor
     ws_route: torch.Tensor
     # backward
+    dyg: Optional[torch.Tensor] = None
     dyp: Optional[torch.Tensor] = None
     dg: Optional[torch.Tensor] = None
     du: Optional[torch.Tensor] = None
@@ -61,6 +62,7 @@ class Buffers:
     # the one-launch decode forward's workspace (decode_buffers)
     ws_decode: Optional[torch.Tensor] = None
     ws_route_bwd: Optional[torch.Tensor] = None
+    ws_expert_bwd: Optional[torch.Tensor] = None
     # the input of the last forward (the router backward reads it)
     x: Optional[torch.Tensor] = None
 
@@ -111,10 +113,10 @@ class MoELayer:
             dst_row=torch.empty(T * k, dtype=torch.int32, **kw),
             src_pair=torch.empty(R, dtype=torch.int32, **kw),
             xp=torch.empty(R, d, dtype=BF16, **kw),
-            g=torch.empty(R, f, dtype=BF16, **kw),
-            u=torch.empty(R, f, dtype=BF16, **kw),
+            g=torch.empty(R, f, dtype=torch.float32, **kw),
+            u=torch.empty(R, f, dtype=torch.float32, **kw),
             a=torch.empty(R, f, dtype=BF16, **kw),
-            yp=torch.empty(R, d, dtype=BF16, **kw),
+            yp=torch.empty(R, d, dtype=torch.float32, **kw),
             y=torch.empty(T, d, dtype=BF16, **kw),
             ws_permute=torch.empty(max(ws_p, 256), dtype=torch.uint8, **kw),
             ws_route=torch.empty(
@@ -123,10 +125,11 @@ class MoELayer:
         )
         if backward:
             ws_r = int(self.lib.moe_workspace_size(_lib.MOE_WS_ROUTE_BWD, T, d, E, k, self.align))
+            b.dyg = torch.empty(R, d, dtype=BF16, **kw)
             b.dyp = torch.empty(R, d, dtype=BF16, **kw)
             b.dg = torch.empty(R, f, dtype=BF16, **kw)
             b.du = torch.empty(R, f, dtype=BF16, **kw)
-            b.dxp = torch.empty(R, d, dtype=BF16, **kw)
+            b.dxp = torch.empty(R, d, dtype=torch.float32, **kw)
             b.d_topk_w = torch.empty(T, k, dtype=torch.float32, **kw)
             b.dx = torch.empty(T, d, dtype=BF16, **kw)
             b.dw_gate = torch.empty(E, d, f, dtype=BF16, **kw)
@@ -135,6 +138,8 @@ class MoELayer:
             b.dw_router = torch.empty(d, E, dtype=torch.float32, **kw)
             b.dbias = torch.empty(E, dtype=torch.float32, **kw)
             b.ws_route_bwd = torch.empty(max(ws_r, 256), dtype=torch.uint8, **kw)
+            ws_e = int(self.lib.moe_expert_bwd_workspace_size(R, f))
+            b.ws_expert_bwd = torch.empty(max(ws_e, 256), dtype=torch.uint8, **kw)
         return b
 
     # ------------------------------------------------------------- calls --
@@ -161,10 +166,11 @@ class MoELayer:
     def expert_bwd(self, dy, b: Buffers, stream=None):
         _lib.call("moe_expert_bwd", _p(dy), _p(b.src_pair), _p(b.dst_row), _p(b.topk_w),
                   _p(b.offsets), b.T, self.k, self.E, self.d, self.f, b.R_cap,
-                  _p(b.xp), _p(b.g), _p(b.u), _p(b.a), _p(b.yp),
+                  _p(b.xp), _p(b.g), _p(b.u), _p(b.a),
                   _p(self.w_gate), _p(self.w_up), _p(self.w_down),
-                  _p(b.dyp), _p(b.dg), _p(b.du), _p(b.dxp), _p(b.d_topk_w),
-                  _p(b.dw_gate), _p(b.dw_up), _p(b.dw_down), _stream(stream))
+                  _p(b.dyg), _p(b.dyp), _p(b.dg), _p(b.du), _p(b.dxp), _p(b.d_topk_w),
+                  _p(b.dw_gate), _p(b.dw_up), _p(b.dw_down), _p(b.ws_expert_bwd),
+                  b.ws_expert_bwd.numel(), _stream(stream))
 
     def route_bwd(self, b: Buffers, fused=True, stream=None, x=None):
         """Router backward. fused: dx = permute transpose of dXp + the router's

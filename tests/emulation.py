@@ -3,10 +3,13 @@ rounding points, for kernel-level numerics tests.
 
 Not the oracle (the oracle is float64 and never rounds): this restates the
 same steps in torch fp32 on the device and rounds to bf16 exactly where the
-kernels store bf16 (G, U, A, Yp, dYp, dG, dU, dXp, y, dx, the weight
-gradients), so a kernel and this emulation should differ only by fp32
-summation order and the odd bf16 rounding it flips. The routing indices are
-inputs (the oracle's), so both sides route identically.
+kernels store bf16 (A, dYp, dG, dU, y, dx, the weight gradients; G, U, Yp
+and dXp stay fp32, the down dgrad multiplies the unscaled rows of dY and
+applies each pair's score to the fp32 product, and the top-k weight gradient
+is <dY W_down^T, silu(G) U> from the fp32 G and U), so a kernel and this
+emulation should differ only by fp32 summation order and the odd bf16
+rounding it flips. The routing indices are inputs (the oracle's), so both
+sides route identically.
 """
 from __future__ import annotations
 
@@ -52,22 +55,33 @@ def emulate(inp: dict, idx, k: int, device="cuda", backward=True) -> dict:
         xe = x[tok[pp]]
         g32 = xe @ wg
         u32 = xe @ wu
-        G[pp] = bf(g32)
-        U[pp] = bf(u32)
+        G[pp] = g32
+        U[pp] = u32
         A[pp] = bf(g32 * torch.sigmoid(g32) * u32)
-        Yu[pp] = bf(A[pp] @ wd)
+        Yu[pp] = A[pp] @ wd
         if backward:
-            dA = dYp[pp] @ wd.T
+            dA = (dy[tok[pp]] @ wd.T) * wf[pp][:, None]
             s = torch.sigmoid(G[pp])
             dG[pp] = bf(dA * U[pp] * (s * (1 + G[pp] * (1 - s))))
             dU[pp] = bf(dA * G[pp] * s)
-            dXp[pp] = bf(dG[pp] @ wg.T + dU[pp] @ wu.T)
+            dXp[pp] = dG[pp] @ wg.T + dU[pp] @ wu.T
             dwg[e] = bf(xe.T @ dG[pp])
             dwu[e] = bf(xe.T @ dU[pp])
             dwd[e] = bf(A[pp].T @ dYp[pp])
     out.update(G=G, U=U, A=A, Yu=Yu, y=bf((wf[:, None] * Yu).reshape(T, k, d).sum(1)))
     if backward:
-        dtw = (dy[tok] * Yu).sum(1).reshape(T, k)
+        # the top-k weight gradient from the unrounded A: <dy W_down^T, silu(G) U>
+        A32 = torch.zeros(P, f, **f32)
+        for e in range(E):
+            pp = (e_of_p == e).nonzero().flatten()
+            if pp.numel():
+                A32[pp] = G[pp] * torch.sigmoid(G[pp]) * U[pp]
+        dtw = torch.zeros(P, **f32)
+        for e in range(E):
+            pp = (e_of_p == e).nonzero().flatten()
+            if pp.numel():
+                dtw[pp] = ((dy[tok[pp]] @ inp["w_down"][e].to(**f32).T) * A32[pp]).sum(1)
+        dtw = dtw.reshape(T, k)
         dl_sel = w * (dtw - (w * dtw).sum(1, keepdim=True))
         dl = torch.zeros(T, E, **f32).scatter_(1, idx, dl_sel)
         dx = bf(dXp.reshape(T, k, d).sum(1) + dl @ wr.T)     # one rounding (fused pass)

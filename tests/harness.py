@@ -3,28 +3,42 @@ run the oracle on the same seeded inputs, and compare.
 
 Comparison rules:
   * integers (routing indices, counts, offsets, dst_row, src_pair): exact;
-  * floating point, every tensor (outputs, gradients and the bf16
-    intermediates G, U, A, Yp, dYp, dG, dU, dXp):
+  * routing: the GPU's top-k must equal, bit for bit, the oracle's selection
+    run on the GPU's own fp32 logits (both take the decision in fp32 — the
+    exact upcast keeps fp32 order — with ties to the lower expert index);
+    against the float64 logits the indices must agree except where two
+    float64 logits lie within the fp32 error band of each other, and there
+    every differing slot must be such a near-tie (PocketLLM "Qwen4-Exp
+    Heterogeneous TP4 Performance", §Numerical gates: exact ties vs real
+    flips). Downstream parity runs with the oracle's indices passed to both
+    sides (forced_idx), so no GPU output feeds the oracle;
+  * the stated bar, max |gpu - oracle| <= 2e-2 RMS(oracle), holds plainly
+    for the fp32 results: logits, topk_w, d_topk_w and the router gradients
+    dW_r, db;
+  * for the layer's bf16 outputs y and dx the same bar holds for the error
+    the computation adds to the rounding of the output format itself:
+    element-wise |gpu - oracle| <= 2e-2 RMS(oracle) + half an ulp of bf16 at
+    the element. The rounding alone is up to 2^-8 of an element's magnitude
+    (an element just above a power of two), so wherever a tensor holds an
+    element of more than 5.12 RMS the correctly rounded oracle itself can
+    miss the plain bar; the plain max|diff|/RMS is reported all the same;
+  * every other tensor — the bf16 operands A, dYp, dG, dU, the fp32 rows G,
+    U (fp32 accumulations: far inside the bar), Yp and dXp, and the bf16
+    weight gradients — is held to
       - RMS-relative error ||gpu - oracle||_2 / ||oracle||_2 <= 1e-2, and
       - element-wise |gpu - oracle| <= max(2e-2 RMS(oracle), MAG_C u M),
-    where 2e-2 x RMS is the stated acceptance bar, u = 2^-8 (bf16) and M is the
-    element's magnitude from a first-order forward error analysis of the
-    kernel chain: the same computation in float64 with every input and
-    product taken in absolute value, each stored bf16 value's own rounding
-    and the rounding it inherits from its inputs propagated through each
-    GEMM (|A| |B| sums) and each element-wise step (|f'| terms). The second
-    term is needed because the bf16 operands of the tensor-core GEMMs (A,
-    dYp, dG, dU) alone put heavy-tailed tensors (a weight gradient built from
-    a few rows, a product of two Gaussians) beyond 2e-2 RMS at their largest
-    elements: an exact emulation of the kernels' rounding points shows it.
-    The stated max-abs metric is reported for every tensor all the same;
-  * routing indices are decided on fp32 logits on the GPU and on float64
-    logits in the oracle. Where the float64 logits of two experts lie within
-    the fp32 error band of each other the two may legitimately order them
-    differently; there the GPU's choice is checked for validity (it is a
-    top-k of the float64 logits up to the band) instead of equality, and the
-    downstream parity runs with the oracle's indices passed in as
-    forced_idx so both sides compute the same routing.
+    u = 2^-8 (bf16), M the element's magnitude from a first-order forward
+    error analysis of the kernel chain: the same computation in float64 with
+    every input and product taken in absolute value, each stored bf16
+    value's own rounding and the rounding it inherits from its inputs
+    propagated through each GEMM (|A| |B| sums) and each element-wise step
+    (|f'| terms). These tensors are heavy-tailed (a weight gradient of a few
+    rows is an outer product; A = silu(G) U is a product of Gaussians; a
+    bf16 operand near a zero of silu' moves dG by more than its own ulp), so
+    the bf16 operands the tensor cores take put their largest elements past
+    2e-2 RMS whatever the kernels do. MAG_C = 1: an fp32 emulation of exactly
+    the kernels' rounding points (tests/emulation.py) reaches 0.5 of this
+    bound at its worst element (a bf16 value's own rounding, dYp).
 """
 from __future__ import annotations
 
@@ -54,12 +68,52 @@ def rel_err(got, ref) -> float:
 
 
 def assert_close(name, got, ref, tol=TOL):
+    """The plain stated bar: max|diff| <= tol * RMS(ref)."""
     e = rel_err(got, ref)
     assert e <= tol, f"{name}: max|diff| / RMS = {e:.3e} > {tol}"
     return e
 
 
-MAG_C = 4.0
+def half_ulp_bf16(v) -> np.ndarray:
+    """Half a unit in the last place of bf16 (8 significant bits) at |v|:
+    2^(floor(log2 |v|) - 8); 0 at v = 0."""
+    a = np.abs(np.asarray(v, dtype=np.float64))
+    out = np.zeros_like(a)
+    nz = a > 0
+    out[nz] = np.exp2(np.floor(np.log2(a[nz])) - 8.0)
+    return out
+
+
+def assert_bf16_out_close(name, got, ref, tol=TOL):
+    """A bf16 output: |got - ref| <= tol RMS(ref) + half an ulp of bf16 at the
+    element (the larger of |got| and |ref|, in case the rounding crossed a
+    power of two). Returns the plain metric max|diff| / RMS(ref)."""
+    ref = np.asarray(ref, dtype=np.float64)
+    got = np.asarray(got, dtype=np.float64)
+    if ref.size == 0:
+        return 0.0
+    rms = float(np.sqrt(np.mean(ref * ref)))
+    diff = np.abs(got - ref)
+    bound = tol * rms + half_ulp_bf16(np.maximum(np.abs(got), np.abs(ref))) + 1e-30
+    ratio = float(np.max(diff / bound))
+    plain = float(np.max(diff)) / rms if rms > 0 else 0.0
+    assert ratio <= 1.0, (f"{name}: worst |diff| / (2e-2 RMS + ulp/2) = {ratio:.3f} > 1 "
+                          f"(max|diff|/RMS = {plain:.3e})")
+    return plain
+
+
+def bf16_floor(ref) -> float:
+    """max|bf16(ref) - ref| / RMS(ref): what the output format's rounding of the
+    exact answer alone makes of the plain metric."""
+    r = np.asarray(ref, dtype=np.float64)
+    if r.size == 0:
+        return 0.0
+    rb = torch.from_numpy(r).to(torch.float32).to(torch.bfloat16).to(torch.float64).numpy()
+    rms = float(np.sqrt(np.mean(r * r)))
+    return float(np.max(np.abs(rb - r))) / rms if rms > 0 else 0.0
+
+
+MAG_C = 1.0
 U_BF16 = 2.0 ** -8
 
 
@@ -185,24 +239,38 @@ def tie_band(logits_gpu, logits_ref) -> float:
 
 
 def check_routing(idx_gpu, idx_ref, logits_ref, band):
-    """Exact where the float64 order is clear; valid top-k within the band elsewhere.
+    """Exact where the float64 order is clear. At a token whose selection
+    differs, every slot whose expert differs must hold an expert whose
+    float64 logit is within the band of the oracle's expert in that slot (a
+    near-tie: an order swap or a swap at the k-th place), and the selection
+    must still be a valid top-k of the float64 logits up to the band.
     Returns the number of tokens that differ."""
     idx_gpu = np.asarray(idx_gpu, dtype=np.int64)
+    idx_ref = np.asarray(idx_ref, dtype=np.int64)
     diff = np.flatnonzero(np.any(idx_gpu != idx_ref, axis=1))
     for t in diff:
         lg = logits_ref[t]
         sel = idx_gpu[t]
         assert len(set(sel.tolist())) == len(sel), f"token {t}: repeated expert"
         rest = np.setdiff1d(np.arange(lg.size), sel)
-        # every selected logit is at least every unselected one, up to the band
         if rest.size:
             assert lg[sel].min() >= lg[rest].max() - band, f"token {t}: not a top-k"
-        # slots in descending order up to the band
-        assert np.all(np.diff(lg[sel]) <= band), f"token {t}: slots out of order"
-        # and the disagreement is a near-tie in float64
-        ref_sel = idx_ref[t]
-        assert abs(lg[sel].sum() - lg[ref_sel].sum()) <= len(sel) * band, f"token {t}: real flip"
+        for j in np.flatnonzero(sel != idx_ref[t]):
+            a, r = int(sel[j]), int(idx_ref[t, j])
+            assert abs(lg[a] - lg[r]) <= band, (
+                f"token {t} slot {j}: expert {a} vs {r}, float64 logits "
+                f"{lg[a]:.9g} vs {lg[r]:.9g} differ by more than the band {band:.3g}")
     return int(diff.size)
+
+
+def check_routing_on_own_logits(idx_gpu, w_gpu, logits_gpu, k):
+    """The GPU's indices equal, bit for bit, the oracle's selection run on
+    the GPU's own fp32 logits; its weights equal the oracle's renormalised
+    softmax of those logits within the stated bar."""
+    lg = np.asarray(logits_gpu, dtype=np.float64)
+    ref = mo.select_topk(lg, k)
+    np.testing.assert_array_equal(np.asarray(idx_gpu, dtype=np.int64), ref)
+    assert_close("topk_w (own logits)", w_gpu, mo.topk_weights(lg, ref))
 
 
 def gpu_forward_backward(layer, inp, forced_idx=None, backward=True, dev="cuda"):
@@ -227,26 +295,26 @@ def compare_full(layer, inp, k, align, backward=True, report=None):
     x64 = mo.as_f64(inp["x"])
     fw = mo.forward(inp["x"], inp["w_router"], inp.get("bias"), inp["w_gate"], inp["w_up"],
                     inp["w_down"], k)
-    # 1) free routing on the GPU: logits within tolerance, indices exact up to near-ties
+    # 1) free routing on the GPU: indices exactly the oracle's selection on the
+    #    GPU's fp32 logits; logits within the bar; against the float64 logits
+    #    exact up to near-ties
     b, _, _ = gpu_forward_backward(layer, inp, None, backward=False)
     lg_gpu = to_np(b.logits)
+    check_routing_on_own_logits(to_np(b.topk_idx), to_np(b.topk_w), lg_gpu, k)
     assert_close("logits", lg_gpu, fw["logits"])
     band = tie_band(lg_gpu, fw["logits"])
     flips = check_routing(to_np(b.topk_idx), fw["idx"], fw["logits"], band)
     # 2) everything downstream, with the oracle's routing forced on both sides
-    b, _, _ = gpu_forward_backward(layer, inp, fw["idx"], backward=backward)
+    b, _, dy = gpu_forward_backward(layer, inp, fw["idx"], backward=backward)
     bw = None
     if backward:
         bw = mo.backward(inp["x"], inp["w_router"], inp.get("bias"), inp["w_gate"], inp["w_up"],
                          inp["w_down"], k, inp["dy"], fwd=fw)
     mag = magnitudes(inp, fw, bw, k)
 
-    def check_out(name, got, ref, key):
-        return assert_mag_close(name, got, ref, mag[key])
-
     out = {"near_tie_tokens": flips}
     np.testing.assert_array_equal(to_np(b.topk_idx), fw["idx"])
-    assert_close("topk_w", to_np(b.topk_w), fw["w"])
+    out["topk_w"] = assert_close("topk_w", to_np(b.topk_w), fw["w"])
     T = x64.shape[0]
     E = layer.E
     maps = mo.permute_maps(fw["idx"], E, align, b.R_cap)
@@ -257,31 +325,37 @@ def compare_full(layer, inp, k, align, backward=True, report=None):
     R_pad = maps["R_pad"]
     dst = maps["dst_row"]
     pad = np.setdiff1d(np.arange(R_pad), dst)
+    tok = np.arange(T * k) // k
 
     def rows(buf):
         return to_np(buf[:R_pad])
 
     xp = rows(b.xp)
-    np.testing.assert_array_equal(xp[dst], x64[np.arange(T * k) // k])   # a copy: exact
+    np.testing.assert_array_equal(xp[dst], x64[tok])   # a copy: exact
     assert np.all(xp[pad] == 0)
     for name, buf in (("G", b.g), ("U", b.u), ("A", b.a), ("Yu", b.yp)):
         r = rows(buf)
         out[name] = assert_mag_close(name, r[dst], fw[name], mag[name])
         assert np.all(r[pad] == 0), f"{name}: padding rows not zero"
-    out["y"] = check_out("y", to_np(b.y), fw["y"], "y")
+    out["y"] = assert_bf16_out_close("y", to_np(b.y), fw["y"])
+    out["y_bf16_floor"] = bf16_floor(fw["y"])
     if not backward:
         return out, b
+    dyg = rows(b.dyg)
+    np.testing.assert_array_equal(dyg[dst], mo.as_f64(inp["dy"])[tok])   # a copy: exact
+    assert np.all(dyg[pad] == 0)
     for name, buf, key in (("dYp", b.dyp, "dYu"), ("dG", b.dg, "dG"), ("dU", b.du, "dU"),
                            ("dXp", b.dxp, "dXp")):
         r = rows(buf)
         out[name] = assert_mag_close(name, r[dst], bw[key], mag[key])
         assert np.all(r[pad] == 0), f"{name}: padding rows not zero"
-    out["d_topk_w"] = check_out("d_topk_w", to_np(b.d_topk_w), bw["d_topk_w"], "d_topk_w")
-    for name, buf, key in (("dx", b.dx, "dx"), ("dw_gate", b.dw_gate, "dw_gate"),
-                           ("dw_up", b.dw_up, "dw_up"), ("dw_down", b.dw_down, "dw_down"),
-                           ("dw_router", b.dw_router, "dw_router")):
-        out[name] = check_out(name, to_np(buf), bw[key], key)
-    out["dbias"] = check_out("dbias", to_np(b.dbias), bw["dbias"], "dbias")
+    out["d_topk_w"] = assert_close("d_topk_w", to_np(b.d_topk_w), bw["d_topk_w"])
+    out["dx"] = assert_bf16_out_close("dx", to_np(b.dx), bw["dx"])
+    out["dx_bf16_floor"] = bf16_floor(bw["dx"])
+    for name, buf in (("dw_gate", b.dw_gate), ("dw_up", b.dw_up), ("dw_down", b.dw_down)):
+        out[name] = assert_mag_close(name, to_np(buf), bw[name], mag[name])
+    for name, buf in (("dw_router", b.dw_router), ("dbias", b.dbias)):
+        out[name] = assert_close(name, to_np(buf), bw[name])
     # experts with no rows get exactly zero weight gradients
     empty = np.flatnonzero(maps["counts"] == 0)
     for e in empty:

@@ -135,3 +135,25 @@ class SampledChecker(SampledLayer):
         return dict(dwg=dwg, dwu=dwu, dwd=dwd,
                     Mdwg=ax.T @ MdG_c + np.abs(dwg), Mdwu=ax.T @ MdU_c + np.abs(dwu),
                     Mdwd=MA[:, c] @ np.abs(dYu) + np.abs(A[:, c]) @ MdYu + np.abs(dwd))
+
+    def expert_mags(self, e):
+        """Magnitudes of every row of expert e (keys MG, MU, MA, MYu and, with
+        dy, MdYu, MdG, MdU, MdXp; rows in ascending pair id) and of its whole
+        weight gradients (Mdwg, Mdwu, Mdwd), by the rules above."""
+        pairs = self.pairs_of[e]
+        pm = self.pairs_mag(pairs)
+        keys = ["G", "U", "A", "Yu"] + (["dYu", "dG", "dU", "dXp"] if self.dy is not None else [])
+        out = {}
+        for key in keys:
+            out[key] = np.stack([pm[int(p)][key] for p in pairs])
+            out["M" + key] = np.stack([pm[int(p)]["M" + key] for p in pairs])
+        if self.dy is not None:
+            ax = np.abs(self.x[pairs // self.k])
+            dwg = self.x[pairs // self.k].T @ out["dG"]
+            dwu = self.x[pairs // self.k].T @ out["dU"]
+            dwd = out["A"].T @ out["dYu"]
+            out.update(dwg=dwg, dwu=dwu, dwd=dwd,
+                       Mdwg=ax.T @ out["MdG"] + np.abs(dwg), Mdwu=ax.T @ out["MdU"] + np.abs(dwu),
+                       Mdwd=out["MA"].T @ np.abs(out["dYu"]) + np.abs(out["A"]).T @ out["MdYu"]
+                       + np.abs(dwd))
+        return out

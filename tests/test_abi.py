@@ -78,6 +78,17 @@ def test_host_argument_checks(lib):
     # expert GEMMs: f not a multiple of 8
     assert lib.moe_expert_fwd(P, P, None, 4, 2, 4, 8, 12, cap, P, P, P, P, P, P, P, None) == L.MOE_ERR_UNSUPPORTED
     assert lib.moe_expert_fwd(P, None, None, 4, 2, 4, 8, 16, cap, P, P, P, P, P, P, P, None) == L.MOE_ERR_ARG
+    # expert backward: a missing row buffer (the gathered dY rows)
+    wse = lib.moe_expert_bwd_workspace_size(cap, 16)
+    assert wse >= cap * 2 * 4                  # at least one n-tile's two partials per row
+    assert lib.moe_expert_bwd_workspace_size(0, 16) == 0
+    ebwd = lambda dyg, ws, nb: lib.moe_expert_bwd(  # noqa: E731
+        P, P, P, P, P, 4, 2, 4, 8, 16, cap, P, P, P, P, P, P, P,
+        dyg, P, P, P, P, P, P, P, P, ws, nb, None)
+    assert ebwd(None, P, wse) == L.MOE_ERR_ARG
+    # expert backward: workspace missing or too small
+    assert ebwd(P, None, wse) == L.MOE_ERR_ARG
+    assert ebwd(P, P, wse - 1) == L.MOE_ERR_ARG
     # combine: k above the slot limit
     assert lib.moe_combine(P, P, None, 4, 33, 8, P, None) == L.MOE_ERR_UNSUPPORTED
     # route backward: workspace missing

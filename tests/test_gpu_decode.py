@@ -3,7 +3,8 @@ oracle.
 
 Free routing: logits within tolerance, top-k indices exact up to near-ties.
 Then the oracle's selection forced on the GPU: indices exact, weights and y
-within the bf16 bar. Cases span one to eight tokens, ragged expert counts
+within the bar (y, a bf16 output: 2e-2 RMS plus half an ulp of bf16; the
+exact top-k of the kernel's own fp32 logits). Cases span one to eight tokens, ragged expert counts
 (E not a multiple of 32), k = 1 and k = 32 (256 pairs), E = 1024, narrow rows
 (several warp groups per row lane set), rows wider than 4096 columns (two
 column blocks), and the decode workloads' full layer shape.
@@ -15,8 +16,8 @@ import pytest
 import torch
 
 import workloads
-from harness import (assert_close, assert_mag_close, check_routing, magnitudes, tie_band,
-                     to_np)
+from harness import (assert_bf16_out_close, assert_close, check_routing,
+                     check_routing_on_own_logits, tie_band, to_np)
 from oracle import moe_oracle as mo
 
 pytestmark = pytest.mark.gpu
@@ -71,14 +72,14 @@ def test_decode_parity(name):
     assert layer.status() == 0
     lg = to_np(b.logits)
     assert_close("logits", lg, fw["logits"])
+    check_routing_on_own_logits(to_np(b.topk_idx), to_np(b.topk_w), lg, k)
     check_routing(to_np(b.topk_idx), fw["idx"], fw["logits"], tie_band(lg, fw["logits"]))
     # the oracle's selection forced
     b = _run(layer, x, fw["idx"])
     assert layer.status() == 0
     np.testing.assert_array_equal(to_np(b.topk_idx), fw["idx"])
     assert_close("topk_w", to_np(b.topk_w), fw["w"])
-    mag = magnitudes(inp, fw, None, k)
-    err = assert_mag_close("y", to_np(b.y), fw["y"], mag["y"])
+    err = assert_bf16_out_close("y", to_np(b.y), fw["y"])
     print(name, "y max|diff|/RMS", round(err, 5))
 
 
@@ -94,10 +95,10 @@ def test_decode_full_workload_shape():
     lg = to_np(b.logits)
     assert_close("logits", lg, fw["logits"])
     check_routing(to_np(b.topk_idx), fw["idx"], fw["logits"], tie_band(lg, fw["logits"]))
+    check_routing_on_own_logits(to_np(b.topk_idx), to_np(b.topk_w), lg, wl.k)
     b = _run(layer, x, fw["idx"])
     assert layer.status() == 0
-    mag = magnitudes(inp, fw, None, wl.k)
-    assert_mag_close("y", to_np(b.y), fw["y"], mag["y"])
+    assert_bf16_out_close("y", to_np(b.y), fw["y"])
 
 
 def test_decode_repeated_expert():
@@ -112,8 +113,7 @@ def test_decode_repeated_expert():
     assert layer.status() == 0
     np.testing.assert_array_equal(to_np(b.topk_idx), forced)
     assert_close("topk_w", to_np(b.topk_w), fw["w"])
-    mag = magnitudes(inp, fw, None, k)
-    assert_mag_close("y", to_np(b.y), fw["y"], mag["y"])
+    assert_bf16_out_close("y", to_np(b.y), fw["y"])
 
 
 def test_decode_bad_forced_index():
@@ -130,13 +130,11 @@ def test_decode_bad_forced_index():
     good = [0, 1, 3]
     sub = {key: (v[good] if key == "x" else v) for key, v in inp.items()}
     fw_good = _oracle(sub, k, idx=forced[good])
-    mag = magnitudes(sub, fw_good, None, k)
     y = to_np(b.y)
-    assert_mag_close("y (valid tokens)", y[good], fw_good["y"], mag["y"])
+    assert_bf16_out_close("y (valid tokens)", y[good], fw_good["y"])
     one = {key: (v[2:3] if key == "x" else v) for key, v in inp.items()}
     fw_one = _oracle(one, k - 1, idx=np.array([[6, 1]]))
-    mag1 = magnitudes(one, fw_one, None, k - 1)
-    assert_mag_close("y (token with a dropped slot)", y[2:3], fw_one["y"], mag1["y"])
+    assert_bf16_out_close("y (token with a dropped slot)", y[2:3], fw_one["y"])
 
 
 def test_decode_two_runs_bitwise_equal():

@@ -1,10 +1,12 @@
-"""The sampled evaluation (oracle/sampled.py + tests/sampled_check.py) agrees
-with the whole-layer oracle and with the whole-tensor error magnitudes."""
+"""The sampled evaluation (oracle/sampled.py + tests/sampled_check.py) and the
+expert-by-expert evaluation (oracle/streamed.py) agree with the whole-layer
+oracle and with the whole-tensor error magnitudes."""
 import numpy as np
 
 import workloads
 from harness import magnitudes
 from oracle import moe_oracle as mo
+from oracle.streamed import stream_layer
 from sampled_check import SampledChecker
 
 
@@ -42,3 +44,38 @@ def test_sampled_matches_full_oracle_and_magnitudes():
                 np.testing.assert_allclose(w["Mdwg"], mag["dw_gate"][e][:, c], rtol=1e-10)
                 np.testing.assert_allclose(w["Mdwu"], mag["dw_up"][e][:, c], rtol=1e-10)
                 np.testing.assert_allclose(w["Mdwd"], mag["dw_down"][e][c, :], rtol=1e-10)
+
+
+def test_streamed_layer_matches_full_oracle():
+    """Skewed routing with empty experts; kept experts' rows and weight
+    gradients, and every token's y, dx, d_topk_w, dW_r, db."""
+    wl = workloads.Workload("st", T=64, d=40, f=24, E=12, k=3, zipf_s=1.2)
+    inp = workloads.generate(wl, tau=1.5)
+    fw = mo.forward(inp["x"], inp["w_router"], inp["bias"], inp["w_gate"], inp["w_up"],
+                    inp["w_down"], wl.k)
+    bw = mo.backward(inp["x"], inp["w_router"], inp["bias"], inp["w_gate"], inp["w_up"],
+                     inp["w_down"], wl.k, inp["dy"], fwd=fw)
+    counts = np.bincount(fw["idx"].reshape(-1), minlength=wl.E)
+    assert (counts == 0).any()
+    keep = [int(e) for e in np.flatnonzero(counts > 0)[:3]]
+    st = stream_layer(inp, fw["logits"], fw["idx"], wl.k, keep=keep)
+    for key, ref in (("y", fw["y"]), ("dx", bw["dx"]), ("d_topk_w", bw["d_topk_w"]),
+                     ("dl", bw["dl"]), ("dw_router", bw["dw_router"]), ("dbias", bw["dbias"])):
+        np.testing.assert_allclose(st[key], ref, rtol=1e-10, atol=1e-12, err_msg=key)
+    mag = magnitudes(inp, fw, bw, wl.k)
+    sc = SampledChecker(inp, fw["logits"], fw["idx"], wl.k)
+    for e in keep:
+        rec = st["experts"][e]
+        pairs = rec["pairs"]
+        np.testing.assert_array_equal(pairs, np.flatnonzero(fw["idx"].reshape(-1) == e))
+        for key, src in (("G", fw), ("U", fw), ("A", fw), ("Yu", fw), ("dYu", bw), ("dG", bw),
+                         ("dU", bw), ("dXp", bw)):
+            np.testing.assert_allclose(rec[key], src[key][pairs], rtol=1e-10, atol=1e-12)
+        for key in ("dw_gate", "dw_up", "dw_down"):
+            np.testing.assert_allclose(rec[key], bw[key][e], rtol=1e-10, atol=1e-12)
+        em = sc.expert_mags(e)
+        for key in ("G", "U", "A", "Yu", "dYu", "dG", "dU", "dXp"):
+            np.testing.assert_allclose(em["M" + key], mag[key][pairs], rtol=1e-10)
+        np.testing.assert_allclose(em["Mdwg"], mag["dw_gate"][e], rtol=1e-10)
+        np.testing.assert_allclose(em["Mdwu"], mag["dw_up"][e], rtol=1e-10)
+        np.testing.assert_allclose(em["Mdwd"], mag["dw_down"][e], rtol=1e-10)
