@@ -139,7 +139,9 @@ int moe_permute(const int32_t* topk_idx, int64_t T, int k, int E, int align,
  *    pairs at E = 64; use moe_permute with a workspace beyond that).
  *  - The first call on each device looks up the array's device address with
  *    cudaGetSymbolAddress (a host-side call with that device current); make
- *    that first call before any stream capture begins.
+ *    that first call before any stream capture begins. The address is kept
+ *    for the life of the process: after cudaDeviceReset on that device it is
+ *    no longer valid, so do not call this entry point again in that process.
  *  - All calls share the one array, and it keeps the last call's contents:
  *    calls whose work overlaps on the GPU (different streams, or different
  *    host threads on one device) race on it and must be serialised by the

@@ -23,7 +23,10 @@ int* device_status_ptr() {
   std::lock_guard<std::mutex> lock(mu);
   if (!ptrs[dev]) {
     void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_moe_status) != cudaSuccess) return nullptr;
+    if (cudaGetSymbolAddress(&p, g_moe_status) != cudaSuccess) {
+      cudaGetLastError();   // leave no stale error for the next call's launch check
+      return nullptr;
+    }
     ptrs[dev] = static_cast<int*>(p);
   }
   return ptrs[dev];

@@ -29,7 +29,10 @@ void* scratch_ptr() {
   std::lock_guard<std::mutex> lock(mu);
   if (!ptrs[dev]) {
     void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_permute_scratch) != cudaSuccess) return nullptr;
+    if (cudaGetSymbolAddress(&p, g_permute_scratch) != cudaSuccess) {
+      cudaGetLastError();   // leave no stale error for the next call's launch check
+      return nullptr;
+    }
     ptrs[dev] = p;
   }
   return ptrs[dev];
