@@ -11,7 +11,14 @@ between a barrier + synchronize on both sides; the slowest rank's time counts.
 Prints one JSON line (rank 0).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                  [--config NAME] [--no-cpu-baseline]
+                  [--config NAME] [--no-cpu-baseline] [--no-side]
+
+With the default workload, the line also carries "configs": the
+Qwen3-30B-A3B-shaped layer, the small-M forward sweep (T = 128 ... 2048) and
+the fine-grained 512-expert layer, each timed in the same run (median step,
+whole-step roofline, every expert GEMM against its bound, the benchmark spec's
+targets, its own clock record). ms_per_step is the median of the timed
+steps; value = tokens / median step.
 
 --impl reference times the float64 CPU oracle (the deliberately slow,
 obviously correct definition) on a bounded sample of the same workload on
@@ -61,6 +68,10 @@ def parse_args(argv=None):
     ap.add_argument("--ref-tokens", type=int, default=1,
                     help="tokens per step of the reference (oracle) arm")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-side", action="store_true",
+                    help="time the headline workload only (not the other workloads)")
+    ap.add_argument("--side-steps", type=int, default=30,
+                    help="timed steps of each other workload")
     ap.add_argument("--path", choices=["auto", "general", "decode"], default="auto",
                     help="decode: the one-launch forward (moe_decode_fwd), forward-only "
                          "workloads of at most 8 tokens; auto: the general path, measured "
@@ -108,7 +119,7 @@ class ClockSampler:
             self.fh = open(self.path, "w")
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={CLOCK_QUERY}",
-                 "--format=csv,noheader", "-lms", "200"], stdout=self.fh,
+                 "--format=csv,noheader", "-lms", "50"], stdout=self.fh,
                 stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
@@ -144,8 +155,16 @@ def parse_clock_rows(rows) -> dict | None:
         return None
     names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
     reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
-    return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx) if mx else None,
-            "samples": len(sm), "reasons": reasons}
+    # samples under load: power draw in the upper half of the range the run saw
+    pw = [mhz(r[3]) for r in rows]
+    load = sm
+    if all(p is not None for p in pw) and len(pw) == len(sm) and max(pw) > min(pw):
+        cut = (max(pw) + min(pw)) / 2
+        load = [c for c, p in zip(sm, pw) if p >= cut] or sm
+    return {"sm_mhz": statistics.median(load), "sm_max_mhz": max(mx) if mx else None,
+            "samples": len(sm), "samples_under_load": len(load),
+            "sm_mhz_all_samples": statistics.median(sm), "reasons": reasons,
+            "period_ms": 50}
 
 
 # ---------------------------------------------------------- distributed --
@@ -237,6 +256,162 @@ def recorded_traffic(kernel: str, config: str):
 
 # ---------------------------------------------------------------- ours --
 
+# the workloads timed beside the headline one, in the same run (fwd+bwd unless
+# the workload is forward-only): Qwen3-30B-A3B-shaped, the small-M sweep and
+# the fine-grained 512-expert layer
+SIDE_CONFIGS = ["qwen3_30b", "smallm_T128", "smallm_T512", "smallm_T1024", "smallm_T2048",
+                "fine512"]
+# the benchmark spec's per-workload targets: expert GEMMs bound by the tensor cores
+# at >= 60% of the bf16 peak, those bound by HBM at >= 70% of its bandwidth
+TARGET_TENSOR = 0.60
+TARGET_HBM = 0.70
+GEMM_KERNELS = ("gateup_fwd", "down_fwd", "down_dgrad", "gateup_dgrad", "wgrad_down",
+                "wgrad_gateup")
+
+
+def kernel_roofline(name, fl, by, ms, peaks):
+    """Achieved rate of one launch against the bound its algorithmic FLOPs and
+    bytes put it under (measured burst peaks; the sustained bf16 fraction too)."""
+    t_tensor = fl / (peaks["bf16_tflops"] * 1e12)
+    t_hbm = by / (peaks["hbm_gbs"] * 1e9)
+    if t_tensor >= t_hbm:
+        achieved = fl / (ms * 1e-3) / 1e12
+        return {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"],
+                "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops"],
+                "frac_of_sustained": achieved / peaks["bf16_tflops_sustained"],
+                "peak_kind": f"bf16 burst, {peaks['source']}"}
+    achieved = by / (ms * 1e-3) / 1e9
+    return {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+            "frac": achieved / peaks["hbm_gbs"], "peak_kind": f"hbm copy, {peaks['source']}"}
+
+
+def time_steps(run, steps, stream, flush_buf, dom_timer=None):
+    """Times `steps` calls of run() with CUDA events on `stream`, one pair of
+    events per step; with flush_buf, L2 is flushed (a write of twice its size)
+    before each step, outside the step's events. Returns per-step ms and the
+    span from the first step's start to the last step's end."""
+    import torch
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
+    pairs = []
+    if flush_buf is None:
+        evs[0].record(stream)
+        for i in range(steps):
+            run()
+            evs[i + 1].record(stream)
+    else:
+        for _ in range(steps):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            flush_buf.zero_()
+            e0.record(stream)
+            run()
+            e1.record(stream)
+            pairs.append((e0, e1))
+    torch.cuda.synchronize()
+    if flush_buf is None:
+        per = [evs[i].elapsed_time(evs[i + 1]) for i in range(steps)]
+        span = evs[0].elapsed_time(evs[steps])
+    else:
+        per = [a.elapsed_time(b) for a, b in pairs]
+        span = sum(per)
+    return per, span
+
+
+def profile_kernels(step, kernels, lib_mod):
+    """Per-launch device ms of each kernel group, from three steps each (the
+    library's event timer, outside any timed region)."""
+    per_kernel = {}
+    for name in kernels:
+        lib_mod.call("moe_timer_start", lib_mod.KERNELS[name], 8)
+        for _ in range(3):
+            step()
+        ms, n = lib_mod.ctypes.c_float(), lib_mod.ctypes.c_int()
+        lib_mod.call("moe_timer_read", lib_mod.ctypes.byref(ms), lib_mod.ctypes.byref(n))
+        per_kernel[name] = ms.value / max(n.value, 1)
+    return per_kernel
+
+
+def run_side(name, dev, local_rank, peaks, steps, warmup):
+    """One of the other workloads, timed in the same run: median step, the
+    whole-step roofline, every expert GEMM against its bound, the small-M
+    sweep's expert-weight streaming rate, and the benchmark spec's targets."""
+    import torch
+    import workloads
+    from mixture_experts_routed_softmax_gb300 import _lib, accounting
+    from mixture_experts_routed_softmax_gb300.layer import MoELayer
+
+    wl = workloads.CONFIGS[name]
+    inp = workloads.generate_device(wl, dev, with_dy=wl.backward)
+    layer = MoELayer(inp["w_router"], inp["bias"], inp["w_gate"], inp["w_up"], inp["w_down"],
+                     wl.k, wl.align)
+    b = layer.buffers(wl.T, backward=wl.backward)
+    x = inp["x"]
+    dy = inp.get("dy")
+
+    def step():
+        layer.forward(x, b)
+        if wl.backward:
+            layer.backward(dy, b)
+
+    sampler = ClockSampler(local_rank).start()
+    for _ in range(max(warmup, 3)):
+        step()
+    st = layer.status()
+    if st != 0:
+        raise RuntimeError(f"{name}: device status {st}: {_lib.status_str(st)}")
+    kernels = STEP_KERNELS if wl.backward else FWD_KERNELS
+    per_kernel = profile_kernels(step, kernels, _lib)
+    shape = accounting.Shape(T=wl.T, d=wl.d, f=wl.f, E=wl.E, k=wl.k,
+                             E_active=int((b.counts > 0).sum()))
+    costs = accounting.kernel_costs(shape, wl.backward)
+    F = sum(c[0] for c in costs.values())
+    B = sum(c[1] for c in costs.values())
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = B < 4 * l2
+    flush_buf = torch.empty(2 * l2, dtype=torch.uint8, device=dev) if flush else None
+    stream = torch.cuda.current_stream()
+    per, span = time_steps(step, steps, stream, flush_buf)
+    clocks = sampler.stop()
+    st = layer.status()
+    if st != 0:
+        raise RuntimeError(f"{name}: device status {st}: {_lib.status_str(st)}")
+    med = statistics.median(per)
+    t_roof = accounting.roofline_seconds(F, B, peaks["bf16_tflops"], peaks["hbm_gbs"])
+    gemms = {}
+    for k_ in GEMM_KERNELS:
+        if k_ in per_kernel:
+            r = kernel_roofline(k_, *costs[k_], per_kernel[k_], peaks)
+            gemms[k_] = {"ms": round(per_kernel[k_], 4), "bound": r["bound"],
+                         "achieved": round(r["achieved"], 1), "unit": r["unit"],
+                         "frac": round(r["frac"], 3)}
+    dominant = max(per_kernel, key=per_kernel.get)
+    dom = kernel_roofline(dominant, *costs[dominant], per_kernel[dominant], peaks)
+    dom.update(kernel=dominant, ms_per_launch=per_kernel[dominant])
+    out = {"workload": f"{wl.name}: {wl.note}", "T": wl.T, "d": wl.d, "f": wl.f, "E": wl.E,
+           "k": wl.k, "align": wl.align, "backward": wl.backward, "tau": inp.get("tau"),
+           "E_active": shape.E_active, "steps": steps, "ms_per_step": med,
+           "ms_per_step_mean": span / steps, "tokens_per_s": wl.T / (med * 1e-3),
+           "l2": "flushed between steps" if flush else "inputs larger than L2",
+           "layer_roofline": {"flops": F, "bytes": B, "t_roof_ms": t_roof * 1e3,
+                              "frac": t_roof * 1e3 / med},
+           "roofline": dom, "gemms": gemms,
+           "kernels_ms": {k_: round(v, 4) for k_, v in per_kernel.items()}, "clocks": clocks}
+    misses = [k_ for k_, g in gemms.items()
+              if g["frac"] < (TARGET_TENSOR if g["bound"] == "tensor" else TARGET_HBM)]
+    if not wl.backward:
+        # the small-M sweep is reported as the rate the forward streams the
+        # active experts' weights (Halo "Performance", §Levers that do not help here)
+        wbytes = 3 * shape.E_active * wl.d * wl.f * 2
+        gbs = wbytes / (med * 1e-3) / 1e9
+        out["weight_stream"] = {"bytes": wbytes, "gbs": gbs, "frac": gbs / peaks["hbm_gbs"]}
+        if gbs / peaks["hbm_gbs"] < TARGET_HBM:
+            misses.append("weight_stream")
+    out["targets"] = {"tensor_bound_gemm_frac": TARGET_TENSOR, "hbm_bound_frac": TARGET_HBM,
+                      "met": not misses, "missed": misses}
+    del layer, b, inp
+    torch.cuda.empty_cache()
+    return out
+
+
 def run_ours(args, rank, world, local_rank):
     import torch
     import workloads
@@ -263,6 +438,7 @@ def run_ours(args, rank, world, local_rank):
     x = inp["x"].to(dev)
     dy = inp["dy"].to(dev) if wl.backward else None
     lib = _lib.load()
+    peaks = load_peaks()
 
     def step():
         fwd(x, b)
@@ -274,6 +450,9 @@ def run_ours(args, rank, world, local_rank):
             return int(torch.unique(b.topk_idx).numel())
         return int((b.counts > 0).sum())
 
+    # SM clocks and throttle reasons are sampled from the first warm-up step to
+    # the end of the timed region
+    sampler = ClockSampler(local_rank).start()
     for _ in range(max(args.warmup, 3)):
         step()
     status = layer.status()
@@ -281,15 +460,7 @@ def run_ours(args, rank, world, local_rank):
         raise RuntimeError(f"device status {status}: {_lib.status_str(status)}")
 
     kernels = ["decode"] if decode else (STEP_KERNELS if wl.backward else FWD_KERNELS)
-    # three profiled steps per kernel group (outside the timed region)
-    per_kernel = {}
-    for name in kernels:
-        _lib.call("moe_timer_start", _lib.KERNELS[name], 8)
-        for _ in range(3):
-            step()
-        ms, n = _lib.ctypes.c_float(), _lib.ctypes.c_int()
-        _lib.call("moe_timer_read", _lib.ctypes.byref(ms), _lib.ctypes.byref(n))
-        per_kernel[name] = ms.value / max(n.value, 1)
+    per_kernel = profile_kernels(step, kernels, _lib)
     # "combine" fires twice per step (y and dx); the timer averaged both
     dominant = max(per_kernel, key=per_kernel.get)
 
@@ -310,6 +481,8 @@ def run_ours(args, rank, world, local_rank):
         for _ in range(3):
             run()
     else:
+        # the dominant kernel's own launches are timed live, on the stream the
+        # library launches them on, inside the timed region
         _lib.call("moe_timer_start", _lib.KERNELS[dominant], args.steps * 2)
     # A step that moves less than four L2s of data would find its weights in
     # L2 again on the next step: then L2 is flushed (a write of twice its
@@ -323,31 +496,11 @@ def run_ours(args, rank, world, local_rank):
     step_bytes = sum(c[1] for c in costs.values())
     flush = step_bytes < 4 * l2_bytes
     flush_buf = torch.empty(2 * l2_bytes, dtype=torch.uint8, device=dev) if flush else None
-    sampler = ClockSampler(local_rank).start()
     launches0 = int(lib.moe_kernel_launches())
     barrier()
     torch.cuda.synchronize()
-    ev0 = torch.cuda.Event(enable_timing=True)
-    ev1 = torch.cuda.Event(enable_timing=True)
-    if flush:
-        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-               for _ in range(args.steps)]
-        for e0, e1 in evs:
-            flush_buf.zero_()
-            e0.record(stream)
-            run()
-            e1.record(stream)
-        torch.cuda.synchronize()
-        barrier()
-        elapsed_ms = sum(e0.elapsed_time(e1) for e0, e1 in evs)
-    else:
-        ev0.record(stream)
-        for _ in range(args.steps):
-            run()
-        ev1.record(stream)
-        torch.cuda.synchronize()
-        barrier()
-        elapsed_ms = ev0.elapsed_time(ev1)
+    per_step, span_ms = time_steps(run, args.steps, stream, flush_buf)
+    barrier()
     launches = int(lib.moe_kernel_launches()) - launches0 + graph_launches * args.steps
     clocks = sampler.stop()
     if args.graph:
@@ -359,7 +512,9 @@ def run_ours(args, rank, world, local_rank):
     status = layer.status()
     if status != 0:
         raise RuntimeError(f"device status {status}: {_lib.status_str(status)}")
-    max_ms = max_over_ranks(elapsed_ms, dev)
+    # the median step (the survey's protocol); the slowest rank's counts
+    med_ms = max_over_ranks(statistics.median(per_step), dev)
+    span_ms = max_over_ranks(span_ms, dev)
 
     # --------------------------------------------------------- end to end --
     # Every step copies its inputs (x, dY) from pinned host memory and its
@@ -384,6 +539,8 @@ def run_ours(args, rank, world, local_rank):
         h2d = [torch.cuda.Event() for _ in range(2)]
         done = [torch.cuda.Event() for _ in range(2)]
         d2h = [torch.cuda.Event() for _ in range(2)]
+        ev0 = torch.cuda.Event(enable_timing=True)
+        ev1 = torch.cuda.Event(enable_timing=True)
 
         def upload(j):
             with torch.cuda.stream(up):
@@ -429,36 +586,31 @@ def run_ours(args, rank, world, local_rank):
                "overlap": "uploads and downloads on two copy streams, two buffer sets"}
 
     # ----------------------------------------------------------- roofline --
-    peaks = load_peaks()
-    key = "combine" if dominant == "combine" else dominant
-    fl, by = costs[key]
-    t_tensor = fl / (peaks["bf16_tflops_sustained"] * 1e12)
-    t_hbm = by / (peaks["hbm_gbs"] * 1e9)
-    if t_tensor >= t_hbm:
-        achieved = fl / (dom_ms * 1e-3) / 1e12
-        roof = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops_sustained"],
-                "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops_sustained"]}
-        roof["peak_kind"] = f"bf16 sustained, {peaks['source']}"
-    else:
-        achieved = by / (dom_ms * 1e-3) / 1e9
-        roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                "frac": achieved / peaks["hbm_gbs"]}
-        roof["peak_kind"] = f"hbm copy, {peaks['source']}"
+    fl, by = costs[dominant]
+    roof = kernel_roofline(dominant, fl, by, dom_ms, peaks)
     roof["kernel"] = dominant
     roof["ms_per_launch"] = dom_ms
     roof["algorithmic_flops_per_launch"] = fl
     roof["algorithmic_bytes_per_launch"] = by
     roof["traffic"] = recorded_traffic(dominant, args.config)
 
-    ms_per_step = max_ms / args.steps
     F = sum(c[0] for c in costs.values())
     B = sum(c[1] for c in costs.values())
     t_roof = accounting.roofline_seconds(F, B, peaks["bf16_tflops"], peaks["hbm_gbs"])
-    value = world * wl.T * args.steps / (max_ms / 1e3)
+    value = world * wl.T / (med_ms / 1e3)
+    gemms = {}
+    for k_ in GEMM_KERNELS:
+        if k_ in per_kernel:
+            r = kernel_roofline(k_, *costs[k_], per_kernel[k_], peaks)
+            gemms[k_] = {"ms": round(per_kernel[k_], 4), "bound": r["bound"],
+                         "achieved": round(r["achieved"], 1), "unit": r["unit"],
+                         "frac": round(r["frac"], 3)}
+    misses = [k_ for k_, g in gemms.items()
+              if g["frac"] < (TARGET_TENSOR if g["bound"] == "tensor" else TARGET_HBM)]
 
     out = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
-        "warmup": max(args.warmup, 3), "ms_per_step": ms_per_step, "higher_is_better": True,
+        "warmup": max(args.warmup, 3), "ms_per_step": med_ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": f"{wl.name}: {wl.note}", "T": wl.T, "d": wl.d, "f": wl.f,
                    "E": wl.E, "k": wl.k, "align": wl.align, "backward": wl.backward,
@@ -469,19 +621,31 @@ def run_ours(args, rank, world, local_rank):
                    "graph": bool(args.graph),
                    "path": "decode (one launch)" if decode else "general",
                    "parallelism": f"replicas x{world}"},
+        "timing": {"ms_per_step": "median of the timed steps (one event pair each)",
+                   "ms_per_step_mean": span_ms / args.steps,
+                   "ms_min": min(per_step), "ms_max": max(per_step)},
         "roofline": roof,
         "layer_roofline": {"flops": F, "bytes": B, "t_roof_ms": t_roof * 1e3,
-                           "frac": t_roof * 1e3 / ms_per_step,
+                           "frac": t_roof * 1e3 / med_ms,
                            "peaks": f"bf16 {peaks['bf16_tflops']} TFLOP/s burst, "
                                     f"HBM {peaks['hbm_gbs']} GB/s, {peaks['source']}",
-                           "tflops_achieved": F / (ms_per_step * 1e-3) / 1e12,
+                           "tflops_achieved": F / (med_ms * 1e-3) / 1e12,
                            "E_active": shape.E_active},
+        "gemms": gemms,
+        "targets": {"tensor_bound_gemm_frac": TARGET_TENSOR, "hbm_bound_frac": TARGET_HBM,
+                    "met": not misses, "missed": misses},
         "pairs_per_s": value * wl.k,
         "kernels_ms": {k_: round(v, 4) for k_, v in per_kernel.items()},
         "gpu_launches": launches,
         "clocks": clocks,
         "e2e": e2e,
     }
+    if not args.no_side and not decode and args.config == DEFAULT_CONFIG:
+        # the other workloads, each timed in this same run (their own clock record)
+        del b
+        torch.cuda.empty_cache()
+        out["configs"] = {n: run_side(n, dev, local_rank, peaks, args.side_steps, 3)
+                          for n in SIDE_CONFIGS}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:   # the oracle beside N = 1 only
         tokens = min(args.cpu_tokens, wl.T)
         secs = oracle_sample(inp, wl, tokens)
@@ -490,7 +654,40 @@ def run_ours(args, rank, world, local_rank):
                                "sample": f"first {tokens} of {wl.T} tokens, all {wl.E} experts, "
                                          f"{'fwd+bwd' if wl.backward else 'fwd'}, float64 numpy",
                                "seconds": secs}
+        one = oracle_single_core_tiny()
+        if one is not None:
+            out["cpu_baseline"]["tiny_single_core"] = one
     return out
+
+
+def oracle_single_core_tiny():
+    """The float64 oracle on the tiny workload (T = 256, d = 128, f = 256,
+    E = 8, top-2), fwd+bwd, on one core: a child process whose BLAS is held
+    to one thread by the environment. Returns its tokens/s record or None."""
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
+               BLIS_NUM_THREADS="1")
+    code = ("import sys, time; sys.path.insert(0, %r)\n"
+            "import workloads\n"
+            "from oracle import moe_oracle as mo\n"
+            "wl = workloads.CONFIGS['tiny']; inp = workloads.generate(wl)\n"
+            "def go():\n"
+            "    fw = mo.forward(inp['x'], inp['w_router'], inp['bias'], inp['w_gate'], inp['w_up'],"
+            " inp['w_down'], wl.k)\n"
+            "    mo.backward(inp['x'], inp['w_router'], inp['bias'], inp['w_gate'], inp['w_up'],"
+            " inp['w_down'], wl.k, inp['dy'], fwd=fw)\n"
+            "go(); t0 = time.perf_counter(); n = 5\n"
+            "for _ in range(n): go()\n"
+            "print((time.perf_counter() - t0) / n)\n" % ROOT)
+    try:
+        r = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True,
+                           timeout=300)
+        secs = float(r.stdout.strip().splitlines()[-1])
+    except Exception:
+        return None
+    return {"value": 256 / secs, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": "tiny workload (T = 256, d = 128, f = 256, E = 8, top-2), fwd+bwd, "
+                      "float64 numpy, BLAS on one thread, mean of 5 passes",
+            "seconds": secs}
 
 
 # ----------------------------------------------------------- reference --

@@ -44,7 +44,10 @@ def test_clock_rows_parse():
             ["0", "1940 MHz", "2070 MHz", "950 W", "0x4", "Not Active", "Not Active", "Not Active", "Active"],
             ["0", "1960 MHz", "2070 MHz", "960 W", "0x0", "Not Active", "Not Active", "Not Active", "Not Active"]]
     c = bench.parse_clock_rows(rows)
-    assert c["sm_mhz"] == 1940.0 and c["sm_max_mhz"] == 2070.0 and c["reasons"] == ["sw_power_cap"]
+    # under load = power in the upper half of the range seen (950 W and 960 W here)
+    assert c["sm_mhz"] == 1950.0 and c["samples_under_load"] == 2
+    assert c["sm_mhz_all_samples"] == 1940.0 and c["samples"] == 3
+    assert c["sm_max_mhz"] == 2070.0 and c["reasons"] == ["sw_power_cap"]
     assert bench.parse_clock_rows([]) is None
 
 

@@ -156,6 +156,34 @@ def generate(wl: Workload, tau: Optional[float] = None, with_dy: bool = True,
     return out
 
 
+def generate_device(wl: Workload, device, with_dy: bool = True) -> dict:
+    """Inputs for timing runs, with the large tensors drawn on the device.
+
+    x, W_r and the bias are the CPU recipe's own (the prefix ``generate``
+    draws first), so the routing, and with it every expert's row count, is
+    the one the parity tests check. The expert weights and dY are drawn from
+    the same distributions by a device generator seeded with ``wl.seed``
+    (drawing billions of values on the host takes minutes; the kernels'
+    timing does not depend on the values, only that they are not zero).
+    Returns device tensors with the keys of ``generate``."""
+    out = generate(wl, router_only=True)
+    out = {k_: (v.to(device) if isinstance(v, torch.Tensor) else v) for k_, v in out.items()}
+    gen = torch.Generator(device=device)
+    gen.manual_seed(wl.seed)
+
+    def draw(shape, std):
+        t = torch.empty(shape, dtype=torch.float32, device=device)
+        t.normal_(0.0, std, generator=gen)
+        return t.to(torch.bfloat16)
+
+    out["w_gate"] = draw((wl.E, wl.d, wl.f), 1.0 / math.sqrt(wl.d))
+    out["w_up"] = draw((wl.E, wl.d, wl.f), 1.0 / math.sqrt(wl.d))
+    out["w_down"] = draw((wl.E, wl.f, wl.d), 1.0 / math.sqrt(wl.f))
+    if with_dy:
+        out["dy"] = draw((wl.T, wl.d), 1.0)
+    return out
+
+
 def stride97_topk(T: int, k: int, E: int) -> torch.Tensor:
     """Exactly balanced routing for the small-M variant: pair p = t*k + j goes
     to expert (97 * p) mod E (prime-rl PR #3885, §Changes, "Spread balanced
