@@ -16,6 +16,7 @@
 //   warps 4-11  epilogue, two warpgroups (each half of the tile's columns):
 //               tcgen05.ld of the accumulator (one row per thread), the fused
 //               element-wise step, TMA stores staged through a 3-slot ring
+//               (per warpgroup, or per warp for the down dgrad)
 // Kinds:
 //   GateUpFwd    [G | U] = Xp . [W_gate[e] | W_up[e]]  (two accumulators),
 //                epilogue A = silu(G) * U; stores G, U (fp32, for the
@@ -71,6 +72,11 @@ struct Tr {
   // tile width chosen per launch (at most BN): the K-major-B kinds, whose B box
   // is exactly the tile's rows, and the router, whose N is the expert count
   static constexpr bool var_bn = (K == Kind::DownDgrad || K == Kind::GateUpDgrad || dense);
+  // each epilogue warp stages and stores its own 32 rows, so warps never wait
+  // for each other at a slice: the down dgrad, whose threads wait on their
+  // rows' G and U loads (the others store 128-row boxes per warpgroup, fewer
+  // and larger TMA stores)
+  static constexpr bool warp_stage = (K == Kind::DownDgrad);
   // bytes TMA lands per stage (A tile + one or two B tiles), and as many stages as fit
   static constexpr int tx_bytes = kABytes + (dual ? 2 : 1) * BN * BK * 2;
   static constexpr int stages = kRingBytes / tx_bytes > kMaxStages ? kMaxStages
@@ -100,12 +106,13 @@ struct Geo {
 constexpr int kTmemCols = 512;                            // 2 accumulator buffers x 256 columns
 constexpr int kEpiWarps = 8;                              // two warpgroups, each half the columns
 constexpr int kThreads = 128 + 32 * kEpiWarps;
-// Epilogues stage their outputs through shared memory for TMA stores: per
-// epilogue warpgroup a ring of kStgSlots slots, each [128 rows x 32 bytes]
-// (16 bf16 or 8 fp32 columns of one output)
+// Epilogues stage their outputs through shared memory for TMA stores: a ring
+// of kStgSlots slots per epilogue warpgroup, each [128 rows x 32 bytes] (16
+// bf16 or 8 fp32 columns of one output), or, for the kinds that stage per
+// warp (Tr::warp_stage), the same bytes as a ring per warp of [32 rows x 32
+// bytes] slots
 constexpr int kStgSlots = 3;
-constexpr int kSlotBytes = 128 * 32;
-constexpr int kStagePerGroup = kStgSlots * kSlotBytes;
+constexpr int kStagePerGroup = kStgSlots * 128 * 32;
 constexpr int kStageOutBytes = (kEpiWarps / 4) * kStagePerGroup;
 // the tile table, rounded up so the staging slots after it sit on 1 KiB
 // boundaries (the 32-byte swizzle pattern is taken from address bits 4-7)
@@ -200,11 +207,7 @@ __device__ __forceinline__ void decode_tile(int tile, const GemmArgs& a, const i
   }
 }
 
-// Named barrier over one epilogue warpgroup (ids 1 and 2; id 0 is __syncthreads).
-__device__ __forceinline__ void group_sync(int group) {
-  asm volatile("bar.sync %0, 128;" ::"r"(group + 1) : "memory");
-}
-// The same barrier, returning whether every thread of the group passed `ok`:
+// The group's named barrier, returning whether every thread of the group passed `ok`:
 // the group decides together whether to go on, so no warp is left waiting at
 // a group barrier that another warp has abandoned.
 __device__ __forceinline__ bool group_all(int group, bool ok) {
@@ -220,58 +223,64 @@ __device__ __forceinline__ bool group_all(int group, bool ok) {
   return r != 0;
 }
 
+// Named barrier over one epilogue warpgroup (ids 1 and 2; id 0 is __syncthreads).
+__device__ __forceinline__ void group_sync(int group) {
+  asm volatile("bar.sync %0, 128;" ::"r"(group + 1) : "memory");
+}
+
 // Writes one 32-byte slice (16 bf16 or 8 fp32 columns, v[o][0..1]) of each of
-// NOUT outputs for this thread's row. When the whole 128-row tile belongs to
-// its group (tile_tma), the warpgroup stages the slices in shared memory, one
-// slot of [128 rows x 32 bytes] per output, and one thread issues one TMA
-// store per slot (coordinates {col, m0} or {col, m0, e}; the maps clip at
-// the tensor edge), each its own bulk group. The slots rotate through a ring
-// of kStgSlots, advancing only with stores issued, so a slot is written again
-// as soon as the store that last used it has read it, while the later stores
-// are still in flight. Rows are
-// stored with the maps' 32-byte swizzle (the two 16-byte halves of rows 4-7
-// of every 8 swapped), so the warp's shared-memory writes hit distinct banks.
-// Otherwise every thread stores its own row with masks. Columns from lim on
-// (the tile's end, or N) are not written; N is the row stride; esz[o] the
-// element size of output o (every output's slice starts at column col).
-template <int NOUT, bool K3D>
+// NOUT outputs for this thread's row. When the rows of the staging unit all
+// belong to the group (stage_tma) — the warpgroup's 128 rows, or with WARP the
+// warp's 32 — the unit stages the slices in its shared memory, one slot of
+// [rows x 32 bytes] per output, and one thread (the warpgroup's first, or the
+// warp's lane 0) issues one TMA store per slot (coordinates {col, r0} or
+// {col, r0, e}, r0 the unit's first row; the maps clip at the tensor edge),
+// each its own bulk group. The slots rotate through the unit's ring of
+// kStgSlots, advancing only with stores issued, so a slot is written again as
+// soon as the store that last used it has read it, while the later stores are
+// still in flight. Rows are stored with the maps' 32-byte swizzle (the two
+// 16-byte halves of rows 4-7 of every 8 swapped), so the warp's shared-memory
+// writes hit distinct banks. Otherwise every thread stores its own row with
+// masks. Columns from lim on (the tile's end, or N) are not written; N is the
+// row stride; esz[o] the element size of output o (every output's slice
+// starts at column col); rloc the thread's row within the unit.
+template <int NOUT, bool K3D, bool WARP>
 __device__ __forceinline__ void put_slice(const uint4 (&v)[NOUT][2], uint8_t* stg, int& slot,
                                           const CUtensorMap* const* maps, uint8_t* const* outs,
-                                          const int* esz, bool tile_tma, bool row_ok, int64_t row,
-                                          int rloc, int col, int N, int lim, int m0, int e,
-                                          int group, bool leader, uint64_t policy) {
+                                          const int* esz, bool stage_tma, bool row_ok,
+                                          int64_t row, int rloc, int col, int N, int lim, int r0,
+                                          int e, int group, bool leader, uint64_t policy) {
   static_assert(NOUT <= kStgSlots, "one slot per output");
-  if (tile_tma) {
+  constexpr int kSlot = (WARP ? 32 : 128) * 32;
+  if (stage_tma) {
     // the stores that last used these NOUT slots have read them
     if (leader) bulk_wait_read_n<kStgSlots - NOUT>();
-    group_sync(group);
+    if constexpr (WARP) __syncwarp(); else group_sync(group);
     const int sw = ((rloc >> 2) & 1) * 16;
 #pragma unroll
     for (int o = 0; o < NOUT; ++o) {
       int so = slot + o;
       so = so >= kStgSlots ? so - kStgSlots : so;
-      uint8_t* d = stg + so * kSlotBytes + rloc * 32;
+      uint8_t* d = stg + so * kSlot + rloc * 32;
       *reinterpret_cast<uint4*>(d + sw) = v[o][0];
       *reinterpret_cast<uint4*>(d + (16 - sw)) = v[o][1];
     }
     fence_async_smem();
-    group_sync(group);
+    if constexpr (WARP) __syncwarp(); else group_sync(group);
     if (leader && col < lim) {
 #pragma unroll
       for (int o = 0; o < NOUT; ++o) {
         int so = slot + o;
         so = so >= kStgSlots ? so - kStgSlots : so;
-        const uint32_t src = smem_u32(stg + so * kSlotBytes);
+        const uint32_t src = smem_u32(stg + so * kSlot);
         if constexpr (K3D)
-          tma_store_3d(maps[o], src, col, m0, e, policy);
+          tma_store_3d(maps[o], src, col, r0, e, policy);
         else
-          tma_store_2d(maps[o], src, col, m0, policy);
+          tma_store_2d(maps[o], src, col, r0, policy);
         bulk_commit();
       }
     }
-    // the ring advances with the stores actually issued (col and lim are the
-    // same in every thread of the warpgroup), so the slot rewritten next was
-    // last read by the store kStgSlots commits back
+    // col and lim are the same in every thread of the unit
     if (col < lim) {
       slot += NOUT;
       slot = slot >= kStgSlots ? slot - kStgSlots : slot;
@@ -679,9 +688,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int c_lo = ((warp - 4) >> 2) * kHalf;
     const int c_hi = c_lo + kHalf < bn ? c_lo + kHalf : bn;
     const int group = (warp - 4) >> 2;
-    const bool leader = (wq == 0 && lane == 0);
-    uint8_t* stg = stage_out + group * kStagePerGroup;
-    int slot = 0;   // next staging slot: the same in every thread of the warpgroup
+    constexpr bool WS = T::warp_stage;
+    // this thread's staging unit: its warp (32 rows) or its warpgroup (128)
+    uint8_t* stg = stage_out + group * kStagePerGroup + (WS ? wq * (kStagePerGroup / 4) : 0);
+    const int srow = WS ? lane : rloc;                  // row within the unit
+    const bool leader = WS ? lane == 0 : (wq == 0 && lane == 0);
+    int slot = 0;   // next staging slot of the unit's ring (the same in all its threads)
     const CUtensorMap* maps[3] = {&mapO0, &mapO1, &mapO2};
     uint8_t* outs[3] = {static_cast<uint8_t*>(args.out0), static_cast<uint8_t*>(args.out1),
                         static_cast<uint8_t*>(args.out2)};
@@ -746,9 +758,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const uint32_t t_row = tmem_base + ((uint32_t)(wq * 32) << 16) + (uint32_t)acc * 256u;
 
-      // the whole 128-row tile inside its group (dW tiles always: TMA clips at M)
-      // -> staged TMA stores by the warpgroup; else masked row stores
-      const bool tile_tma = T::kgrouped ? ti.m0 < args.M : ti.m0 + BM <= ti.row_end;
+      // the staging unit's rows inside its group (dW tiles: TMA clips at M) ->
+      // staged TMA stores; else masked row stores
+      const int64_t r0 = ti.m0 + (WS ? wq * 32 : 0);
+      const int urows = WS ? 32 : BM;
+      const bool tile_tma = T::kgrouped ? r0 < args.M : r0 + urows <= ti.row_end;
       if constexpr (T::gateup_fwd) {
         // G, U fp32 in 8-column slices, A bf16 in 16-column slices (each
         // with the first of every two G / U slices)
@@ -779,12 +793,12 @@ __global__ void __launch_bounds__(kThreads, 1)
               const int h = q >> 1;
               v[2][0] = make_uint4(pa[8 * h + 0], pa[8 * h + 1], pa[8 * h + 2], pa[8 * h + 3]);
               v[2][1] = make_uint4(pa[8 * h + 4], pa[8 * h + 5], pa[8 * h + 6], pa[8 * h + 7]);
-              put_slice<3, false>(v, stg, slot, maps, outs, es, tile_tma, row_ok, row, rloc, col,
-                                  args.N, col_lim, (int)ti.m0, 0, group, leader, pol_out);
+              put_slice<3, false, WS>(v, stg, slot, maps, outs, es, tile_tma, row_ok, row, srow, col,
+                                  args.N, col_lim, (int)r0, 0, group, leader, pol_out);
             } else {
               uint4 w2[2][2] = {{v[0][0], v[0][1]}, {v[1][0], v[1][1]}};
-              put_slice<2, false>(w2, stg, slot, maps, outs, es, tile_tma, row_ok, row, rloc,
-                                  col, args.N, col_lim, (int)ti.m0, 0, group, leader, pol_out);
+              put_slice<2, false, WS>(w2, stg, slot, maps, outs, es, tile_tma, row_ok, row, srow,
+                                  col, args.N, col_lim, (int)r0, 0, group, leader, pol_out);
             }
           }
         }
@@ -808,9 +822,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint4 v[NO][2];
             slice_of<NO, 16>(pk, h, v);
             constexpr int es[2] = {2, 2};
-            put_slice<NO, true>(v, stg, slot, maps, outs, es, tile_tma, false, row, rloc,
-                                ti.n0 + c + 16 * h, args.N, col_lim, (int)ti.m0, ti.e, group,
-                                leader, pol_out);
+            put_slice<NO, true, WS>(v, stg, slot, maps, outs, es, tile_tma, false, row, srow,
+                                    ti.n0 + c + 16 * h, args.N, col_lim, (int)r0, ti.e, group,
+                                    leader, pol_out);
           }
         }
       } else if constexpr (T::dense) {
@@ -877,9 +891,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (h == 0 && c + 32 < c_end) load_gu(c + 32, gn, un);
             uint4 vv[2][2];
             slice_of<2, 8>(pk, 0, vv);
-            put_slice<2, false>(vv, stg, slot, maps, outs, es, tile_tma, row_ok, row, rloc,
-                                ti.n0 + c + 16 * h, args.N, col_lim, (int)ti.m0, 0, group,
-                                leader, pol_out);
+            put_slice<2, false, WS>(vv, stg, slot, maps, outs, es, tile_tma, row_ok, row, srow,
+                                    ti.n0 + c + 16 * h, args.N, col_lim, (int)r0, 0, group,
+                                    leader, pol_out);
           }
         }
         if (row_ok)
@@ -903,9 +917,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                                  __float_as_uint(__uint_as_float(r[8 * q + 6]) * rscale),
                                  __float_as_uint(__uint_as_float(r[8 * q + 7]) * rscale));
             constexpr int es[1] = {4};
-            put_slice<1, false>(v, stg, slot, maps, outs, es, tile_tma, row_ok, row, rloc,
-                                ti.n0 + c + 8 * q, args.N, col_lim, (int)ti.m0, 0, group,
-                                leader, pol_out);
+            put_slice<1, false, WS>(v, stg, slot, maps, outs, es, tile_tma, row_ok, row, srow,
+                                    ti.n0 + c + 8 * q, args.N, col_lim, (int)r0, 0, group,
+                                    leader, pol_out);
           }
         }
       }
@@ -919,7 +933,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
     }
-    if (wq == 0 && lane == 0) bulk_wait_all();   // the staged stores finish before the CTA exits
+    if (leader) bulk_wait_all();   // the unit's staged stores finish before the CTA exits
   }
   tc_fence_before();
   __syncthreads();
@@ -984,15 +998,17 @@ static bool map3d(CUtensorMap* m, const void* ptr, uint64_t d0, uint64_t d1, uin
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// Maps for the epilogues' TMA stores: boxes of 128 rows x 32 bytes (16 bf16 or
-// 8 fp32 columns) with the 32-byte swizzle the staging slots are written in.
+// Maps for the epilogues' TMA stores: boxes of `rows` rows x 32 bytes (16 bf16
+// or 8 fp32 columns: one staging slot, 128 rows per warpgroup or 32 per warp)
+// with the 32-byte swizzle the slots are written in.
 // 2-D over a row buffer [R, N]; esz = 2 (bf16) or 4 (fp32).
-static bool map2d_out(CUtensorMap* m, const void* ptr, uint64_t N, uint64_t R, int esz = 2) {
+static bool map2d_out(CUtensorMap* m, const void* ptr, uint64_t N, uint64_t R, int esz = 2,
+                      uint32_t rows = 128) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
   cuuint64_t dims[2] = {N, R};
   cuuint64_t strides[1] = {N * (uint64_t)esz};
-  cuuint32_t box[2] = {(cuuint32_t)(32 / esz), 128};
+  cuuint32_t box[2] = {(cuuint32_t)(32 / esz), rows};
   cuuint32_t es[2] = {1, 1};
   return fn(m, esz == 4 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
             const_cast<void*>(ptr), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -1273,7 +1289,7 @@ cudaError_t launch_down_dgrad(const GroupedDims& g, const moe_bf16* dyg, const f
   if (!g.src_pair) return cudaErrorInvalidValue;
   if (!map2d(&a0, dyg, g.d, g.R_cap, BM) ||
       !map3d(&b0, w_down, g.d, g.f, g.E, pair ? bn / 2 : bn) ||
-      !map2d_out(&o0, dG, g.f, g.R_cap) || !map2d_out(&o1, dU, g.f, g.R_cap))
+      !map2d_out(&o0, dG, g.f, g.R_cap, 2, 32) || !map2d_out(&o1, dU, g.f, g.R_cap, 2, 32))
     return cudaErrorInvalidValue;
   GemmArgs a = base_args(g, status);
   a.N = g.f;
