@@ -1100,9 +1100,10 @@ static cudaError_t launch_kind(const CUtensorMap& a0, const CUtensorMap& a1,
 
 // CTA pairs (M = 256 MMAs over two SMs: half the B traffic per SM, a deeper
 // ring) for the M-grouped kinds when the experts average at least 1024 rows,
-// where 256-row tiles waste little (the down dgrad excepted, below). Not by
-// default for the K-grouped weight gradients: their rows (d or f, e.g.
-// 2880 = 11.25 x 256) leave a mostly empty last 256-row tile.
+// where 256-row tiles waste little (the down dgrad excepted, below); the
+// gate/up forward and dgrad, which move two weight matrices per tile, from 512
+// rows. Not by default for the K-grouped weight gradients: their rows (d or
+// f, e.g. 2880 = 11.25 x 256) leave a mostly empty last 256-row tile.
 // MOE_GEMM_PAIRS=0 or 1 in the environment turns pairs off or on for every
 // grouped kind (a tuning and testing knob; the results are the same).
 static int pairs_env() {
@@ -1112,9 +1113,9 @@ static int pairs_env() {
   }();
   return v;
 }
-static bool pairs_mgrouped(const GroupedDims& g) {
+static bool pairs_mgrouped(const GroupedDims& g, int min_rows = 1024) {
   const int e = pairs_env();
-  return e >= 0 ? e == 1 : g.P >= (int64_t)1024 * g.E;
+  return e >= 0 ? e == 1 : g.P >= (int64_t)min_rows * g.E;
 }
 static bool pairs_kgrouped() { return pairs_env() == 1; }
 
@@ -1243,7 +1244,7 @@ cudaError_t launch_gateup_fwd(const GroupedDims& g, const moe_bf16* xp, const mo
   if (tiles < 8 * (int64_t)num_sms())
     return launch_kind<Kind::GateUpFwdNarrow, false>(
         a0, a0, b0, b1, a, mgrouped_tiles_upper(g, g.f, 64), s, &o0, &o1, &o2);
-  if (pairs_mgrouped(g))
+  if (pairs_mgrouped(g, 512))
     return launch_kind<Kind::GateUpFwd, true>(
         a0, a0, b0, b1, a, mgrouped_tiles_upper(g, g.f, 128, 2 * BM), s, &o0, &o1, &o2);
   return launch_kind<Kind::GateUpFwd, false>(a0, a0, b0, b1, a, mgrouped_tiles_upper(g, g.f, 128),
@@ -1312,7 +1313,7 @@ cudaError_t launch_gateup_dgrad(const GroupedDims& g, const moe_bf16* dG, const 
                                 int* status, cudaStream_t s) {
   CUtensorMap a0, a1, b0, b1, o0;
   const int bn = pick_bn(g.d, 16);
-  const bool pair = pairs_mgrouped(g);
+  const bool pair = pairs_mgrouped(g, 512);
   const int brows = pair ? bn / 2 : bn;   // a pair's CTAs load bn / 2 rows of B each
   // dXp[r, i] = sum_c dG[r, c] W_gate[e][i, c] + dU[r, c] W_up[e][i, c]:
   // B is W_gate[e] / W_up[e] read as [N = d rows, K = f]
