@@ -74,9 +74,10 @@ struct Tr {
   static constexpr bool var_bn = (K == Kind::DownDgrad || K == Kind::GateUpDgrad || dense);
   // each epilogue warp stages and stores its own 32 rows, so warps never wait
   // for each other at a slice: the down dgrad, whose threads wait on their
-  // rows' G and U loads (the others store 128-row boxes per warpgroup, fewer
-  // and larger TMA stores)
-  static constexpr bool warp_stage = (K == Kind::DownDgrad);
+  // rows' G and U loads, and the weight gradients, bound by their stores when
+  // experts hold few rows (the others store 128-row boxes per warpgroup,
+  // fewer and larger TMA stores)
+  static constexpr bool warp_stage = (K == Kind::DownDgrad || kgrouped);
   // bytes TMA lands per stage (A tile + one or two B tiles), and as many stages as fit
   static constexpr int tx_bytes = kABytes + (dual ? 2 : 1) * BN * BK * 2;
   static constexpr int stages = kRingBytes / tx_bytes > kMaxStages ? kMaxStages
@@ -1016,13 +1017,14 @@ static bool map2d_out(CUtensorMap* m, const void* ptr, uint64_t N, uint64_t R, i
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// 3-D bf16 map over [E, M, N] (N innermost), same boxes
-static bool map3d_out(CUtensorMap* m, const void* ptr, uint64_t N, uint64_t M, uint64_t E) {
+// 3-D bf16 map over [E, M, N] (N innermost), boxes of one warp's 32 rows
+static bool map3d_out(CUtensorMap* m, const void* ptr, uint64_t N, uint64_t M, uint64_t E,
+                      uint32_t rows = 32) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
   cuuint64_t dims[3] = {N, M, E};
   cuuint64_t strides[2] = {N * 2, N * M * 2};
-  cuuint32_t box[3] = {16, 128, 1};
+  cuuint32_t box[3] = {16, rows, 1};
   cuuint32_t es[3] = {1, 1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box,
             es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_32B,

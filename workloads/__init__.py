@@ -97,6 +97,10 @@ CONFIGS["gptoss20b_T4096"] = Workload("gptoss20b_T4096", T=4096, d=2880, f=2880,
 # half the bench batch (2 x 4096 tokens, 1024 rows per expert): a profiling size
 CONFIGS["gptoss20b_T8192"] = Workload("gptoss20b_T8192", T=8192, d=2880, f=2880, E=32, k=4,
                                       note="GPT-OSS-20B-shaped layer, batch 2 x 4096")
+# the fine-grained expert shape (d = 2560, f = 640, top-10, ~160 rows per
+# expert) over 128 experts instead of 512: a profiling size (a few GB on the device)
+CONFIGS["fine_E128_T2048"] = Workload("fine_E128_T2048", T=2048, d=2560, f=640, E=128, k=10,
+                                      note="fine-grained expert shape, 128 experts, 2048 tokens")
 for _T in (128, 512, 1024, 2048):
     CONFIGS[f"smallm_T{_T}"] = Workload(
         f"smallm_T{_T}", T=_T, d=2048, f=768, E=128, k=8, backward=False,
