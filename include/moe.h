@@ -34,6 +34,14 @@
  *     ascending pair id, then zero padding up to a multiple of `align`.
  *     R_cap >= T*k + E*(align-1) bounds the padded size for any routing, so
  *     the host never needs the counts.
+ *   - Shared experts (S >= 0 of them): experts every token goes through with
+ *     weight 1, whose outputs are added to the routed ones ([PRL "Fused FP8
+ *     shared expert"]: routed and shared outputs summed in the write-back).
+ *     Their weights follow the E routed experts' in the same [E+S, ...]
+ *     tensors; in the layout they are groups E .. E+S-1, each holding the T
+ *     pairs T*k + s*T + t (t = 0 .. T-1, token order) after the T*k routed
+ *     pairs t*k + j. With S shared experts R_cap >= T*(k+S) + (E+S)*(align-1)
+ *     (moe_row_capacity(T, k + S, E + S, align)); k + S <= 32, E + S <= 1024.
  *   - Return codes below; MOE_ERR_ARG etc. are detected on the host before
  *     anything is enqueued. MOE_ERR_DEVICE_* are raised by kernels into a
  *     per-device status word and reported by moe_status().
@@ -55,6 +63,20 @@ extern "C" {
 
 typedef uint16_t moe_bf16;
 typedef struct CUstream_st* moe_stream_t; /* the same handle as cudaStream_t */
+
+/* The experts' gated activation (a HOST pointer to it is passed; NULL means
+ * the plain SwiGLU, A = silu(G) * U [HALO §Levers that help, fused GLU]):
+ *   A = h(min(G, limit)) * (clamp(U, -limit, limit) + up_offset),
+ *   h(g) = g * sigmoid(alpha * g);
+ * the clamped SwiGLU of [PRL "FP8 routed experts"], whose constants the pages
+ * do not print; GPT-OSS-20B's are limit 7, alpha 1.702, up_offset 1. The plain
+ * SwiGLU is {INFINITY, 1, 0}. No gradient passes a clamp at its limit.
+ * limit must be > 0 (INFINITY allowed); alpha and up_offset finite. */
+typedef struct {
+  float limit;
+  float alpha;
+  float up_offset;
+} moe_swiglu;
 
 #define MOE_OK                 0
 #define MOE_ERR_ARG            1 /* null required pointer, size <= 0, k > E, bad align, ... */
@@ -103,10 +125,11 @@ int moe_route(const moe_bf16* x, const float* w_router, const float* bias,
  *
  *  topk_idx [T, k] int32 in (ids outside [0, E) raise MOE_ERR_DEVICE_INDEX;
  *           such pairs are dropped from the layout, their dst_row is -1)
+ *  S        shared experts (groups E .. E+S-1, every token in token order)
  *  x        [T, d] bf16 in
- *  counts   [E] int32 out: n_e
- *  offsets  [E+1] int64 out: offsets[e] = sum_{e'<e} ceil(n_e'/align)*align
- *  dst_row  [T*k] int32 out: row of pair p
+ *  counts   [E+S] int32 out: n_e (T for a shared expert)
+ *  offsets  [E+S+1] int64 out: offsets[e] = sum_{e'<e} ceil(n_e'/align)*align
+ *  dst_row  [T*(k+S)] int32 out: row of pair p
  *  src_pair [R_cap] int32 out: pair held by row r, -1 for padding and for
  *           rows past offsets[E]
  *  xp       [R_cap, d] bf16 out: xp[r] = x[src_pair[r] / k]; padding rows
@@ -116,13 +139,14 @@ int moe_route(const moe_bf16* x, const float* w_router, const float* bias,
  *           multiple of 16 rows)
  *  ws       workspace of moe_workspace_size(MOE_WS_PERMUTE, ...) bytes
  * ------------------------------------------------------------------------ */
-int moe_permute(const int32_t* topk_idx, int64_t T, int k, int E, int align,
+int moe_permute(const int32_t* topk_idx, int64_t T, int k, int E, int S, int align,
                 const moe_bf16* x, int d, int64_t R_cap,
                 int32_t* counts, int64_t* offsets, int32_t* dst_row, int32_t* src_pair,
                 moe_bf16* xp, void* ws, size_t ws_bytes, moe_stream_t stream);
 
 /* ------------------------------------------------------------------------
- * moe_permute_noalloc — moe_permute without a workspace argument.
+ * moe_permute_noalloc — moe_permute without a workspace argument (routed
+ * experts only: S = 0).
  * (No counterpart on the source pages: this is a calling convention of this
  * library, not part of the method.)
  * For callers that cannot allocate device memory: a host application that
@@ -159,14 +183,16 @@ int moe_permute_noalloc(const int32_t* topk_idx, int64_t T, int k, int E, int al
  * GLU; [PRL "Kept expert activations"] G and U are kept for backward (in
  * fp32, so the backward's SwiGLU gradient starts from unrounded values).
  * Per expert e on its rows:  G = Xp.W_gate[e], U = Xp.W_up[e] (fp32
- * accumulation in tensor memory), A = silu(G)*U from the fp32 accumulators,
+ * accumulation in tensor memory), A = act(G, U) from the fp32 accumulators,
  * Yp = A.W_down[e] (times row_w[r] in fp32 when row_w is given), kept in
  * fp32 so the combine's gather-sum rounds each output once.
  *
- *  xp [R_cap, d] bf16, offsets [E+1] int64 (from moe_permute)
- *  T, k: tokens and top-k of the routing (T*k pairs; sizes the tile schedule:
- *        with few rows per expert the gate/up GEMM uses narrower tiles)
- *  w_gate, w_up [E, d, f] bf16;  w_down [E, f, d] bf16
+ *  xp [R_cap, d] bf16, offsets [E+S+1] int64 (from moe_permute)
+ *  act: host pointer to the activation (moe_swiglu), or NULL: plain SwiGLU
+ *  T, k, E, S: tokens, top-k, routed and shared experts (T*(k+S) pairs over
+ *        E+S groups; sizes the tile schedule: with few rows per expert the
+ *        gate/up GEMM uses narrower tiles)
+ *  w_gate, w_up [E+S, d, f] bf16;  w_down [E+S, f, d] bf16
  *  row_w [R_cap] fp32 or NULL (NULL: Yp is the unscaled expert output, the
  *        layout the combine and moe_expert_bwd expect)
  *  g, u [R_cap, f] fp32 out;  a [R_cap, f] bf16 out (the down GEMM's operand);
@@ -176,7 +202,8 @@ int moe_permute_noalloc(const int32_t* topk_idx, int64_t T, int k, int E, int al
  * Limits: d, f multiples of 8 (16-byte rows for TMA); E <= 1024.
  * ------------------------------------------------------------------------ */
 int moe_expert_fwd(const moe_bf16* xp, const int64_t* offsets, const float* row_w,
-                   int64_t T, int k, int E, int d, int f, int64_t R_cap,
+                   const moe_swiglu* act, int64_t T, int k, int E, int S, int d, int f,
+                   int64_t R_cap,
                    const moe_bf16* w_gate, const moe_bf16* w_up, const moe_bf16* w_down,
                    float* g, float* u, moe_bf16* a, float* yp,
                    moe_stream_t stream);
@@ -184,14 +211,15 @@ int moe_expert_fwd(const moe_bf16* xp, const int64_t* offsets, const float* row_
 /* ------------------------------------------------------------------------
  * moe_combine — fp32 score-weighted gather-sum back to token order.
  * [PRL "Single-pass DeepEP local layout"] out[t] = sum_{j<k} w[t,j] *
- * rows[dst_row[t*k+j]], accumulated in fp32 in slot order, rounded once to
+ * rows[dst_row[t*k+j]] + sum_{s<S} rows[dst_row[T*k + s*T + t]] (the shared
+ * experts with weight 1), accumulated in fp32 in slot order, rounded once to
  * bf16. With topk_w == NULL the weights are 1: that is the permute's
- * transpose (dx_t = sum_j dXp[dst_row]) used in backward.
- *  rows [R_cap, d] fp32 in (Yp or dXp);  dst_row [T*k] int32;
+ * transpose (dx_t = sum over the token's pairs of dXp) used in backward.
+ *  rows [R_cap, d] fp32 in (Yp or dXp);  dst_row [T*(k+S)] int32;
  *  topk_w [T, k] fp32 or NULL;  out [T, d] bf16 out
  * ------------------------------------------------------------------------ */
 int moe_combine(const float* rows, const int32_t* dst_row, const float* topk_w,
-                int64_t T, int k, int d, moe_bf16* out, moe_stream_t stream);
+                int64_t T, int k, int S, int d, moe_bf16* out, moe_stream_t stream);
 
 /* ------------------------------------------------------------------------
  * moe_expert_bwd — backward of the combine and of the experts.
@@ -200,31 +228,33 @@ int moe_combine(const float* rows, const int32_t* dst_row, const float* topk_w,
  * K-grouped wgrad; [PRL "dispatch.type = mega_moe"] gradient of the top-k
  * weights. Steps:
  *   combine transpose:  dyg[r] = dy[t(p)] (the gathered rows, an exact copy),
- *                       dyp[r] = w(p) * dy[t(p)] (bf16), both 0 on padding rows
+ *                       dyp[r] = w(p) * dy[t(p)] (bf16; w = 1 for a shared
+ *                       expert's pair), both 0 on padding rows
  *   down dgrad:         dAu = dyg . W_down[e]^T (fp32 accumulator), and in its
  *                       epilogue dA = w(p) * dAu (so dA carries no bf16
- *                       rounding of w * dy), dg = dA * U * silu'(G),
- *                       du = dA * silu(G), and d_topk_w[p] = <dy[t(p)], Yu> as
- *                       <dAu, silu(G) * U> from the fp32 G and U (the expert
- *                       output of the unrounded A), summed over the column
- *                       tiles in a fixed order
+ *                       rounding of w * dy), dg = dA * dact/dG,
+ *                       du = dA * dact/dU, and for the routed pairs
+ *                       d_topk_w[p] = <dy[t(p)], Yu> as <dAu, act(G, U)> from
+ *                       the fp32 G and U (the expert output of the unrounded
+ *                       A), summed over the column tiles in a fixed order
  *   gate/up dgrad:      dxp = dg . W_gate[e]^T + du . W_up[e]^T  (one K = 2f
  *                       sum, stored in fp32 so dx is rounded once)
  *   K-grouped wgrad:    dW_down[e] = A_e^T . dyp_e, dW_gate[e] = Xp_e^T . dg_e,
  *                       dW_up[e] = Xp_e^T . du_e   (an empty expert gets zeros)
- *  dy [T, d] bf16; src_pair [R_cap], dst_row [T*k] int32; topk_w [T, k] fp32;
- *  offsets [E+1]; xp, a (bf16), g, u (fp32) as written by moe_permute /
- *  moe_expert_fwd; weights as in moe_expert_fwd.
+ *  dy [T, d] bf16; src_pair [R_cap], dst_row [T*(k+S)] int32; topk_w [T, k]
+ *  fp32; offsets [E+S+1]; act, T, k, E, S as in moe_expert_fwd; xp, a
+ *  (bf16), g, u (fp32) as written by moe_permute / moe_expert_fwd; weights
+ *  as in moe_expert_fwd.
  *  ws: moe_expert_bwd_workspace_size(R_cap, f) bytes, 256-byte aligned (the
  *  top-k weight gradient's per-tile partials; scratch after the call).
  *  Outputs (row buffers, caller-owned, may be reused after the call):
  *  dyg, dyp [R_cap, d] bf16; dg, du [R_cap, f] bf16; dxp [R_cap, d] fp32;
  *  d_topk_w [T, k] fp32 (pairs dropped from the layout get no value);
- *  dw_gate, dw_up [E, d, f], dw_down [E, f, d] bf16 (overwritten).
+ *  dw_gate, dw_up [E+S, d, f], dw_down [E+S, f, d] bf16 (overwritten).
  * ------------------------------------------------------------------------ */
 int moe_expert_bwd(const moe_bf16* dy, const int32_t* src_pair, const int32_t* dst_row,
-                   const float* topk_w, const int64_t* offsets,
-                   int64_t T, int k, int E, int d, int f, int64_t R_cap,
+                   const float* topk_w, const int64_t* offsets, const moe_swiglu* act,
+                   int64_t T, int k, int E, int S, int d, int f, int64_t R_cap,
                    const moe_bf16* xp, const float* g, const float* u, const moe_bf16* a,
                    const moe_bf16* w_gate, const moe_bf16* w_up, const moe_bf16* w_down,
                    moe_bf16* dyg, moe_bf16* dyp, moe_bf16* dg, moe_bf16* du, float* dxp,
@@ -241,30 +271,32 @@ size_t moe_expert_bwd_workspace_size(int64_t R_cap, int f);
  * elsewhere; the selection is piecewise constant); then
  *   dx[t] += sum_j dl_t,j W_r[:, S_j]        (dxp == NULL: read-modify-write of
  *                                             bf16 dx, sum in fp32), or
- *   dx[t]  = sum_j dxp[dst_row[t*k+j]] + sum_j dl_t,j W_r[:, S_j]
+ *   dx[t]  = sum_p dxp[dst_row[p]] + sum_j dl_t,j W_r[:, S_j]
  *                                            (dxp given: the permute's transpose
- *                                             fused in, fp32, rounded once)
+ *                                             over the token's k routed and S
+ *                                             shared pairs fused in, fp32,
+ *                                             rounded once)
  *   dW_r = x^T . dl   (dl as a dense [T, E] matrix; fp32 accumulation of
  *                      exact products on the tensor cores, fixed order)
  *   dbias[e] = sum over e's rows of the padded layout of dl (fp32, row order)
  *  d_topk_w, topk_w [T, k] fp32; topk_idx [T, k] int32; w_router [d, E] fp32;
  *  x [T, d] bf16: the layer input (16-byte aligned);
- *  offsets, src_pair from moe_permute (with the same `align`).
+ *  offsets, src_pair from moe_permute (with the same `align` and S).
  *  dx_inout [T, d] bf16 (added to, or overwritten when dxp is given);
- *  dxp [R_cap, d] fp32 or NULL (from moe_expert_bwd); dst_row [T*k] int32
+ *  dxp [R_cap, d] fp32 or NULL (from moe_expert_bwd); dst_row [T*(k+S)] int32
  *  (required with dxp); dw_router [d, E] fp32 out; dbias [E] fp32 out or NULL.
  *  ws: moe_workspace_size(MOE_WS_ROUTE_BWD, ...) bytes, 256-byte aligned.
  * ------------------------------------------------------------------------ */
 int moe_route_bwd(const float* d_topk_w, const float* topk_w, const int32_t* topk_idx,
                   const float* w_router, const int64_t* offsets, const int32_t* src_pair,
-                  const moe_bf16* x, int64_t T, int d, int E, int k, int align,
+                  const moe_bf16* x, int64_t T, int d, int E, int k, int S, int align,
                   moe_bf16* dx_inout, const float* dxp, const int32_t* dst_row,
                   float* dw_router, float* dbias,
                   void* ws, size_t ws_bytes, moe_stream_t stream);
 
 /* ------------------------------------------------------------------------
  * moe_decode_fwd — the whole forward for a handful of tokens (decode), in one
- * cooperative kernel.
+ * cooperative kernel (routed experts with the plain SwiGLU; no shared experts).
  * [HALO §Levers that do not help here] small-M experts are bound by reading
  * their weights; [PLLM §Runtime architecture] top-k routing. For T <= 8 the
  * general path's seven launches cost more than the work: this call computes

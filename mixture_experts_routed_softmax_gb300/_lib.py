@@ -17,16 +17,17 @@ _SZ = ctypes.c_size_t
 
 SIGNATURES = {
     "moe_route": (_I, [_P, _P, _P, _P, _I64, _I, _I, _I, _P, _P, _P, _P, _SZ, _P]),
-    "moe_permute": (_I, [_P, _I64, _I, _I, _I, _P, _I, _I64, _P, _P, _P, _P, _P, _P, _SZ, _P]),
+    "moe_permute": (_I, [_P, _I64, _I, _I, _I, _I, _P, _I, _I64, _P, _P, _P, _P, _P, _P, _SZ,
+                         _P]),
     "moe_permute_noalloc": (_I, [_P, _I64, _I, _I, _I, _P, _I, _I64, _P, _P, _P, _P, _P, _P]),
-    "moe_expert_fwd": (_I, [_P, _P, _P, _I64, _I, _I, _I, _I, _I64, _P, _P, _P, _P, _P, _P, _P,
-                            _P]),
-    "moe_combine": (_I, [_P, _P, _P, _I64, _I, _I, _P, _P]),
-    "moe_expert_bwd": (_I, [_P, _P, _P, _P, _P, _I64, _I, _I, _I, _I, _I64,
+    "moe_expert_fwd": (_I, [_P, _P, _P, _P, _I64, _I, _I, _I, _I, _I, _I64, _P, _P, _P, _P, _P,
+                            _P, _P, _P]),
+    "moe_combine": (_I, [_P, _P, _P, _I64, _I, _I, _I, _P, _P]),
+    "moe_expert_bwd": (_I, [_P, _P, _P, _P, _P, _P, _I64, _I, _I, _I, _I, _I, _I64,
                             _P, _P, _P, _P, _P, _P, _P,
                             _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
     "moe_expert_bwd_workspace_size": (_SZ, [_I64, _I]),
-    "moe_route_bwd": (_I, [_P, _P, _P, _P, _P, _P, _P, _I64, _I, _I, _I, _I,
+    "moe_route_bwd": (_I, [_P, _P, _P, _P, _P, _P, _P, _I64, _I, _I, _I, _I, _I,
                            _P, _P, _P, _P, _P, _P, _SZ, _P]),
     "moe_decode_fwd": (_I, [_P, _P, _P, _P, _I64, _I, _I, _I, _I, _P, _P, _P,
                             _P, _P, _P, _P, _P, _SZ, _P]),
@@ -47,6 +48,13 @@ MOE_ERR_CAPACITY = 3
 MOE_ERR_CUDA = 4
 MOE_ERR_DEVICE_INDEX = 5
 MOE_ERR_DEVICE_TIMEOUT = 6
+
+class Swiglu(ctypes.Structure):
+    """moe_swiglu: A = h(min(G, limit)) (clamp(U, -limit, limit) + up_offset),
+    h(g) = g sigmoid(alpha g)."""
+    _fields_ = [("limit", ctypes.c_float), ("alpha", ctypes.c_float),
+                ("up_offset", ctypes.c_float)]
+
 
 MOE_WS_PERMUTE = 1
 MOE_WS_ROUTE_BWD = 2

@@ -75,6 +75,17 @@ void timer_after(int kernel, cudaStream_t s) {
 using namespace moe;
 
 static bool is_pow2(int v) { return v > 0 && (v & (v - 1)) == 0; }
+// the activation's parameters (NULL: the plain SwiGLU); a limit <= 0, NaN or
+// a NaN alpha / offset is rejected
+static bool act_of(const moe_swiglu* a, ActParams* out) {
+  if (!a) {
+    *out = ActParams{INFINITY, 1.0f, 0.0f};
+    return true;
+  }
+  if (!(a->limit > 0.0f) || a->alpha != a->alpha || a->up_offset != a->up_offset) return false;
+  *out = ActParams{a->limit, a->alpha, a->up_offset};
+  return true;
+}
 static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 static int cuda_code(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
 
@@ -191,23 +202,24 @@ int moe_route(const moe_bf16* x, const float* w_router, const float* bias,
   return cuda_code(e);
 }
 
-int moe_permute(const int32_t* topk_idx, int64_t T, int k, int E, int align, const moe_bf16* x,
-                int d, int64_t R_cap, int32_t* counts, int64_t* offsets, int32_t* dst_row,
-                int32_t* src_pair, moe_bf16* xp, void* ws, size_t ws_bytes,
+int moe_permute(const int32_t* topk_idx, int64_t T, int k, int E, int S, int align,
+                const moe_bf16* x, int d, int64_t R_cap, int32_t* counts, int64_t* offsets,
+                int32_t* dst_row, int32_t* src_pair, moe_bf16* xp, void* ws, size_t ws_bytes,
                 moe_stream_t stream) {
   if (!counts || !offsets || !src_pair || !xp || (T > 0 && (!topk_idx || !x || !dst_row)))
     return MOE_ERR_ARG;
-  if (T < 0 || k <= 0 || E <= 0 || d <= 0 || k > E) return MOE_ERR_ARG;
+  if (T < 0 || k <= 0 || E <= 0 || d <= 0 || k > E || S < 0) return MOE_ERR_ARG;
   if (!is_pow2(align) || align < 16 || align > 256) return MOE_ERR_ARG;
-  if (E > kMaxExperts || d % 8 != 0) return MOE_ERR_UNSUPPORTED;
-  if (R_cap < moe_row_capacity(T, k, E, align)) return MOE_ERR_CAPACITY;
-  if (R_cap >= ((int64_t)1 << 31) || T * k >= ((int64_t)1 << 31)) return MOE_ERR_UNSUPPORTED;
+  if (E + S > kMaxExperts || k + S > kMaxTopK || d % 8 != 0) return MOE_ERR_UNSUPPORTED;
+  if (R_cap < moe_row_capacity(T, k + S, E + S, align)) return MOE_ERR_CAPACITY;
+  if (R_cap >= ((int64_t)1 << 31) || T * (k + S) >= ((int64_t)1 << 31))
+    return MOE_ERR_UNSUPPORTED;
   if (!aligned16(x) || !aligned16(xp)) return MOE_ERR_ARG;
   const size_t need = permute_ws_bytes(T, k, E);
   if (need > 0 && (!ws || ws_bytes < need)) return MOE_ERR_ARG;
   int* st = device_status_ptr();
   if (!st) return MOE_ERR_CUDA;
-  return cuda_code(launch_permute(topk_idx, T, k, E, align, x, d, R_cap, counts, offsets,
+  return cuda_code(launch_permute(topk_idx, T, k, E, S, align, x, d, R_cap, counts, offsets,
                                   dst_row, src_pair, xp, ws, st,
                                   reinterpret_cast<cudaStream_t>(stream)));
 }
@@ -219,15 +231,18 @@ static int check_expert_dims(int E, int d, int f, int64_t R_cap) {
   return MOE_OK;
 }
 
-int moe_expert_fwd(const moe_bf16* xp, const int64_t* offsets, const float* row_w, int64_t T,
-                   int k, int E, int d, int f, int64_t R_cap, const moe_bf16* w_gate,
-                   const moe_bf16* w_up, const moe_bf16* w_down, float* g, float* u,
-                   moe_bf16* a, float* yp, moe_stream_t stream) {
+int moe_expert_fwd(const moe_bf16* xp, const int64_t* offsets, const float* row_w,
+                   const moe_swiglu* act, int64_t T, int k, int E, int S, int d, int f,
+                   int64_t R_cap, const moe_bf16* w_gate, const moe_bf16* w_up,
+                   const moe_bf16* w_down, float* g, float* u, moe_bf16* a, float* yp,
+                   moe_stream_t stream) {
   if (!xp || !offsets || !w_gate || !w_up || !w_down || !g || !u || !a || !yp) return MOE_ERR_ARG;
-  if (T < 0 || k <= 0 || k > E) return MOE_ERR_ARG;
-  int rc = check_expert_dims(E, d, f, R_cap);
+  if (T < 0 || k <= 0 || k > E || S < 0) return MOE_ERR_ARG;
+  ActParams ap;
+  if (!act_of(act, &ap)) return MOE_ERR_ARG;
+  int rc = check_expert_dims(E + S, d, f, R_cap);
   if (rc) return rc;
-  if (R_cap < T * k) return MOE_ERR_CAPACITY;
+  if (R_cap < T * (k + S)) return MOE_ERR_CAPACITY;
   for (const void* p : {(const void*)xp, (const void*)w_gate, (const void*)w_up,
                         (const void*)w_down, (const void*)g, (const void*)u, (const void*)a,
                         (const void*)yp})
@@ -235,26 +250,28 @@ int moe_expert_fwd(const moe_bf16* xp, const int64_t* offsets, const float* row_
   int* st = device_status_ptr();
   if (!st) return MOE_ERR_CUDA;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  GroupedDims gd{offsets, E, d, f, R_cap, T * k};
-  cudaError_t e = launch_gateup_fwd(gd, xp, w_gate, w_up, g, u, a, st, s);
+  GroupedDims gd{offsets, E + S, d, f, R_cap, T * (k + S)};
+  gd.P_routed = T * k;
+  cudaError_t e = launch_gateup_fwd(gd, xp, w_gate, w_up, g, u, a, ap, st, s);
   if (e == cudaSuccess) e = launch_down_fwd(gd, a, w_down, row_w, yp, st, s);
   return cuda_code(e);
 }
 
 int moe_combine(const float* rows, const int32_t* dst_row, const float* topk_w, int64_t T,
-                int k, int d, moe_bf16* out, moe_stream_t stream) {
+                int k, int S, int d, moe_bf16* out, moe_stream_t stream) {
   if (!rows || (T > 0 && (!dst_row || !out))) return MOE_ERR_ARG;
-  if (T < 0 || k <= 0 || d <= 0) return MOE_ERR_ARG;
-  if (k > kMaxTopK || d % 8 != 0) return MOE_ERR_UNSUPPORTED;
+  if (T < 0 || k <= 0 || d <= 0 || S < 0) return MOE_ERR_ARG;
+  if (k + S > kMaxTopK || d % 8 != 0) return MOE_ERR_UNSUPPORTED;
   if (!aligned16(rows) || !aligned16(out)) return MOE_ERR_ARG;
   if (T == 0) return MOE_OK;
-  return cuda_code(
-      launch_combine(rows, dst_row, topk_w, T, k, d, out, reinterpret_cast<cudaStream_t>(stream)));
+  return cuda_code(launch_combine(rows, dst_row, topk_w, T, k, S, d, out,
+                                  reinterpret_cast<cudaStream_t>(stream)));
 }
 
 int moe_expert_bwd(const moe_bf16* dy, const int32_t* src_pair, const int32_t* dst_row,
-                   const float* topk_w, const int64_t* offsets, int64_t T, int k, int E, int d,
-                   int f, int64_t R_cap, const moe_bf16* xp, const float* g,
+                   const float* topk_w, const int64_t* offsets, const moe_swiglu* act,
+                   int64_t T, int k, int E, int S, int d, int f, int64_t R_cap,
+                   const moe_bf16* xp, const float* g,
                    const float* u, const moe_bf16* a,
                    const moe_bf16* w_gate, const moe_bf16* w_up, const moe_bf16* w_down,
                    moe_bf16* dyg, moe_bf16* dyp, moe_bf16* dg, moe_bf16* du, float* dxp,
@@ -264,10 +281,12 @@ int moe_expert_bwd(const moe_bf16* dy, const int32_t* src_pair, const int32_t* d
       !dyg || !dyp || !dg || !du || !dxp || !dw_gate || !dw_up || !dw_down ||
       (T > 0 && (!dy || !dst_row || !topk_w || !d_topk_w)))
     return MOE_ERR_ARG;
-  if (T < 0 || k <= 0 || k > E) return MOE_ERR_ARG;
-  int rc = check_expert_dims(E, d, f, R_cap);
+  if (T < 0 || k <= 0 || k > E || S < 0) return MOE_ERR_ARG;
+  ActParams ap;
+  if (!act_of(act, &ap)) return MOE_ERR_ARG;
+  int rc = check_expert_dims(E + S, d, f, R_cap);
   if (rc) return rc;
-  if (R_cap < T * k) return MOE_ERR_CAPACITY;
+  if (R_cap < T * (k + S)) return MOE_ERR_CAPACITY;
   if (!ws || ws_bytes < moe_expert_bwd_workspace_size(R_cap, f) ||
       (reinterpret_cast<uintptr_t>(ws) & 255u))
     return MOE_ERR_ARG;
@@ -280,11 +299,14 @@ int moe_expert_bwd(const moe_bf16* dy, const int32_t* src_pair, const int32_t* d
   int* st = device_status_ptr();
   if (!st) return MOE_ERR_CUDA;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  GroupedDims gd{offsets, E, d, f, R_cap, T * k, src_pair};
+  GroupedDims gd{offsets, E + S, d, f, R_cap, T * (k + S)};
+  gd.P_routed = T * k;
+  gd.src_pair = src_pair;
   float* part = static_cast<float*>(ws);
-  cudaError_t e = launch_combine_bwd(dy, src_pair, topk_w, offsets, k, E, d, R_cap, dyg, dyp, s);
+  cudaError_t e = launch_combine_bwd(dy, src_pair, topk_w, offsets, T, k, E + S, d, R_cap, dyg,
+                                     dyp, s);
   if (e == cudaSuccess)
-    e = launch_down_dgrad(gd, dyg, topk_w, w_down, g, u, dg, du, part, st, s);
+    e = launch_down_dgrad(gd, dyg, topk_w, w_down, g, u, dg, du, part, ap, st, s);
   if (e == cudaSuccess)
     e = launch_dtw_finalize(part, down_dgrad_dtw_slots(f), dst_row, T * k, d_topk_w, s);
   if (e == cudaSuccess) e = launch_gateup_dgrad(gd, dg, du, w_gate, w_up, dxp, st, s);
@@ -330,7 +352,7 @@ int moe_decode_fwd(const moe_bf16* x, const float* w_router, const float* bias,
 
 int moe_route_bwd(const float* d_topk_w, const float* topk_w, const int32_t* topk_idx,
                   const float* w_router, const int64_t* offsets, const int32_t* src_pair,
-                  const moe_bf16* x, int64_t T, int d, int E, int k, int align,
+                  const moe_bf16* x, int64_t T, int d, int E, int k, int S, int align,
                   moe_bf16* dx_inout, const float* dxp, const int32_t* dst_row,
                   float* dw_router, float* dbias, void* ws, size_t ws_bytes,
                   moe_stream_t stream) {
@@ -338,17 +360,17 @@ int moe_route_bwd(const float* d_topk_w, const float* topk_w, const int32_t* top
       (T > 0 && (!d_topk_w || !topk_w || !topk_idx || !x || !dx_inout)))
     return MOE_ERR_ARG;
   if (dxp && ((T > 0 && !dst_row) || !aligned16(dxp))) return MOE_ERR_ARG;
-  if (T < 0 || d <= 0 || E <= 0 || k <= 0 || k > E) return MOE_ERR_ARG;
+  if (T < 0 || d <= 0 || E <= 0 || k <= 0 || k > E || S < 0) return MOE_ERR_ARG;
   if (!is_pow2(align) || align < 16 || align > 256) return MOE_ERR_ARG;
-  if (k > kMaxTopK || E > kMaxExperts || d % 8 != 0) return MOE_ERR_UNSUPPORTED;
-  if (moe_row_capacity(T, k, E, align) >= ((int64_t)1 << 31)) return MOE_ERR_UNSUPPORTED;
+  if (k + S > kMaxTopK || E + S > kMaxExperts || d % 8 != 0) return MOE_ERR_UNSUPPORTED;
+  if (moe_row_capacity(T, k + S, E + S, align) >= ((int64_t)1 << 31)) return MOE_ERR_UNSUPPORTED;
   if (!aligned16(x) || !aligned16(dx_inout)) return MOE_ERR_ARG;
   const size_t need = route_bwd_ws_bytes(T, d, E, k, align);
   if (!ws || ws_bytes < need || (reinterpret_cast<uintptr_t>(ws) & 255u)) return MOE_ERR_ARG;
   int* st = device_status_ptr();
   if (!st) return MOE_ERR_CUDA;
   return cuda_code(launch_route_bwd(d_topk_w, topk_w, topk_idx, w_router, offsets, src_pair, x,
-                                    T, d, E, k, align, dx_inout, dxp, dst_row, dw_router, dbias,
+                                    T, d, E, k, S, align, dx_inout, dxp, dst_row, dw_router, dbias,
                                     ws, st, reinterpret_cast<cudaStream_t>(stream)));
 }
 

@@ -11,13 +11,14 @@
 
 namespace moe {
 
-// out[t] = sum_j w[t, j] * rows[dst_row[t*k + j]]  (fp32 rows, slot order, fp32
+// out[t] = sum_j w[t, j] * rows[dst_row[t*k + j]] + sum_s rows[dst_row[T*k + s*T + t]]
+// (fp32 rows, slot order, the S shared experts' rows last with weight 1, fp32
 // sum, rounded to bf16 once); one warp per (token, 256 columns), so a handful
 // of tokens still spreads over many warps
 __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ rows,
                                                       const int32_t* __restrict__ dst_row,
                                                       const float* __restrict__ topk_w,
-                                                      int64_t T, int k, int d,
+                                                      int64_t T, int k, int S, int d,
                                                       moe_bf16* __restrict__ out) {
   const int lane = threadIdx.x & 31;
   const int nv = d / 8;
@@ -31,11 +32,15 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
   if (lane < k) {
     my_r = dst_row[t * k + lane];
     my_w = topk_w ? topk_w[t * k + lane] : 1.f;
+  } else if (lane < k + S) {
+    my_r = dst_row[T * k + (int64_t)(lane - k) * T + t];
+    my_w = 1.f;
   }
+  const int slots = k + S;
   float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
   // the 8-column pieces of up to four slots' rows are loaded together, then
   // summed in slot order
-  for (int j0 = 0; j0 < k; j0 += 4) {
+  for (int j0 = 0; j0 < slots; j0 += 4) {
     float4 rv[4][2];
     float wv[4];
 #pragma unroll
@@ -43,7 +48,7 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
       const int j = j0 + q;
       const int32_t r = __shfl_sync(0xFFFFFFFFu, my_r, j & 31);
       wv[q] = __shfl_sync(0xFFFFFFFFu, my_w, j & 31);
-      const bool ok = j < k && r >= 0 && v < nv;
+      const bool ok = j < slots && r >= 0 && v < nv;
       if (ok) {
         const float4* src = reinterpret_cast<const float4*>(rows + (int64_t)r * d) + 2 * v;
         rv[q][0] = src[0];
@@ -65,17 +70,19 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
 }
 
 cudaError_t launch_combine(const float* rows, const int32_t* dst_row, const float* topk_w,
-                           int64_t T, int k, int d, moe_bf16* out, cudaStream_t s) {
+                           int64_t T, int k, int S, int d, moe_bf16* out, cudaStream_t s) {
   timer_before(MOE_KERNEL_COMBINE, s);
   const int64_t warps = T * (((int64_t)d / 8 + 31) / 32);
-  combine_kernel<<<(unsigned)((warps + 7) / 8), 256, 0, s>>>(rows, dst_row, topk_w, T, k, d, out);
+  combine_kernel<<<(unsigned)((warps + 7) / 8), 256, 0, s>>>(rows, dst_row, topk_w, T, k, S, d,
+                                                             out);
   note_launches(1);
   timer_after(MOE_KERNEL_COMBINE, s);
   return cudaGetLastError();
 }
 
 // Transpose of the weighted combine, one warp per row r of the layout, with
-// p = src_pair[r] and t its token:
+// p = src_pair[r] and t its token (a routed pair p < T*k: t = p / k, weight
+// w(p); a shared expert's pair T*k + s*T + t: weight 1):
 //   dyg[r] = dy[t]                 (the gathered upstream gradient, unscaled:
 //                                   the down dgrad's operand; the score is
 //                                   applied there to the fp32 accumulator)
@@ -85,8 +92,8 @@ cudaError_t launch_combine(const float* rows, const int32_t* dst_row, const floa
 // epilogue instead, where dy . W_down^T and the unrounded A meet.
 __global__ void __launch_bounds__(256) combine_bwd_kernel(
     const moe_bf16* __restrict__ dy, const int32_t* __restrict__ src_pair,
-    const float* __restrict__ topk_w, const int64_t* __restrict__ offsets, int k, int E, int d,
-    int64_t R_cap, moe_bf16* __restrict__ dyg, moe_bf16* __restrict__ dyp) {
+    const float* __restrict__ topk_w, const int64_t* __restrict__ offsets, int64_t T, int k,
+    int E, int d, int64_t R_cap, moe_bf16* __restrict__ dyg, moe_bf16* __restrict__ dyp) {
   const int lane = threadIdx.x & 31;
   const int64_t r = (int64_t)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
   if (r >= R_cap || r >= offsets[E]) return;
@@ -101,8 +108,9 @@ __global__ void __launch_bounds__(256) combine_bwd_kernel(
     }
     return;
   }
-  const int64_t t = p / k;
-  const float w = topk_w[p];
+  const int64_t Pr = T * k;
+  const int64_t t = p < Pr ? p / k : (p - Pr) % T;
+  const float w = p < Pr ? topk_w[p] : 1.f;
   const uint4* g = reinterpret_cast<const uint4*>(dy + t * d);
   // four 8-column pieces of the row in flight per lane
   for (int v0 = lane; v0 < nv; v0 += 128) {
@@ -127,11 +135,11 @@ __global__ void __launch_bounds__(256) combine_bwd_kernel(
 }
 
 cudaError_t launch_combine_bwd(const moe_bf16* dy, const int32_t* src_pair, const float* topk_w,
-                               const int64_t* offsets, int k, int E, int d, int64_t R_cap,
-                               moe_bf16* dyg, moe_bf16* dyp, cudaStream_t s) {
+                               const int64_t* offsets, int64_t T, int k, int E, int d,
+                               int64_t R_cap, moe_bf16* dyg, moe_bf16* dyp, cudaStream_t s) {
   timer_before(MOE_KERNEL_COMBINE_BWD, s);
   combine_bwd_kernel<<<(unsigned)((R_cap + 7) / 8), 256, 0, s>>>(dy, src_pair, topk_w, offsets,
-                                                                 k, E, d, R_cap, dyg, dyp);
+                                                                 T, k, E, d, R_cap, dyg, dyp);
   note_launches(1);
   timer_after(MOE_KERNEL_COMBINE_BWD, s);
   return cudaGetLastError();

@@ -19,15 +19,17 @@
 //               (per warpgroup, or per warp for the down dgrad)
 // Kinds:
 //   GateUpFwd    [G | U] = Xp . [W_gate[e] | W_up[e]]  (two accumulators),
-//                epilogue A = silu(G) * U; stores G, U (fp32, for the
-//                backward's SwiGLU gradient) and A (bf16)      (M-grouped)
+//                epilogue A = act(G, U) (the SwiGLU, clamped or plain:
+//                swiglu() below); stores G, U (fp32, for the backward's
+//                activation gradient) and A (bf16)            (M-grouped)
 //   DownFwd      Yp = A . W_down[e]  (optionally * row_w), fp32  (M-grouped)
 //   DownDgrad    dAu = dY[t(r)] . W_down[e]^T from the unscaled gathered rows
 //                of dY; epilogue dA = w(r) * dAu (the pair's score on the
-//                fp32 accumulator), dG = dA*U*silu'(G), dU = dA*silu(G), and
-//                the row's share of the top-k weight gradient
-//                <dAu, silu(G)*U> (= <dY, A.W_down> with A unrounded), one
-//                fp32 partial per (n-tile, column half)         (M-grouped)
+//                fp32 accumulator; 1 for a shared expert's row),
+//                dG = dA * dact/dG, dU = dA * dact/dU, and the row's share of
+//                the top-k weight gradient <dAu, act(G, U)> (= <dY, A.W_down>
+//                with A unrounded), one fp32 partial per (n-tile, column
+//                half)                                          (M-grouped)
 //   GateUpDgrad  dXp = dG . W_gate[e]^T + dU . W_up[e]^T (two K segments), fp32
 //   WgradDown    dW_down[e] = A_e^T . dYp_e                     (K-grouped)
 //   WgradGateUp  dW_gate[e] = Xp_e^T . dG_e, dW_up[e] = Xp_e^T . dU_e
@@ -120,6 +122,20 @@ constexpr int kStageOutBytes = (kEpiWarps / 4) * kStagePerGroup;
 constexpr int kTstartBytes = (4 * (kMaxExperts + 1) + 1023) & ~1023;
 constexpr int kSmemBytes = kRingBytes + 1024 /*bars*/ + kTstartBytes + kStageOutBytes + 1024;
 
+// The experts' gated activation, A = h(min(G, L)) * (clamp(U, -L, L) + c) with
+// h(g) = g * sigmoid(alpha g): the clamped SwiGLU of GPT-OSS-style layers
+// (prime-rl PR #3885, §Changes, "FP8 routed experts"), and with L = inf,
+// alpha = 1, c = 0 the plain SwiGLU silu(G) * U (Halo "Performance", §Levers
+// that help, fused GLU).
+struct Act {
+  float limit, alpha, c;
+};
+__device__ __forceinline__ float swiglu(float g, float u, const Act& a) {
+  const float gc = fminf(g, a.limit);
+  const float uc = fminf(fmaxf(u, -a.limit), a.limit);
+  return __fdividef(gc, 1.0f + __expf(-a.alpha * gc)) * (uc + a.c);
+}
+
 struct GemmArgs {
   const int64_t* offsets;
   int E;
@@ -132,7 +148,9 @@ struct GemmArgs {
   const float* in0;          // DownDgrad: the saved G, U (fp32)
   const float* in1;
   const float* row_w;
-  const float* pair_w;       // DownDgrad: the score of each pair ([T*k], via src_pair)
+  const float* pair_w;       // DownDgrad: the score of each routed pair ([T*k], via src_pair)
+  int64_t p_routed;          // DownDgrad: pairs below this are routed; the rest shared (weight 1)
+  Act act;                   // GateUpFwd, DownDgrad: the activation
   float* dtw_part;           // DownDgrad: [R_cap][dtw_slots] partials of the top-k weight grad
   int dtw_slots;             // 2 per n-tile (one per epilogue warpgroup)
   // RouterLogits: fp32 output, bias, number of K segments and the K offset of each in B
@@ -748,7 +766,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         rscale = 0.0f;
         if (row_ok) {
           const int32_t p = args.src_pair[row];
-          if (p >= 0) rscale = args.pair_w[p];
+          if (p >= 0) rscale = p < args.p_routed ? args.pair_w[p] : 1.0f;
         }
         if (c_lo < c_end) load_gu(c_lo, gc, uc);
       } else if constexpr (T::down_fwd) {
@@ -779,8 +797,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int i = 0; i < 16; ++i) {
             const float g0 = __uint_as_float(g[2 * i]), g1 = __uint_as_float(g[2 * i + 1]);
             const float u0 = __uint_as_float(u[2 * i]), u1 = __uint_as_float(u[2 * i + 1]);
-            pa[i] = pack_bf16(__fdividef(g0, 1.0f + __expf(-g0)) * u0,
-                              __fdividef(g1, 1.0f + __expf(-g1)) * u1);
+            pa[i] = pack_bf16(swiglu(g0, u0, args.act), swiglu(g1, u1, args.act));
           }
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
@@ -875,14 +892,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int q = 2 * i + j;
                 const float au = __uint_as_float(r[16 * h + q]);
                 const float f = au * rscale;
-                const float sg = __fdividef(1.0f, 1.0f + __expf(-gf[q]));
-                const float sl = gf[q] * sg;   // silu(G)
+                // h = gc sigmoid(alpha gc), h' = s + alpha gc s (1 - s); the
+                // clamps pass no gradient past their limits
+                const float gc = fminf(gf[q], args.act.limit);
+                const float uc = fminf(fmaxf(uf[q], -args.act.limit), args.act.limit) + args.act.c;
+                const float sg = __fdividef(1.0f, 1.0f + __expf(-args.act.alpha * gc));
+                const float hg = gc * sg;
+                const float h1 = fmaf(args.act.alpha * gc, sg * (1.0f - sg), sg);
                 // only the tile's real columns: past them the accumulator was
                 // never written (the MMA's N stops at the tile width) and the
                 // G, U registers may hold the previous half
-                if (ti.n0 + c + 16 * h + q < col_lim) dtw = fmaf(au, sl * uf[q], dtw);
-                dg[j] = f * uf[q] * (sg * (1.0f + gf[q] * (1.0f - sg)));
-                du[j] = f * sl;
+                if (ti.n0 + c + 16 * h + q < col_lim) dtw = fmaf(au, hg * uc, dtw);
+                dg[j] = gf[q] <= args.act.limit ? f * uc * h1 : 0.0f;
+                du[j] = fabsf(uf[q]) <= args.act.limit ? f * hg : 0.0f;
               }
               pk[0][i] = pack_bf16(dg[0], dg[1]);
               pk[1][i] = pack_bf16(du[0], du[1]);
@@ -1229,7 +1251,7 @@ static int64_t mgrouped_tiles_upper(const GroupedDims& g, int N, int BN, int TM 
 
 cudaError_t launch_gateup_fwd(const GroupedDims& g, const moe_bf16* xp, const moe_bf16* w_gate,
                               const moe_bf16* w_up, float* G, float* U, moe_bf16* A,
-                              int* status, cudaStream_t s) {
+                              const ActParams& act, int* status, cudaStream_t s) {
   CUtensorMap a0, b0, b1, o0, o1, o2;
   if (!map2d(&a0, xp, g.d, g.R_cap, BM) || !map3d(&b0, w_gate, g.f, g.d, g.E, BK) ||
       !map3d(&b1, w_up, g.f, g.d, g.E, BK) || !map2d_out(&o0, G, g.f, g.R_cap, 4) ||
@@ -1239,6 +1261,7 @@ cudaError_t launch_gateup_fwd(const GroupedDims& g, const moe_bf16* xp, const mo
   a.N = g.f;
   a.nk_seg = (g.d + BK - 1) / BK;
   a.out0 = G; a.out1 = U; a.out2 = A;
+  a.act = Act{act.limit, act.alpha, act.c};
   // Few rows per expert (the weight-bound regime): 128-wide tiles leave too few
   // tiles to fill every SM's last round of weight streaming; halve them.
   const int64_t rows = (g.P + g.E - 1) / g.E;
@@ -1280,8 +1303,8 @@ int down_dgrad_dtw_slots(int f) {
 
 cudaError_t launch_down_dgrad(const GroupedDims& g, const moe_bf16* dyg, const float* pair_w,
                               const moe_bf16* w_down, const float* G, const float* U,
-                              moe_bf16* dG, moe_bf16* dU, float* dtw_part, int* status,
-                              cudaStream_t s) {
+                              moe_bf16* dG, moe_bf16* dU, float* dtw_part,
+                              const ActParams& act, int* status, cudaStream_t s) {
   CUtensorMap a0, b0, o0, o1;
   const int bn = pick_bn(g.f, 16);
   // no pairs by default: this kernel is bound by its epilogue (G and U read,
@@ -1300,6 +1323,8 @@ cudaError_t launch_down_dgrad(const GroupedDims& g, const moe_bf16* dyg, const f
   a.in0 = G; a.in1 = U;
   a.out0 = dG; a.out1 = dU;
   a.pair_w = pair_w;
+  a.p_routed = g.P_routed;
+  a.act = Act{act.limit, act.alpha, act.c};
   a.dtw_part = dtw_part;
   a.dtw_slots = down_dgrad_dtw_slots(g.f);
   a.bn = bn;

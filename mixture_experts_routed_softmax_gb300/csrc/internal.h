@@ -36,23 +36,23 @@ size_t route_bwd_ws_bytes(int64_t T, int d, int E, int k, int align);
 cudaError_t launch_route_bwd(const float* d_topk_w, const float* topk_w, const int32_t* topk_idx,
                              const float* w_router, const int64_t* offsets,
                              const int32_t* src_pair, const moe_bf16* x, int64_t T, int d, int E,
-                             int k, int align, moe_bf16* dx_inout, const float* dxp,
+                             int k, int S, int align, moe_bf16* dx_inout, const float* dxp,
                              const int32_t* dst_row, float* dw_router, float* dbias, void* ws,
                              int* status, cudaStream_t s);
 
 // permute.cu
 size_t permute_ws_bytes(int64_t T, int k, int E);
-cudaError_t launch_permute(const int32_t* topk_idx, int64_t T, int k, int E, int align,
+cudaError_t launch_permute(const int32_t* topk_idx, int64_t T, int k, int E, int S, int align,
                            const moe_bf16* x, int d, int64_t R_cap, int32_t* counts,
                            int64_t* offsets, int32_t* dst_row, int32_t* src_pair, moe_bf16* xp,
                            void* ws, int* status, cudaStream_t s);
 
 // combine.cu
 cudaError_t launch_combine(const float* rows, const int32_t* dst_row, const float* topk_w,
-                           int64_t T, int k, int d, moe_bf16* out, cudaStream_t s);
+                           int64_t T, int k, int S, int d, moe_bf16* out, cudaStream_t s);
 cudaError_t launch_combine_bwd(const moe_bf16* dy, const int32_t* src_pair, const float* topk_w,
-                               const int64_t* offsets, int k, int E, int d, int64_t R_cap,
-                               moe_bf16* dyg, moe_bf16* dyp, cudaStream_t s);
+                               const int64_t* offsets, int64_t T, int k, int E, int d,
+                               int64_t R_cap, moe_bf16* dyg, moe_bf16* dyp, cudaStream_t s);
 // d_topk_w[p] = sum over the slots, in order, of part[dst_row[p]][slot]
 cudaError_t launch_dtw_finalize(const float* part, int slots, const int32_t* dst_row, int64_t P,
                                 float* d_topk_w, cudaStream_t s);
@@ -77,11 +77,17 @@ cudaError_t launch_router_wgrad_gemm(const moe_bf16* x, const moe_bf16* dl3, int
 cudaError_t launch_router_gemm(const moe_bf16* x, const moe_bf16* w_split, const float* bias,
                                int64_t T, int d, int E, int E8, int ksplit, float* out,
                                int* status, cudaStream_t s);
+// The experts' activation: A = h(min(G, L)) (clamp(U, -L, L) + c),
+// h(g) = g sigmoid(alpha g); the plain SwiGLU is {inf, 1, 0}.
+struct ActParams {
+  float limit, alpha, c;
+};
 struct GroupedDims {
   const int64_t* offsets;
-  int E, d, f;
+  int E, d, f;      // E: every group of the layout (routed and shared experts)
   int64_t R_cap;
-  int64_t P;        // token-expert pairs (T * k): sizes the tile schedule
+  int64_t P;        // pairs of the layout (T * (k + S)): sizes the tile schedule
+  int64_t P_routed = 0;   // routed pairs (T * k): the rest are shared, weight 1
   // the pair held by each row of the layout (-1: padding), or NULL: lets the
   // K-grouped weight gradients stop each expert's reduction at its real rows;
   // the down dgrad needs it (it finds each row's score through it)
@@ -89,14 +95,14 @@ struct GroupedDims {
 };
 cudaError_t launch_gateup_fwd(const GroupedDims& g, const moe_bf16* xp, const moe_bf16* w_gate,
                               const moe_bf16* w_up, float* G, float* U, moe_bf16* A,
-                              int* status, cudaStream_t s);
+                              const ActParams& act, int* status, cudaStream_t s);
 cudaError_t launch_down_fwd(const GroupedDims& g, const moe_bf16* A, const moe_bf16* w_down,
                             const float* row_w, float* yp, int* status, cudaStream_t s);
 int down_dgrad_dtw_slots(int f);
 cudaError_t launch_down_dgrad(const GroupedDims& g, const moe_bf16* dyg, const float* pair_w,
                               const moe_bf16* w_down, const float* G, const float* U,
-                              moe_bf16* dG, moe_bf16* dU, float* dtw_part, int* status,
-                              cudaStream_t s);
+                              moe_bf16* dG, moe_bf16* dU, float* dtw_part,
+                              const ActParams& act, int* status, cudaStream_t s);
 cudaError_t launch_gateup_dgrad(const GroupedDims& g, const moe_bf16* dG, const moe_bf16* dU,
                                 const moe_bf16* w_gate, const moe_bf16* w_up, float* dxp,
                                 int* status, cudaStream_t s);

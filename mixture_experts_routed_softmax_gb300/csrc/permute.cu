@@ -17,6 +17,10 @@
 //   scatter dst_row[p] = offsets[e] + block base + rank; src_pair[dst] = p.
 //   gather  xp[r] = x[src_pair[r] / k] for real rows, zeros for padding rows.
 // Pair p's rank inside its expert is therefore its rank in ascending p.
+// Shared experts (S of them, every token's copy with weight 1: prime-rl PR
+// #3885, §Changes, "Fused FP8 shared expert") follow the routed groups: group
+// E + s holds the T pairs T*k + s*T + t in token order (padded to `align`);
+// the scan writes their counts and offsets, the gather their rows and maps.
 #include "common.cuh"
 #include "internal.h"
 
@@ -93,8 +97,20 @@ __global__ void __launch_bounds__(kHistWarps * 32) permute_hist_kernel(
 }
 
 // One CTA of 1024 threads; thread e owns expert e.
+// counts and offsets of the S shared groups after the routed total
+__device__ __forceinline__ void shared_groups(int E, int S, int64_t T, int align,
+                                              int64_t routed_end, int32_t* counts,
+                                              int64_t* offsets) {
+  const int64_t Tp = ((T + align - 1) / align) * align;
+  for (int s = 0; s < S; ++s) {
+    counts[E + s] = (int32_t)T;
+    offsets[E + 1 + s] = routed_end + (int64_t)(s + 1) * Tp;
+  }
+}
+
 __global__ void __launch_bounds__(1024) permute_scan_kernel(int32_t* __restrict__ blk_count,
-                                                            int64_t nblk, int E, int align,
+                                                            int64_t nblk, int E, int S, int64_t T,
+                                                            int align,
                                                             int32_t* __restrict__ counts,
                                                             int64_t* __restrict__ offsets) {
   __shared__ int64_t warp_tot[32];
@@ -134,7 +150,10 @@ __global__ void __launch_bounds__(1024) permute_scan_kernel(int32_t* __restrict_
     offsets[e] = excl;
     for (int64_t b = 0; b < nblk; ++b) blk_count[b * E + e] += (int32_t)excl;
   }
-  if (e == E - 1) offsets[E] = excl + padded;
+  if (e == E - 1) {
+    offsets[E] = excl + padded;
+    shared_groups(E, S, T, align, excl + padded, counts, offsets);
+  }
 }
 
 __global__ void permute_scatter_kernel(const int32_t* __restrict__ idx, int64_t P, int E,
@@ -160,7 +179,8 @@ __global__ void permute_scatter_kernel(const int32_t* __restrict__ idx, int64_t 
 // layout as the four-kernel path.
 constexpr int kSmallPairs = 256;
 __global__ void __launch_bounds__(1024) permute_small_kernel(
-    const int32_t* __restrict__ idx, int64_t P, int E, int align, int32_t* __restrict__ counts,
+    const int32_t* __restrict__ idx, int64_t P, int E, int S, int64_t T, int align,
+    int32_t* __restrict__ counts,
     int64_t* __restrict__ offsets, int32_t* __restrict__ dst_row,
     int32_t* __restrict__ src_pair, int* status) {
   __shared__ int32_t s_idx[kSmallPairs];
@@ -198,7 +218,10 @@ __global__ void __launch_bounds__(1024) permute_small_kernel(
     counts[tid] = (int32_t)n;
     offsets[tid] = excl;
   }
-  if (tid == E - 1) offsets[E] = excl + padded;
+  if (tid == E - 1) {
+    offsets[E] = excl + padded;
+    shared_groups(E, S, T, align, excl + padded, counts, offsets);
+  }
   __syncthreads();
   for (int p = tid; p < P; p += blockDim.x) {
     const int e = s_idx[p];
@@ -223,25 +246,36 @@ __device__ __forceinline__ int expert_of_row_p(const int64_t* offsets, int E, in
   return lo;
 }
 
-// one warp per row
+// one warp per row; a shared expert's row also writes its pair's maps
 __global__ void __launch_bounds__(256) permute_gather_kernel(
-    const moe_bf16* __restrict__ x, int d, int k, const int64_t* __restrict__ offsets,
-    const int32_t* __restrict__ counts, int E, int64_t R_cap, int32_t* __restrict__ src_pair,
-    moe_bf16* __restrict__ xp) {
+    const moe_bf16* __restrict__ x, int d, int k, int64_t T, const int64_t* __restrict__ offsets,
+    const int32_t* __restrict__ counts, int E, int S, int64_t R_cap,
+    int32_t* __restrict__ src_pair, int32_t* __restrict__ dst_row, moe_bf16* __restrict__ xp) {
   const int lane = threadIdx.x & 31;
   const int64_t r = (int64_t)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
   if (r >= R_cap) return;
-  const int64_t R_pad = offsets[E];
+  const int64_t R_pad = offsets[E + S];
   if (r >= R_pad) {
     if (lane == 0) src_pair[r] = -1;
     return;
   }
-  const int e = expert_of_row_p(offsets, E, r);
-  const bool real = (r - offsets[e]) < (int64_t)counts[e];
+  const int e = expert_of_row_p(offsets, E + S, r);
+  const int64_t i = r - offsets[e];
+  const bool real = i < (int64_t)counts[e];
   uint4* dst = reinterpret_cast<uint4*>(xp + r * d);
   const int nv = d / 8;
   if (real) {
-    const int64_t t = src_pair[r] / k;
+    int64_t t;
+    if (e < E) {
+      t = src_pair[r] / k;
+    } else {
+      t = i;
+      const int64_t p = T * k + (int64_t)(e - E) * T + i;
+      if (lane == 0) {
+        src_pair[r] = (int32_t)p;
+        dst_row[p] = (int32_t)r;
+      }
+    }
     const uint4* src = reinterpret_cast<const uint4*>(x + t * d);
     // four 16-byte pieces in flight per lane
     for (int v0 = lane; v0 < nv; v0 += 128) {
@@ -259,7 +293,7 @@ __global__ void __launch_bounds__(256) permute_gather_kernel(
   }
 }
 
-cudaError_t launch_permute(const int32_t* topk_idx, int64_t T, int k, int E, int align,
+cudaError_t launch_permute(const int32_t* topk_idx, int64_t T, int k, int E, int S, int align,
                            const moe_bf16* x, int d, int64_t R_cap, int32_t* counts,
                            int64_t* offsets, int32_t* dst_row, int32_t* src_pair, moe_bf16* xp,
                            void* ws, int* status, cudaStream_t s) {
@@ -276,20 +310,20 @@ cudaError_t launch_permute(const int32_t* topk_idx, int64_t T, int k, int E, int
   timer_before(MOE_KERNEL_PERMUTE, s);
   int launches = 2;
   if (P > 0 && P <= kSmallPairs) {
-    permute_small_kernel<<<1, 1024, 0, s>>>(topk_idx, P, E, align, counts, offsets, dst_row,
-                                            src_pair, status);
+    permute_small_kernel<<<1, 1024, 0, s>>>(topk_idx, P, E, S, T, align, counts, offsets,
+                                            dst_row, src_pair, status);
   } else {
     if (P > 0)
       permute_hist_kernel<<<(unsigned)nblk, kHistWarps * 32, hist_smem, s>>>(
           topk_idx, P, E, blk_count, rank_in_blk, status);
-    permute_scan_kernel<<<1, 1024, 0, s>>>(blk_count, nblk, E, align, counts, offsets);
+    permute_scan_kernel<<<1, 1024, 0, s>>>(blk_count, nblk, E, S, T, align, counts, offsets);
     if (P > 0)
       permute_scatter_kernel<<<(unsigned)((P + 255) / 256), 256, 0, s>>>(
           topk_idx, P, E, blk_count, rank_in_blk, dst_row, src_pair);
     launches = P > 0 ? 4 : 2;
   }
-  permute_gather_kernel<<<(unsigned)((R_cap + 7) / 8), 256, 0, s>>>(x, d, k, offsets, counts, E,
-                                                                    R_cap, src_pair, xp);
+  permute_gather_kernel<<<(unsigned)((R_cap + 7) / 8), 256, 0, s>>>(
+      x, d, k, T, offsets, counts, E, S, R_cap, src_pair, dst_row, xp);
   note_launches(launches);
   timer_after(MOE_KERNEL_PERMUTE, s);
   return cudaGetLastError();

@@ -62,7 +62,7 @@ extern "C" int moe_permute_noalloc(const int32_t* topk_idx, int64_t T, int k, in
   if (!ws || !st) return MOE_ERR_CUDA;
   // The permute kernels write every scratch word before they read it, so the
   // previous call's leftovers need no clearing.
-  const cudaError_t e = moe::launch_permute(topk_idx, T, k, E, align, x, d, R_cap, counts,
+  const cudaError_t e = moe::launch_permute(topk_idx, T, k, E, 0, align, x, d, R_cap, counts,
                                             offsets, dst_row, src_pair, xp, ws, st,
                                             reinterpret_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;

@@ -330,14 +330,15 @@ __global__ void transpose_f32_kernel(const float* __restrict__ in, int rows, int
 
 // one warp per token: dl for its k slots (to dl_pair, and as three bf16 parts
 // into the token's dense row of dl3), then dx[t]. With dxp (fp32 rows) given,
-// dx[t] = sum_j dxp[dst_row[t, j]] + sum_j dl_j W_r[:, e_j] in fp32, rounded to
-// bf16 once (the permute transpose fused in); without it, dx[t] += sum_j dl_j
+// dx[t] = sum_j dxp[dst_row[t, j]] + sum_s dxp[dst_row[T*k + s*T + t]] +
+// sum_j dl_j W_r[:, e_j] in fp32, rounded to bf16 once (the permute transpose,
+// shared experts' rows included, fused in); without it, dx[t] += sum_j dl_j
 // W_r[:, e_j]. The dxp rows of up to four slots are loaded together; few
 // registers, so that many warps per SM keep enough loads in flight.
 __global__ void __launch_bounds__(256, 4) route_bwd_token_kernel(
     const float* __restrict__ d_topk_w, const float* __restrict__ topk_w,
     const int32_t* __restrict__ topk_idx, const float* __restrict__ wrT, int64_t T, int d, int E,
-    int E8, int k, float* __restrict__ dl_pair, moe_bf16* __restrict__ dl3,
+    int E8, int k, int S, float* __restrict__ dl_pair, moe_bf16* __restrict__ dl3,
     moe_bf16* __restrict__ dx, const float* __restrict__ dxp,
     const int32_t* __restrict__ dst_row) {
   const int lane = threadIdx.x & 31;
@@ -351,7 +352,10 @@ __global__ void __launch_bounds__(256, 4) route_bwd_token_kernel(
     e = topk_idx[t * k + lane];
     if (e < 0 || e >= E) { e = -1; w = 0.f; dw = 0.f; }
     if (dxp) r = dst_row[t * k + lane];
+  } else if (lane < k + S && dxp) {
+    r = dst_row[T * k + (int64_t)(lane - k) * T + t];
   }
+  const int slots = k + S;
   float inner = w * dw;
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) inner += __shfl_xor_sync(0xFFFFFFFFu, inner, off);
@@ -382,13 +386,13 @@ __global__ void __launch_bounds__(256, 4) route_bwd_token_kernel(
     float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
     if (in && !dxp) unpack8(*reinterpret_cast<const uint4*>(dxr + c), acc);
     if (dxp) {
-      for (int j0 = 0; j0 < k; j0 += 4) {
+      for (int j0 = 0; j0 < slots; j0 += 4) {
         float4 v[4][2];
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
           const int j = j0 + q;
           const int rj = __shfl_sync(0xFFFFFFFFu, r, j & 31);
-          if (in && j < k && rj >= 0) {
+          if (in && j < slots && rj >= 0) {
             const float4* src = reinterpret_cast<const float4*>(dxp + (int64_t)rj * d + c);
             v[q][0] = src[0];
             v[q][1] = src[1];
@@ -459,7 +463,7 @@ __global__ void __launch_bounds__(256) route_bwd_reduce_kernel(
 cudaError_t launch_route_bwd(const float* d_topk_w, const float* topk_w, const int32_t* topk_idx,
                              const float* w_router, const int64_t* offsets,
                              const int32_t* src_pair, const moe_bf16* x, int64_t T, int d, int E,
-                             int k, int align, moe_bf16* dx_inout, const float* dxp,
+                             int k, int S, int align, moe_bf16* dx_inout, const float* dxp,
                              const int32_t* dst_row, float* dw_router, float* dbias, void* ws,
                              int* status, cudaStream_t s) {
   (void)align;
@@ -481,7 +485,7 @@ cudaError_t launch_route_bwd(const float* d_topk_w, const float* topk_w, const i
   note_launches(1);
   if (T > 0) {
     route_bwd_token_kernel<<<(unsigned)((T + 7) / 8), 256, 0, s>>>(
-        d_topk_w, topk_w, topk_idx, wrT, T, d, E, E8, k, dl_pair, dl3, dx_inout, dxp, dst_row);
+        d_topk_w, topk_w, topk_idx, wrT, T, d, E, E8, k, S, dl_pair, dl3, dx_inout, dxp, dst_row);
     note_launches(1);
   }
   cudaError_t err = cudaGetLastError();

@@ -70,36 +70,48 @@ class Buffers:
 class MoELayer:
     """Weights of one layer (device tensors) and the calls that run it.
 
-    w_router [d, E] fp32, bias [E] fp32 or None, w_gate / w_up [E, d, f] bf16,
-    w_down [E, f, d] bf16; top-k routing; ``align`` pads each expert's rows.
+    w_router [d, E] fp32, bias [E] fp32 or None, w_gate / w_up [E+S, d, f]
+    bf16, w_down [E+S, f, d] bf16 (the E routed experts, then the S shared
+    experts every token goes through with weight 1); top-k routing; ``align``
+    pads each expert's rows; ``act`` = (limit, alpha, up_offset) of the
+    clamped SwiGLU, or None for the plain SwiGLU.
     """
 
-    def __init__(self, w_router, bias, w_gate, w_up, w_down, k: int, align: int = 128):
+    def __init__(self, w_router, bias, w_gate, w_up, w_down, k: int, align: int = 128,
+                 act=None):
         self.lib = _lib.load()
         self.w_router = w_router.contiguous()
         self.bias = None if bias is None else bias.contiguous()
         self.w_gate = w_gate.contiguous()
         self.w_up = w_up.contiguous()
         self.w_down = w_down.contiguous()
-        self.E, self.d, self.f = w_gate.shape
+        self.E = int(w_router.shape[1])
+        EE, self.d, self.f = w_gate.shape
+        self.S = int(EE) - self.E
+        if self.S < 0:
+            raise ValueError("w_gate holds fewer experts than the router")
         self.k = k
         self.align = align
+        self.act = None if act is None else _lib.Swiglu(*[float(v) for v in act])
         dev = w_gate.device
         if dev.type != "cuda":
             raise RuntimeError("MoELayer runs on a CUDA device only")
         self.device = dev
 
     @classmethod
-    def from_inputs(cls, inp: dict, k: int, align: int = 128, device="cuda"):
+    def from_inputs(cls, inp: dict, k: int, align: int = 128, device="cuda", act=None):
         mv = lambda t: None if t is None else t.to(device)  # noqa: E731
         return cls(mv(inp["w_router"]), mv(inp.get("bias")), mv(inp["w_gate"]),
-                   mv(inp["w_up"]), mv(inp["w_down"]), k, align)
+                   mv(inp["w_up"]), mv(inp["w_down"]), k, align, act)
+
+    def _act(self):
+        return None if self.act is None else _lib.ctypes.addressof(self.act)
 
     def row_capacity(self, T: int) -> int:
-        return int(self.lib.moe_row_capacity(T, self.k, self.E, self.align))
+        return int(self.lib.moe_row_capacity(T, self.k + self.S, self.E + self.S, self.align))
 
     def buffers(self, T: int, backward: bool = True) -> Buffers:
-        E, d, f, k = self.E, self.d, self.f, self.k
+        E, d, f, k, S = self.E, self.d, self.f, self.k, self.S
         R = self.row_capacity(T)
         kw = dict(device=self.device)
         ws_p = int(self.lib.moe_workspace_size(_lib.MOE_WS_PERMUTE, T, d, E, k, self.align))
@@ -108,9 +120,9 @@ class MoELayer:
             logits=torch.empty(T, E, dtype=torch.float32, **kw),
             topk_idx=torch.empty(T, k, dtype=torch.int32, **kw),
             topk_w=torch.empty(T, k, dtype=torch.float32, **kw),
-            counts=torch.empty(E, dtype=torch.int32, **kw),
-            offsets=torch.empty(E + 1, dtype=torch.int64, **kw),
-            dst_row=torch.empty(T * k, dtype=torch.int32, **kw),
+            counts=torch.empty(E + S, dtype=torch.int32, **kw),
+            offsets=torch.empty(E + S + 1, dtype=torch.int64, **kw),
+            dst_row=torch.empty(T * (k + S), dtype=torch.int32, **kw),
             src_pair=torch.empty(R, dtype=torch.int32, **kw),
             xp=torch.empty(R, d, dtype=BF16, **kw),
             g=torch.empty(R, f, dtype=torch.float32, **kw),
@@ -132,9 +144,9 @@ class MoELayer:
             b.dxp = torch.empty(R, d, dtype=torch.float32, **kw)
             b.d_topk_w = torch.empty(T, k, dtype=torch.float32, **kw)
             b.dx = torch.empty(T, d, dtype=BF16, **kw)
-            b.dw_gate = torch.empty(E, d, f, dtype=BF16, **kw)
-            b.dw_up = torch.empty(E, d, f, dtype=BF16, **kw)
-            b.dw_down = torch.empty(E, f, d, dtype=BF16, **kw)
+            b.dw_gate = torch.empty(E + S, d, f, dtype=BF16, **kw)
+            b.dw_up = torch.empty(E + S, d, f, dtype=BF16, **kw)
+            b.dw_down = torch.empty(E + S, f, d, dtype=BF16, **kw)
             b.dw_router = torch.empty(d, E, dtype=torch.float32, **kw)
             b.dbias = torch.empty(E, dtype=torch.float32, **kw)
             b.ws_route_bwd = torch.empty(max(ws_r, 256), dtype=torch.uint8, **kw)
@@ -150,22 +162,22 @@ class MoELayer:
 
     def permute(self, x, b: Buffers, topk_idx=None, stream=None):
         idx = b.topk_idx if topk_idx is None else topk_idx
-        _lib.call("moe_permute", _p(idx), b.T, self.k, self.E, self.align, _p(x), self.d,
+        _lib.call("moe_permute", _p(idx), b.T, self.k, self.E, self.S, self.align, _p(x), self.d,
                   b.R_cap, _p(b.counts), _p(b.offsets), _p(b.dst_row), _p(b.src_pair),
                   _p(b.xp), _p(b.ws_permute), b.ws_permute.numel(), _stream(stream))
 
     def expert_fwd(self, b: Buffers, row_w=None, stream=None):
-        _lib.call("moe_expert_fwd", _p(b.xp), _p(b.offsets), _p(row_w), b.T, self.k, self.E,
-                  self.d, self.f, b.R_cap, _p(self.w_gate), _p(self.w_up), _p(self.w_down), _p(b.g), _p(b.u),
-                  _p(b.a), _p(b.yp), _stream(stream))
+        _lib.call("moe_expert_fwd", _p(b.xp), _p(b.offsets), _p(row_w), self._act(), b.T, self.k,
+                  self.E, self.S, self.d, self.f, b.R_cap, _p(self.w_gate), _p(self.w_up),
+                  _p(self.w_down), _p(b.g), _p(b.u), _p(b.a), _p(b.yp), _stream(stream))
 
     def combine(self, rows, b: Buffers, out, weights=True, stream=None):
         _lib.call("moe_combine", _p(rows), _p(b.dst_row), _p(b.topk_w) if weights else None,
-                  b.T, self.k, self.d, _p(out), _stream(stream))
+                  b.T, self.k, self.S, self.d, _p(out), _stream(stream))
 
     def expert_bwd(self, dy, b: Buffers, stream=None):
         _lib.call("moe_expert_bwd", _p(dy), _p(b.src_pair), _p(b.dst_row), _p(b.topk_w),
-                  _p(b.offsets), b.T, self.k, self.E, self.d, self.f, b.R_cap,
+                  _p(b.offsets), self._act(), b.T, self.k, self.E, self.S, self.d, self.f, b.R_cap,
                   _p(b.xp), _p(b.g), _p(b.u), _p(b.a),
                   _p(self.w_gate), _p(self.w_up), _p(self.w_down),
                   _p(b.dyg), _p(b.dyp), _p(b.dg), _p(b.du), _p(b.dxp), _p(b.d_topk_w),
@@ -179,7 +191,7 @@ class MoELayer:
         x = b.x if x is None else x
         _lib.call("moe_route_bwd", _p(b.d_topk_w), _p(b.topk_w), _p(b.topk_idx),
                   _p(self.w_router), _p(b.offsets), _p(b.src_pair), _p(x), b.T, self.d,
-                  self.E, self.k, self.align, _p(b.dx), _p(b.dxp) if fused else None,
+                  self.E, self.k, self.S, self.align, _p(b.dx), _p(b.dxp) if fused else None,
                   _p(b.dst_row) if fused else None, _p(b.dw_router), _p(b.dbias),
                   _p(b.ws_route_bwd), b.ws_route_bwd.numel(), _stream(stream))
 
@@ -221,7 +233,11 @@ class MoELayer:
 
     def decode_fwd(self, x, b: Buffers, forced_idx=None, stream=None):
         """The whole forward of T <= 8 tokens in one launch (moe_decode_fwd);
-        b from decode_buffers(T). Fills b.logits, b.topk_idx, b.topk_w, b.y."""
+        b from decode_buffers(T). Fills b.logits, b.topk_idx, b.topk_w, b.y.
+        Routed experts with the plain SwiGLU only."""
+        if self.S or self.act is not None:
+            raise ValueError("the one-launch decode forward takes routed experts with the plain "
+                             "SwiGLU only")
         b.x = x
         _lib.call("moe_decode_fwd", _p(x), _p(self.w_router), _p(self.bias), _p(forced_idx),
                   b.T, self.d, self.f, self.E, self.k, _p(self.w_gate), _p(self.w_up),

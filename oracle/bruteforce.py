@@ -45,14 +45,34 @@ def _sigmoid(g):
     return 1.0 / (1.0 + math.exp(-g))
 
 
-def layer(x, wr, b, wg, wu, wd, k, dy):
+def _act(g, u, act):
+    """The gated activation and its two partial derivatives at one element:
+    A = gc * sigmoid(alpha gc) * (uc + c), gc = g clamped above at L, uc = u
+    clamped to [-L, L]; act = (L, alpha, c), or None for silu(g) * u."""
+    if act is None:
+        s = _sigmoid(g)
+        return g * s * u, u * (s + g * s * (1.0 - s)), g * s
+    L, al, c = act
+    gc = g if g <= L else L
+    uc = u if -L <= u <= L else (L if u > L else -L)
+    s = _sigmoid(al * gc)
+    a = gc * s * (uc + c)
+    da_dg = (s + al * gc * s * (1.0 - s)) * (uc + c) if g <= L else 0.0
+    da_du = gc * s if -L <= u <= L else 0.0
+    return a, da_dg, da_du
+
+
+def layer(x, wr, b, wg, wu, wd, k, dy, act=None, shared=0):
     """Forward and backward with nested lists of Python floats.
 
-    x [T][d], wr [d][E], b [E] or None, wg/wu [E][d][f], wd [E][f][d],
-    dy [T][d]. Returns a dict of nested lists: logits, idx, w, y, dx, dwr, db,
-    dwg, dwu, dwd, dtw (gradient of the top-k weights).
+    x [T][d], wr [d][E], b [E] or None, wg/wu [E+S][d][f], wd [E+S][f][d] (the
+    last S = ``shared`` experts are shared: every token goes through them with
+    weight 1), dy [T][d], act as in ``_act``. Returns a dict of nested lists:
+    logits, idx, w, y, dx, dwr, db, dwg, dwu, dwd, dtw (gradient of the top-k
+    weights).
     """
     T, d, E, f = len(x), len(x[0]), len(wr[0]), len(wg[0][0])
+    EE = E + shared
     logits = [[sum(x[t][i] * wr[i][e] for i in range(d)) + (b[e] if b is not None else 0.0)
                for e in range(E)] for t in range(T)]
     idx = [topk_enumerate(logits[t], k) for t in range(T)]
@@ -68,28 +88,29 @@ def layer(x, wr, b, wg, wu, wd, k, dy):
 
     y = [[0.0] * d for _ in range(T)]
     dx = [[0.0] * d for _ in range(T)]
-    dwg = [[[0.0] * f for _ in range(d)] for _ in range(E)]
-    dwu = [[[0.0] * f for _ in range(d)] for _ in range(E)]
-    dwd = [[[0.0] * d for _ in range(f)] for _ in range(E)]
+    dwg = [[[0.0] * f for _ in range(d)] for _ in range(EE)]
+    dwu = [[[0.0] * f for _ in range(d)] for _ in range(EE)]
+    dwd = [[[0.0] * d for _ in range(f)] for _ in range(EE)]
     dtw = [[0.0] * k for _ in range(T)]
     for t in range(T):
-        for j in range(k):
-            e = idx[t][j]
+        # slots j < k: the routed experts with their weights; then the shared
+        # experts with weight 1
+        for j in range(k + shared):
+            e = idx[t][j] if j < k else E + (j - k)
+            wj = w[t][j] if j < k else 1.0
             g = [sum(x[t][i] * wg[e][i][c] for i in range(d)) for c in range(f)]
             u = [sum(x[t][i] * wu[e][i][c] for i in range(d)) for c in range(f)]
-            a = [g[c] * _sigmoid(g[c]) * u[c] for c in range(f)]
+            act_gu = [_act(g[c], u[c], act) for c in range(f)]
+            a = [v[0] for v in act_gu]
             yu = [sum(a[c] * wd[e][c][o] for c in range(f)) for o in range(d)]
             for o in range(d):
-                y[t][o] += w[t][j] * yu[o]
-            dtw[t][j] = sum(dy[t][o] * yu[o] for o in range(d))
-            dyu = [w[t][j] * dy[t][o] for o in range(d)]
+                y[t][o] += wj * yu[o]
+            if j < k:
+                dtw[t][j] = sum(dy[t][o] * yu[o] for o in range(d))
+            dyu = [wj * dy[t][o] for o in range(d)]
             da = [sum(dyu[o] * wd[e][c][o] for o in range(d)) for c in range(f)]
-            dg = []
-            du = []
-            for c in range(f):
-                s = _sigmoid(g[c])
-                dg.append(da[c] * u[c] * (s + g[c] * s * (1.0 - s)))
-                du.append(da[c] * g[c] * s)
+            dg = [da[c] * act_gu[c][1] for c in range(f)]
+            du = [da[c] * act_gu[c][2] for c in range(f)]
             for i in range(d):
                 dx[t][i] += sum(dg[c] * wg[e][i][c] + du[c] * wu[e][i][c] for c in range(f))
             for c in range(f):

@@ -145,11 +145,23 @@ def assert_mag_close(name, got, ref, mag):
     return float(np.max(diff)) / rms if rms > 0 else 0.0
 
 
-def _sig(g):
-    return 1.0 / (1.0 + np.exp(-g))
+def act_derivs(G, U, act=None):
+    """The activation A(G, U) of act = (L, alpha, c) (None: the plain SwiGLU)
+    and its first and second partial derivatives, element-wise:
+    A, A_g, A_u, A_gg, A_gu (A_uu = 0). Zero past the clamps."""
+    L, al, c = mo.PLAIN_SWIGLU if act is None else act
+    gc = np.minimum(G, L)
+    uc = np.clip(U, -L, L)
+    s = 1.0 / (1.0 + np.exp(-al * gc))
+    h = gc * s
+    h1 = s + al * gc * s * (1 - s)
+    h2 = al * s * (1 - s) * (2 + al * gc * (1 - 2 * s))
+    ing = (G <= L).astype(np.float64)
+    inu = ((U >= -L) & (U <= L)).astype(np.float64)
+    return h * (uc + c), h1 * (uc + c) * ing, h * inu, h2 * (uc + c) * ing, h1 * ing * inu
 
 
-def magnitudes(inp, fw, bw, k):
+def magnitudes(inp, fw, bw, k, act=None, shared=0):
     """Per-element first-order error magnitudes (see the module docstring).
     Keys follow the oracle's: G, U, A, Yu, y, dYu, dA, dG, dU, dXp, dx,
     d_topk_w, dw_gate, dw_up, dw_down, dw_router, dbias, logits."""
@@ -158,16 +170,14 @@ def magnitudes(inp, fw, bw, k):
     T, d = x.shape
     idx = fw["idx"]
     E = int(np.asarray(mo.as_f64(inp["w_router"])).shape[1])
-    P = T * k
-    w = fw["w"].reshape(-1)
-    tok = np.arange(P) // k
+    EE = E + shared
+    P = T * (k + shared)
+    e_of_p = mo.pair_experts(idx, E, shared)
+    tok = np.concatenate([np.arange(T * k) // k] + [np.arange(T)] * shared)
+    w = np.concatenate([fw["w"].reshape(-1)] + [np.ones(T)] * shared)
     G, U, A = fw["G"], fw["U"], fw["A"]
-    sG = _sig(G)
-    silu = G * sG
-    dsilu = sG * (1 + G * (1 - sG))
-    ddsilu = sG * (1 - sG) * (2 + G * (1 - 2 * sG))
+    _, Ag, Au, Agg, Agu = act_derivs(G, U, act)
     f = G.shape[1]
-    M = {k_: None for k_ in ("G", "U", "A", "Yu")}
     MG = np.zeros((P, f)); MU = np.zeros((P, f)); MYu = np.zeros((P, d))
     have_bw = bw is not None
     if have_bw:
@@ -177,21 +187,18 @@ def magnitudes(inp, fw, bw, k):
         MdYu = np.abs(w)[:, None] * ady[tok] + np.abs(bw["dYu"])
         MdA = np.zeros((P, f)); MdXp = np.zeros((P, d))
         MdG = np.zeros((P, f)); MdU = np.zeros((P, f))
-        Mdwg = np.zeros((E, d, f)); Mdwu = np.zeros((E, d, f)); Mdwd = np.zeros((E, f, d))
-    e_of_p = idx.reshape(-1)
-    MA = None
-    for e in range(E):
+        Mdwg = np.zeros((EE, d, f)); Mdwu = np.zeros((EE, d, f)); Mdwd = np.zeros((EE, f, d))
+    for e in range(EE):
         pairs = np.flatnonzero(e_of_p == e)
         if pairs.size == 0:
             continue
         awg = np.abs(mo.as_f64(inp["w_gate"][e]))
         awu = np.abs(mo.as_f64(inp["w_up"][e]))
-        awd = np.abs(mo.as_f64(inp["w_down"][e]))
         xe = ax[tok[pairs]]
         MG[pairs] = xe @ awg + np.abs(G[pairs])
         MU[pairs] = xe @ awu + np.abs(U[pairs])
-    MA = np.abs(dsilu * U) * MG + np.abs(silu) * MU + np.abs(A)
-    for e in range(E):
+    MA = np.abs(Ag) * MG + np.abs(Au) * MU + np.abs(A)
+    for e in range(EE):
         pairs = np.flatnonzero(e_of_p == e)
         if pairs.size == 0:
             continue
@@ -202,9 +209,10 @@ def magnitudes(inp, fw, bw, k):
             awu = np.abs(mo.as_f64(inp["w_up"][e]))
             MdA[pairs] = MdYu[pairs] @ awd.T
             p_ = pairs
-            MdG[p_] = (MdA[p_] * np.abs(U[p_] * dsilu[p_]) + np.abs(dA[p_]) * MU[p_] * np.abs(dsilu[p_])
-                       + np.abs(dA[p_] * U[p_] * ddsilu[p_]) * MG[p_] + np.abs(dG[p_]))
-            MdU[p_] = MdA[p_] * np.abs(silu[p_]) + np.abs(dA[p_] * dsilu[p_]) * MG[p_] + np.abs(dU[p_])
+            MdG[p_] = (MdA[p_] * np.abs(Ag[p_])
+                       + np.abs(dA[p_]) * (np.abs(Agg[p_]) * MG[p_] + np.abs(Agu[p_]) * MU[p_])
+                       + np.abs(dG[p_]))
+            MdU[p_] = MdA[p_] * np.abs(Au[p_]) + np.abs(dA[p_] * Agu[p_]) * MG[p_] + np.abs(dU[p_])
             MdXp[p_] = MdG[p_] @ awg.T + MdU[p_] @ awu.T + np.abs(bw["dXp"][p_])
             xe = ax[tok[p_]]
             Mdwg[e] = xe.T @ MdG[p_] + np.abs(bw["dw_gate"][e])
@@ -220,14 +228,16 @@ def magnitudes(inp, fw, bw, k):
     if have_bw:
         out.update(dYu=MdYu, dA=MdA, dG=MdG, dU=MdU, dXp=MdXp, dw_gate=Mdwg, dw_up=Mdwu,
                    dw_down=Mdwd)
-        Mdtw = np.einsum("pd,pd->p", ady[tok], MYu).reshape(T, k)
+        Mdtw = np.einsum("pd,pd->p", ady[tok[:T * k]], MYu[:T * k]).reshape(T, k)
         out["d_topk_w"] = Mdtw
         aw = np.abs(fw["w"])
         Mdl_sel = aw * (Mdtw + (aw * Mdtw).sum(1, keepdims=True)) + np.abs(
             np.take_along_axis(bw["dl"], idx, 1))
         Mdl = np.zeros((T, E))
         np.put_along_axis(Mdl, idx, Mdl_sel, axis=1)
-        Mdx = MdXp.reshape(T, k, d).sum(1) + Mdl @ awr.T + np.abs(bw["dx"])
+        Mdx = np.zeros((T, d))
+        np.add.at(Mdx, tok, MdXp)
+        Mdx = Mdx + Mdl @ awr.T + np.abs(bw["dx"])
         out["dx"] = Mdx
         out["dw_router"] = ax.T @ Mdl
         out["dbias"] = Mdl.sum(0)
@@ -289,12 +299,20 @@ def gpu_forward_backward(layer, inp, forced_idx=None, backward=True, dev="cuda")
     return b, x, dy
 
 
+def layer_act(layer):
+    """The layer's activation as the oracle's (L, alpha, c) tuple, or None."""
+    a = layer.act
+    return None if a is None else (float(a.limit), float(a.alpha), float(a.up_offset))
+
+
 def compare_full(layer, inp, k, align, backward=True, report=None):
     """Complete parity of every output against the float64 oracle. Returns
-    ({tensor: max|diff| / RMS}, buffers)."""
+    ({tensor: max|diff| / RMS}, buffers). The layer's activation and shared
+    experts (layer.act, layer.S) are the oracle's act and shared."""
+    act, S = layer_act(layer), layer.S
     x64 = mo.as_f64(inp["x"])
     fw = mo.forward(inp["x"], inp["w_router"], inp.get("bias"), inp["w_gate"], inp["w_up"],
-                    inp["w_down"], k)
+                    inp["w_down"], k, act=act, shared=S)
     # 1) free routing on the GPU: indices exactly the oracle's selection on the
     #    GPU's fp32 logits; logits within the bar; against the float64 logits
     #    exact up to near-ties
@@ -309,15 +327,15 @@ def compare_full(layer, inp, k, align, backward=True, report=None):
     bw = None
     if backward:
         bw = mo.backward(inp["x"], inp["w_router"], inp.get("bias"), inp["w_gate"], inp["w_up"],
-                         inp["w_down"], k, inp["dy"], fwd=fw)
-    mag = magnitudes(inp, fw, bw, k)
+                         inp["w_down"], k, inp["dy"], fwd=fw, act=act, shared=S)
+    mag = magnitudes(inp, fw, bw, k, act=act, shared=S)
 
     out = {"near_tie_tokens": flips}
     np.testing.assert_array_equal(to_np(b.topk_idx), fw["idx"])
     out["topk_w"] = assert_close("topk_w", to_np(b.topk_w), fw["w"])
     T = x64.shape[0]
     E = layer.E
-    maps = mo.permute_maps(fw["idx"], E, align, b.R_cap)
+    maps = mo.permute_maps(fw["idx"], E, align, b.R_cap, shared=S)
     np.testing.assert_array_equal(to_np(b.counts), maps["counts"])
     np.testing.assert_array_equal(to_np(b.offsets), maps["offsets"])
     np.testing.assert_array_equal(to_np(b.dst_row), maps["dst_row"])
@@ -325,7 +343,7 @@ def compare_full(layer, inp, k, align, backward=True, report=None):
     R_pad = maps["R_pad"]
     dst = maps["dst_row"]
     pad = np.setdiff1d(np.arange(R_pad), dst)
-    tok = np.arange(T * k) // k
+    tok = np.concatenate([np.arange(T * k) // k] + [np.arange(T)] * S)
 
     def rows(buf):
         return to_np(buf[:R_pad])
@@ -361,7 +379,8 @@ def compare_full(layer, inp, k, align, backward=True, report=None):
     for e in empty:
         for buf in (b.dw_gate, b.dw_up, b.dw_down):
             assert torch.count_nonzero(buf[e]).item() == 0
-        assert float(b.dbias[e]) == 0.0
+        if e < E:
+            assert float(b.dbias[e]) == 0.0
     if report is not None:
         report.update(out)
     return out, b

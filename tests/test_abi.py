@@ -1,6 +1,7 @@
 """The C ABI library loads and exports every entry point include/moe.h
 declares; host-side argument checks reject bad calls before any CUDA work
 (these calls never reach the device, so they run without a GPU)."""
+import ctypes
 import os
 import re
 
@@ -68,34 +69,42 @@ def test_host_argument_checks(lib):
     cap = lib.moe_row_capacity(4, 2, 4, 16)
     # align not a power of two / out of range
     for align in (0, 24, 8, 512):
-        assert lib.moe_permute(P, 4, 2, 4, align, P, 8, cap, P, P, P, P, P, P, ws, None) == L.MOE_ERR_ARG
+        assert lib.moe_permute(P, 4, 2, 4, 0, align, P, 8, cap, P, P, P, P, P, P, ws, None) == L.MOE_ERR_ARG
     # capacity too small
-    assert lib.moe_permute(P, 4, 2, 4, 16, P, 8, cap - 1, P, P, P, P, P, P, ws, None) == L.MOE_ERR_CAPACITY
+    assert lib.moe_permute(P, 4, 2, 4, 0, 16, P, 8, cap - 1, P, P, P, P, P, P, ws, None) == L.MOE_ERR_CAPACITY
+    # with a shared expert the capacity counts its T rows and group
+    cap1 = lib.moe_row_capacity(4, 3, 5, 16)
+    assert lib.moe_permute(P, 4, 2, 4, 1, 16, P, 8, cap, P, P, P, P, P, P, ws, None) == L.MOE_ERR_CAPACITY
+    assert lib.moe_permute(P, 4, 2, 4, -1, 16, P, 8, cap1, P, P, P, P, P, P, ws, None) == L.MOE_ERR_ARG
     # workspace too small
-    assert lib.moe_permute(P, 4, 2, 4, 16, P, 8, cap, P, P, P, P, P, P, ws - 1, None) == L.MOE_ERR_ARG
+    assert lib.moe_permute(P, 4, 2, 4, 0, 16, P, 8, cap, P, P, P, P, P, P, ws - 1, None) == L.MOE_ERR_ARG
     # misaligned activation pointer
-    assert lib.moe_permute(P, 4, 2, 4, 16, P + 2, 8, cap, P, P, P, P, P, P, ws, None) == L.MOE_ERR_ARG
+    assert lib.moe_permute(P, 4, 2, 4, 0, 16, P + 2, 8, cap, P, P, P, P, P, P, ws, None) == L.MOE_ERR_ARG
     # expert GEMMs: f not a multiple of 8
-    assert lib.moe_expert_fwd(P, P, None, 4, 2, 4, 8, 12, cap, P, P, P, P, P, P, P, None) == L.MOE_ERR_UNSUPPORTED
-    assert lib.moe_expert_fwd(P, None, None, 4, 2, 4, 8, 16, cap, P, P, P, P, P, P, P, None) == L.MOE_ERR_ARG
+    assert lib.moe_expert_fwd(P, P, None, None, 4, 2, 4, 0, 8, 12, cap, P, P, P, P, P, P, P, None) == L.MOE_ERR_UNSUPPORTED
+    assert lib.moe_expert_fwd(P, None, None, None, 4, 2, 4, 0, 8, 16, cap, P, P, P, P, P, P, P, None) == L.MOE_ERR_ARG
+    # a clamped SwiGLU needs a positive limit
+    bad = L.Swiglu(0.0, 1.702, 1.0)
+    assert lib.moe_expert_fwd(P, P, None, ctypes.addressof(bad), 4, 2, 4, 0, 8, 16, cap, P, P, P, P, P, P, P, None) == L.MOE_ERR_ARG
     # expert backward: a missing row buffer (the gathered dY rows)
     wse = lib.moe_expert_bwd_workspace_size(cap, 16)
     assert wse >= cap * 2 * 4                  # at least one n-tile's two partials per row
     assert lib.moe_expert_bwd_workspace_size(0, 16) == 0
     ebwd = lambda dyg, ws, nb: lib.moe_expert_bwd(  # noqa: E731
-        P, P, P, P, P, 4, 2, 4, 8, 16, cap, P, P, P, P, P, P, P,
+        P, P, P, P, P, None, 4, 2, 4, 0, 8, 16, cap, P, P, P, P, P, P, P,
         dyg, P, P, P, P, P, P, P, P, ws, nb, None)
     assert ebwd(None, P, wse) == L.MOE_ERR_ARG
     # expert backward: workspace missing or too small
     assert ebwd(P, None, wse) == L.MOE_ERR_ARG
     assert ebwd(P, P, wse - 1) == L.MOE_ERR_ARG
     # combine: k above the slot limit
-    assert lib.moe_combine(P, P, None, 4, 33, 8, P, None) == L.MOE_ERR_UNSUPPORTED
+    assert lib.moe_combine(P, P, None, 4, 33, 0, 8, P, None) == L.MOE_ERR_UNSUPPORTED
+    assert lib.moe_combine(P, P, None, 4, 30, 3, 8, P, None) == L.MOE_ERR_UNSUPPORTED   # k + S > 32
     # route backward: workspace missing
-    assert lib.moe_route_bwd(P, P, P, P, P, P, P, 4, 8, 4, 2, 16, P, None, None, P, None, None, 0, None) == L.MOE_ERR_ARG
+    assert lib.moe_route_bwd(P, P, P, P, P, P, P, 4, 8, 4, 2, 0, 16, P, None, None, P, None, None, 0, None) == L.MOE_ERR_ARG
     # route backward: dxp without dst_row
     wsb = lib.moe_workspace_size(2, 4, 8, 4, 2, 16)
-    assert lib.moe_route_bwd(P, P, P, P, P, P, P, 4, 8, 4, 2, 16, P, P, None, P, None, P, wsb, None) == L.MOE_ERR_ARG
+    assert lib.moe_route_bwd(P, P, P, P, P, P, P, 4, 8, 4, 2, 0, 16, P, P, None, P, None, P, wsb, None) == L.MOE_ERR_ARG
     # decode: T above 8, d not a multiple of 64, k > E, null x, workspace too small
     wd = lib.moe_decode_workspace_size(2, 128, 64, 4, 2)
     assert wd >= 256 + 2 * 2 * 64 * 4          # at least the barrier word and A

@@ -201,3 +201,42 @@ def test_exact_ties_pick_the_lower_index(T):
     ref = mo.select_topk(mo.router_logits(mo.as_f64(inp["x"]), mo.as_f64(wr)), k)
     tied = [t for t in range(T) if ({5, 6} & set(idx[t].tolist()))]
     np.testing.assert_array_equal(idx[tied], ref[tied])
+
+
+
+# -------------------------------------------- clamped SwiGLU and shared experts
+# (prime-rl PR #3885, §Changes, "FP8 routed experts" and "Fused FP8 shared
+# expert"; the clamp constants are GPT-OSS-20B's, the others are a limit that
+# binds at these scales)
+F2_CASES = {
+    # name: (T, d, f, E, k, S, align, act)
+    "clamp_gptoss": (256, 128, 256, 8, 2, 0, 16, (7.0, 1.702, 1.0)),
+    "clamp_binding": (300, 200, 136, 6, 2, 0, 16, (0.75, 1.702, 1.0)),
+    "shared1": (300, 200, 136, 6, 2, 1, 16, None),
+    "shared2_clamped": (520, 392, 520, 8, 3, 2, 128, (1.0, 1.702, 1.0)),
+    "shared1_wide_E": (256, 128, 64, 160, 6, 1, 16, (1.5, 1.702, 1.0)),
+    "qwen_like_shared": (1024, 2048, 768, 128, 8, 1, 16, (7.0, 1.702, 1.0)),
+}
+
+
+def _f2_case(name, T, d, f, E, k, S, align):
+    """Inputs with E + S experts' weights; the router sees the first E."""
+    wl = workloads.Workload(name, T=T, d=d, f=f, E=E + S, k=k, align=align)
+    inp = workloads.generate(wl)
+    inp["w_router"] = inp["w_router"][:, :E].contiguous()
+    return inp
+
+
+@pytest.mark.parametrize("name", sorted(F2_CASES))
+def test_clamped_swiglu_and_shared_experts(name):
+    from mixture_experts_routed_softmax_gb300.layer import MoELayer
+    T, d, f, E, k, S, align, act = F2_CASES[name]
+    inp = _f2_case(name, T, d, f, E, k, S, align)
+    layer = MoELayer.from_inputs(inp, k, align, act=act)
+    assert layer.S == S and layer.E == E
+    out, b = compare_full(layer, inp, k, align)
+    if act is not None and act[0] < 2:
+        # the clamps bind somewhere, in both directions of U
+        G, U = b.g[:int(b.offsets[-1])], b.u[:int(b.offsets[-1])]
+        assert (G > act[0]).any() and (U > act[0]).any() and (U < -act[0]).any()
+    print(name, {k_: (round(v, 5) if isinstance(v, float) else v) for k_, v in out.items()})

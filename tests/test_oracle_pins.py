@@ -143,3 +143,101 @@ def test_backward_matches_finite_differences(T, d, f, E, k):
             arr[pos] = old
             num[pos] = (lp - lm) / (2 * eps)
         np.testing.assert_allclose(bw[gname], num, rtol=1e-6, atol=1e-8, err_msg=gname)
+
+
+# ----------------------------------------------------- clamped SwiGLU, shared experts
+# (prime-rl PR #3885, §Changes, "FP8 routed experts" and "Fused FP8 shared
+# expert": a clamped SwiGLU, and shared experts whose output is added to the
+# routed one in the write-back; the clamp's constants are the GPT-OSS-20B
+# model's, the pages do not print them)
+
+def test_clamped_swiglu_closed_forms():
+    rng = np.random.default_rng(3)
+    G = rng.standard_normal(4000) * 8
+    U = rng.standard_normal(4000) * 8
+    L, al, c = mo.CLAMPED_SWIGLU_GPT_OSS
+    A = mo.swiglu(G, U, mo.CLAMPED_SWIGLU_GPT_OSS)
+    # where neither clamp binds: g * sigmoid(alpha g) * (u + 1), written out here
+    free = (G < L) & (np.abs(U) < L)
+    assert free.sum() > 1000 and (~free).sum() > 500
+    np.testing.assert_allclose(A[free], G[free] / (1 + np.exp(-al * G[free])) * (U[free] + c),
+                               rtol=1e-14)
+    # G above the limit: A no longer depends on G; U past the limit: nor on U
+    big = G > L
+    np.testing.assert_allclose(A[big], L / (1 + np.exp(-al * L)) * (np.clip(U[big], -L, L) + c),
+                               rtol=1e-14)
+    # the plain activation is the special case (inf, 1, 0), bitwise
+    assert np.array_equal(mo.swiglu(G, U, (np.inf, 1.0, 0.0)), mo.silu(G) * U)
+    # and the derivatives match central differences away from the kinks
+    ok = (np.abs(G - L) > 1e-3) & (np.abs(np.abs(U) - L) > 1e-3)
+    eps = 1e-6
+    dg, du = mo.swiglu_grad(G, U, mo.CLAMPED_SWIGLU_GPT_OSS)
+    ng = (mo.swiglu(G + eps, U, mo.CLAMPED_SWIGLU_GPT_OSS)
+          - mo.swiglu(G - eps, U, mo.CLAMPED_SWIGLU_GPT_OSS)) / (2 * eps)
+    nu = (mo.swiglu(G, U + eps, mo.CLAMPED_SWIGLU_GPT_OSS)
+          - mo.swiglu(G, U - eps, mo.CLAMPED_SWIGLU_GPT_OSS)) / (2 * eps)
+    np.testing.assert_allclose(dg[ok], ng[ok], rtol=1e-6, atol=1e-7)
+    np.testing.assert_allclose(du[ok], nu[ok], rtol=1e-6, atol=1e-7)
+    assert np.all(dg[G > L] == 0) and np.all(du[np.abs(U) > L] == 0)
+
+
+@pytest.mark.parametrize("S", [1, 2])
+def test_shared_experts_add_a_dense_mlp(S):
+    """With S shared experts the layer is the routed layer plus, per shared
+    expert, a dense SwiGLU MLP of every token; the gradients add the same
+    way, and the routing gradients do not see the shared experts."""
+    rng = np.random.default_rng(40 + S)
+    T, d, f, E, k = 7, 5, 6, 4, 2
+    x, wr, b, wg, wu, wd, dy = _rand_layer(rng, T, d, f, E + S)
+    fw0 = mo.forward(x, wr[:, :E], b[:E], wg[:E], wu[:E], wd[:E], k)
+    bw0 = mo.backward(x, wr[:, :E], b[:E], wg[:E], wu[:E], wd[:E], k, dy, fwd=fw0)
+    fw = mo.forward(x, wr[:, :E], b[:E], wg, wu, wd, k, shared=S)
+    bw = mo.backward(x, wr[:, :E], b[:E], wg, wu, wd, k, dy, fwd=fw, shared=S)
+    y, dx = fw0["y"].copy(), bw0["dx"].copy()
+    for s in range(S):
+        ys, dxs, dwg, dwu, dwd = _dense_mlp(x, wg[E + s], wu[E + s], wd[E + s], dy)
+        y += ys
+        dx += dxs
+        np.testing.assert_allclose(bw["dw_gate"][E + s], dwg, rtol=1e-10, atol=1e-12)
+        np.testing.assert_allclose(bw["dw_up"][E + s], dwu, rtol=1e-10, atol=1e-12)
+        np.testing.assert_allclose(bw["dw_down"][E + s], dwd, rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(fw["y"], y, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(bw["dx"], dx, rtol=1e-10, atol=1e-12)
+    for key in ("d_topk_w", "dl", "dw_router", "dbias"):
+        np.testing.assert_allclose(bw[key], bw0[key], rtol=1e-12, atol=1e-14, err_msg=key)
+    for key in ("dw_gate", "dw_up", "dw_down"):
+        np.testing.assert_allclose(bw[key][:E], bw0[key], rtol=1e-12, atol=1e-14, err_msg=key)
+    # the layout: each shared expert holds every token once, in token order
+    maps = mo.permute_maps(fw["idx"], E, 4, shared=S)
+    for s in range(S):
+        g0 = maps["offsets"][E + s]
+        assert maps["counts"][E + s] == T
+        np.testing.assert_array_equal(maps["src_pair"][g0:g0 + T], T * k + s * T + np.arange(T))
+
+
+@pytest.mark.parametrize("S", [0, 1])
+def test_clamped_and_shared_backward_matches_finite_differences(S):
+    T, d, f, E, k = 4, 3, 4, 4, 2
+    act = (0.8, 1.702, 1.0)          # a limit that binds at these scales
+    x, wr, b, wg, wu, wd, dy = _separated_layer(91 + S, T, d, f, E + S, k)
+    wr, b = wr[:, :E], b[:E]
+    lg = np.sort(mo.router_logits(x, wr, b), axis=1)[:, ::-1]
+    assert np.min(lg[:, k - 1] - lg[:, k]) > 1e-3
+    fw = mo.forward(x, wr, b, wg, wu, wd, k, act=act, shared=S)
+    G, U = fw["G"], fw["U"]
+    assert (G > act[0]).any() and (np.abs(U) > act[0]).any()          # the clamps bind
+    assert np.min(np.abs(G - act[0])) > 1e-4 and np.min(np.abs(np.abs(U) - act[0])) > 1e-4
+    bw = mo.backward(x, wr, b, wg, wu, wd, k, dy, fwd=fw, act=act, shared=S)
+    eps = 1e-6
+    for gname, arr in {"dx": x, "dw_router": wr, "dw_gate": wg, "dw_up": wu,
+                       "dw_down": wd}.items():
+        num = np.zeros_like(arr)
+        for pos in itertools.product(*[range(s_) for s_ in arr.shape]):
+            old = arr[pos]
+            arr[pos] = old + eps
+            lp = mo.layer_loss(x, wr, b, wg, wu, wd, k, dy, act=act, shared=S)
+            arr[pos] = old - eps
+            lm = mo.layer_loss(x, wr, b, wg, wu, wd, k, dy, act=act, shared=S)
+            arr[pos] = old
+            num[pos] = (lp - lm) / (2 * eps)
+        np.testing.assert_allclose(bw[gname], num, rtol=1e-6, atol=1e-8, err_msg=gname)
