@@ -46,7 +46,7 @@ def test_noalloc_permute_matches_workspace_permute_twice():
         ref = _outputs(R_cap, T, k, E, d, dev)
         ws_bytes = int(lib.moe_workspace_size(_lib.MOE_WS_PERMUTE, T, d, E, k, align))
         ws = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=dev)
-        _lib.call("moe_permute", _p(idx), T, k, E, align, _p(x), d, R_cap, _p(ref["counts"]),
+        _lib.call("moe_permute", _p(idx), T, k, E, 0, align, _p(x), d, R_cap, _p(ref["counts"]),
                   _p(ref["offsets"]), _p(ref["dst_row"]), _p(ref["src_pair"]), _p(ref["xp"]),
                   _p(ws), ws.numel(), stream)
         got = _outputs(R_cap, T, k, E, d, dev)
