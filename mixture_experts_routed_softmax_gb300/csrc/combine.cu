@@ -20,6 +20,7 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
                                                       const float* __restrict__ topk_w,
                                                       int64_t T, int k, int S, int d,
                                                       moe_bf16* __restrict__ out) {
+  pdl_enter();
   const int lane = threadIdx.x & 31;
   const int nv = d / 8;
   const int nchunk = (nv + 31) / 32;
@@ -73,8 +74,8 @@ cudaError_t launch_combine(const float* rows, const int32_t* dst_row, const floa
                            int64_t T, int k, int S, int d, moe_bf16* out, cudaStream_t s) {
   timer_before(MOE_KERNEL_COMBINE, s);
   const int64_t warps = T * (((int64_t)d / 8 + 31) / 32);
-  combine_kernel<<<(unsigned)((warps + 7) / 8), 256, 0, s>>>(rows, dst_row, topk_w, T, k, S, d,
-                                                             out);
+  launch_pdl(pdl_for_tokens(T), combine_kernel, dim3((unsigned)((warps + 7) / 8)), dim3(256), 0, s,
+             rows, dst_row, topk_w, T, k, S, d, out);
   note_launches(1);
   timer_after(MOE_KERNEL_COMBINE, s);
   return cudaGetLastError();
@@ -94,6 +95,7 @@ __global__ void __launch_bounds__(256) combine_bwd_kernel(
     const moe_bf16* __restrict__ dy, const int32_t* __restrict__ src_pair,
     const float* __restrict__ topk_w, const int64_t* __restrict__ offsets, int64_t T, int k,
     int E, int d, int64_t R_cap, moe_bf16* __restrict__ dyg, moe_bf16* __restrict__ dyp) {
+  pdl_enter();
   const int lane = threadIdx.x & 31;
   const int64_t r = (int64_t)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
   if (r >= R_cap || r >= offsets[E]) return;
@@ -138,8 +140,8 @@ cudaError_t launch_combine_bwd(const moe_bf16* dy, const int32_t* src_pair, cons
                                const int64_t* offsets, int64_t T, int k, int E, int d,
                                int64_t R_cap, moe_bf16* dyg, moe_bf16* dyp, cudaStream_t s) {
   timer_before(MOE_KERNEL_COMBINE_BWD, s);
-  combine_bwd_kernel<<<(unsigned)((R_cap + 7) / 8), 256, 0, s>>>(dy, src_pair, topk_w, offsets,
-                                                                 T, k, E, d, R_cap, dyg, dyp);
+  launch_pdl(pdl_for_tokens(T), combine_bwd_kernel, dim3((unsigned)((R_cap + 7) / 8)), dim3(256), 0,
+             s, dy, src_pair, topk_w, offsets, T, k, E, d, R_cap, dyg, dyp);
   note_launches(1);
   timer_after(MOE_KERNEL_COMBINE_BWD, s);
   return cudaGetLastError();
@@ -152,6 +154,7 @@ __global__ void __launch_bounds__(256) dtw_finalize_kernel(const float* __restri
                                                            int slots,
                                                            const int32_t* __restrict__ dst_row,
                                                            int64_t P, float* __restrict__ d_topk_w) {
+  pdl_enter();
   const int64_t p = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (p >= P) return;
   const int32_t r = dst_row[p];
@@ -165,8 +168,8 @@ __global__ void __launch_bounds__(256) dtw_finalize_kernel(const float* __restri
 cudaError_t launch_dtw_finalize(const float* part, int slots, const int32_t* dst_row, int64_t P,
                                 float* d_topk_w, cudaStream_t s) {
   if (P == 0) return cudaSuccess;
-  dtw_finalize_kernel<<<(unsigned)((P + 255) / 256), 256, 0, s>>>(part, slots, dst_row, P,
-                                                                  d_topk_w);
+  launch_pdl(pdl_for_pairs(P), dtw_finalize_kernel, dim3((unsigned)((P + 255) / 256)), dim3(256), 0,
+             s, part, slots, dst_row, P, d_topk_w);
   note_launches(1);
   return cudaGetLastError();
 }

@@ -36,6 +36,41 @@ __device__ __forceinline__ uint4 pack8(const float* f) {
                     pack_bf16(f[6], f[7]));
 }
 
+// ------------------------------------------------- dependent launches --
+// For small problems every kernel of the layer is launched with programmatic
+// stream serialization (launch_pdl below with pdl = true): it may be
+// scheduled while the kernel before it in the stream is still running, and
+// waits at pdl_enter() until that kernel has finished and its writes are
+// visible; it then lets the next kernel be scheduled in turn. The launch
+// latency and the block scheduling of a kernel thus overlap the tail of the
+// one before (measured on GB300: one-token forward 45.1 -> 43.0 us as a CUDA
+// graph, the 512-token small-M forward -4%; the 16k-token layer step +0.7%,
+// hence the size limit). Both instructions do nothing in a kernel launched
+// without the attribute.
+constexpr int64_t kPdlMaxTokens = 4096;
+inline bool pdl_for_tokens(int64_t T) { return T <= kPdlMaxTokens; }
+inline bool pdl_for_pairs(int64_t P) { return P <= 8 * kPdlMaxTokens; }
+__device__ __forceinline__ void pdl_enter() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(bool pdl, void (*kernel)(KArgs...), dim3 grid, dim3 block,
+                              size_t smem, cudaStream_t s, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 // ---------------------------------------------------------------- status --
 // Kernels record the first error they see; moe_status() reads and clears it.
 __device__ __forceinline__ void raise_status(int* status, int code) {

@@ -343,6 +343,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const __grid_constant__ CUtensorMap mapO0,
                         const __grid_constant__ CUtensorMap mapO1,
                         const __grid_constant__ CUtensorMap mapO2, const GemmArgs args) {
+  pdl_enter();
   using T = Tr<K>;
   using G = Geo<K, PAIR>;
   static_assert(!PAIR || (!T::dense && !T::narrow), "pairs: grouped kinds");
@@ -1061,7 +1062,7 @@ static cudaError_t launch_kind(const CUtensorMap& a0, const CUtensorMap& a1,
                                const CUtensorMap& b0, const CUtensorMap& b1, const GemmArgs& args,
                                int64_t tiles_upper, cudaStream_t s,
                                const CUtensorMap* o0 = nullptr, const CUtensorMap* o1 = nullptr,
-                               const CUtensorMap* o2 = nullptr) {
+                               const CUtensorMap* o2 = nullptr, bool pdl = false) {
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   static int units = 0;
@@ -1101,21 +1102,23 @@ static cudaError_t launch_kind(const CUtensorMap& a0, const CUtensorMap& a1,
   const CUtensorMap& m2 = o2 ? *o2 : m0;
   if constexpr (PAIR) {
     cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute at[1];
+    cudaLaunchAttribute at[2];
     at[0].id = cudaLaunchAttributeClusterDimension;
     at[0].val.clusterDim.x = 2;
     at[0].val.clusterDim.y = 1;
     at[0].val.clusterDim.z = 1;
+    at[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;   // as launch_pdl
+    at[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.gridDim = dim3((unsigned)(2 * grid));
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = kSmemBytes;
     cfg.stream = s;
     cfg.attrs = at;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = pdl ? 2 : 1;
     cudaLaunchKernelEx(&cfg, grouped_gemm_kernel<K, PAIR>, a0, a1, b0, b1, m0, m1, m2, args);
   } else {
-    grouped_gemm_kernel<K, PAIR><<<(unsigned)grid, kThreads, kSmemBytes, s>>>(a0, a1, b0, b1, m0,
-                                                                             m1, m2, args);
+    launch_pdl(pdl, grouped_gemm_kernel<K, PAIR>, dim3((unsigned)grid), dim3(kThreads), kSmemBytes,
+               s, a0, a1, b0, b1, m0, m1, m2, args);
   }
   note_launches(1);
   if constexpr (!Tr<K>::dense) timer_after(Tr<K>::kernel_id, s);
@@ -1209,7 +1212,8 @@ cudaError_t launch_router_gemm(const moe_bf16* x, const moe_bf16* w_split, const
   a.status = status;
   a.bn = pick_bn(E, 64);
   const int64_t tiles = ((T + BM - 1) / BM) * ((E + a.bn - 1) / a.bn) * a.ksplit;
-  return launch_kind<Kind::RouterLogits, false>(a0, a0, b0, b0, a, tiles, s);
+  return launch_kind<Kind::RouterLogits, false>(a0, a0, b0, b0, a, tiles, s, nullptr, nullptr,
+                                                  nullptr, pdl_for_tokens(T));
 }
 
 // The number of K chunks of the router-weight gradient GEMM (at least 8 k-steps each).
@@ -1241,7 +1245,8 @@ cudaError_t launch_router_wgrad_gemm(const moe_bf16* x, const moe_bf16* dl3, int
   a.status = status;
   a.bn = pick_bn(N3, 64);
   const int64_t tiles = (int64_t)((d + BM - 1) / BM) * ((N3 + a.bn - 1) / a.bn) * a.ksplit;
-  return launch_kind<Kind::RouterWgrad, false>(a0, a0, b0, b0, a, tiles, s);
+  return launch_kind<Kind::RouterWgrad, false>(a0, a0, b0, b0, a, tiles, s, nullptr, nullptr,
+                                                 nullptr, pdl_for_tokens(T));
 }
 
 static int64_t mgrouped_tiles_upper(const GroupedDims& g, int N, int BN, int TM = BM) {
@@ -1258,6 +1263,7 @@ cudaError_t launch_gateup_fwd(const GroupedDims& g, const moe_bf16* xp, const mo
       !map2d_out(&o1, U, g.f, g.R_cap, 4) || !map2d_out(&o2, A, g.f, g.R_cap))
     return cudaErrorInvalidValue;
   GemmArgs a = base_args(g, status);
+  const bool pdl = pdl_for_pairs(g.P);
   a.N = g.f;
   a.nk_seg = (g.d + BK - 1) / BK;
   a.out0 = G; a.out1 = U; a.out2 = A;
@@ -1268,12 +1274,12 @@ cudaError_t launch_gateup_fwd(const GroupedDims& g, const moe_bf16* xp, const mo
   const int64_t tiles = (int64_t)g.E * ((rows + BM - 1) / BM) * ((g.f + 127) / 128);
   if (tiles < 8 * (int64_t)num_sms())
     return launch_kind<Kind::GateUpFwdNarrow, false>(
-        a0, a0, b0, b1, a, mgrouped_tiles_upper(g, g.f, 64), s, &o0, &o1, &o2);
+        a0, a0, b0, b1, a, mgrouped_tiles_upper(g, g.f, 64), s, &o0, &o1, &o2, pdl);
   if (pairs_mgrouped(g, 512))
     return launch_kind<Kind::GateUpFwd, true>(
-        a0, a0, b0, b1, a, mgrouped_tiles_upper(g, g.f, 128, 2 * BM), s, &o0, &o1, &o2);
+        a0, a0, b0, b1, a, mgrouped_tiles_upper(g, g.f, 128, 2 * BM), s, &o0, &o1, &o2, pdl);
   return launch_kind<Kind::GateUpFwd, false>(a0, a0, b0, b1, a, mgrouped_tiles_upper(g, g.f, 128),
-                                             s, &o0, &o1, &o2);
+                                             s, &o0, &o1, &o2, pdl);
 }
 
 cudaError_t launch_down_fwd(const GroupedDims& g, const moe_bf16* A, const moe_bf16* w_down,
@@ -1283,15 +1289,17 @@ cudaError_t launch_down_fwd(const GroupedDims& g, const moe_bf16* A, const moe_b
       !map2d_out(&o0, yp, g.d, g.R_cap, 4))
     return cudaErrorInvalidValue;
   GemmArgs a = base_args(g, status);
+  const bool pdl = pdl_for_pairs(g.P);
   a.N = g.d;
   a.nk_seg = (g.f + BK - 1) / BK;
   a.out0 = yp;
   a.row_w = row_w;
   if (pairs_mgrouped(g))
     return launch_kind<Kind::DownFwd, true>(a0, a0, b0, b0, a,
-                                            mgrouped_tiles_upper(g, g.d, 256, 2 * BM), s, &o0);
+                                            mgrouped_tiles_upper(g, g.d, 256, 2 * BM), s, &o0,
+                                            nullptr, nullptr, pdl);
   return launch_kind<Kind::DownFwd, false>(a0, a0, b0, b0, a, mgrouped_tiles_upper(g, g.d, 256), s,
-                                           &o0);
+                                           &o0, nullptr, nullptr, pdl);
 }
 
 // Partial slots per row of the down dgrad's top-k weight gradient: one per
@@ -1318,6 +1326,7 @@ cudaError_t launch_down_dgrad(const GroupedDims& g, const moe_bf16* dyg, const f
       !map2d_out(&o0, dG, g.f, g.R_cap, 2, 32) || !map2d_out(&o1, dU, g.f, g.R_cap, 2, 32))
     return cudaErrorInvalidValue;
   GemmArgs a = base_args(g, status);
+  const bool pdl = pdl_for_pairs(g.P);
   a.N = g.f;
   a.nk_seg = (g.d + BK - 1) / BK;
   a.in0 = G; a.in1 = U;
@@ -1330,9 +1339,9 @@ cudaError_t launch_down_dgrad(const GroupedDims& g, const moe_bf16* dyg, const f
   a.bn = bn;
   if (pair)
     return launch_kind<Kind::DownDgrad, true>(
-        a0, a0, b0, b0, a, mgrouped_tiles_upper(g, g.f, bn, 2 * BM), s, &o0, &o1);
+        a0, a0, b0, b0, a, mgrouped_tiles_upper(g, g.f, bn, 2 * BM), s, &o0, &o1, nullptr, pdl);
   return launch_kind<Kind::DownDgrad, false>(a0, a0, b0, b0, a, mgrouped_tiles_upper(g, g.f, bn),
-                                             s, &o0, &o1);
+                                             s, &o0, &o1, nullptr, pdl);
 }
 
 cudaError_t launch_gateup_dgrad(const GroupedDims& g, const moe_bf16* dG, const moe_bf16* dU,
@@ -1349,15 +1358,17 @@ cudaError_t launch_gateup_dgrad(const GroupedDims& g, const moe_bf16* dG, const 
       !map2d_out(&o0, dxp, g.d, g.R_cap, 4))
     return cudaErrorInvalidValue;
   GemmArgs a = base_args(g, status);
+  const bool pdl = pdl_for_pairs(g.P);
   a.N = g.d;
   a.nk_seg = (g.f + BK - 1) / BK;
   a.out0 = dxp;
   a.bn = bn;
   if (pair)
     return launch_kind<Kind::GateUpDgrad, true>(a0, a1, b0, b1, a,
-                                                mgrouped_tiles_upper(g, g.d, bn, 2 * BM), s, &o0);
+                                                mgrouped_tiles_upper(g, g.d, bn, 2 * BM), s, &o0,
+                                                nullptr, nullptr, pdl);
   return launch_kind<Kind::GateUpDgrad, false>(a0, a1, b0, b1, a, mgrouped_tiles_upper(g, g.d, bn),
-                                               s, &o0);
+                                               s, &o0, nullptr, nullptr, pdl);
 }
 
 cudaError_t launch_wgrad_down(const GroupedDims& g, const moe_bf16* A, const moe_bf16* dyp,
@@ -1368,6 +1379,7 @@ cudaError_t launch_wgrad_down(const GroupedDims& g, const moe_bf16* A, const moe
       !map3d_out(&o0, dw_down, g.d, g.f, g.E))
     return cudaErrorInvalidValue;
   GemmArgs a = base_args(g, status);
+  const bool pdl = pdl_for_pairs(g.P);
   a.M = g.f;
   a.N = g.d;
   a.out0 = dw_down;
@@ -1375,9 +1387,10 @@ cudaError_t launch_wgrad_down(const GroupedDims& g, const moe_bf16* A, const moe
   if (pairs_kgrouped())
     return launch_kind<Kind::WgradDown, true>(a0, a0, b0, b0, a,
                                               (int64_t)g.E * ((g.f + 2 * BM - 1) / (2 * BM)) * nN,
-                                              s, &o0);
+                                              s, &o0, nullptr, nullptr, pdl);
   return launch_kind<Kind::WgradDown, false>(a0, a0, b0, b0, a,
-                                             (int64_t)g.E * ((g.f + BM - 1) / BM) * nN, s, &o0);
+                                             (int64_t)g.E * ((g.f + BM - 1) / BM) * nN, s, &o0,
+                                             nullptr, nullptr, pdl);
 }
 
 cudaError_t launch_wgrad_gateup(const GroupedDims& g, const moe_bf16* xp, const moe_bf16* dG,
@@ -1390,6 +1403,7 @@ cudaError_t launch_wgrad_gateup(const GroupedDims& g, const moe_bf16* xp, const 
       !map3d_out(&o1, dw_up, g.f, g.d, g.E))
     return cudaErrorInvalidValue;
   GemmArgs a = base_args(g, status);
+  const bool pdl = pdl_for_pairs(g.P);
   a.M = g.d;
   a.N = g.f;
   a.out0 = dw_gate;
@@ -1397,10 +1411,11 @@ cudaError_t launch_wgrad_gateup(const GroupedDims& g, const moe_bf16* xp, const 
   const int64_t nN = (g.f + 127) / 128;
   if (pairs_kgrouped())
     return launch_kind<Kind::WgradGateUp, true>(
-        a0, a0, b0, b1, a, (int64_t)g.E * ((g.d + 2 * BM - 1) / (2 * BM)) * nN, s, &o0, &o1);
+        a0, a0, b0, b1, a, (int64_t)g.E * ((g.d + 2 * BM - 1) / (2 * BM)) * nN, s, &o0, &o1,
+        nullptr, pdl);
   return launch_kind<Kind::WgradGateUp, false>(a0, a0, b0, b1, a,
                                                (int64_t)g.E * ((g.d + BM - 1) / BM) * nN, s, &o0,
-                                               &o1);
+                                               &o1, nullptr, pdl);
 }
 
 }  // namespace moe

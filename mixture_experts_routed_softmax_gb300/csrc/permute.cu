@@ -53,6 +53,7 @@ __device__ __forceinline__ int valid_expert(const int32_t* idx, int64_t p, int64
 __global__ void __launch_bounds__(kHistWarps * 32) permute_hist_kernel(
     const int32_t* __restrict__ idx, int64_t P, int E, int32_t* __restrict__ blk_count,
     int32_t* __restrict__ rank_in_blk, int* status) {
+  pdl_enter();
   extern __shared__ int32_t hist[];   // [kHistWarps][E]
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   for (int i = threadIdx.x; i < kHistWarps * E; i += blockDim.x) hist[i] = 0;
@@ -113,6 +114,7 @@ __global__ void __launch_bounds__(1024) permute_scan_kernel(int32_t* __restrict_
                                                             int align,
                                                             int32_t* __restrict__ counts,
                                                             int64_t* __restrict__ offsets) {
+  pdl_enter();
   __shared__ int64_t warp_tot[32];
   const int e = threadIdx.x;
   const int lane = e & 31, w = e >> 5;
@@ -161,6 +163,7 @@ __global__ void permute_scatter_kernel(const int32_t* __restrict__ idx, int64_t 
                                        const int32_t* __restrict__ rank_in_blk,
                                        int32_t* __restrict__ dst_row,
                                        int32_t* __restrict__ src_pair) {
+  pdl_enter();
   const int64_t p = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (p >= P) return;
   const int e = idx[p];
@@ -183,6 +186,7 @@ __global__ void __launch_bounds__(1024) permute_small_kernel(
     int32_t* __restrict__ counts,
     int64_t* __restrict__ offsets, int32_t* __restrict__ dst_row,
     int32_t* __restrict__ src_pair, int* status) {
+  pdl_enter();
   __shared__ int32_t s_idx[kSmallPairs];
   __shared__ int64_t warp_tot[32];
   __shared__ int64_t s_off[1024];
@@ -251,6 +255,7 @@ __global__ void __launch_bounds__(256) permute_gather_kernel(
     const moe_bf16* __restrict__ x, int d, int k, int64_t T, const int64_t* __restrict__ offsets,
     const int32_t* __restrict__ counts, int E, int S, int64_t R_cap,
     int32_t* __restrict__ src_pair, int32_t* __restrict__ dst_row, moe_bf16* __restrict__ xp) {
+  pdl_enter();
   const int lane = threadIdx.x & 31;
   const int64_t r = (int64_t)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
   if (r >= R_cap) return;
@@ -310,20 +315,22 @@ cudaError_t launch_permute(const int32_t* topk_idx, int64_t T, int k, int E, int
   timer_before(MOE_KERNEL_PERMUTE, s);
   int launches = 2;
   if (P > 0 && P <= kSmallPairs) {
-    permute_small_kernel<<<1, 1024, 0, s>>>(topk_idx, P, E, S, T, align, counts, offsets,
-                                            dst_row, src_pair, status);
+    launch_pdl(pdl_for_tokens(T), permute_small_kernel, dim3(1), dim3(1024), 0, s, topk_idx, P, E,
+               S, T, align, counts, offsets, dst_row, src_pair, status);
   } else {
     if (P > 0)
-      permute_hist_kernel<<<(unsigned)nblk, kHistWarps * 32, hist_smem, s>>>(
-          topk_idx, P, E, blk_count, rank_in_blk, status);
-    permute_scan_kernel<<<1, 1024, 0, s>>>(blk_count, nblk, E, S, T, align, counts, offsets);
+      launch_pdl(pdl_for_tokens(T), permute_hist_kernel, dim3((unsigned)nblk),
+                 dim3(kHistWarps * 32), hist_smem, s, topk_idx, P, E, blk_count, rank_in_blk,
+                 status);
+    launch_pdl(pdl_for_tokens(T), permute_scan_kernel, dim3(1), dim3(1024), 0, s, blk_count, nblk,
+               E, S, T, align, counts, offsets);
     if (P > 0)
-      permute_scatter_kernel<<<(unsigned)((P + 255) / 256), 256, 0, s>>>(
-          topk_idx, P, E, blk_count, rank_in_blk, dst_row, src_pair);
+      launch_pdl(pdl_for_tokens(T), permute_scatter_kernel, dim3((unsigned)((P + 255) / 256)),
+                 dim3(256), 0, s, topk_idx, P, E, blk_count, rank_in_blk, dst_row, src_pair);
     launches = P > 0 ? 4 : 2;
   }
-  permute_gather_kernel<<<(unsigned)((R_cap + 7) / 8), 256, 0, s>>>(
-      x, d, k, T, offsets, counts, E, S, R_cap, src_pair, dst_row, xp);
+  launch_pdl(pdl_for_tokens(T), permute_gather_kernel, dim3((unsigned)((R_cap + 7) / 8)), dim3(256),
+             0, s, x, d, k, T, offsets, counts, E, S, R_cap, src_pair, dst_row, xp);
   note_launches(launches);
   timer_after(MOE_KERNEL_PERMUTE, s);
   return cudaGetLastError();

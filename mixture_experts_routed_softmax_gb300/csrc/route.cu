@@ -59,6 +59,7 @@ size_t route_ws_bytes(int64_t T, int d, int E) {
 // logits = sum of the split-K partials in split order, plus the bias
 __global__ void router_reduce_kernel(const float* __restrict__ part, int ksplit, int64_t n, int E,
                                      const float* __restrict__ bias, float* __restrict__ logits) {
+  pdl_enter();
   const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= n) return;
   float acc = 0.f;
@@ -68,6 +69,7 @@ __global__ void router_reduce_kernel(const float* __restrict__ part, int ksplit,
 
 __global__ void split_router_weight_kernel(const float* __restrict__ wr, int d, int E, int E8,
                                            moe_bf16* __restrict__ w_split) {
+  pdl_enter();
   const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= (int64_t)d * E8) return;
   const int row = (int)(i / E8), e = (int)(i % E8);
@@ -92,6 +94,7 @@ __global__ void split_router_weight_kernel(const float* __restrict__ wr, int d, 
 __global__ void __launch_bounds__(kSmallWarps * 32) router_small_partial_kernel(
     const moe_bf16* __restrict__ x, const float* __restrict__ w_router, int64_t T, int d, int E,
     int rs, float* __restrict__ part) {
+  pdl_enter();
   __shared__ float4 red[kSmallWarps][kSmallTok][32];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int e0 = blockIdx.x * kSmallCols + 4 * lane;
@@ -159,6 +162,7 @@ __global__ void __launch_bounds__(256) router_small_topk_kernel(
     const float* __restrict__ bias, const int32_t* __restrict__ forced,
     float* __restrict__ logits, int32_t* __restrict__ topk_idx, float* __restrict__ topk_w,
     int* status) {
+  pdl_enter();
   __shared__ float lrow[kMaxExperts];
   const int64_t t = blockIdx.x;
   for (int e = threadIdx.x; e < E; e += blockDim.x) {
@@ -185,8 +189,8 @@ template <int NV>
 static void launch_small_topk(const float* part, int ns, int64_t T, int E, int k,
                               const float* bias, const int32_t* forced, float* logits,
                               int32_t* topk_idx, float* topk_w, int* status, cudaStream_t s) {
-  router_small_topk_kernel<NV><<<(unsigned)T, 256, 0, s>>>(part, ns, T, E, k, bias, forced, logits,
-                                                           topk_idx, topk_w, status);
+  launch_pdl(pdl_for_tokens(T), router_small_topk_kernel<NV>, dim3((unsigned)T), dim3(256), 0, s,
+             part, ns, T, E, k, bias, forced, logits, topk_idx, topk_w, status);
 }
 
 // The whole routing of a few tokens: two launches (partials; logits + top-k).
@@ -199,7 +203,8 @@ cudaError_t launch_route_small(const moe_bf16* x, const float* w_router, const f
   const dim3 grid((unsigned)((E + kSmallCols - 1) / kSmallCols), (unsigned)ns,
                   (unsigned)((T + kSmallTok - 1) / kSmallTok));
   timer_before(MOE_KERNEL_ROUTER_LOGITS, s);
-  router_small_partial_kernel<<<grid, kSmallWarps * 32, 0, s>>>(x, w_router, T, d, E, rs, part);
+  launch_pdl(pdl_for_tokens(T), router_small_partial_kernel, dim3(grid), dim3(kSmallWarps * 32), 0,
+             s, x, w_router, T, d, E, rs, part);
   note_launches(1);
   timer_after(MOE_KERNEL_ROUTER_LOGITS, s);
   cudaError_t e = cudaGetLastError();
@@ -225,8 +230,8 @@ cudaError_t launch_router_logits(const moe_bf16* x, const float* w_router, const
   moe_bf16* w_split = static_cast<moe_bf16*>(ws);
   const int64_t n = (int64_t)d * E8;
   timer_before(MOE_KERNEL_ROUTER_LOGITS, s);
-  split_router_weight_kernel<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(w_router, d, E, E8,
-                                                                        w_split);
+  launch_pdl(pdl_for_tokens(T), split_router_weight_kernel, dim3((unsigned)((n + 255) / 256)),
+             dim3(256), 0, s, w_router, d, E, E8, w_split);
   note_launches(1);
   cudaError_t e = cudaGetLastError();
   const int sp = router_ksplit(T, d, E);
@@ -238,8 +243,8 @@ cudaError_t launch_router_logits(const moe_bf16* x, const float* w_router, const
     if (e == cudaSuccess) e = launch_router_gemm(x, w_split, bias, T, d, E, E8, sp, part, status, s);
     if (e == cudaSuccess) {
       const int64_t nel = T * E;
-      router_reduce_kernel<<<(unsigned)((nel + 255) / 256), 256, 0, s>>>(part, sp, nel, E, bias,
-                                                                         logits);
+      launch_pdl(pdl_for_tokens(T), router_reduce_kernel, dim3((unsigned)((nel + 255) / 256)),
+                 dim3(256), 0, s, part, sp, nel, E, bias, logits);
       note_launches(1);
       e = cudaGetLastError();
     }
@@ -256,6 +261,7 @@ __global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ log
                                                    const int32_t* __restrict__ forced, int64_t T,
                                                    int E, int k, int32_t* __restrict__ topk_idx,
                                                    float* __restrict__ topk_w, int* status) {
+  pdl_enter();
   const int lane = threadIdx.x & 31;
   const int64_t t = (int64_t)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
   if (t >= T) return;
@@ -270,18 +276,23 @@ cudaError_t launch_topk(const float* logits, const int32_t* forced_idx, int64_t 
   timer_before(MOE_KERNEL_TOPK, s);
   const int nv = (E + 31) / 32;
   if (nv <= 1)
-    topk_kernel<1><<<grid, warps * 32, 0, s>>>(logits, forced_idx, T, E, k, topk_idx, topk_w, status);
+    launch_pdl(pdl_for_tokens(T), topk_kernel<1>, dim3(grid), dim3(warps * 32), 0, s, logits,
+               forced_idx, T, E, k, topk_idx, topk_w, status);
   else if (nv <= 2)
-    topk_kernel<2><<<grid, warps * 32, 0, s>>>(logits, forced_idx, T, E, k, topk_idx, topk_w, status);
+    launch_pdl(pdl_for_tokens(T), topk_kernel<2>, dim3(grid), dim3(warps * 32), 0, s, logits,
+               forced_idx, T, E, k, topk_idx, topk_w, status);
   else if (nv <= 4)
-    topk_kernel<4><<<grid, warps * 32, 0, s>>>(logits, forced_idx, T, E, k, topk_idx, topk_w, status);
+    launch_pdl(pdl_for_tokens(T), topk_kernel<4>, dim3(grid), dim3(warps * 32), 0, s, logits,
+               forced_idx, T, E, k, topk_idx, topk_w, status);
   else if (nv <= 8)
-    topk_kernel<8><<<grid, warps * 32, 0, s>>>(logits, forced_idx, T, E, k, topk_idx, topk_w, status);
+    launch_pdl(pdl_for_tokens(T), topk_kernel<8>, dim3(grid), dim3(warps * 32), 0, s, logits,
+               forced_idx, T, E, k, topk_idx, topk_w, status);
   else if (nv <= 16)
-    topk_kernel<16><<<grid, warps * 32, 0, s>>>(logits, forced_idx, T, E, k, topk_idx, topk_w, status);
+    launch_pdl(pdl_for_tokens(T), topk_kernel<16>, dim3(grid), dim3(warps * 32), 0, s, logits,
+               forced_idx, T, E, k, topk_idx, topk_w, status);
   else
-    topk_kernel<kMaxExperts / 32><<<grid, warps * 32, 0, s>>>(logits, forced_idx, T, E, k,
-                                                              topk_idx, topk_w, status);
+    launch_pdl(pdl_for_tokens(T), topk_kernel<kMaxExperts / 32>, dim3(grid), dim3(warps * 32), 0, s,
+               logits, forced_idx, T, E, k, topk_idx, topk_w, status);
   note_launches(1);
   timer_after(MOE_KERNEL_TOPK, s);
   return cudaGetLastError();
@@ -314,6 +325,7 @@ size_t route_bwd_ws_bytes(int64_t T, int d, int E, int k, int align) {
 
 __global__ void transpose_f32_kernel(const float* __restrict__ in, int rows, int cols,
                                      float* __restrict__ out) {
+  pdl_enter();
   __shared__ float tile[32][33];
   const int c = blockIdx.x * 32 + threadIdx.x;
   for (int i = threadIdx.y; i < 32; i += 8) {
@@ -341,6 +353,7 @@ __global__ void __launch_bounds__(256, 4) route_bwd_token_kernel(
     int E8, int k, int S, float* __restrict__ dl_pair, moe_bf16* __restrict__ dl3,
     moe_bf16* __restrict__ dx, const float* __restrict__ dxp,
     const int32_t* __restrict__ dst_row) {
+  pdl_enter();
   const int lane = threadIdx.x & 31;
   const int64_t t = (int64_t)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
   if (t >= T) return;
@@ -433,6 +446,7 @@ __global__ void __launch_bounds__(256) route_bwd_reduce_kernel(
     const float* __restrict__ part, int ksplit, int d, int E, int E8,
     const int64_t* __restrict__ offsets, const int32_t* __restrict__ src_pair,
     const float* __restrict__ dl_pair, float* __restrict__ dw_router, float* __restrict__ dbias) {
+  pdl_enter();
   if (blockIdx.y == 0) {
     const int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (idx >= (int64_t)d * E) return;
@@ -480,12 +494,13 @@ cudaError_t launch_route_bwd(const float* d_topk_w, const float* topk_w, const i
   float* part = reinterpret_cast<float*>(p);
 
   timer_before(MOE_KERNEL_ROUTE_BWD, s);
-  transpose_f32_kernel<<<dim3((E + 31) / 32, (d + 31) / 32), dim3(32, 8), 0, s>>>(w_router, d, E,
-                                                                                  wrT);
+  launch_pdl(pdl_for_tokens(T), transpose_f32_kernel, dim3((E + 31) / 32, (d + 31) / 32),
+             dim3(32, 8), 0, s, w_router, d, E, wrT);
   note_launches(1);
   if (T > 0) {
-    route_bwd_token_kernel<<<(unsigned)((T + 7) / 8), 256, 0, s>>>(
-        d_topk_w, topk_w, topk_idx, wrT, T, d, E, E8, k, S, dl_pair, dl3, dx_inout, dxp, dst_row);
+    launch_pdl(pdl_for_tokens(T), route_bwd_token_kernel, dim3((unsigned)((T + 7) / 8)), dim3(256),
+               0, s, d_topk_w, topk_w, topk_idx, wrT, T, d, E, E8, k, S, dl_pair, dl3, dx_inout,
+               dxp, dst_row);
     note_launches(1);
   }
   cudaError_t err = cudaGetLastError();
@@ -493,8 +508,8 @@ cudaError_t launch_route_bwd(const float* d_topk_w, const float* topk_w, const i
   if (err == cudaSuccess) {
     const int64_t n = (int64_t)d * E;
     const unsigned gx = (unsigned)std::max<int64_t>((n + 255) / 256, (E + 7) / 8);
-    route_bwd_reduce_kernel<<<dim3(gx, dbias ? 2 : 1), 256, 0, s>>>(
-        part, sp, d, E, E8, offsets, src_pair, dl_pair, dw_router, dbias);
+    launch_pdl(pdl_for_tokens(T), route_bwd_reduce_kernel, dim3(gx, dbias ? 2 : 1), dim3(256), 0, s,
+               part, sp, d, E, E8, offsets, src_pair, dl_pair, dw_router, dbias);
     note_launches(1);
     err = cudaGetLastError();
   }
