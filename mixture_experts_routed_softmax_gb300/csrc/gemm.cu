@@ -8,7 +8,9 @@
 //
 // One persistent, warp-specialised kernel template serves all six GEMMs:
 //   warp 0      TMA producer: tiles of A and B into a shared-memory ring of
-//               as many stages as fit 192 KiB (4 of 48 KiB, 6 of 32 KiB)
+//               as many stages as fit 192 KiB (4 of 48 KiB, 6 of 32 KiB; the
+//               down dgrad of a CTA pair keeps 4 and gives 64 KiB to its
+//               epilogue's G/U loads)
 //   warp 1      MMA issuer: tcgen05.mma 128 x N x 16 (bf16 in, fp32 in tensor
 //               memory), two accumulator buffers so the epilogue of one tile
 //               overlaps the main loop of the next
@@ -57,6 +59,7 @@ constexpr int BK = 64;             // k per stage: one 128-byte swizzle atom of 
 constexpr int kABytes = BM * BK * 2;                      // 16 KiB
 constexpr int kRingBytes = 192 * 1024;                    // the TMA ring: 4 x 48 KiB, 6 x 32 KiB
 constexpr int kMaxStages = 8;
+constexpr int kEpiWarps = 8;       // epilogue warps: two warpgroups, each half the columns
 
 template <Kind K>
 struct Tr {
@@ -97,17 +100,25 @@ struct Tr {
 
 // Shared-memory ring per CTA: one A tile and all of B's tile (or, in a CTA
 // pair, this CTA's half of B's columns) per stage, as many stages as fit.
+// The down dgrad of a CTA pair (half the B bytes per stage) gives the ring's
+// tail to its epilogue: gu_slots slots per epilogue warp, each 8 fp32 columns
+// of the warp's 32 rows of G and of U ([32 rows x 32 bytes] x 2, loaded by
+// TMA), so the saved activations arrive several slices ahead of use without
+// holding registers. A single CTA keeps its four 48 KiB stages and loads G
+// and U into registers.
 template <Kind K, bool PAIR>
 struct Geo {
   using T = Tr<K>;
   static constexpr int b_bytes = (T::dual ? 2 : 1) * T::BN * BK * 2 / (PAIR ? 2 : 1);
   static constexpr int stage_bytes = kABytes + b_bytes;
-  static constexpr int stages =
-      kRingBytes / stage_bytes > kMaxStages ? kMaxStages : kRingBytes / stage_bytes;
+  static constexpr int gu_slots = (K == Kind::DownDgrad && PAIR) ? 4 : 0;
+  static constexpr int gu_slot_bytes = 2 * 32 * 32;
+  static constexpr int gu_bytes = gu_slots * kEpiWarps * gu_slot_bytes;
+  static constexpr int ring = kRingBytes - gu_bytes;
+  static constexpr int stages = ring / stage_bytes > kMaxStages ? kMaxStages : ring / stage_bytes;
 };
 
 constexpr int kTmemCols = 512;                            // 2 accumulator buffers x 256 columns
-constexpr int kEpiWarps = 8;                              // two warpgroups, each half the columns
 constexpr int kThreads = 128 + 32 * kEpiWarps;
 // Epilogues stage their outputs through shared memory for TMA stores: a ring
 // of kStgSlots slots per epilogue warpgroup, each [128 rows x 32 bytes] (16
@@ -145,9 +156,9 @@ struct GemmArgs {
   void* out0;      // bf16, or fp32 (G, U of GateUpFwd; DownFwd; GateUpDgrad)
   void* out1;
   void* out2;
-  const float* in0;          // DownDgrad: the saved G, U (fp32)
-  const float* in1;
   const float* row_w;
+  const float* in0;          // DownDgrad in one CTA: the saved G, U (fp32; a pair reads them by TMA)
+  const float* in1;
   const float* pair_w;       // DownDgrad: the score of each routed pair ([T*k], via src_pair)
   int64_t p_routed;          // DownDgrad: pairs below this are routed; the rest shared (weight 1)
   Act act;                   // GateUpFwd, DownDgrad: the activation
@@ -361,6 +372,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto tfull_bar = [&](int b) { return bar0 + 8u * (2 * kMaxStages + b); };
   auto tempty_bar = [&](int b) { return bar0 + 8u * (2 * kMaxStages + 2 + b); };
   const uint32_t drain_bar = bar0 + 8u * (2 * kMaxStages + 4);
+  // the down dgrad's G/U slots: one barrier per slot of each epilogue warp
+  auto gu_bar = [&](int ew, int s) { return bar0 + 256u + 8u * (ew * 4 + s); };
+  static_assert(G::gu_slots <= 4, "G/U slot barriers");
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bars + 2 * kMaxStages + 5);
   volatile int* s_abort = reinterpret_cast<volatile int*>(s_tmem + 1);
   int* tstart = reinterpret_cast<int*>(smem + kRingBytes + 1024);
@@ -387,6 +401,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(tempty_bar(b), PAIR ? 2 * kEpiWarps : kEpiWarps);
     }
     mbar_init(drain_bar, 1);
+    for (int ew = 0; ew < kEpiWarps; ++ew)
+      for (int b = 0; b < G::gu_slots; ++b) mbar_init(gu_bar(ew, b), 1);
     *s_abort = 0;
     fence_mbar_init();
   }
@@ -482,7 +498,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     b_bytes = T::b_mn ? (uint32_t)nbox * (BK * 128) : (uint32_t)bn * (BK * 2);
   const uint32_t tx_bytes =
       (PAIR || T::var_bn) ? (uint32_t)kABytes + b_bytes : (uint32_t)G::stage_bytes;
-  static_assert(kStages * kStageBytes <= kRingBytes && kStageBytes % 8192 == 0, "ring layout");
+  static_assert(kStages * kStageBytes <= G::ring && kStageBytes % 8192 == 0, "ring layout");
 
   if (warp == 0) {
     if (lane == 0) {
@@ -719,6 +735,72 @@ __global__ void __launch_bounds__(kThreads, 1)
                         static_cast<uint8_t*>(args.out2)};
     int acc = 0;
     uint32_t acc_phase = 0;
+    // DownDgrad: the saved G and U of this warp's rows come by TMA into its
+    // slots, 8 columns per chunk, in the order the epilogue reads them. A
+    // cursor walks this warp's chunks over the CTA's tiles and keeps the
+    // slots filled (up to gu_slots chunks ahead of the one being read, across
+    // tile boundaries); lane 0 issues, every lane keeps the same counters.
+    constexpr int NS = G::gu_slots > 0 ? G::gu_slots : 1;
+    const int ew = warp - 4;
+    const uint8_t* gu_mem = smem + kStages * kStageBytes + ew * NS * G::gu_slot_bytes;
+    int gu_issue = 0, gu_use = 0, gu_done = 0;   // chunks issued, read, seen complete
+    int cur_tile = GEMM_CID, cur_j = 0, cur_n = 0, cur_row0 = 0, cur_col0 = 0;
+    const uint64_t pol_in = l2_evict_first();    // read once
+    // the cursor's tile: this warp's rows and chunk count (none when the
+    // warp's rows all lie past the group: nothing of them is stored)
+    auto gu_tile = [&]() {
+      TileInfo tt;
+      decode_tile<K, PAIR>(cur_tile, args, tstart, nN, rank, tt);
+      const int ce = min(c_hi, args.N - tt.n0);
+      cur_row0 = (int)tt.m0 + wq * 32;
+      cur_n = (ce > c_lo && cur_row0 < tt.row_end) ? (ce - c_lo + 7) >> 3 : 0;
+      cur_col0 = tt.n0 + c_lo;
+    };
+    auto gu_fill = [&]() {   // issue chunks while a slot is free (warp-uniform)
+      if (__shfl_sync(0xFFFFFFFFu, *s_abort, 0)) return;
+      while (gu_issue < gu_done + NS && gu_issue < gu_use + NS && cur_tile < total) {
+        if (cur_j < cur_n) {
+          if (lane == 0) {
+            const int sl = gu_issue % NS;
+            const uint32_t bar = gu_bar(ew, sl);
+            const uint32_t dst = smem_u32(gu_mem + sl * G::gu_slot_bytes);
+            const int x = cur_col0 + 8 * cur_j;
+            mbar_arrive_expect_tx(bar, (uint32_t)G::gu_slot_bytes);
+            tma_load_2d_hint(dst, &mapA1, bar, x, cur_row0, pol_in);
+            tma_load_2d_hint(dst + G::gu_slot_bytes / 2, &mapB1, bar, x, cur_row0, pol_in);
+          }
+          ++gu_issue;
+          ++cur_j;
+        } else {
+          cur_tile += GEMM_NCL;
+          cur_j = 0;
+          if (cur_tile < total) gu_tile();
+        }
+      }
+    };
+    // 8 columns of G and U of this thread's row from the next chunk's slot
+    // (the slot's two boxes carry the 32-byte swizzle: halves of rows 4-7 swapped)
+    auto gu_get = [&](float* gf, float* uf) {
+      const int sl = gu_use % NS;
+      const bool ok = mbar_wait_bounded(gu_bar(ew, sl), (uint32_t)((gu_use / NS) & 1), s_abort,
+                                        args.status);
+      const uint8_t* p = gu_mem + sl * G::gu_slot_bytes + lane * 32;
+      const int sw = ((lane >> 2) & 1) * 16;
+      const float4 g0 = *reinterpret_cast<const float4*>(p + sw);
+      const float4 g1 = *reinterpret_cast<const float4*>(p + (16 - sw));
+      const float4 u0 = *reinterpret_cast<const float4*>(p + G::gu_slot_bytes / 2 + sw);
+      const float4 u1 = *reinterpret_cast<const float4*>(p + G::gu_slot_bytes / 2 + (16 - sw));
+      gf[0] = g0.x; gf[1] = g0.y; gf[2] = g0.z; gf[3] = g0.w;
+      gf[4] = g1.x; gf[5] = g1.y; gf[6] = g1.z; gf[7] = g1.w;
+      uf[0] = u0.x; uf[1] = u0.y; uf[2] = u0.z; uf[3] = u0.w;
+      uf[4] = u1.x; uf[5] = u1.y; uf[6] = u1.z; uf[7] = u1.w;
+      if (ok && gu_done == gu_use) ++gu_done;
+      ++gu_use;
+    };
+    if constexpr (G::gu_slots > 0) {
+      if (cur_tile < total) gu_tile();
+      gu_fill();
+    }
     for (int tile = GEMM_CID; tile < total; tile += GEMM_NCL) {
       TileInfo ti;
       decode_tile<K, PAIR>(tile, args, tstart, nN, rank, ti);
@@ -744,9 +826,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool row_ok = T::kgrouped ? false : (row < ti.row_end);
       const int c_end = min(c_hi, args.N - ti.n0);   // columns of this half that exist
       const int col_lim = ti.n0 + c_end;
-      // DownDgrad: the saved G, U of the next 16 columns are loaded while the
-      // current ones are computed; the first loads and the row's score go out
-      // before the accumulator is ready
+      // DownDgrad in one CTA: the saved G, U of the next 16 columns are loaded
+      // while the current ones are computed; the first loads and the row's
+      // score go out before the accumulator is ready
       const int64_t gu_base = row * args.N;
       float4 gc[4], uc[4];
       auto load_gu = [&](int c, float4* g, float4* u) {   // 16 fp32 columns of G and U
@@ -769,7 +851,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int32_t p = args.src_pair[row];
           if (p >= 0) rscale = p < args.p_routed ? args.pair_w[p] : 1.0f;
         }
-        if (c_lo < c_end) load_gu(c_lo, gc, uc);
+        if constexpr (G::gu_slots == 0)
+          if (c_lo < c_end) load_gu(c_lo, gc, uc);
       } else if constexpr (T::down_fwd) {
         if (args.row_w && row_ok) rscale = args.row_w[row];
       }
@@ -865,25 +948,51 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       } else if constexpr (K == Kind::DownDgrad) {
-        // dA = w * acc; dG = dA * U * silu'(G), dU = dA * silu(G), 16 columns
-        // at a time, the next 16 columns' G and U loaded while these are computed
+        // dA = w * acc; dG = dA * U * h'(G), dU = dA * h(G), 16 columns at a
+        // time: from two chunks of the slots (none past the half's last
+        // column or for rows all past the group: zeros there, nothing is
+        // stored), or in one CTA from registers, the next 16 columns' G and U
+        // loaded while these are computed
         constexpr int es[2] = {2, 2};
+        const int nch = (c_end > c_lo && r0 < ti.row_end) ? (c_end - c_lo + 7) >> 3 : 0;
+        float dtw = 0.0f;   // this row's <dAu, h(G) U> over this warpgroup's columns
         float4 gn[4], un[4];
-        float dtw = 0.0f;   // this row's <dAu, silu(G) U> over this warpgroup's columns
 #pragma unroll 1
         for (int c = c_lo; c < c_end; c += 32) {
           uint32_t r[32];
           tmem_ld32(t_row + c, r);
-          if (c + 16 < c_end) load_gu(c + 16, gn, un);
-          tmem_ld_wait();
+          const int j0 = (c - c_lo) >> 3;
+          if constexpr (G::gu_slots == 0) {
+            if (c + 16 < c_end) load_gu(c + 16, gn, un);
+            tmem_ld_wait();
+          }
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
-            const float gf[16] = {gc[0].x, gc[0].y, gc[0].z, gc[0].w, gc[1].x, gc[1].y,
-                                  gc[1].z, gc[1].w, gc[2].x, gc[2].y, gc[2].z, gc[2].w,
-                                  gc[3].x, gc[3].y, gc[3].z, gc[3].w};
-            const float uf[16] = {uc[0].x, uc[0].y, uc[0].z, uc[0].w, uc[1].x, uc[1].y,
-                                  uc[1].z, uc[1].w, uc[2].x, uc[2].y, uc[2].z, uc[2].w,
-                                  uc[3].x, uc[3].y, uc[3].z, uc[3].w};
+            float gf[16], uf[16];
+            if constexpr (G::gu_slots > 0) {
+#pragma unroll
+              for (int q = 0; q < 2; ++q) {
+                if (j0 + 2 * h + q < nch) {
+                  gu_get(gf + 8 * q, uf + 8 * q);
+                } else {
+#pragma unroll
+                  for (int i = 0; i < 8; ++i) { gf[8 * q + i] = 0.0f; uf[8 * q + i] = 0.0f; }
+                }
+              }
+              // every lane has read the two slots: they take the next chunks
+              __syncwarp();
+              if (lane == 0) fence_async_smem();
+              gu_fill();
+              if (h == 0) tmem_ld_wait();
+            } else {
+#pragma unroll
+              for (int v = 0; v < 4; ++v) {
+                gf[4 * v + 0] = gc[v].x; gf[4 * v + 1] = gc[v].y;
+                gf[4 * v + 2] = gc[v].z; gf[4 * v + 3] = gc[v].w;
+                uf[4 * v + 0] = uc[v].x; uf[4 * v + 1] = uc[v].y;
+                uf[4 * v + 2] = uc[v].z; uf[4 * v + 3] = uc[v].w;
+              }
+            }
             uint32_t pk[2][8];
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
@@ -910,9 +1019,11 @@ __global__ void __launch_bounds__(kThreads, 1)
               pk[0][i] = pack_bf16(dg[0], dg[1]);
               pk[1][i] = pack_bf16(du[0], du[1]);
             }
+            if constexpr (G::gu_slots == 0) {
 #pragma unroll
-            for (int v = 0; v < 4; ++v) { gc[v] = gn[v]; uc[v] = un[v]; }
-            if (h == 0 && c + 32 < c_end) load_gu(c + 32, gn, un);
+              for (int v = 0; v < 4; ++v) { gc[v] = gn[v]; uc[v] = un[v]; }
+              if (h == 0 && c + 32 < c_end) load_gu(c + 32, gn, un);
+            }
             uint4 vv[2][2];
             slice_of<2, 8>(pk, 0, vv);
             put_slice<2, false, WS>(vv, stg, slot, maps, outs, es, tile_tma, row_ok, row, srow,
@@ -958,6 +1069,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
     }
     if (leader) bulk_wait_all();   // the unit's staged stores finish before the CTA exits
+    if constexpr (K == Kind::DownDgrad) {
+      // after an abort: the G/U loads still in flight land before shared memory goes away
+      if (lane == 0)
+        for (int q = gu_done; q < gu_issue; ++q)
+          drain_wait(gu_bar(ew, q % NS), (uint32_t)((q / NS) & 1), args.status);
+    }
   }
   tc_fence_before();
   __syncthreads();
@@ -1038,6 +1155,21 @@ static bool map2d_out(CUtensorMap* m, const void* ptr, uint64_t N, uint64_t R, i
             const_cast<void*>(ptr), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
             CU_TENSOR_MAP_SWIZZLE_32B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// The down dgrad's loads of the saved G or U [R, N] (fp32): boxes of 8
+// columns x 32 rows with the 32-byte swizzle, a whole 128-byte line brought
+// into L2 per miss (the row's next chunks follow).
+static bool map2d_gu(CUtensorMap* m, const float* ptr, uint64_t N, uint64_t R) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {N, R};
+  cuuint64_t strides[1] = {N * 4};
+  cuuint32_t box[2] = {8, 32};
+  cuuint32_t es[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(ptr), dims, strides, box,
+            es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_32B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 // 3-D bf16 map over [E, M, N] (N innermost), boxes of one warp's 32 rows
@@ -1127,9 +1259,9 @@ static cudaError_t launch_kind(const CUtensorMap& a0, const CUtensorMap& a1,
 
 // CTA pairs (M = 256 MMAs over two SMs: half the B traffic per SM, a deeper
 // ring) for the M-grouped kinds when the experts average at least 1024 rows,
-// where 256-row tiles waste little (the down dgrad excepted, below); the
-// gate/up forward and dgrad, which move two weight matrices per tile, from 512
-// rows. Not by default for the K-grouped weight gradients: their rows (d or
+// where 256-row tiles waste little; the gate/up forward and dgrad, which move
+// two weight matrices per tile, and the down dgrad, whose pair form also
+// loads G and U ahead by TMA, from 512 rows. Not by default for the K-grouped weight gradients: their rows (d or
 // f, e.g. 2880 = 11.25 x 256) leave a mostly empty last 256-row tile.
 // MOE_GEMM_PAIRS=0 or 1 in the environment turns pairs off or on for every
 // grouped kind (a tuning and testing knob; the results are the same).
@@ -1313,17 +1445,20 @@ cudaError_t launch_down_dgrad(const GroupedDims& g, const moe_bf16* dyg, const f
                               const moe_bf16* w_down, const float* G, const float* U,
                               moe_bf16* dG, moe_bf16* dU, float* dtw_part,
                               const ActParams& act, int* status, cudaStream_t s) {
-  CUtensorMap a0, b0, o0, o1;
+  CUtensorMap a0, b0, o0, o1, mg, mu;
   const int bn = pick_bn(g.f, 16);
-  // no pairs by default: this kernel is bound by its epilogue (G and U read,
-  // dG and dU written), which pairs do not shorten
-  const bool pair = pairs_env() == 1;
+  // pairs from 512 rows per expert on average: half the weight bytes per SM
+  // from L2, and G and U loaded by TMA ahead of the epilogue (fewer rows: the
+  // last 256-row tile of each group would be mostly empty)
+  const bool pair = pairs_mgrouped(g, 512);
   // dA[r, c] = w(r) sum_j dyg[r, j] W_down[e][c, j]: B is W_down[e] read as
-  // [N = f rows, K = d] (a pair's CTAs load bn / 2 rows each)
+  // [N = f rows, K = d] (a pair's CTAs load bn / 2 rows each); G and U come
+  // to the epilogue through the second A and B maps
   if (!g.src_pair) return cudaErrorInvalidValue;
   if (!map2d(&a0, dyg, g.d, g.R_cap, BM) ||
       !map3d(&b0, w_down, g.d, g.f, g.E, pair ? bn / 2 : bn) ||
-      !map2d_out(&o0, dG, g.f, g.R_cap, 2, 32) || !map2d_out(&o1, dU, g.f, g.R_cap, 2, 32))
+      !map2d_out(&o0, dG, g.f, g.R_cap, 2, 32) || !map2d_out(&o1, dU, g.f, g.R_cap, 2, 32) ||
+      !map2d_gu(&mg, G, g.f, g.R_cap) || !map2d_gu(&mu, U, g.f, g.R_cap))
     return cudaErrorInvalidValue;
   GemmArgs a = base_args(g, status);
   const bool pdl = pdl_for_pairs(g.P);
@@ -1339,8 +1474,8 @@ cudaError_t launch_down_dgrad(const GroupedDims& g, const moe_bf16* dyg, const f
   a.bn = bn;
   if (pair)
     return launch_kind<Kind::DownDgrad, true>(
-        a0, a0, b0, b0, a, mgrouped_tiles_upper(g, g.f, bn, 2 * BM), s, &o0, &o1, nullptr, pdl);
-  return launch_kind<Kind::DownDgrad, false>(a0, a0, b0, b0, a, mgrouped_tiles_upper(g, g.f, bn),
+        a0, mg, b0, mu, a, mgrouped_tiles_upper(g, g.f, bn, 2 * BM), s, &o0, &o1, nullptr, pdl);
+  return launch_kind<Kind::DownDgrad, false>(a0, mg, b0, mu, a, mgrouped_tiles_upper(g, g.f, bn),
                                              s, &o0, &o1, nullptr, pdl);
 }
 
