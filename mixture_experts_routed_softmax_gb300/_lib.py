@@ -22,6 +22,9 @@ SIGNATURES = {
     "moe_permute_noalloc": (_I, [_P, _I64, _I, _I, _I, _P, _I, _I64, _P, _P, _P, _P, _P, _P]),
     "moe_expert_fwd": (_I, [_P, _P, _P, _P, _I64, _I, _I, _I, _I, _I, _I64, _P, _P, _P, _P, _P,
                             _P, _P, _P]),
+    "moe_expert_fwd_fused": (_I, [_P, _P, _P, _P, _P, _I64, _I, _I, _I, _I, _I, _I64, _P, _P,
+                                  _P, _P, _P, _P, _SZ, _P]),
+    "moe_expert_fwd_fused_workspace_size": (_SZ, [_I64, _I, _I]),
     "moe_combine": (_I, [_P, _P, _P, _I64, _I, _I, _I, _P, _P]),
     "moe_expert_bwd": (_I, [_P, _P, _P, _P, _P, _P, _I64, _I, _I, _I, _I, _I, _I64,
                             _P, _P, _P, _P, _P, _P, _P,
@@ -64,7 +67,7 @@ KERNELS = {
     "router_logits": 1, "topk": 2, "permute": 3, "gateup_fwd": 4, "down_fwd": 5,
     "combine": 6, "combine_bwd": 7, "down_dgrad": 8, "gateup_dgrad": 9,
     "wgrad_down": 10, "wgrad_gateup": 11, "route_bwd": 12,
-    "decode": 13,
+    "decode": 13, "fused_fwd": 14,
 }
 
 _lib = None

@@ -51,7 +51,8 @@ namespace moe {
 enum class Kind {
   GateUpFwd, DownFwd, DownDgrad, GateUpDgrad, WgradDown, WgradGateUp, RouterLogits,
   RouterWgrad,      // dW_r partials = x^T . dl (dl's three bf16 parts side by side in N)
-  GateUpFwdNarrow   // GateUpFwd with 64-column tiles, for experts of at most ~128 rows
+  GateUpFwdNarrow,  // GateUpFwd with 64-column tiles, for experts of at most ~128 rows
+  FusedFwd          // the fused expert forward: gather + gate/up + act, then down (below)
 };
 
 constexpr int BM = 128;            // tile rows (TMEM lanes)
@@ -64,7 +65,10 @@ constexpr int kEpiWarps = 8;       // epilogue warps: two warpgroups, each half 
 template <Kind K>
 struct Tr {
   static constexpr bool gateup_fwd = (K == Kind::GateUpFwd || K == Kind::GateUpFwdNarrow);
-  static constexpr bool dual = (gateup_fwd || K == Kind::WgradGateUp);
+  static constexpr bool fused = (K == Kind::FusedFwd);
+  // dual: two B tiles side by side, one N = 256 MMA (the fused forward's down
+  // tiles use the same stage layout with one 256-column B tile)
+  static constexpr bool dual = (gateup_fwd || K == Kind::WgradGateUp || fused);
   static constexpr bool two_seg = (K == Kind::GateUpDgrad);
   static constexpr bool kgrouped = (K == Kind::WgradDown || K == Kind::WgradGateUp);
   // one group of M rows, fp32 output (split K: one partial per chunk)
@@ -72,7 +76,7 @@ struct Tr {
   static constexpr bool a_mn = kgrouped || K == Kind::RouterWgrad;         // A is M-contiguous
   static constexpr bool down_fwd = (K == Kind::DownFwd);
   static constexpr bool narrow = (K == Kind::GateUpFwdNarrow);
-  static constexpr bool b_mn = (gateup_fwd || down_fwd || kgrouped || dense);
+  static constexpr bool b_mn = (gateup_fwd || down_fwd || kgrouped || dense || fused);
   static constexpr int BN = narrow ? 64 : dual ? 128 : 256;   // per accumulator
   // tile width chosen per launch (at most BN): the K-major-B kinds, whose B box
   // is exactly the tile's rows, and the router, whose N is the expert count
@@ -88,7 +92,8 @@ struct Tr {
   static constexpr int stages = kRingBytes / tx_bytes > kMaxStages ? kMaxStages
                                                                    : kRingBytes / tx_bytes;
   static constexpr int kernel_id =
-      gateup_fwd ? MOE_KERNEL_GATEUP_FWD
+      fused ? MOE_KERNEL_FUSED_FWD
+      : gateup_fwd ? MOE_KERNEL_GATEUP_FWD
       : down_fwd ? MOE_KERNEL_DOWN_FWD
       : K == Kind::DownDgrad ? MOE_KERNEL_DOWN_DGRAD
       : K == Kind::GateUpDgrad ? MOE_KERNEL_GATEUP_DGRAD
@@ -172,12 +177,25 @@ struct GemmArgs {
   int ksplit;         // RouterLogits: K split into this many chunks (1: write logits + bias)
   int ksteps_split;   // k-steps per chunk
   int bn;             // single-accumulator kinds: tile width (multiple of 16, <= 256)
-  const int32_t* src_pair;   // pair of each layout row (-1: padding): K-grouped (or NULL), DownDgrad
+  const int32_t* src_pair;   // pair of each layout row (-1: padding): K-grouped (or NULL), DownDgrad, FusedFwd
   int* status;
+  // FusedFwd: N = f (gate/up tiles, nk_seg k-steps over d), N2 = d (down
+  // tiles, nk2 k-steps over f); out2 = A (bf16), out3 = Yp (fp32, scaled by
+  // each row's score via src_pair / pair_w); tokens T_tok with ktop routed
+  // slots each; ready[m-tile] counts the gate/up tiles done
+  int N2;
+  int nk2;
+  void* out3;
+  int* ready;
+  int64_t T_tok;
+  int ktop;
+  const moe_bf16* xsrc;   // FusedFwd: x [T_tok, N2], the rows the gate/up tiles gather
 };
 
 struct TileInfo {
   int e;
+  int ph;           // FusedFwd: 0 gate/up tile, 1 down tile
+  int mt;           // FusedFwd: the m-tile's index in the tile table
   int64_t m0;       // first output row (M-grouped: row of the layout; K-grouped: row of dW[e])
   int n0;
   int nk;           // k-steps
@@ -200,9 +218,28 @@ __device__ __forceinline__ void decode_tile(int tile, const GemmArgs& a, const i
   using T = Tr<K>;
   constexpr int TM = PAIR ? 2 * BM : BM;
   const int bn = tile_bn<K>(a);
-  const int nt = tile % nN;
-  const int mt = tile / nN;
+  int nt = tile % nN;
+  int mt = tile / nN;
   ti.n0 = nt * bn;
+  ti.ph = 0;
+  if constexpr (T::fused) {
+    // gate/up tiles (128 + 128 columns of f) of every m-tile first, then the
+    // down tiles (256 columns of d); both in the tile table's expert order
+    const int nN1 = (a.N + 127) / 128, nN2 = (a.N2 + 255) / 256;
+    const int tiles1 = tstart[a.E] * nN1;
+    if (tile < tiles1) {
+      mt = tile / nN1;
+      ti.n0 = (tile % nN1) * 128;
+      ti.nk = a.nk_seg;
+    } else {
+      const int t2 = tile - tiles1;
+      ti.ph = 1;
+      mt = t2 / nN2;
+      ti.n0 = (t2 % nN2) * 256;
+      ti.nk = a.nk2;
+    }
+    ti.mt = mt;
+  }
   if constexpr (T::dense) {
     // tile = (m-tile * nN + n-tile) * ksplit + split; e holds the split
     const int sp = tile % a.ksplit;
@@ -233,7 +270,7 @@ __device__ __forceinline__ void decode_tile(int tile, const GemmArgs& a, const i
     ti.m0 = a.offsets[lo] + (int64_t)(mt - tstart[lo]) * TM + rank * BM;
     ti.row_end = a.offsets[lo + 1];
     ti.kbeg = 0;
-    ti.nk = a.nk_seg * (T::two_seg ? 2 : 1);
+    if constexpr (!T::fused) ti.nk = a.nk_seg * (T::two_seg ? 2 : 1);
   }
 }
 
@@ -345,6 +382,46 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, int* s
   mbar_wait_bounded(bar, parity, &never, status);
 }
 
+// Waits until the count at `cnt` (bumped with release by other CTAs) reaches
+// `target`, then orders the async proxy's later reads after it. Gives up like
+// mbar_wait_bounded: false on the CTA's abort flag, or after kWaitLimitNs
+// (then it sets the flag and raises MOE_ERR_DEVICE_TIMEOUT).
+__device__ __noinline__ bool wait_count(const int* cnt, int target, volatile int* abort_flag,
+                                        int* status) {
+  const uint64_t t0 = global_ns();
+  for (uint32_t i = 0;; ++i) {
+    if (ld_acquire_gpu(cnt) >= target) {
+      fence_async_global();
+      return true;
+    }
+    if ((i & 15u) == 15u) {
+      if (*abort_flag) return false;
+      if (global_ns() - t0 > (uint64_t)kWaitLimitNs) {
+        *abort_flag = 1;
+        raise_status(status, MOE_ERR_DEVICE_TIMEOUT);
+        return false;
+      }
+    }
+    __nanosleep(128);
+  }
+}
+
+// The barrier over all eight epilogue warps (id 3), returning whether every
+// thread passed `ok`: the fused forward's epilogue decides together, because
+// its gate/up tiles end at a barrier of both warpgroups.
+__device__ __forceinline__ bool epi_all(bool ok) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred pin, pout;\n\t"
+      "setp.ne.u32 pin, %1, 0;\n\t"
+      "bar.red.and.pred pout, 3, %2, pin;\n\t"
+      "selp.u32 %0, 1, 0, pout;\n\t}\n"
+      : "=r"(r)
+      : "r"((uint32_t)ok), "n"(32 * kEpiWarps)
+      : "memory");
+  return r != 0;
+}
+
 template <Kind K, bool PAIR>
 __global__ void __launch_bounds__(kThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA0,
@@ -353,8 +430,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const __grid_constant__ CUtensorMap mapB1,
                         const __grid_constant__ CUtensorMap mapO0,
                         const __grid_constant__ CUtensorMap mapO1,
-                        const __grid_constant__ CUtensorMap mapO2, const GemmArgs args) {
-  pdl_enter();
+                        const __grid_constant__ CUtensorMap mapO2,
+                        const __grid_constant__ CUtensorMap mapB2,
+                        const __grid_constant__ CUtensorMap mapO3, const GemmArgs args) {
+  if constexpr (Tr<K>::fused)
+    pdl_wait();   // CTAs wait on one another: no dependent kernel is scheduled before the end
+  else
+    pdl_enter();
   using T = Tr<K>;
   using G = Geo<K, PAIR>;
   static_assert(!PAIR || (!T::dense && !T::narrow), "pairs: grouped kinds");
@@ -393,7 +475,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(full_bar(s), 1);
+      // the fused forward: the producer's lane 0 (with the TMA bytes) and
+      // each of its 32 lanes once its copies of the stage have landed
+      mbar_init(full_bar(s), T::fused ? 33 : 1);
       mbar_init(empty_bar(s), 1);
     }
     for (int b = 0; b < 2; ++b) {
@@ -477,6 +561,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     total = args.E * ((args.M + TM - 1) / TM) * nN;
   } else if constexpr (T::dense) {
     total = ((args.M + BM - 1) / BM) * nN * args.ksplit;
+  } else if constexpr (T::fused) {
+    total = tstart[args.E] * (nN + (args.N2 + 255) / 256);
   } else {
     total = tstart[args.E] * nN;
   }
@@ -500,7 +586,106 @@ __global__ void __launch_bounds__(kThreads, 1)
       (PAIR || T::var_bn) ? (uint32_t)kABytes + b_bytes : (uint32_t)G::stage_bytes;
   static_assert(kStages * kStageBytes <= G::ring && kStageBytes % 8192 == 0, "ring layout");
 
-  if (warp == 0) {
+  if (warp == 0 && T::fused) {
+    // ------------------------------------------- producer (fused forward) --
+    // The whole warp. Gate/up tiles gather their A rows from x: lane
+    // (8 q + c) copies 16-byte chunk c of rows q, q + 4, ..., q + 124 with
+    // cp.async into the 128-byte-swizzled tile (chunk c of row r at
+    // 16 (c ^ (r mod 8))), each lane's copies of a stage completing on the
+    // stage's full barrier; a row's token is its pair's (routed: p / k,
+    // shared: (p - T k) mod T), and padding rows and rows past the group are
+    // zero-filled (no read). Down tiles read A from the activations buffer
+    // by TMA once every gate/up tile of their rows has published it (a
+    // bounded wait on the m-tile's count). B (the weights) by TMA.
+    const uint64_t pol_w = l2_evict_last();
+    const int nN1 = nN;
+    const int q4 = lane >> 3, ch = lane & 7;
+    int stage = 0;
+    uint32_t phase = 0;
+    int fills = 0;
+    bool ok = true;
+    for (int tile = GEMM_CID; tile < total && ok; tile += GEMM_NCL) {
+      TileInfo ti;
+      decode_tile<K, PAIR>(tile, args, tstart, nN, 0, ti);
+      int tok[32];
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        const int64_t r = ti.m0 + q4 + 4 * j;
+        int t = -1;
+        if (ti.ph == 0 && r < ti.row_end) {
+          const int32_t p = args.src_pair[r];
+          if (p >= 0)
+            t = p < args.p_routed ? (int)(p / args.ktop)
+                                  : (int)((p - args.p_routed) % args.T_tok);
+        }
+        tok[j] = t;
+      }
+      if (ti.ph == 1) {
+        int rdy = 1;
+        if (lane == 0) rdy = wait_count(args.ready + ti.mt, nN1, s_abort, args.status) ? 1 : 0;
+        if (!__shfl_sync(0xFFFFFFFFu, rdy, 0)) {
+          ok = false;
+          break;
+        }
+      }
+      for (int ks = 0; ks < ti.nk; ++ks) {
+        int go = 1;
+        if (lane == 0)
+          go = mbar_wait_bounded(empty_bar(stage), phase ^ 1u, s_abort, args.status) ? 1 : 0;
+        if (!__shfl_sync(0xFFFFFFFFu, go, 0)) {
+          ok = false;
+          break;
+        }
+        const uint32_t fb = full_bar(stage);
+        const uint32_t sA = s_base + stage * kStageBytes;
+        const uint32_t sB0 = sA + kABytes;
+        const int kk = ks * BK;
+        if (ti.ph == 0) {
+          if (lane == 0) {
+            mbar_arrive_expect_tx(fb, tx_bytes - (uint32_t)kABytes);
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+              tma_load_3d_hint(sB0 + j * (BK * 128), &mapB0, fb, ti.n0 + 64 * j, kk, ti.e, pol_w);
+              tma_load_3d_hint(sB0 + kBBytes + j * (BK * 128), &mapB1, fb, ti.n0 + 64 * j, kk,
+                               ti.e, pol_w);
+            }
+          }
+          const int col = kk + 8 * ch;
+          const bool col_ok = col < args.N2;
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const int r = q4 + 4 * j;
+            const bool in = col_ok && tok[j] >= 0;
+            const moe_bf16* src = in ? args.xsrc + (int64_t)tok[j] * args.N2 + col : args.xsrc;
+            cp_async16_zfill(sA + (uint32_t)r * 128u + (uint32_t)((ch ^ (r & 7)) << 4), src, in);
+          }
+          cp_async_arrive_noinc(fb);
+        } else {
+          if (lane == 0) {
+            mbar_arrive_expect_tx(fb, tx_bytes);
+            tma_load_2d(sA, &mapA1, fb, kk, (int)ti.m0);
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+              tma_load_3d_hint(sB0 + j * (BK * 128), &mapB2, fb, ti.n0 + 64 * j, kk, ti.e, pol_w);
+          }
+          mbar_arrive(fb);
+        }
+        ++fills;
+        if (++stage == kStages) { stage = 0; phase ^= 1u; }
+      }
+    }
+    cp_async_wait_all();   // this lane's copies land before shared memory goes away
+    if (lane == 0 && *s_abort) {
+      // let the copies already issued land before the CTA's shared memory goes away
+      const int outstanding = fills < kStages ? fills : kStages;
+      int st = stage;
+      uint32_t ph = phase;
+      for (int i = 0; i < outstanding; ++i) {
+        if (--st < 0) { st = kStages - 1; ph ^= 1u; }
+        drain_wait(full_bar(st), ph, args.status);
+      }
+    }
+  } else if (warp == 0) {
     if (lane == 0) {
       // ------------------------------------------------------ producer --
       const uint64_t pol_w = l2_evict_last();   // expert weights: re-read by every m-tile
@@ -673,6 +858,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           tc_fence_after();
+          // the fused forward's gathered A tiles were written by cp.async (the
+          // generic proxy); the MMA reads them through the async proxy
+          if constexpr (T::fused) fence_async_smem();
           const uint32_t sA = s_base + stage * kStageBytes;
           const uint32_t sB0 = sA + kABytes;
           int nsub = BK / 16;
@@ -857,7 +1045,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (args.row_w && row_ok) rscale = args.row_w[row];
       }
       const bool got = mbar_wait_bounded(tfull_bar(acc), acc_phase, s_abort, args.status);
-      if (!group_all(group, got)) break;
+      if (!(T::fused ? epi_all(got) : group_all(group, got))) break;
       tc_fence_after();
       const uint32_t t_row = tmem_base + ((uint32_t)(wq * 32) << 16) + (uint32_t)acc * 256u;
 
@@ -945,6 +1133,73 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int col = ti.n0 + c + i;
             if (col < col_lim)
               orow[col] = __uint_as_float(r[i]) + (whole && args.bias ? args.bias[col] : 0.f);
+          }
+        }
+      } else if constexpr (T::fused) {
+        // gate/up tile: A = act(G, U) from the two 128-column accumulators,
+        // bf16 in 16-column slices (each warpgroup 64 columns); down tile:
+        // the row's score times the fp32 accumulator in 8-column slices
+        // (each warpgroup 128 columns)
+        const int fhalf = ti.ph ? 128 : 64;
+        const int flo = group * fhalf;
+        const int fN = ti.ph ? args.N2 : args.N;
+        const int fend = min(flo + fhalf, fN - ti.n0);
+        const int flim = ti.n0 + fend;
+        if (ti.ph == 0) {
+          const CUtensorMap* mA[1] = {&mapO2};
+          uint8_t* oA[1] = {static_cast<uint8_t*>(args.out2)};
+          constexpr int esA[1] = {2};
+#pragma unroll 1
+          for (int c = flo; c < fend; c += 32) {
+            uint32_t g[32], u[32];
+            tmem_ld32(t_row + c, g);
+            tmem_ld32(t_row + 128 + c, u);
+            tmem_ld_wait();
+            uint32_t pa[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+              pa[i] = pack_bf16(swiglu(__uint_as_float(g[2 * i]), __uint_as_float(u[2 * i]), args.act),
+                                swiglu(__uint_as_float(g[2 * i + 1]), __uint_as_float(u[2 * i + 1]),
+                                       args.act));
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              uint4 v[1][2];
+              v[0][0] = make_uint4(pa[8 * h + 0], pa[8 * h + 1], pa[8 * h + 2], pa[8 * h + 3]);
+              v[0][1] = make_uint4(pa[8 * h + 4], pa[8 * h + 5], pa[8 * h + 6], pa[8 * h + 7]);
+              put_slice<1, false, false>(v, stg, slot, mA, oA, esA, tile_tma, row_ok, row, srow,
+                                         ti.n0 + c + 16 * h, fN, flim, (int)r0, 0, group, leader,
+                                         pol_out);
+            }
+          }
+        } else {
+          float w = 0.0f;
+          if (row_ok) {
+            const int32_t p = args.src_pair[row];
+            if (p >= 0) w = p < args.p_routed ? args.pair_w[p] : 1.0f;
+          }
+          const CUtensorMap* mY[1] = {&mapO3};
+          uint8_t* oY[1] = {static_cast<uint8_t*>(args.out3)};
+          constexpr int esY[1] = {4};
+#pragma unroll 1
+          for (int c = flo; c < fend; c += 32) {
+            uint32_t r[32];
+            tmem_ld32(t_row + c, r);
+            tmem_ld_wait();
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              uint4 v[1][2];
+              v[0][0] = make_uint4(__float_as_uint(__uint_as_float(r[8 * q + 0]) * w),
+                                   __float_as_uint(__uint_as_float(r[8 * q + 1]) * w),
+                                   __float_as_uint(__uint_as_float(r[8 * q + 2]) * w),
+                                   __float_as_uint(__uint_as_float(r[8 * q + 3]) * w));
+              v[0][1] = make_uint4(__float_as_uint(__uint_as_float(r[8 * q + 4]) * w),
+                                   __float_as_uint(__uint_as_float(r[8 * q + 5]) * w),
+                                   __float_as_uint(__uint_as_float(r[8 * q + 6]) * w),
+                                   __float_as_uint(__uint_as_float(r[8 * q + 7]) * w));
+              put_slice<1, false, false>(v, stg, slot, mY, oY, esY, tile_tma, row_ok, row, srow,
+                                         ti.n0 + c + 8 * q, fN, flim, (int)r0, 0, group, leader,
+                                         pol_out);
+            }
           }
         }
       } else if constexpr (K == Kind::DownDgrad) {
@@ -1067,6 +1322,20 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_arrive(tempty_bar(acc));
       }
       if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+      if constexpr (T::fused) {
+        // a gate/up tile publishes its rows of A: its TMA stores complete
+        // (and its masked row stores are fenced) before the m-tile's count
+        // goes up with release; down tiles of these rows wait for the count
+        if (ti.ph == 0) {
+          if (leader) {
+            bulk_wait_all();
+            fence_async_global();
+          }
+          __threadfence();
+          epi_all(true);
+          if (warp == 4 && lane == 0) red_release_gpu_add(args.ready + ti.mt, 1);
+        }
+      }
     }
     if (leader) bulk_wait_all();   // the unit's staged stores finish before the CTA exits
     if constexpr (K == Kind::DownDgrad) {
@@ -1194,7 +1463,8 @@ static cudaError_t launch_kind(const CUtensorMap& a0, const CUtensorMap& a1,
                                const CUtensorMap& b0, const CUtensorMap& b1, const GemmArgs& args,
                                int64_t tiles_upper, cudaStream_t s,
                                const CUtensorMap* o0 = nullptr, const CUtensorMap* o1 = nullptr,
-                               const CUtensorMap* o2 = nullptr, bool pdl = false) {
+                               const CUtensorMap* o2 = nullptr, bool pdl = false,
+                               const CUtensorMap* b2 = nullptr, const CUtensorMap* o3 = nullptr) {
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   static int units = 0;
@@ -1232,6 +1502,8 @@ static cudaError_t launch_kind(const CUtensorMap& a0, const CUtensorMap& a1,
   const CUtensorMap& m0 = o0 ? *o0 : a0;
   const CUtensorMap& m1 = o1 ? *o1 : m0;
   const CUtensorMap& m2 = o2 ? *o2 : m0;
+  const CUtensorMap& mb2 = b2 ? *b2 : b0;
+  const CUtensorMap& m3 = o3 ? *o3 : m0;
   if constexpr (PAIR) {
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute at[2];
@@ -1247,10 +1519,11 @@ static cudaError_t launch_kind(const CUtensorMap& a0, const CUtensorMap& a1,
     cfg.stream = s;
     cfg.attrs = at;
     cfg.numAttrs = pdl ? 2 : 1;
-    cudaLaunchKernelEx(&cfg, grouped_gemm_kernel<K, PAIR>, a0, a1, b0, b1, m0, m1, m2, args);
+    cudaLaunchKernelEx(&cfg, grouped_gemm_kernel<K, PAIR>, a0, a1, b0, b1, m0, m1, m2, mb2, m3,
+                       args);
   } else {
     launch_pdl(pdl, grouped_gemm_kernel<K, PAIR>, dim3((unsigned)grid), dim3(kThreads), kSmemBytes,
-               s, a0, a1, b0, b1, m0, m1, m2, args);
+               s, a0, a1, b0, b1, m0, m1, m2, mb2, m3, args);
   }
   note_launches(1);
   if constexpr (!Tr<K>::dense) timer_after(Tr<K>::kernel_id, s);
@@ -1432,6 +1705,48 @@ cudaError_t launch_down_fwd(const GroupedDims& g, const moe_bf16* A, const moe_b
                                             nullptr, nullptr, pdl);
   return launch_kind<Kind::DownFwd, false>(a0, a0, b0, b0, a, mgrouped_tiles_upper(g, g.d, 256), s,
                                            &o0, nullptr, nullptr, pdl);
+}
+
+// The fused expert forward's counts: one per m-tile of the tile table.
+size_t fused_fwd_ws_bytes(int64_t R_cap, int E) {
+  return (size_t)4 * (size_t)((R_cap + BM - 1) / BM + E + 1);
+}
+
+// The fused expert forward (one persistent launch, FusedFwd): gate/up tiles
+// gather their rows of x by TMA and store A = act(G, U); down tiles, once
+// every gate/up tile of their rows has published its part of A, store
+// Yp = score * (A . W_down[e]) in fp32. One CTA per SM and a grid of at most
+// the SMs, so every CTA is resident while others wait for it.
+cudaError_t launch_fused_fwd(const GroupedDims& g, const moe_bf16* x, int64_t T, int k,
+                             const moe_bf16* w_gate, const moe_bf16* w_up,
+                             const moe_bf16* w_down, const float* pair_w, moe_bf16* A, float* yp,
+                             int* ready, const ActParams& act, int* status, cudaStream_t s) {
+  CUtensorMap aa, b0, b1, b2, o2, o3;
+  if (!g.src_pair || T <= 0) return cudaErrorInvalidValue;
+  if (!map2d(&aa, A, g.f, g.R_cap, BM) ||
+      !map3d(&b0, w_gate, g.f, g.d, g.E, BK) || !map3d(&b1, w_up, g.f, g.d, g.E, BK) ||
+      !map3d(&b2, w_down, g.d, g.f, g.E, BK) || !map2d_out(&o2, A, g.f, g.R_cap) ||
+      !map2d_out(&o3, yp, g.d, g.R_cap, 4))
+    return cudaErrorInvalidValue;
+  GemmArgs a = base_args(g, status);
+  a.N = g.f;
+  a.nk_seg = (g.d + BK - 1) / BK;
+  a.N2 = g.d;
+  a.nk2 = (g.f + BK - 1) / BK;
+  a.out2 = A;
+  a.out3 = yp;
+  a.ready = ready;
+  a.T_tok = T;
+  a.ktop = k;
+  a.p_routed = g.P_routed;
+  a.pair_w = pair_w;
+  a.xsrc = x;
+  a.act = Act{act.limit, act.alpha, act.c};
+  cudaError_t e = cudaMemsetAsync(ready, 0, fused_fwd_ws_bytes(g.R_cap, g.E), s);
+  if (e != cudaSuccess) return e;
+  const int64_t tiles = mgrouped_tiles_upper(g, g.f, 128) + mgrouped_tiles_upper(g, g.d, 256);
+  return launch_kind<Kind::FusedFwd, false>(aa, aa, b0, b1, a, tiles, s, nullptr, nullptr, &o2,
+                                            false, &b2, &o3);
 }
 
 // Partial slots per row of the down dgrad's top-k weight gradient: one per

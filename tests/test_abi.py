@@ -86,6 +86,18 @@ def test_host_argument_checks(lib):
     # a clamped SwiGLU needs a positive limit
     bad = L.Swiglu(0.0, 1.702, 1.0)
     assert lib.moe_expert_fwd(P, P, None, ctypes.addressof(bad), 4, 2, 4, 0, 8, 16, cap, P, P, P, P, P, P, P, None) == L.MOE_ERR_ARG
+    # fused expert forward: T = 0 does nothing; a missing map, a short
+    # workspace, f not a multiple of 8
+    wsf = lib.moe_expert_fwd_fused_workspace_size(cap, 4, 0)
+    assert wsf >= 4 * (cap // 128 + 4)
+    assert lib.moe_expert_fwd_fused(None, None, None, None, None, 0, 2, 4, 0, 8, 16, cap,
+                                    None, None, None, None, None, None, 0, None) == L.MOE_OK
+    assert lib.moe_expert_fwd_fused(P, None, P, P, None, 4, 2, 4, 0, 8, 16, cap, P, P, P, P,
+                                    P, P, wsf, None) == L.MOE_ERR_ARG
+    assert lib.moe_expert_fwd_fused(P, P, P, P, None, 4, 2, 4, 0, 8, 16, cap, P, P, P, P,
+                                    P, P, wsf - 1, None) == L.MOE_ERR_ARG
+    assert lib.moe_expert_fwd_fused(P, P, P, P, None, 4, 2, 4, 0, 8, 12, cap, P, P, P, P,
+                                    P, P, wsf, None) == L.MOE_ERR_UNSUPPORTED
     # expert backward: a missing row buffer (the gathered dY rows)
     wse = lib.moe_expert_bwd_workspace_size(cap, 16)
     assert wse >= cap * 2 * 4                  # at least one n-tile's two partials per row
@@ -122,4 +134,4 @@ def test_host_argument_checks(lib):
     assert dec(0, 128, 64, 4, 2, x=None) == L.MOE_OK      # nothing to do
     # timer: bad kernel id
     assert lib.moe_timer_start(0, 4) == L.MOE_ERR_ARG
-    assert lib.moe_timer_start(L.KERNELS["decode"] + 1, 4) == L.MOE_ERR_ARG
+    assert lib.moe_timer_start(max(L.KERNELS.values()) + 1, 4) == L.MOE_ERR_ARG
