@@ -133,9 +133,7 @@ int moe_route(const moe_bf16* x, const float* w_router, const float* bias,
  *  src_pair [R_cap] int32 out: pair held by row r, -1 for padding and for
  *           rows past offsets[E]
  *  xp       [R_cap, d] bf16 out: xp[r] = x[src_pair[r] / k]; padding rows
- *           inside groups are 0; rows >= offsets[E] are not written.
- *           NULL: the maps only (x may then be NULL too), for
- *           moe_expert_fwd_fused, which reads x itself
+ *           inside groups are 0; rows >= offsets[E] are not written
  *  align    power of two in [16, 256] (the grouped GEMMs consume rows in
  *           steps of 16, one bf16 MMA K-step, so every group must be a
  *           multiple of 16 rows)
@@ -211,25 +209,23 @@ int moe_expert_fwd(const moe_bf16* xp, const int64_t* offsets, const float* row_
                    moe_stream_t stream);
 
 /* ------------------------------------------------------------------------
- * moe_expert_fwd_fused — the expert layer's forward in one persistent launch
- * (inference: nothing is kept for a backward).
+ * moe_expert_fwd_fused — the expert GEMMs of the forward in one persistent
+ * launch (inference: G and U are not kept for a backward).
  * [PRL "FP8 Mega MoE", "dispatch.type = mega_moe"] the routed-expert layer as
  * one fused op in expert-major order; [PRL "Single-pass DeepEP local
  * layout"] the score-weighted fp32 partials a gather-sum adds up.
- * Per expert e on its rows r of the layout (moe_permute's maps; xp is not
- * needed): the gate/up tiles read x[token(r)] directly (TMA row gathers:
- * token(r) = p / k for a routed pair p = src_pair[r], (p - T*k) mod T for a
- * shared one; zeros for padding), G = x.W_gate[e], U = x.W_up[e] in fp32,
- * A = act(G, U) rounded to bf16 into `a`; the down tiles of a 128-row tile
- * wait (bounded, on a count in ws) until every gate/up tile of those rows
- * has stored its part of A, then Yp = w(r) * (A.W_down[e]) in fp32, w(r) the
- * pair's score topk_w[p] (1 for a shared expert's pair, 0 for padding).
+ * Per expert e on its rows r of the layout: G = Xp.W_gate[e], U = Xp.W_up[e]
+ * in fp32 (tensor memory only), A = act(G, U) rounded to bf16 into `a`; the
+ * down tiles of a 128-row tile (256 in a CTA pair) wait (bounded, on a count
+ * in ws) until every gate/up tile of those rows has stored its part of A,
+ * then Yp = w(r) * (A.W_down[e]) in fp32, w(r) the pair's score topk_w[p]
+ * for p = src_pair[r] (1 for a shared expert's pair, 0 for padding).
  * y = moe_combine(yp, dst_row, NULL, ...): the same gather-sum, weights 1.
- * Results equal moe_expert_fwd's A and, up to one fp32 rounding of the
- * product with the score, its Yp times the score.
+ * A equals moe_expert_fwd's; Yp is its Yp times the score, rounded once.
  *
- *  x [T, d] bf16; src_pair [R_cap] int32, offsets [E+S+1] int64 (moe_permute)
- *  topk_w [T, k] fp32 (moe_route);  act: as in moe_expert_fwd
+ *  xp [R_cap, d] bf16, src_pair [R_cap] int32, offsets [E+S+1] int64
+ *     (moe_permute);  topk_w [T, k] fp32 (moe_route);  act: as in
+ *     moe_expert_fwd;  T, k, E, S as in moe_expert_fwd
  *  w_gate, w_up [E+S, d, f] bf16;  w_down [E+S, f, d] bf16
  *  a [R_cap, f] bf16 out;  yp [R_cap, d] fp32 out (rows of every group;
  *     rows >= offsets[E+S] are not written)
@@ -240,7 +236,7 @@ int moe_expert_fwd(const moe_bf16* xp, const int64_t* offsets, const float* row_
  * (1.5 s) makes the call report MOE_ERR_DEVICE_TIMEOUT instead of hanging.
  * Limits: d, f multiples of 8; E + S <= 1024; T >= 1 (T = 0 does nothing).
  * ------------------------------------------------------------------------ */
-int moe_expert_fwd_fused(const moe_bf16* x, const int32_t* src_pair, const int64_t* offsets,
+int moe_expert_fwd_fused(const moe_bf16* xp, const int32_t* src_pair, const int64_t* offsets,
                          const float* topk_w, const moe_swiglu* act, int64_t T, int k, int E,
                          int S, int d, int f, int64_t R_cap, const moe_bf16* w_gate,
                          const moe_bf16* w_up, const moe_bf16* w_down, moe_bf16* a, float* yp,

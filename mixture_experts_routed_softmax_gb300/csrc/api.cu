@@ -206,8 +206,7 @@ int moe_permute(const int32_t* topk_idx, int64_t T, int k, int E, int S, int ali
                 const moe_bf16* x, int d, int64_t R_cap, int32_t* counts, int64_t* offsets,
                 int32_t* dst_row, int32_t* src_pair, moe_bf16* xp, void* ws, size_t ws_bytes,
                 moe_stream_t stream) {
-  // xp == NULL: the maps only (the fused forward gathers the rows itself)
-  if (!counts || !offsets || !src_pair || (T > 0 && (!topk_idx || !dst_row || (xp && !x))))
+  if (!counts || !offsets || !src_pair || !xp || (T > 0 && (!topk_idx || !x || !dst_row)))
     return MOE_ERR_ARG;
   if (T < 0 || k <= 0 || E <= 0 || d <= 0 || k > E || S < 0) return MOE_ERR_ARG;
   if (!is_pow2(align) || align < 16 || align > 256) return MOE_ERR_ARG;
@@ -263,14 +262,14 @@ size_t moe_expert_fwd_fused_workspace_size(int64_t R_cap, int E, int S) {
   return fused_fwd_ws_bytes(R_cap, E + S);
 }
 
-int moe_expert_fwd_fused(const moe_bf16* x, const int32_t* src_pair, const int64_t* offsets,
+int moe_expert_fwd_fused(const moe_bf16* xp, const int32_t* src_pair, const int64_t* offsets,
                          const float* topk_w, const moe_swiglu* act, int64_t T, int k, int E,
                          int S, int d, int f, int64_t R_cap, const moe_bf16* w_gate,
                          const moe_bf16* w_up, const moe_bf16* w_down, moe_bf16* a, float* yp,
                          void* ws, size_t ws_bytes, moe_stream_t stream) {
   if (T < 0 || k <= 0 || k > E || S < 0) return MOE_ERR_ARG;
   if (T == 0) return MOE_OK;
-  if (!x || !src_pair || !offsets || !topk_w || !w_gate || !w_up || !w_down || !a || !yp || !ws)
+  if (!xp || !src_pair || !offsets || !topk_w || !w_gate || !w_up || !w_down || !a || !yp || !ws)
     return MOE_ERR_ARG;
   ActParams ap;
   if (!act_of(act, &ap)) return MOE_ERR_ARG;
@@ -278,7 +277,7 @@ int moe_expert_fwd_fused(const moe_bf16* x, const int32_t* src_pair, const int64
   if (rc) return rc;
   if (R_cap < T * (k + S)) return MOE_ERR_CAPACITY;
   if (ws_bytes < fused_fwd_ws_bytes(R_cap, E + S)) return MOE_ERR_ARG;
-  for (const void* p : {(const void*)x, (const void*)w_gate, (const void*)w_up,
+  for (const void* p : {(const void*)xp, (const void*)w_gate, (const void*)w_up,
                         (const void*)w_down, (const void*)a, (const void*)yp, (const void*)ws})
     if (!aligned16(p)) return MOE_ERR_ARG;
   int* st = device_status_ptr();
@@ -287,7 +286,7 @@ int moe_expert_fwd_fused(const moe_bf16* x, const int32_t* src_pair, const int64
   GroupedDims gd{offsets, E + S, d, f, R_cap, T * (k + S)};
   gd.P_routed = T * k;
   gd.src_pair = src_pair;
-  return cuda_code(launch_fused_fwd(gd, x, T, k, w_gate, w_up, w_down, topk_w, a, yp,
+  return cuda_code(launch_fused_fwd(gd, xp, w_gate, w_up, w_down, topk_w, a, yp,
                                     static_cast<int*>(ws), ap, st, s));
 }
 

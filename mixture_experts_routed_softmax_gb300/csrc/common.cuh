@@ -234,20 +234,6 @@ __device__ __forceinline__ void bulk_wait_all() {
 __device__ __forceinline__ void fence_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
-// 16-byte asynchronous copy global -> shared (cp.async, L2 only); zeros and
-// no read when !in. cp_async_arrive_noinc: the mbarrier counts one arrival of
-// this thread once all its earlier cp.async copies have landed.
-__device__ __forceinline__ void cp_async16_zfill(uint32_t dst, const void* src, bool in) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
-               "r"(in ? 16 : 0)
-               : "memory");
-}
-__device__ __forceinline__ void cp_async_arrive_noinc(uint32_t bar) {
-  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
-}
-__device__ __forceinline__ void cp_async_wait_all() {
-  asm volatile("cp.async.wait_all;" ::: "memory");
-}
 // the same between the proxies for global memory: TMA stores that have
 // completed before a generic release, and TMA loads after a generic acquire
 __device__ __forceinline__ void fence_async_global() {

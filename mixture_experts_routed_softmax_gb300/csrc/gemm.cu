@@ -181,15 +181,12 @@ struct GemmArgs {
   int* status;
   // FusedFwd: N = f (gate/up tiles, nk_seg k-steps over d), N2 = d (down
   // tiles, nk2 k-steps over f); out2 = A (bf16), out3 = Yp (fp32, scaled by
-  // each row's score via src_pair / pair_w); tokens T_tok with ktop routed
-  // slots each; ready[m-tile] counts the gate/up tiles done
+  // each row's score via src_pair / pair_w); ready[m-tile] counts the
+  // gate/up tiles done
   int N2;
   int nk2;
   void* out3;
   int* ready;
-  int64_t T_tok;
-  int ktop;
-  const moe_bf16* xsrc;   // FusedFwd: x [T_tok, N2], the rows the gate/up tiles gather
 };
 
 struct TileInfo {
@@ -475,9 +472,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
-      // the fused forward: the producer's lane 0 (with the TMA bytes) and
-      // each of its 32 lanes once its copies of the stage have landed
-      mbar_init(full_bar(s), T::fused ? 33 : 1);
+      mbar_init(full_bar(s), 1);
       mbar_init(empty_bar(s), 1);
     }
     for (int b = 0; b < 2; ++b) {
@@ -587,102 +582,86 @@ __global__ void __launch_bounds__(kThreads, 1)
   static_assert(kStages * kStageBytes <= G::ring && kStageBytes % 8192 == 0, "ring layout");
 
   if (warp == 0 && T::fused) {
-    // ------------------------------------------- producer (fused forward) --
-    // The whole warp. Gate/up tiles gather their A rows from x: lane
-    // (8 q + c) copies 16-byte chunk c of rows q, q + 4, ..., q + 124 with
-    // cp.async into the 128-byte-swizzled tile (chunk c of row r at
-    // 16 (c ^ (r mod 8))), each lane's copies of a stage completing on the
-    // stage's full barrier; a row's token is its pair's (routed: p / k,
-    // shared: (p - T k) mod T), and padding rows and rows past the group are
-    // zero-filled (no read). Down tiles read A from the activations buffer
-    // by TMA once every gate/up tile of their rows has published it (a
-    // bounded wait on the m-tile's count). B (the weights) by TMA.
-    const uint64_t pol_w = l2_evict_last();
-    const int nN1 = nN;
-    const int q4 = lane >> 3, ch = lane & 7;
-    int stage = 0;
-    uint32_t phase = 0;
-    int fills = 0;
-    bool ok = true;
-    for (int tile = GEMM_CID; tile < total && ok; tile += GEMM_NCL) {
-      TileInfo ti;
-      decode_tile<K, PAIR>(tile, args, tstart, nN, 0, ti);
-      int tok[32];
-#pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        const int64_t r = ti.m0 + q4 + 4 * j;
-        int t = -1;
-        if (ti.ph == 0 && r < ti.row_end) {
-          const int32_t p = args.src_pair[r];
-          if (p >= 0)
-            t = p < args.p_routed ? (int)(p / args.ktop)
-                                  : (int)((p - args.p_routed) % args.T_tok);
-        }
-        tok[j] = t;
-      }
-      if (ti.ph == 1) {
-        int rdy = 1;
-        if (lane == 0) rdy = wait_count(args.ready + ti.mt, nN1, s_abort, args.status) ? 1 : 0;
-        if (!__shfl_sync(0xFFFFFFFFu, rdy, 0)) {
-          ok = false;
+    if (lane == 0) {
+      // ----------------------------------------- producer (fused forward) --
+      // Gate/up tiles: A from the gathered rows xp, B = W_gate and W_up
+      // (in a pair: rank 0 W_gate, rank 1 W_up). Down tiles: A from the
+      // activations buffer once every gate/up tile of their rows has
+      // published it (a bounded wait on the m-tile's count), B = W_down (in
+      // a pair each CTA half of the 256 columns). All by TMA; in a pair each
+      // CTA loads its own 128 rows and its half of B for rank 0's barrier.
+      const uint64_t pol_w = l2_evict_last();
+      const int nN1 = nN;
+      int stage = 0;
+      uint32_t phase = 0;
+      int fills = 0;
+      bool ok = true;
+      for (int tile = GEMM_CID; tile < total && ok; tile += GEMM_NCL) {
+        TileInfo ti;
+        decode_tile<K, PAIR>(tile, args, tstart, nN, rank, ti);
+        if (ti.ph == 1 &&
+            !wait_count(args.ready + ti.mt, nN1 * (PAIR ? 2 : 1), s_abort, args.status))
           break;
-        }
-      }
-      for (int ks = 0; ks < ti.nk; ++ks) {
-        int go = 1;
-        if (lane == 0)
-          go = mbar_wait_bounded(empty_bar(stage), phase ^ 1u, s_abort, args.status) ? 1 : 0;
-        if (!__shfl_sync(0xFFFFFFFFu, go, 0)) {
-          ok = false;
-          break;
-        }
-        const uint32_t fb = full_bar(stage);
-        const uint32_t sA = s_base + stage * kStageBytes;
-        const uint32_t sB0 = sA + kABytes;
-        const int kk = ks * BK;
-        if (ti.ph == 0) {
-          if (lane == 0) {
-            mbar_arrive_expect_tx(fb, tx_bytes - (uint32_t)kABytes);
+        // rank 1's half of a group's last pair tile may lie past the group:
+        // its rows then come from past the buffer (zeros, no traffic)
+        const int arow = (PAIR && ti.m0 >= ti.row_end) ? (int)args.R_cap : (int)ti.m0;
+        const void* mA = ti.ph ? (const void*)&mapA1 : (const void*)&mapA0;
+        for (int ks = 0; ks < ti.nk; ++ks) {
+          if (!mbar_wait_bounded(empty_bar(stage), phase ^ 1u, s_abort, args.status)) {
+            ok = false;
+            break;
+          }
+          const uint32_t fb = full_bar(stage);
+          const uint32_t sA = s_base + stage * kStageBytes;
+          const uint32_t sB0 = sA + kABytes;
+          const int kk = ks * BK;
+          if constexpr (PAIR) {
+            const uint32_t fbl = rank0 ? fb : mapa_shared(fb, 0);
+            if (rank0) mbar_arrive_expect_tx(fb, 2u * tx_bytes);
+            tma_load_2d_pair(sA, mA, fbl, kk, arow);
+            const void* mB = ti.ph ? (const void*)&mapB2
+                                   : (rank ? (const void*)&mapB1 : (const void*)&mapB0);
+            const int bcol = ti.ph ? ti.n0 + 128 * rank : ti.n0;
 #pragma unroll
-            for (int j = 0; j < 2; ++j) {
-              tma_load_3d_hint(sB0 + j * (BK * 128), &mapB0, fb, ti.n0 + 64 * j, kk, ti.e, pol_w);
-              tma_load_3d_hint(sB0 + kBBytes + j * (BK * 128), &mapB1, fb, ti.n0 + 64 * j, kk,
-                               ti.e, pol_w);
+            for (int j = 0; j < 2; ++j)
+              tma_load_3d_pair(sB0 + j * (BK * 128), mB, fbl, bcol + 64 * j, kk, ti.e, pol_w);
+          } else {
+            mbar_arrive_expect_tx(fb, tx_bytes);
+            tma_load_2d(sA, mA, fb, kk, arow);
+            if (ti.ph == 0) {
+#pragma unroll
+              for (int j = 0; j < 2; ++j) {
+                tma_load_3d_hint(sB0 + j * (BK * 128), &mapB0, fb, ti.n0 + 64 * j, kk, ti.e,
+                                 pol_w);
+                tma_load_3d_hint(sB0 + kBBytes + j * (BK * 128), &mapB1, fb, ti.n0 + 64 * j, kk,
+                                 ti.e, pol_w);
+              }
+            } else {
+#pragma unroll
+              for (int j = 0; j < 4; ++j)
+                tma_load_3d_hint(sB0 + j * (BK * 128), &mapB2, fb, ti.n0 + 64 * j, kk, ti.e,
+                                 pol_w);
             }
           }
-          const int col = kk + 8 * ch;
-          const bool col_ok = col < args.N2;
-#pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            const int r = q4 + 4 * j;
-            const bool in = col_ok && tok[j] >= 0;
-            const moe_bf16* src = in ? args.xsrc + (int64_t)tok[j] * args.N2 + col : args.xsrc;
-            cp_async16_zfill(sA + (uint32_t)r * 128u + (uint32_t)((ch ^ (r & 7)) << 4), src, in);
-          }
-          cp_async_arrive_noinc(fb);
-        } else {
-          if (lane == 0) {
-            mbar_arrive_expect_tx(fb, tx_bytes);
-            tma_load_2d(sA, &mapA1, fb, kk, (int)ti.m0);
-#pragma unroll
-            for (int j = 0; j < 4; ++j)
-              tma_load_3d_hint(sB0 + j * (BK * 128), &mapB2, fb, ti.n0 + 64 * j, kk, ti.e, pol_w);
-          }
-          mbar_arrive(fb);
+          ++fills;
+          if (++stage == kStages) { stage = 0; phase ^= 1u; }
         }
-        ++fills;
-        if (++stage == kStages) { stage = 0; phase ^= 1u; }
       }
-    }
-    cp_async_wait_all();   // this lane's copies land before shared memory goes away
-    if (lane == 0 && *s_abort) {
-      // let the copies already issued land before the CTA's shared memory goes away
-      const int outstanding = fills < kStages ? fills : kStages;
-      int st = stage;
-      uint32_t ph = phase;
-      for (int i = 0; i < outstanding; ++i) {
-        if (--st < 0) { st = kStages - 1; ph ^= 1u; }
-        drain_wait(full_bar(st), ph, args.status);
+      if (*s_abort) {
+        // let the copies already issued land before the CTA's shared memory goes away
+        if (!PAIR || rank0) {
+          const int outstanding = fills < kStages ? fills : kStages;
+          int st = stage;
+          uint32_t ph = phase;
+          for (int i = 0; i < outstanding; ++i) {
+            if (--st < 0) { st = kStages - 1; ph ^= 1u; }
+            drain_wait(full_bar(st), ph, args.status);
+          }
+        } else {
+          const uint64_t t0 = global_ns();
+          while (global_ns() - t0 < 200000ull) {
+          }
+        }
       }
     }
   } else if (warp == 0) {
@@ -858,9 +837,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           tc_fence_after();
-          // the fused forward's gathered A tiles were written by cp.async (the
-          // generic proxy); the MMA reads them through the async proxy
-          if constexpr (T::fused) fence_async_smem();
           const uint32_t sA = s_base + stage * kStageBytes;
           const uint32_t sB0 = sA + kABytes;
           int nsub = BK / 16;
@@ -1713,17 +1689,18 @@ size_t fused_fwd_ws_bytes(int64_t R_cap, int E) {
 }
 
 // The fused expert forward (one persistent launch, FusedFwd): gate/up tiles
-// gather their rows of x by TMA and store A = act(G, U); down tiles, once
+// store A = act(G, U) (G and U stay in tensor memory); down tiles, once
 // every gate/up tile of their rows has published its part of A, store
-// Yp = score * (A . W_down[e]) in fp32. One CTA per SM and a grid of at most
-// the SMs, so every CTA is resident while others wait for it.
-cudaError_t launch_fused_fwd(const GroupedDims& g, const moe_bf16* x, int64_t T, int k,
-                             const moe_bf16* w_gate, const moe_bf16* w_up,
-                             const moe_bf16* w_down, const float* pair_w, moe_bf16* A, float* yp,
-                             int* ready, const ActParams& act, int* status, cudaStream_t s) {
-  CUtensorMap aa, b0, b1, b2, o2, o3;
-  if (!g.src_pair || T <= 0) return cudaErrorInvalidValue;
-  if (!map2d(&aa, A, g.f, g.R_cap, BM) ||
+// Yp = score * (A . W_down[e]) in fp32. One CTA (or pair) per SM (pair of
+// SMs) and a grid of at most that many, so every CTA is resident while
+// others wait for it.
+cudaError_t launch_fused_fwd(const GroupedDims& g, const moe_bf16* xp, const moe_bf16* w_gate,
+                             const moe_bf16* w_up, const moe_bf16* w_down, const float* pair_w,
+                             moe_bf16* A, float* yp, int* ready, const ActParams& act,
+                             int* status, cudaStream_t s) {
+  CUtensorMap ax, aa, b0, b1, b2, o2, o3;
+  if (!g.src_pair) return cudaErrorInvalidValue;
+  if (!map2d(&ax, xp, g.d, g.R_cap, BM) || !map2d(&aa, A, g.f, g.R_cap, BM) ||
       !map3d(&b0, w_gate, g.f, g.d, g.E, BK) || !map3d(&b1, w_up, g.f, g.d, g.E, BK) ||
       !map3d(&b2, w_down, g.d, g.f, g.E, BK) || !map2d_out(&o2, A, g.f, g.R_cap) ||
       !map2d_out(&o3, yp, g.d, g.R_cap, 4))
@@ -1736,16 +1713,20 @@ cudaError_t launch_fused_fwd(const GroupedDims& g, const moe_bf16* x, int64_t T,
   a.out2 = A;
   a.out3 = yp;
   a.ready = ready;
-  a.T_tok = T;
-  a.ktop = k;
   a.p_routed = g.P_routed;
   a.pair_w = pair_w;
-  a.xsrc = x;
   a.act = Act{act.limit, act.alpha, act.c};
   cudaError_t e = cudaMemsetAsync(ready, 0, fused_fwd_ws_bytes(g.R_cap, g.E), s);
   if (e != cudaSuccess) return e;
+  // CTA pairs from 512 rows per expert on average, as the five-call forward
+  if (pairs_mgrouped(g, 512)) {
+    const int64_t tiles = mgrouped_tiles_upper(g, g.f, 128, 2 * BM) +
+                          mgrouped_tiles_upper(g, g.d, 256, 2 * BM);
+    return launch_kind<Kind::FusedFwd, true>(ax, aa, b0, b1, a, tiles, s, nullptr, nullptr, &o2,
+                                             false, &b2, &o3);
+  }
   const int64_t tiles = mgrouped_tiles_upper(g, g.f, 128) + mgrouped_tiles_upper(g, g.d, 256);
-  return launch_kind<Kind::FusedFwd, false>(aa, aa, b0, b1, a, tiles, s, nullptr, nullptr, &o2,
+  return launch_kind<Kind::FusedFwd, false>(ax, aa, b0, b1, a, tiles, s, nullptr, nullptr, &o2,
                                             false, &b2, &o3);
 }
 

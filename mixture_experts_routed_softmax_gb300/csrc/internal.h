@@ -99,10 +99,10 @@ cudaError_t launch_gateup_fwd(const GroupedDims& g, const moe_bf16* xp, const mo
 cudaError_t launch_down_fwd(const GroupedDims& g, const moe_bf16* A, const moe_bf16* w_down,
                             const float* row_w, float* yp, int* status, cudaStream_t s);
 size_t fused_fwd_ws_bytes(int64_t R_cap, int E);
-cudaError_t launch_fused_fwd(const GroupedDims& g, const moe_bf16* x, int64_t T, int k,
-                             const moe_bf16* w_gate, const moe_bf16* w_up,
-                             const moe_bf16* w_down, const float* pair_w, moe_bf16* A, float* yp,
-                             int* ready, const ActParams& act, int* status, cudaStream_t s);
+cudaError_t launch_fused_fwd(const GroupedDims& g, const moe_bf16* xp, const moe_bf16* w_gate,
+                             const moe_bf16* w_up, const moe_bf16* w_down, const float* pair_w,
+                             moe_bf16* A, float* yp, int* ready, const ActParams& act,
+                             int* status, cudaStream_t s);
 int down_dgrad_dtw_slots(int f);
 cudaError_t launch_down_dgrad(const GroupedDims& g, const moe_bf16* dyg, const float* pair_w,
                               const moe_bf16* w_down, const float* G, const float* U,

@@ -15,8 +15,7 @@
 //           block's base), the padded sizes ceil(n_e/align)*align and their
 //           exclusive scan over experts (the 64-bit offsets).
 //   scatter dst_row[p] = offsets[e] + block base + rank; src_pair[dst] = p.
-//   gather  xp[r] = x[src_pair[r] / k] for real rows, zeros for padding rows
-//           (with xp NULL only the maps of padding and shared rows).
+//   gather  xp[r] = x[src_pair[r] / k] for real rows, zeros for padding rows.
 // Pair p's rank inside its expert is therefore its rank in ascending p.
 // Shared experts (S of them, every token's copy with weight 1: prime-rl PR
 // #3885, §Changes, "Fused FP8 shared expert") follow the routed groups: group
@@ -281,7 +280,6 @@ __global__ void __launch_bounds__(256) permute_gather_kernel(
         dst_row[p] = (int32_t)r;
       }
     }
-    if (!xp) return;   // the maps only
     uint4* dst = reinterpret_cast<uint4*>(xp + r * d);
     const uint4* src = reinterpret_cast<const uint4*>(x + t * d);
     // four 16-byte pieces in flight per lane
@@ -296,7 +294,6 @@ __global__ void __launch_bounds__(256) permute_gather_kernel(
     }
   } else {
     if (lane == 0) src_pair[r] = -1;
-    if (!xp) return;
     uint4* dst = reinterpret_cast<uint4*>(xp + r * d);
     for (int v = lane; v < nv; v += 32) dst[v] = make_uint4(0u, 0u, 0u, 0u);
   }

@@ -216,8 +216,8 @@ class MoELayer:
 
     # ------------------------------------------------------ fused forward --
     def fused_buffers(self, T: int) -> Buffers:
-        """Buffers for forward_fused: routing, the maps, A, the scored Yp, y and
-        the fused forward's counts (no xp, G or U: nothing is kept for a backward)."""
+        """Buffers for forward_fused: routing, the layout, A, the scored Yp, y
+        and the fused forward's counts (no G or U: nothing is kept for a backward)."""
         E, d, f, k, S = self.E, self.d, self.f, self.k, self.S
         R = self.row_capacity(T)
         kw = dict(device=self.device)
@@ -232,7 +232,7 @@ class MoELayer:
             offsets=torch.empty(E + S + 1, dtype=torch.int64, **kw),
             dst_row=torch.empty(T * (k + S), dtype=torch.int32, **kw),
             src_pair=torch.empty(R, dtype=torch.int32, **kw),
-            xp=None, g=None, u=None,
+            xp=torch.empty(R, d, dtype=BF16, **kw), g=None, u=None,
             a=torch.empty(R, f, dtype=BF16, **kw),
             yp=torch.empty(R, d, dtype=torch.float32, **kw),
             y=torch.empty(T, d, dtype=BF16, **kw),
@@ -243,22 +243,21 @@ class MoELayer:
             ws_fused=torch.empty(max(ws_f, 256), dtype=torch.uint8, **kw),
         )
 
-    def expert_fwd_fused(self, x, b: Buffers, stream=None):
-        """The expert layer's forward in one launch (moe_expert_fwd_fused): A
-        into b.a and the scored rows into b.yp."""
-        _lib.call("moe_expert_fwd_fused", _p(x), _p(b.src_pair), _p(b.offsets), _p(b.topk_w),
+    def expert_fwd_fused(self, b: Buffers, stream=None):
+        """The expert GEMMs of the forward in one launch (moe_expert_fwd_fused):
+        A into b.a and the scored rows into b.yp."""
+        _lib.call("moe_expert_fwd_fused", _p(b.xp), _p(b.src_pair), _p(b.offsets), _p(b.topk_w),
                   self._act(), b.T, self.k, self.E, self.S, self.d, self.f, b.R_cap,
                   _p(self.w_gate), _p(self.w_up), _p(self.w_down), _p(b.a), _p(b.yp),
                   _p(b.ws_fused), b.ws_fused.numel(), _stream(stream))
 
     def forward_fused(self, x, b: Buffers, forced_idx=None, stream=None):
-        """y = layer(x) for inference, b from fused_buffers(T): route, the
-        permute's maps (no gather), the fused expert forward, and the
-        gather-sum of the already scored rows."""
+        """y = layer(x) for inference, b from fused_buffers(T): route, permute,
+        the fused expert GEMMs, and the gather-sum of the already scored rows."""
         b.x = x
         self.route(x, b, forced_idx, stream)
-        self.permute(None, b, None, stream)
-        self.expert_fwd_fused(x, b, stream)
+        self.permute(x, b, None, stream)
+        self.expert_fwd_fused(b, stream)
         self.combine(b.yp, b, b.y, False, stream)
         return b.y
 

@@ -1,10 +1,10 @@
 """Parity of the fused expert forward (moe_expert_fwd_fused: one persistent
-launch that gathers each row's token from x by TMA, runs gate/up and the
-activation, then the down projection with the pair's score) with the float64
-oracle, through the C ABI.
+launch that runs gate/up and the activation, then the down projection with
+the pair's score, the down tiles waiting on the gate/up tiles of their rows)
+with the float64 oracle, through the C ABI.
 
-The permute's maps (xp not written) are exact; A and the scored Yp rows of
-every pair within the rules of tests/harness.py (padding rows exactly 0);
+The permute's maps are exact; A and the scored Yp rows of every pair within
+the rules of tests/harness.py (padding rows exactly 0);
 y within 2e-2 x RMS plus bf16's half-ulp. Cases: several tiles in every
 dimension, ragged d and f, skewed loads with empty experts, one token, wide
 and maximal E with top-32, shared experts with the clamped SwiGLU; at full
