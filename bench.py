@@ -17,8 +17,10 @@ With the default workload, the line also carries "configs": the
 Qwen3-30B-A3B-shaped layer, the small-M forward sweep (T = 128 ... 2048) and
 the fine-grained 512-expert layer, each timed in the same run (median step,
 whole-step roofline, every expert GEMM against its bound, the benchmark spec's
-targets, its own clock record). ms_per_step is the median of the timed
-steps; value = tokens / median step.
+targets, its own clock record) and, under "forward", its inference forward
+timed two ways: the five calls and the fused expert GEMMs
+(moe_expert_fwd_fused), each with its bytes and roofline fraction.
+ms_per_step is the median of the timed steps; value = tokens / median step.
 
 --impl reference times the float64 CPU oracle (the deliberately slow,
 obviously correct definition) on a bounded sample of the same workload on
@@ -330,6 +332,45 @@ def profile_kernels(step, kernels, lib_mod):
     return per_kernel
 
 
+def forward_compare(layer, wl, x, stream, flush_buf, steps, shape, peaks):
+    """The inference forward two ways on the same inputs: the five calls
+    (route, permute, gate/up, down, combine; G and U kept for a backward)
+    and the fused expert GEMMs (moe_expert_fwd_fused: one persistent launch,
+    G and U never leave tensor memory); median of `steps` each, with their
+    algorithmic bytes and whole-forward roofline fractions."""
+    from mixture_experts_routed_softmax_gb300 import accounting
+    b5 = layer.buffers(wl.T, backward=False)
+    bf = layer.fused_buffers(wl.T)
+
+    def five():
+        layer.forward(x, b5)
+
+    def fused():
+        layer.forward_fused(x, bf)
+
+    for _ in range(3):
+        five()
+        fused()
+    st = layer.status()
+    if st != 0:
+        raise RuntimeError(f"forward comparison: device status {st}")
+    out = {}
+    for nm, fn, costs in (("five_call", five, accounting.kernel_costs(shape, backward=False)),
+                          ("fused", fused, accounting.fused_forward_costs(shape))):
+        per, _ = time_steps(fn, steps, stream, flush_buf)
+        med = statistics.median(per)
+        F = sum(c[0] for c in costs.values())
+        B = sum(c[1] for c in costs.values())
+        t_roof = accounting.roofline_seconds(F, B, peaks["bf16_tflops"], peaks["hbm_gbs"])
+        out[nm] = {"ms": round(med, 4), "bytes": B, "roofline_frac": round(t_roof * 1e3 / med, 3)}
+    st = layer.status()
+    if st != 0:
+        raise RuntimeError(f"forward comparison: device status {st}")
+    out["fused_speedup"] = round(out["five_call"]["ms"] / out["fused"]["ms"], 3)
+    del b5, bf
+    return out
+
+
 def run_side(name, dev, local_rank, peaks, steps, warmup):
     """One of the other workloads, timed in the same run: median step, the
     whole-step roofline, every expert GEMM against its bound, the small-M
@@ -407,7 +448,9 @@ def run_side(name, dev, local_rank, peaks, steps, warmup):
             misses.append("weight_stream")
     out["targets"] = {"tensor_bound_gemm_frac": TARGET_TENSOR, "hbm_bound_frac": TARGET_HBM,
                       "met": not misses, "missed": misses}
-    del layer, b, inp
+    del b
+    out["forward"] = forward_compare(layer, wl, x, stream, flush_buf, steps, shape, peaks)
+    del layer, inp
     torch.cuda.empty_cache()
     return out
 

@@ -68,6 +68,20 @@ def kernel_costs(s: Shape, backward: bool = True) -> dict:
     return c
 
 
+def fused_forward_costs(s: Shape) -> dict:
+    """{kernel: (flops, bytes)} of the inference forward with the fused
+    expert GEMMs (moe_expert_fwd_fused): the router, top-k and permute as in
+    kernel_costs, one fused launch (Xp read, the three weight matrices of
+    each active expert, A written and read back, the scored Yp written; G
+    and U stay in tensor memory), and the combine of the scored rows."""
+    P, d, f = s.P, s.d, s.f
+    W1 = s.E_active * d * f * 2
+    c = kernel_costs(s, backward=False)
+    del c["gateup_fwd"], c["down_fwd"]
+    c["fused_fwd"] = (6 * P * d * f, P * d * 2 + 3 * W1 + 2 * P * f * 2 + P * d * 2)
+    return c
+
+
 def decode_costs(s: Shape) -> tuple[int, int]:
     """(flops, bytes) of the one-launch decode forward: the router and every
     pair's three expert products; x, W_r, logits, top-k, y and the three
