@@ -19,7 +19,9 @@ the fine-grained 512-expert layer, each timed in the same run (median step,
 whole-step roofline, every expert GEMM against its bound, the benchmark spec's
 targets, its own clock record) and, under "forward", its inference forward
 timed two ways: the five calls and the fused expert GEMMs
-(moe_expert_fwd_fused), each with its bytes and roofline fraction.
+(moe_expert_fwd_fused), each with its bytes and roofline fraction; and the
+decode workloads (1 and 8 tokens, forward) replayed as CUDA graphs, general
+path and one-launch forward, against their weight-streaming bound.
 ms_per_step is the median of the timed steps; value = tokens / median step.
 
 --impl reference times the float64 CPU oracle (the deliberately slow,
@@ -371,6 +373,61 @@ def forward_compare(layer, wl, x, stream, flush_buf, steps, shape, peaks):
     return out
 
 
+DECODE_SIDE = ["decode_T1", "decode_T8"]
+
+
+def run_decode_side(name, dev, peaks, steps):
+    """A decode workload (forward only, a few tokens), each step replayed as
+    one captured CUDA graph with L2 flushed between steps: the general path
+    (seven launches) and the one-launch decode forward, against the time the
+    active experts' weights take to stream at the measured HBM rate."""
+    import torch
+    import workloads
+    from mixture_experts_routed_softmax_gb300 import accounting
+    from mixture_experts_routed_softmax_gb300.layer import MoELayer
+
+    wl = workloads.CONFIGS[name]
+    inp = workloads.generate_device(wl, dev, with_dy=False)
+    layer = MoELayer(inp["w_router"], inp["bias"], inp["w_gate"], inp["w_up"], inp["w_down"],
+                     wl.k, wl.align)
+    x = inp["x"]
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush_buf = torch.empty(2 * l2, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+    out = {"workload": f"{wl.name}: {wl.note}", "T": wl.T, "d": wl.d, "f": wl.f, "E": wl.E,
+           "k": wl.k, "steps": steps, "l2": "flushed between steps", "graph": True}
+    for path, bufs, fwd in (("general", lambda: layer.buffers(wl.T, backward=False),
+                             layer.forward),
+                            ("one_launch", lambda: layer.decode_buffers(wl.T), layer.decode_fwd)):
+        b = bufs()
+        for _ in range(3):
+            fwd(x, b)
+        st = layer.status()
+        if st != 0:
+            raise RuntimeError(f"{name}/{path}: device status {st}")
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            fwd(x, b)
+        for _ in range(3):
+            g.replay()
+        per, _ = time_steps(g.replay, steps, stream, flush_buf)
+        if layer.status() != 0:
+            raise RuntimeError(f"{name}/{path}: device status")
+        out[path + "_us"] = round(statistics.median(per) * 1e3, 2)
+        if path == "general":
+            e_act = int(torch.unique(b.topk_idx).numel())
+    shape = accounting.Shape(T=wl.T, d=wl.d, f=wl.f, E=wl.E, k=wl.k, E_active=e_act)
+    fl, by = accounting.decode_costs(shape)
+    bound_us = by / (peaks["hbm_gbs"] * 1e9) * 1e6
+    best = min(out["general_us"], out["one_launch_us"])
+    out.update(E_active=e_act, weight_bound_us=round(bound_us, 2),
+               frac_of_bound=round(bound_us / best, 3),
+               path_auto="general" if out["general_us"] <= out["one_launch_us"] else "one_launch")
+    del layer, inp
+    torch.cuda.empty_cache()
+    return out
+
+
 def run_side(name, dev, local_rank, peaks, steps, warmup):
     """One of the other workloads, timed in the same run: median step, the
     whole-step roofline, every expert GEMM against its bound, the small-M
@@ -689,6 +746,8 @@ def run_ours(args, rank, world, local_rank):
         torch.cuda.empty_cache()
         out["configs"] = {n: run_side(n, dev, local_rank, peaks, args.side_steps, 3)
                           for n in SIDE_CONFIGS}
+        for n in DECODE_SIDE:
+            out["configs"][n] = run_decode_side(n, dev, peaks, 5 * args.side_steps)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:   # the oracle beside N = 1 only
         tokens = min(args.cpu_tokens, wl.T)
         secs = oracle_sample(inp, wl, tokens)

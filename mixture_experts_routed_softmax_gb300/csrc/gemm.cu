@@ -9,7 +9,7 @@
 // One persistent, warp-specialised kernel template serves all six GEMMs:
 //   warp 0      TMA producer: tiles of A and B into a shared-memory ring of
 //               as many stages as fit 192 KiB (4 of 48 KiB, 6 of 32 KiB; the
-//               down dgrad of a CTA pair keeps 4 and gives 64 KiB to its
+//               down dgrad of a CTA pair keeps 5 and gives 32 KiB to its
 //               epilogue's G/U loads)
 //   warp 1      MMA issuer: tcgen05.mma 128 x N x 16 (bf16 in, fp32 in tensor
 //               memory), two accumulator buffers so the epilogue of one tile
@@ -108,15 +108,16 @@ struct Tr {
 // The down dgrad of a CTA pair (half the B bytes per stage) gives the ring's
 // tail to its epilogue: gu_slots slots per epilogue warp, each 8 fp32 columns
 // of the warp's 32 rows of G and of U ([32 rows x 32 bytes] x 2, loaded by
-// TMA), so the saved activations arrive several slices ahead of use without
-// holding registers. A single CTA keeps its four 48 KiB stages and loads G
-// and U into registers.
+// TMA), so the saved activations arrive ahead of use without holding
+// registers (two slots and five 32 KiB stages measured faster than four and
+// four, or none and six). A single CTA keeps its four 48 KiB stages and loads
+// G and U into registers.
 template <Kind K, bool PAIR>
 struct Geo {
   using T = Tr<K>;
   static constexpr int b_bytes = (T::dual ? 2 : 1) * T::BN * BK * 2 / (PAIR ? 2 : 1);
   static constexpr int stage_bytes = kABytes + b_bytes;
-  static constexpr int gu_slots = (K == Kind::DownDgrad && PAIR) ? 4 : 0;
+  static constexpr int gu_slots = (K == Kind::DownDgrad && PAIR) ? 2 : 0;
   static constexpr int gu_slot_bytes = 2 * 32 * 32;
   static constexpr int gu_bytes = gu_slots * kEpiWarps * gu_slot_bytes;
   static constexpr int ring = kRingBytes - gu_bytes;
