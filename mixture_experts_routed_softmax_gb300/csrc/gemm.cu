@@ -52,7 +52,8 @@ enum class Kind {
   GateUpFwd, DownFwd, DownDgrad, GateUpDgrad, WgradDown, WgradGateUp, RouterLogits,
   RouterWgrad,      // dW_r partials = x^T . dl (dl's three bf16 parts side by side in N)
   GateUpFwdNarrow,  // GateUpFwd with 64-column tiles, for experts of at most ~128 rows
-  FusedFwd          // the fused expert forward: gather + gate/up + act, then down (below)
+  FusedFwd,         // the fused expert forward: gate/up + act, then down (below)
+  DownFwdNarrow     // DownFwd with 128-column tiles, for experts of at most ~128 rows
 };
 
 constexpr int BM = 128;            // tile rows (TMEM lanes)
@@ -74,10 +75,11 @@ struct Tr {
   // one group of M rows, fp32 output (split K: one partial per chunk)
   static constexpr bool dense = (K == Kind::RouterLogits || K == Kind::RouterWgrad);
   static constexpr bool a_mn = kgrouped || K == Kind::RouterWgrad;         // A is M-contiguous
-  static constexpr bool down_fwd = (K == Kind::DownFwd);
+  static constexpr bool down_fwd = (K == Kind::DownFwd || K == Kind::DownFwdNarrow);
   static constexpr bool narrow = (K == Kind::GateUpFwdNarrow);
+  static constexpr bool down_narrow = (K == Kind::DownFwdNarrow);
   static constexpr bool b_mn = (gateup_fwd || down_fwd || kgrouped || dense || fused);
-  static constexpr int BN = narrow ? 64 : dual ? 128 : 256;   // per accumulator
+  static constexpr int BN = narrow ? 64 : (dual || down_narrow) ? 128 : 256;   // per accumulator
   // tile width chosen per launch (at most BN): the K-major-B kinds, whose B box
   // is exactly the tile's rows, and the router, whose N is the expert count
   static constexpr bool var_bn = (K == Kind::DownDgrad || K == Kind::GateUpDgrad || dense);
@@ -437,7 +439,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     pdl_enter();
   using T = Tr<K>;
   using G = Geo<K, PAIR>;
-  static_assert(!PAIR || (!T::dense && !T::narrow), "pairs: grouped kinds");
+  static_assert(!PAIR || (!T::dense && !T::narrow && !T::down_narrow), "pairs: grouped kinds");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~(uintptr_t)1023);
@@ -1676,6 +1678,17 @@ cudaError_t launch_down_fwd(const GroupedDims& g, const moe_bf16* A, const moe_b
   a.nk_seg = (g.f + BK - 1) / BK;
   a.out0 = yp;
   a.row_w = row_w;
+  // So few pairs that the 256-wide tiles of the experts that can hold rows
+  // (at most min(E, P)) are fewer than the SMs (a few decoded tokens): halve
+  // the tiles so more SMs stream the weights (measured: one token 43 -> 41 us
+  // a step; from eight tokens on the wide tiles are faster)
+  const int64_t groups = g.P < (int64_t)g.E ? g.P : (int64_t)g.E;
+  const int64_t rows = groups > 0 ? (g.P + groups - 1) / groups : 0;
+  const int64_t tiles = groups * ((rows + BM - 1) / BM) * ((g.d + 255) / 256);
+  if (tiles < (int64_t)num_sms())
+    return launch_kind<Kind::DownFwdNarrow, false>(a0, a0, b0, b0, a,
+                                                   mgrouped_tiles_upper(g, g.d, 128), s, &o0,
+                                                   nullptr, nullptr, pdl);
   if (pairs_mgrouped(g))
     return launch_kind<Kind::DownFwd, true>(a0, a0, b0, b0, a,
                                             mgrouped_tiles_upper(g, g.d, 256, 2 * BM), s, &o0,

@@ -36,7 +36,7 @@ static inline size_t al256r(size_t b) { return (b + 255) & ~(size_t)255; }
 constexpr int kRouterSmallMaxT = 32;   // route_is_small
 constexpr int kSmallTok = 8;        // tokens a CTA of the partial kernel multiplies
 constexpr int kSmallCols = 128;     // experts a CTA covers: 4 per lane
-constexpr int kSmallSlices = 16;
+constexpr int kSmallSlices = 32;
 constexpr int kSmallWarps = 8;
 
 static inline int small_slice_rows(int d) {
