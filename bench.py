@@ -56,6 +56,7 @@ STEP_KERNELS = ["router_logits", "topk", "permute", "gateup_fwd", "down_fwd", "c
                 "combine_bwd", "down_dgrad", "gateup_dgrad", "wgrad_down", "wgrad_gateup",
                 "route_bwd"]
 FWD_KERNELS = STEP_KERNELS[:6]
+FUSED_KERNELS = ["router_logits", "topk", "permute", "fused_fwd", "combine"]
 
 
 def parse_args(argv=None):
@@ -76,10 +77,12 @@ def parse_args(argv=None):
                     help="time the headline workload only (not the other workloads)")
     ap.add_argument("--side-steps", type=int, default=30,
                     help="timed steps of each other workload")
-    ap.add_argument("--path", choices=["auto", "general", "decode"], default="auto",
+    ap.add_argument("--path", choices=["auto", "general", "decode", "fused"], default="auto",
                     help="decode: the one-launch forward (moe_decode_fwd), forward-only "
-                         "workloads of at most 8 tokens; auto: the general path, measured "
-                         "faster than the one-launch forward at every decode size")
+                         "workloads of at most 8 tokens; fused: the inference forward with the "
+                         "fused expert GEMMs (moe_expert_fwd_fused), forward only; auto: the "
+                         "general path, measured faster than the one-launch forward at every "
+                         "decode size")
     ap.add_argument("--graph", action="store_true",
                     help="launch each timed step as one captured CUDA graph (launch-bound sizes)")
     return ap.parse_args(argv)
@@ -270,7 +273,7 @@ SIDE_CONFIGS = ["qwen3_30b", "smallm_T128", "smallm_T512", "smallm_T1024", "smal
 TARGET_TENSOR = 0.60
 TARGET_HBM = 0.70
 GEMM_KERNELS = ("gateup_fwd", "down_fwd", "down_dgrad", "gateup_dgrad", "wgrad_down",
-                "wgrad_gateup")
+                "wgrad_gateup", "fused_fwd")
 
 
 def kernel_roofline(name, fl, by, ms, peaks):
@@ -523,6 +526,9 @@ def run_ours(args, rank, world, local_rank):
     wl = workloads.CONFIGS[args.config]
     if args.align:
         wl = wl.with_(align=args.align)
+    fused = args.path == "fused"
+    if fused:
+        wl = wl.with_(backward=False)
     inp = workloads.generate(wl, with_dy=wl.backward)
     layer = MoELayer.from_inputs(inp, wl.k, wl.align, device=dev)
     decode = args.path == "decode"
@@ -531,6 +537,9 @@ def run_ours(args, rank, world, local_rank):
     if decode:
         new_buffers = lambda: layer.decode_buffers(wl.T)  # noqa: E731
         fwd = layer.decode_fwd
+    elif fused:
+        new_buffers = lambda: layer.fused_buffers(wl.T)  # noqa: E731
+        fwd = layer.forward_fused
     else:
         new_buffers = lambda: layer.buffers(wl.T, backward=wl.backward)  # noqa: E731
         fwd = layer.forward
@@ -559,7 +568,8 @@ def run_ours(args, rank, world, local_rank):
     if status != 0:
         raise RuntimeError(f"device status {status}: {_lib.status_str(status)}")
 
-    kernels = ["decode"] if decode else (STEP_KERNELS if wl.backward else FWD_KERNELS)
+    kernels = (["decode"] if decode else FUSED_KERNELS if fused
+               else STEP_KERNELS if wl.backward else FWD_KERNELS)
     per_kernel = profile_kernels(step, kernels, _lib)
     # "combine" fires twice per step (y and dx); the timer averaged both
     dominant = max(per_kernel, key=per_kernel.get)
@@ -591,6 +601,8 @@ def run_ours(args, rank, world, local_rank):
     shape = accounting.Shape(T=wl.T, d=wl.d, f=wl.f, E=wl.E, k=wl.k, E_active=active_experts())
     if decode:
         costs = {"decode": accounting.decode_costs(shape)}
+    elif fused:
+        costs = accounting.fused_forward_costs(shape)
     else:
         costs = accounting.kernel_costs(shape, wl.backward)
     step_bytes = sum(c[1] for c in costs.values())
@@ -719,7 +731,8 @@ def run_ours(args, rank, world, local_rank):
                           if flush else
                           "inputs larger than L2 (no flush): one step moves several GB"),
                    "graph": bool(args.graph),
-                   "path": "decode (one launch)" if decode else "general",
+                   "path": ("decode (one launch)" if decode else
+                            "fused expert GEMMs (inference)" if fused else "general"),
                    "parallelism": f"replicas x{world}"},
         "timing": {"ms_per_step": "median of the timed steps (one event pair each)",
                    "ms_per_step_mean": span_ms / args.steps,
@@ -740,7 +753,7 @@ def run_ours(args, rank, world, local_rank):
         "clocks": clocks,
         "e2e": e2e,
     }
-    if not args.no_side and not decode and args.config == DEFAULT_CONFIG:
+    if not args.no_side and not decode and not fused and args.config == DEFAULT_CONFIG:
         # the other workloads, each timed in this same run (their own clock record)
         del b
         torch.cuda.empty_cache()
