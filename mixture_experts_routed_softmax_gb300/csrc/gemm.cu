@@ -6,7 +6,8 @@
 // routed experts"), the weight gradient as a K-grouped GEMM and the bf16
 // gate/up output kept for backward ("FP8 Mega MoE").
 //
-// One persistent, warp-specialised kernel template serves all six GEMMs:
+// One persistent, warp-specialised kernel template serves the six GEMMs of the
+// layer, the router's two and the fused forward:
 //   warp 0      TMA producer: tiles of A and B into a shared-memory ring of
 //               as many stages as fit 192 KiB (4 of 48 KiB, 6 of 32 KiB; the
 //               down dgrad of a CTA pair keeps 5 and gives 32 KiB to its
@@ -35,6 +36,12 @@
 //   GateUpDgrad  dXp = dG . W_gate[e]^T + dU . W_up[e]^T (two K segments), fp32
 //   WgradDown    dW_down[e] = A_e^T . dYp_e                     (K-grouped)
 //   WgradGateUp  dW_gate[e] = Xp_e^T . dG_e, dW_up[e] = Xp_e^T . dU_e
+//   FusedFwd     GateUpFwd's tiles (A only) and then DownFwd's (Yp scaled by
+//                the pair's score) in one launch, each down tile waiting for
+//                the gate/up tiles of its rows (prime-rl PR #3885, §Changes,
+//                "FP8 Mega MoE": the expert layer as one op)
+//   RouterLogits, RouterWgrad: the router's GEMMs (route.cu); GateUpFwdNarrow
+//   and DownFwdNarrow: 64- and 128-wide tiles for few rows per expert
 // "M-grouped": expert e's output rows are its rows [offsets[e], offsets[e+1])
 // of the padded layout, cut into 128-row tiles (a tile may run past the group
 // end; those rows are computed and not stored). "K-grouped": the reduction
