@@ -101,3 +101,20 @@ def test_decode_costs_match_the_forward_arithmetic():
     assert fl == acc.totals(s, backward=False)[0]       # the same products, one launch
     w = 3 * 52 * 2048 * 768 * 2
     assert w < by < w + 2 * 2**20                       # weights dominate; the rest is small
+
+
+def test_fused_forward_costs_drop_only_the_kept_activations():
+    """The fused inference forward moves the five-call forward's bytes less
+    the G and U rows it keeps in tensor memory (2 P f in the bf16 layout),
+    with the same FLOPs: 6 P d f for the experts plus the router's."""
+    from mixture_experts_routed_softmax_gb300 import accounting as acc
+    s = acc.Shape(T=8192, d=2048, f=768, E=128, k=8, E_active=128)
+    five = acc.kernel_costs(s, backward=False)
+    fused = acc.fused_forward_costs(s)
+    f5 = sum(c[0] for c in five.values())
+    ff = sum(c[0] for c in fused.values())
+    b5 = sum(c[1] for c in five.values())
+    bf = sum(c[1] for c in fused.values())
+    assert ff == f5 == 6 * s.P * s.d * s.f + 2 * s.T * s.d * s.E
+    assert b5 - bf == 2 * s.P * s.f * 2
+    assert set(fused) == {"router_logits", "topk", "permute", "fused_fwd", "combine"}
