@@ -919,7 +919,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint8_t* gu_mem = smem + kStages * kStageBytes + ew * NS * G::gu_slot_bytes;
     int gu_issue = 0, gu_use = 0, gu_done = 0;   // chunks issued, read, seen complete
     int cur_tile = GEMM_CID, cur_j = 0, cur_n = 0, cur_row0 = 0, cur_col0 = 0;
-    const uint64_t pol_in = l2_evict_first();    // read once
+    // (no evict_first hint on these loads: each brings a whole 128-byte line
+    // whose other three chunks the warp asks for next; with the hint the line
+    // was often gone by then — Qwen3-30B-A3B shape 0.283 -> 0.260 ms)
     // the cursor's tile: this warp's rows and chunk count (none when the
     // warp's rows all lie past the group: nothing of them is stored)
     auto gu_tile = [&]() {
@@ -940,8 +942,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t dst = smem_u32(gu_mem + sl * G::gu_slot_bytes);
             const int x = cur_col0 + 8 * cur_j;
             mbar_arrive_expect_tx(bar, (uint32_t)G::gu_slot_bytes);
-            tma_load_2d_hint(dst, &mapA1, bar, x, cur_row0, pol_in);
-            tma_load_2d_hint(dst + G::gu_slot_bytes / 2, &mapB1, bar, x, cur_row0, pol_in);
+            tma_load_2d(dst, &mapA1, bar, x, cur_row0);
+            tma_load_2d(dst + G::gu_slot_bytes / 2, &mapB1, bar, x, cur_row0);
           }
           ++gu_issue;
           ++cur_j;
